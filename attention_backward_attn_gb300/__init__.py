@@ -1,0 +1,258 @@
+"""Python binding of the GB300 fused attention backward C ABI (include/attn_bwd.h).
+
+Argument marshalling only: every function here builds the C descriptors from
+torch tensors (shapes, element strides, device pointers, the current CUDA
+stream) and calls the same-named entry point of libattn_bwd.so. All
+arithmetic runs in the library's CUDA kernels. Importing this package fails
+loudly if the library has not been built (see `_build.build`).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+__all__ = [
+    "AttnError", "Problem", "Mask", "Sparse", "lib", "status_string",
+    "problem_from", "mask_from", "sparse_from",
+    "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
+    "attn_read_device_status", "attn_bwd_path", "BackwardPlan",
+]
+
+ATTN_OK = 0
+STATUS_NAMES = {
+    0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+    4: "ATTN_ERR_DEVICE_TIMEOUT", 5: "ATTN_ERR_INDEX_OOB", 6: "ATTN_ERR_RANGE",
+    7: "ATTN_ERR_WORKSPACE",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hk", ctypes.c_int32),
+        ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("do_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class Mask(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+                ("num_sink", ctypes.c_int32)]
+
+
+class Sparse(ctypes.Structure):
+    _fields_ = [
+        ("ori_kv", ctypes.c_void_p), ("cmp_kv", ctypes.c_void_p), ("cmp_idx", ctypes.c_void_p),
+        ("n_ori", ctypes.c_int32), ("n_cmp", ctypes.c_int32), ("topk", ctypes.c_int32),
+        ("ori_win_left", ctypes.c_int32), ("ori_win_right", ctypes.c_int32),
+        ("d_ori_kv", ctypes.c_void_p), ("d_cmp_kv", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    L.attn_fwd_lse.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp]
+    L.attn_fwd_lse.restype = st
+    L.attn_bwd_workspace_size.argtypes = [P(Problem), P(Mask), P(Sparse)]
+    L.attn_bwd_workspace_size.restype = sz
+    L.attn_bwd_preprocess.argtypes = [P(Problem), P(Sparse), vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      sz, vp]
+    L.attn_bwd_preprocess.restype = st
+    L.attn_bwd.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp,
+                           vp, vp, vp, vp, vp, sz, vp]
+    L.attn_bwd.restype = st
+    L.attn_read_device_status.argtypes = [vp, vp, P(ctypes.c_int32)]
+    L.attn_read_device_status.restype = st
+    L.attn_status_string.argtypes = [st]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_bwd_path.argtypes = [P(Problem), P(Mask), P(Sparse)]
+    L.attn_bwd_path.restype = ctypes.c_int32
+    return L
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.attn_status_string(code).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _strides(t):
+    s = t.stride()
+    return (ctypes.c_int64 * 3)(s[0], s[1], s[2])
+
+
+def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = None,
+                 Sk: Optional[int] = None, Hk: Optional[int] = None) -> Problem:
+    """Problem descriptor from BSHD tensors (q [B, Sq, Hq, D], k / v [B, Sk, Hk, D])."""
+    B, Sq, Hq, D = q.shape
+    p = Problem()
+    p.B, p.Sq, p.Hq, p.D = B, Sq, Hq, D
+    p.Sk = k.shape[1] if k is not None else (Sk or 0)
+    p.Hk = k.shape[2] if k is not None else (Hk or Hq)
+    p.scale = float(scale if scale is not None else D ** -0.5)
+    p.q_stride = _strides(q)
+    p.k_stride = _strides(k if k is not None else q)
+    p.v_stride = _strides(v if v is not None else (k if k is not None else q))
+    p.o_stride = _strides(o if o is not None else q)
+    p.do_stride = _strides(do if do is not None else (o if o is not None else q))
+    return p
+
+
+def mask_from(window_left: int = -1, window_right: int = -1, num_sink: int = 0) -> Optional[Mask]:
+    if window_left < 0 and window_right < 0 and num_sink == 0:
+        return None
+    return Mask(window_left, window_right, num_sink)
+
+
+def sparse_from(ori_kv, cmp_kv=None, cmp_idx=None, ori_win_left=-1, ori_win_right=-1,
+                d_ori_kv=None, d_cmp_kv=None) -> Sparse:
+    s = Sparse()
+    s.ori_kv = _ptr(ori_kv)
+    s.cmp_kv = _ptr(cmp_kv)
+    s.cmp_idx = _ptr(cmp_idx)
+    s.n_ori = ori_kv.shape[0]
+    s.n_cmp = cmp_kv.shape[0] if cmp_kv is not None else 0
+    s.topk = cmp_idx.shape[-1] if cmp_idx is not None else 0
+    s.ori_win_left, s.ori_win_right = ori_win_left, ori_win_right
+    s.d_ori_kv = _ptr(d_ori_kv)
+    s.d_cmp_kv = _ptr(d_cmp_kv)
+    return s
+
+
+def attn_bwd_workspace_size(prob: Problem, mask: Optional[Mask] = None,
+                            sparse: Optional[Sparse] = None) -> int:
+    return int(lib.attn_bwd_workspace_size(ctypes.byref(prob), _ref(mask), _ref(sparse)))
+
+
+def attn_bwd_path(prob: Problem, mask: Optional[Mask] = None,
+                  sparse: Optional[Sparse] = None) -> int:
+    return int(lib.attn_bwd_path(ctypes.byref(prob), _ref(mask), _ref(sparse)))
+
+
+def attn_fwd_lse(prob, mask, sparse, q, k, v, bias, o, lse, stream=None):
+    _check(lib.attn_fwd_lse(ctypes.byref(prob), _ref(mask), _ref(sparse), _ptr(q), _ptr(k),
+                            _ptr(v), _ptr(bias), _ptr(o), _ptr(lse), _stream(stream)),
+           "attn_fwd_lse")
+
+
+def attn_bwd_preprocess(prob, sparse, q, k, v, o, do, delta, dq, dbias, workspace,
+                        workspace_bytes, stream=None):
+    _check(lib.attn_bwd_preprocess(ctypes.byref(prob), _ref(sparse), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(o), _ptr(do), _ptr(delta), _ptr(dq), _ptr(dbias),
+                                   _ptr(workspace), workspace_bytes, _stream(stream)),
+           "attn_bwd_preprocess")
+
+
+def attn_bwd(prob, mask, sparse, q, k, v, do, lse, delta, bias, dq, dk, dv, dbias,
+             workspace, workspace_bytes, stream=None):
+    _check(lib.attn_bwd(ctypes.byref(prob), _ref(mask), _ref(sparse), _ptr(q), _ptr(k), _ptr(v),
+                        _ptr(do), _ptr(lse), _ptr(delta), _ptr(bias), _ptr(dq), _ptr(dk),
+                        _ptr(dv), _ptr(dbias), _ptr(workspace), workspace_bytes,
+                        _stream(stream)),
+           "attn_bwd")
+
+
+def attn_read_device_status(workspace, stream=None):
+    detail = ctypes.c_int32(0)
+    code = lib.attn_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(detail))
+    return int(code), int(detail.value)
+
+
+class BackwardPlan:
+    """Preallocated outputs + workspace for repeated backward calls.
+
+    Dense: q, k, v, o, do bf16 BSHD; lse fp32 [B, Hq, Sq]; bias fp32 [Hq, Sq, Sk]
+    or None. Sparse (pass ori_kv etc. and k = v = None): q, o, do [1, Sq, Hq, D].
+    run() enqueues attn_bwd_preprocess then attn_bwd on the current stream.
+    """
+
+    def __init__(self, q, k, v, o, do, lse, scale, mask: Optional[Mask] = None, bias=None,
+                 want_dbias=False, ori_kv=None, cmp_kv=None, cmp_idx=None,
+                 ori_win_left=-1, ori_win_right=-1):
+        import torch
+        dev = q.device
+        self.q, self.k, self.v, self.o, self.do, self.lse, self.bias = q, k, v, o, do, lse, bias
+        B, Sq, Hq, D = q.shape
+        self.sparse = None
+        if ori_kv is not None:
+            Hk = ori_kv.shape[1]
+            self.d_ori = torch.empty(ori_kv.shape, dtype=torch.float32, device=dev)
+            self.d_cmp = (torch.empty(cmp_kv.shape, dtype=torch.float32, device=dev)
+                          if cmp_kv is not None else None)
+            self.sparse = sparse_from(ori_kv, cmp_kv, cmp_idx, ori_win_left, ori_win_right,
+                                      self.d_ori, self.d_cmp)
+            self._keep = (ori_kv, cmp_kv, cmp_idx)
+            self.prob = problem_from(q, None, None, o, do, scale, Sk=0, Hk=Hk)
+            self.dk = self.dv = None
+        else:
+            self.prob = problem_from(q, k, v, o, do, scale)
+            self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+            self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        self.mask = mask
+        self.dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        self.delta = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
+        self.dbias = None
+        if want_dbias:
+            self.dbias = torch.empty((Hq, Sq, k.shape[1]), dtype=torch.float32, device=dev)
+        self.ws_bytes = attn_bwd_workspace_size(self.prob, mask, self.sparse)
+        if self.ws_bytes == 0:
+            raise AttnError(1, "attn_bwd_workspace_size")
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.path = attn_bwd_path(self.prob, mask, self.sparse)
+
+    def run(self, stream=None):
+        attn_bwd_preprocess(self.prob, self.sparse, self.q, self.k, self.v, self.o, self.do,
+                            self.delta, self.dq, self.dbias, self.workspace, self.ws_bytes,
+                            stream)
+        attn_bwd(self.prob, self.mask, self.sparse, self.q, self.k, self.v, self.do, self.lse,
+                 self.delta, self.bias, self.dq, self.dk, self.dv, self.dbias, self.workspace,
+                 self.ws_bytes, stream)
+
+    def device_status(self, stream=None):
+        return attn_read_device_status(self.workspace, stream)

@@ -1,0 +1,281 @@
+// C ABI entry points: argument validation, workspace layout, kernel dispatch.
+// See include/attn_bwd.h for the contract of each function.
+
+#include "internal.h"
+
+#include <math.h>
+
+namespace attn {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool strides_ok(const int64_t* s) {
+  for (int t = 0; t < 3; ++t)
+    if (s[t] < 0 || (s[t] % 8) != 0) return false;
+  return true;
+}
+
+// Validates the shared problem / mask / sparse descriptors and fills `out`.
+attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
+                           const attn_sparse_t* sp, Problem* out) {
+  if (prob == nullptr) return ATTN_ERR_INVALID_ARG;
+  const attn_problem_t& a = *prob;
+  if (a.B < 0 || a.Hq < 1 || a.Hk < 1 || a.Sq < 0 || a.D < 1) return ATTN_ERR_INVALID_ARG;
+  if (a.Hq % a.Hk != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(a.scale > 0.f) || !isfinite(a.scale)) return ATTN_ERR_INVALID_ARG;
+  if (!strides_ok(a.q_stride) || !strides_ok(a.o_stride) || !strides_ok(a.do_stride))
+    return ATTN_ERR_INVALID_ARG;
+  if (a.D != 64 && a.D != 128 && a.D != 512) return ATTN_ERR_UNSUPPORTED;
+  Problem p{};
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hk = a.Hk;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.D = a.D;
+  p.scale = a.scale;
+  for (int t = 0; t < 3; ++t) {
+    p.qs[t] = a.q_stride[t];
+    p.ks[t] = a.k_stride[t];
+    p.vs[t] = a.v_stride[t];
+    p.os[t] = a.o_stride[t];
+    p.dos[t] = a.do_stride[t];
+  }
+  p.mask = MaskSpec{-1, -1, 0};
+  if (mask != nullptr) {
+    if (mask->num_sink < 0) return ATTN_ERR_INVALID_ARG;
+    p.mask = MaskSpec{mask->window_left < 0 ? -1 : mask->window_left,
+                      mask->window_right < 0 ? -1 : mask->window_right, mask->num_sink};
+  }
+  p.sparse = sp != nullptr;
+  if (p.sparse) {
+    if (mask != nullptr) return ATTN_ERR_INVALID_ARG;  // the sparse window replaces it
+    if (a.B != 1) return ATTN_ERR_INVALID_ARG;
+    if (sp->n_ori < 0) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(sp->ori_kv) || !aligned16(sp->cmp_kv)) return ATTN_ERR_INVALID_ARG;
+    if (sp->cmp_kv != nullptr) {
+      if (sp->cmp_idx == nullptr) return ATTN_ERR_UNSUPPORTED;  // all-rows CFA variant
+      if (sp->n_cmp < 1 || sp->topk < 1) return ATTN_ERR_INVALID_ARG;
+    } else if (sp->cmp_idx != nullptr) {
+      return ATTN_ERR_INVALID_ARG;
+    }
+    p.n_ori = sp->n_ori;
+    p.n_cmp = sp->cmp_kv ? sp->n_cmp : 0;
+    p.topk = sp->cmp_kv ? sp->topk : 0;
+    p.ori_wl = sp->ori_win_left < 0 ? -1 : sp->ori_win_left;
+    p.ori_wr = sp->ori_win_right < 0 ? -1 : sp->ori_win_right;
+    p.Sk = 0;
+  } else {
+    if (a.Sk < 0) return ATTN_ERR_INVALID_ARG;
+    if (!strides_ok(a.k_stride) || !strides_ok(a.v_stride)) return ATTN_ERR_INVALID_ARG;
+  }
+  *out = p;
+  return ATTN_OK;
+}
+
+// Element counts of the tensors of a problem. A pointer may be NULL only for
+// a tensor with no elements.
+struct Sizes {
+  int64_t q, k, rows, ori;
+};
+
+Sizes sizes_of(const Problem& p) {
+  Sizes n;
+  n.q = (int64_t)p.B * p.Sq * p.Hq * p.D;
+  n.k = (int64_t)p.B * p.Sk * p.Hk * p.D;
+  n.rows = (int64_t)p.B * p.Hq * p.Sq;
+  n.ori = (int64_t)p.n_ori * p.Hk * p.D;
+  return n;
+}
+
+bool need(const void* ptr, int64_t count) { return count == 0 || ptr != nullptr; }
+
+bool use_tensor_cores(const Problem& p) { return !p.sparse && tc_supported(p); }
+
+attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
+  WorkspaceLayout w;
+  size_t off = sizeof(DevStatus);
+  if (tensor_core_path) {
+    const size_t qbytes = (size_t)p.B * p.Hq * p.Sq * p.D * sizeof(__half);
+    const size_t kbytes = (size_t)p.B * p.Hk * p.Sk * p.D * sizeof(__half);
+    off = align_up(off, 1024);
+    w.q16 = off;
+    off = align_up(off + qbytes, 1024);
+    w.do16 = off;
+    off = align_up(off + qbytes, 1024);
+    w.k16 = off;
+    off = align_up(off + kbytes, 1024);
+    w.v16 = off;
+    off = align_up(off + kbytes, 1024);
+    w.staged = true;
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_INDEX_OOB: return "ATTN_ERR_INDEX_OOB";
+    case ATTN_ERR_RANGE: return "ATTN_ERR_RANGE";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
+                      const attn_sparse_t* sparse) {
+  Problem p;
+  if (make_problem(prob, mask, sparse, &p) != ATTN_OK) return 0;
+  return use_tensor_cores(p) ? 1 : 2;
+}
+
+size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
+                               const attn_sparse_t* sparse) {
+  Problem p;
+  if (make_problem(prob, mask, sparse, &p) != ATTN_OK) return 0;
+  return workspace_layout(p, use_tensor_cores(p)).total;
+}
+
+attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
+                           const attn_sparse_t* sparse, const void* q, const void* k,
+                           const void* v, const float* bias, void* o, float* lse,
+                           cudaStream_t stream) {
+  Problem p;
+  attn_status_t s = make_problem(prob, mask, sparse, &p);
+  if (s != ATTN_OK) return s;
+  const Sizes n = sizes_of(p);
+  if (!need(q, n.q) || !need(o, n.q) || !need(lse, n.rows)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(bias))
+    return ATTN_ERR_INVALID_ARG;
+  if (p.sparse) {
+    if (k != nullptr || v != nullptr || bias != nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!need(sparse->ori_kv, n.ori)) return ATTN_ERR_INVALID_ARG;
+  } else {
+    if (!need(k, n.k) || !need(v, n.k) || !aligned16(k) || !aligned16(v))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  // Device conditions of the forward (bad sparse indices) are skipped but not
+  // recorded: the forward has no workspace.
+  return cuda_status(launch_fwd_simt(p, q, k, v, bias, sparse ? sparse->ori_kv : nullptr,
+                                     sparse ? sparse->cmp_kv : nullptr,
+                                     sparse ? sparse->cmp_idx : nullptr, o, lse, nullptr,
+                                     stream));
+}
+
+attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
+                                  const void* q, const void* k, const void* v,
+                                  const void* o, const void* dO, float* delta, float* dq,
+                                  float* dbias, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+  Problem p;
+  attn_status_t s = make_problem(prob, nullptr, sparse, &p);
+  if (s != ATTN_OK) return s;
+  const Sizes n = sizes_of(p);
+  if (!need(o, n.q) || !need(dO, n.q) || !need(delta, n.rows) || !need(dq, n.q))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(dbias))
+    return ATTN_ERR_INVALID_ARG;
+  float* d_ori = nullptr;
+  float* d_cmp = nullptr;
+  if (p.sparse) {
+    if (dbias != nullptr) return ATTN_ERR_INVALID_ARG;
+    d_ori = sparse->d_ori_kv;
+    d_cmp = sparse->cmp_kv ? sparse->d_cmp_kv : nullptr;
+    if (!need(d_ori, n.ori) || (sparse->cmp_kv && d_cmp == nullptr)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(d_ori) || !aligned16(d_cmp)) return ATTN_ERR_INVALID_ARG;
+  }
+  const bool tc = use_tensor_cores(p);
+  if (tc && (!need(q, n.q) || !need(k, n.k) || !need(v, n.k) || !aligned16(q) ||
+             !aligned16(k) || !aligned16(v)))
+    return ATTN_ERR_INVALID_ARG;
+  const WorkspaceLayout w = workspace_layout(p, tc);
+  if (workspace == nullptr || workspace_bytes < w.total || !aligned16(workspace))
+    return ATTN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  DevStatus* st = reinterpret_cast<DevStatus*>(ws + w.status);
+  __half* do16 = w.staged ? reinterpret_cast<__half*>(ws + w.do16) : nullptr;
+  cudaError_t e = launch_preprocess(p, o, dO, delta, dq, dbias, d_ori, d_cmp, do16, st, stream);
+  if (e != cudaSuccess || !tc) return cuda_status(e);
+  return cuda_status(launch_stage_qkv(p, q, k, v, reinterpret_cast<__half*>(ws + w.q16),
+                                      reinterpret_cast<__half*>(ws + w.k16),
+                                      reinterpret_cast<__half*>(ws + w.v16), st, stream));
+}
+
+attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
+                       const attn_sparse_t* sparse, const void* q, const void* k,
+                       const void* v, const void* dO, const float* lse, const float* delta,
+                       const float* bias, float* dq, float* dk, float* dv, float* dbias,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Problem p;
+  attn_status_t s = make_problem(prob, mask, sparse, &p);
+  if (s != ATTN_OK) return s;
+  const Sizes n = sizes_of(p);
+  if (!need(q, n.q) || !need(dO, n.q) || !need(lse, n.rows) || !need(delta, n.rows) ||
+      !need(dq, n.q))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(dO) || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
+  if (p.sparse) {
+    if (k || v || bias || dk || dv || dbias) return ATTN_ERR_INVALID_ARG;
+    if (!need(sparse->d_ori_kv, n.ori) || !need(sparse->ori_kv, n.ori) ||
+        (sparse->cmp_kv && sparse->d_cmp_kv == nullptr))
+      return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(sparse->d_ori_kv) || !aligned16(sparse->d_cmp_kv)) return ATTN_ERR_INVALID_ARG;
+  } else {
+    if (!need(k, n.k) || !need(v, n.k) || !need(dk, n.k) || !need(dv, n.k))
+      return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) || !aligned16(bias) ||
+        !aligned16(dbias))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  const bool tc = use_tensor_cores(p);
+  const WorkspaceLayout w = workspace_layout(p, tc);
+  if (workspace == nullptr || workspace_bytes < w.total || !aligned16(workspace))
+    return ATTN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  DevStatus* st = reinterpret_cast<DevStatus*>(ws + w.status);
+  if (tc) {
+    const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16);
+    const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16);
+    const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16);
+    const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16);
+    return cuda_status(launch_bwd_tc(p, q16, k16, v16, do16, lse, delta, bias, dq, dk, dv,
+                                     dbias, st, stream));
+  }
+  return cuda_status(launch_bwd_simt(p, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias,
+                                     sparse ? sparse->ori_kv : nullptr,
+                                     sparse ? sparse->cmp_kv : nullptr,
+                                     sparse ? sparse->cmp_idx : nullptr,
+                                     sparse ? sparse->d_ori_kv : nullptr,
+                                     sparse ? sparse->d_cmp_kv : nullptr, st, stream));
+}
+
+attn_status_t attn_read_device_status(const void* workspace, cudaStream_t stream,
+                                      int32_t* detail) {
+  if (workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int32_t host[2] = {0, 0};
+  if (cudaMemcpy(host, workspace, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (detail != nullptr) *detail = host[1];
+  return static_cast<attn_status_t>(host[0]);
+}
+
+}  // extern "C"

@@ -1,0 +1,132 @@
+// Internal helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "attn_bwd.h"
+
+namespace attn {
+
+// Status record at the start of every workspace. Kernels record the first
+// device-side condition; attn_read_device_status copies it back.
+struct DevStatus {
+  int32_t code;
+  int32_t detail;
+  int32_t reserved[62];
+};
+static_assert(sizeof(DevStatus) == 256, "status record is 256 bytes");
+
+__device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t detail) {
+  if (st == nullptr) return;
+  if (atomicCAS(&st->code, 0, code) == 0) {
+    atomicExch(&st->detail, detail);
+  }
+}
+
+// live(i, j) = j < sink || (i - wl <= j <= i + wr); negative bound = unbounded
+// ("22_sink_tokens_fmha.py" mask builders, top-left aligned).
+struct MaskSpec {
+  int wl;
+  int wr;
+  int sink;
+};
+
+__host__ __device__ __forceinline__ bool mask_live(const MaskSpec& m, int i, int j) {
+  if (j < m.sink) return true;
+  if (m.wl >= 0 && j < i - m.wl) return false;
+  if (m.wr >= 0 && j > i + m.wr) return false;
+  return true;
+}
+
+// Non-sink key range [lo, hi] (inclusive, clipped to [0, n)) live for row i.
+__host__ __device__ __forceinline__ void mask_row_range(const MaskSpec& m, int i, int n,
+                                                        int* lo, int* hi) {
+  int a = (m.wl >= 0) ? i - m.wl : 0;
+  int b = (m.wr >= 0) ? i + m.wr : n - 1;
+  *lo = a < 0 ? 0 : a;
+  *hi = b > n - 1 ? n - 1 : b;
+}
+
+// Non-sink query range [lo, hi] live for key j (j >= sink), clipped to [0, n).
+__host__ __device__ __forceinline__ void mask_col_range(const MaskSpec& m, int j, int n,
+                                                        int* lo, int* hi) {
+  int a = (m.wr >= 0) ? j - m.wr : 0;
+  int b = (m.wl >= 0) ? j + m.wl : n - 1;
+  *lo = a < 0 ? 0 : a;
+  *hi = b > n - 1 ? n - 1 : b;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Load EPL consecutive bf16 values (EPL in {2, 4, 8, 16}) as floats.
+template <int EPL>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float* out) {
+  if constexpr (EPL == 2) {
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+    float2 f = __bfloat1622float2(v);
+    out[0] = f.x; out[1] = f.y;
+  } else if constexpr (EPL == 4) {
+    uint2 raw = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      float2 f = __bfloat1622float2(h[t]);
+      out[2 * t] = f.x; out[2 * t + 1] = f.y;
+    }
+  } else {
+    static_assert(EPL % 8 == 0, "EPL must be 2, 4 or a multiple of 8");
+#pragma unroll
+    for (int c = 0; c < EPL / 8; ++c) {
+      uint4 raw = *reinterpret_cast<const uint4*>(p + 8 * c);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float2 f = __bfloat1622float2(h[t]);
+        out[8 * c + 2 * t] = f.x; out[8 * c + 2 * t + 1] = f.y;
+      }
+    }
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* p, const float* in) {
+#pragma unroll
+  for (int t = 0; t < EPL; t += 2) {
+    *reinterpret_cast<__nv_bfloat162*>(p + t) = __floats2bfloat162_rn(in[t], in[t + 1]);
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void store_f32(float* p, const float* in) {
+  if constexpr (EPL % 4 == 0) {
+#pragma unroll
+    for (int t = 0; t < EPL; t += 4)
+      *reinterpret_cast<float4*>(p + t) = make_float4(in[t], in[t + 1], in[t + 2], in[t + 3]);
+  } else {
+#pragma unroll
+    for (int t = 0; t < EPL; t += 2)
+      *reinterpret_cast<float2*>(p + t) = make_float2(in[t], in[t + 1]);
+  }
+}
+
+// Host-side view of a launch: validated problem plus derived values.
+struct Problem {
+  int B, Hq, Hk, Sq, Sk, D;
+  float scale;
+  int64_t qs[3], ks[3], vs[3], os[3], dos[3];
+  MaskSpec mask;
+  bool sparse;
+  // sparse fields
+  int n_ori, n_cmp, topk, ori_wl, ori_wr;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace attn

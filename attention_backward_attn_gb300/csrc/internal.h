@@ -1,0 +1,55 @@
+// Host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+// Workspace layout: [DevStatus (256 B)] then, for the tensor-core path, fp16
+// copies of Q, dO [B, Hq, Sq, D] and K, V [B, Hk, Sk, D] (head-major rows),
+// each region aligned to 1 KiB.
+struct WorkspaceLayout {
+  size_t status = 0;
+  size_t q16 = 0, k16 = 0, v16 = 0, do16 = 0;
+  size_t total = 0;
+  bool staged = false;
+};
+
+WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path);
+
+// ---- simt_kernels.cu ----
+cudaError_t launch_fwd_simt(const Problem& p, const void* q, const void* k, const void* v,
+                            const float* bias, const void* ori_kv, const void* cmp_kv,
+                            const int32_t* cmp_idx, void* o, float* lse, DevStatus* st,
+                            cudaStream_t stream);
+
+cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, const void* v,
+                            const void* dO, const float* lse, const float* delta,
+                            const float* bias, float* dq, float* dk, float* dv, float* dbias,
+                            const void* ori_kv, const void* cmp_kv, const int32_t* cmp_idx,
+                            float* d_ori, float* d_cmp, DevStatus* st, cudaStream_t stream);
+
+// ---- preprocess.cu ----
+// Clears the status record and zeroes the accumulated outputs, then computes
+// delta, zeroes dq and (if do16 != nullptr) stages dO as fp16 head-major.
+cudaError_t launch_preprocess(const Problem& p, const void* o, const void* dO, float* delta,
+                              float* dq, float* dbias, float* d_ori, float* d_cmp,
+                              __half* do16, DevStatus* st, cudaStream_t stream);
+
+// Stages q, k, v as fp16 head-major copies for the tensor-core path.
+cudaError_t launch_stage_qkv(const Problem& p, const void* q, const void* k, const void* v,
+                             __half* q16, __half* k16, __half* v16, DevStatus* st,
+                             cudaStream_t stream);
+
+// ---- tc_bwd.cu ----
+bool tc_supported(const Problem& p);
+cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16,
+                          const __half* v16, const __half* do16, const float* lse,
+                          const float* delta, const float* bias, float* dq, float* dk,
+                          float* dv, float* dbias, DevStatus* st, cudaStream_t stream);
+
+}  // namespace attn

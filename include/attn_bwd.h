@@ -1,0 +1,186 @@
+/*
+ * attn_bwd.h -- C ABI of the GB300 (sm_103a) fused attention backward library.
+ *
+ * The library computes, for softmax attention with an optional mask, an
+ * optional elementwise bias and grouped-query heads,
+ *
+ *   S  = scale * Q K^T + bias            (masked entries excluded)
+ *   P  = exp(S - LSE)                    (LSE given by the forward)
+ *   D  = rowsum(dO * O)
+ *   dP = dO V^T,   dS = P * (dP - D)
+ *   dQ = scale * dS K,   dK = scale * dS^T Q,   dV = P^T dO,
+ *   dbias = sum over the batch of dS,
+ *
+ * following composable_kernel "34_bwd_gqa_fmha.py" (docstring "CPU backward
+ * reference" and cpu_bwd_gqa), "28_backward_dbias_fmha.py"
+ * (cpu_attention_bwd_dbias) and "22_sink_tokens_fmha.py" (mask builders), and
+ * a selected-KV sparse variant with shared latent KV (K = V) following the
+ * Ascend "sparse_flash_mla_grad" formula (phases 1-3).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    allocates no device memory and keeps no state between calls; all work is
+ *    enqueued on `stream` and nothing blocks except attn_read_device_status.
+ *  - Host-side argument checks return an error code synchronously and enqueue
+ *    nothing. Conditions found on the device (an out-of-range sparse index, an
+ *    fp16 range overflow of the staged operands, a bounded wait that ran out)
+ *    never trap: the kernel records the first such condition in the status
+ *    record at the start of the workspace and skips the offending work;
+ *    attn_read_device_status returns it.
+ *  - Layouts: q, o, dO are [B, Sq, Hq, D] and k, v are [B, Sk, Hk, D]
+ *    ("BSHD", the flash-attn layout of the ring-attention page), addressed
+ *    through the element strides in attn_problem_t; the last (D) dimension
+ *    must be contiguous. bf16 inputs. lse and delta are fp32 [B, Hq, Sq],
+ *    contiguous, natural log. bias and dbias are fp32 [Hq, Sq, Sk],
+ *    contiguous, broadcast / summed over the batch. dq is fp32 contiguous
+ *    [B, Sq, Hq, D]; dk, dv are fp32 contiguous [B, Sk, Hk, D].
+ *  - Query head h reads KV head h / (Hq / Hk) (consecutive grouping, np.repeat
+ *    in "34_bwd_gqa_fmha.py"); dk / dv are summed over each group.
+ */
+#ifndef ATTN_BWD_H
+#define ATTN_BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null pointer, bad shape, bad stride, bad scale */
+  ATTN_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  ATTN_ERR_CUDA = 3,           /* a CUDA runtime call failed (launch, attribute) */
+  ATTN_ERR_DEVICE_TIMEOUT = 4, /* device: a bounded wait ran out; outputs invalid */
+  ATTN_ERR_INDEX_OOB = 5,      /* device: a sparse index >= n_cmp or < -1; entry skipped */
+  ATTN_ERR_RANGE = 6,          /* device: an input is outside the fp16 range of the
+                                  tensor-core path (|x| > 65504); outputs invalid */
+  ATTN_ERR_WORKSPACE = 7       /* workspace null or smaller than attn_bwd_workspace_size */
+} attn_status_t;
+
+/* Problem shape and input layout (the FmhaProblem pattern of
+ * "34_bwd_gqa_fmha.py": batch, nhead_q, nhead_k, seqlen_q, seqlen_k, hdim).
+ * Head dims of q/k and v/o are equal (D). Strides are in ELEMENTS for the
+ * (batch, sequence, head) dimensions; each must be a multiple of 8 (16-byte
+ * rows) and the base pointers 16-byte aligned. Hq % Hk == 0. */
+typedef struct attn_problem {
+  int32_t B, Hq, Hk, Sq, Sk, D;
+  float scale;            /* softmax scale, finite and > 0 (usually 1/sqrt(D)) */
+  int64_t q_stride[3];
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];    /* o (written by attn_fwd_lse, read by preprocess) */
+  int64_t do_stride[3];
+} attn_problem_t;
+
+/* Key mask, positions aligned top-left ("22_sink_tokens_fmha.py"):
+ *   live(i, j) = (j < num_sink) || (i - window_left <= j && j <= i + window_right)
+ * with a negative window bound meaning that side is unbounded. Causal is
+ * (-1, 0, 0); causal + n sinks is (-1, 0, n); sliding window of w keys plus n
+ * sinks is (w - 1, 0, n). A NULL mask pointer means every entry is live.
+ * A row with no live key gets LSE = -inf, O = 0 and no gradient. */
+typedef struct attn_mask {
+  int32_t window_left;
+  int32_t window_right;
+  int32_t num_sink;
+} attn_mask_t;
+
+/* Selected-KV sparse attention with shared latent KV (Ascend
+ * "sparse_flash_mla_grad": selectedKv = concat(oriKv window,
+ * Gather(cmpKv, topkIndices[i])), K = V = selectedKv).
+ * One sequence: the problem's B must be 1, its Sk is ignored, k / v / bias /
+ * dk / dv / dbias must be NULL. Query i sits at position p = (n_ori - Sq) + i
+ * and selects original rows [p - ori_win_left, p + ori_win_right] clipped to
+ * [0, n_ori) (negative bound = unbounded) plus the compressed rows listed in
+ * cmp_idx[i, g, :] (-1 = unused slot; indices may repeat and then count
+ * twice). cmp_kv == NULL means no compressed rows (the sliding-window case).
+ * All arrays contiguous: ori_kv bf16 [n_ori, Hk, D], cmp_kv bf16
+ * [n_cmp, Hk, D], cmp_idx int32 [Sq, Hk, topk]; gradients d_ori_kv fp32
+ * [n_ori, Hk, D] and d_cmp_kv fp32 [n_cmp, Hk, D] receive dKV = dK + dV,
+ * summed over every query and head that selected the row. */
+typedef struct attn_sparse {
+  const void* ori_kv;
+  const void* cmp_kv;
+  const int32_t* cmp_idx;
+  int32_t n_ori, n_cmp, topk;
+  int32_t ori_win_left, ori_win_right;
+  float* d_ori_kv;
+  float* d_cmp_kv;
+} attn_sparse_t;
+
+/* Forward with log-sum-exp, used to produce the backward's O and LSE inputs
+ * ("34_bwd_gqa_fmha.py" cpu_fwd_with_intermediates, "28_backward_dbias_fmha.py"
+ * cpu_attention_fwd_bias, "22_sink_tokens_fmha.py" cpu_attention_fwd_masked).
+ * Writes o (bf16, o_stride layout) and lse (fp32 [B, Hq, Sq], natural log).
+ * sparse != NULL selects the sparse variant (k, v, bias must then be NULL). */
+attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
+                           const attn_sparse_t* sparse,
+                           const void* q, const void* k, const void* v,
+                           const float* bias, void* o, float* lse,
+                           cudaStream_t stream);
+
+/* Bytes of device workspace that attn_bwd_preprocess and attn_bwd need for
+ * this problem (a status record plus fp16 staging of the operands of the
+ * tensor-core path). Returns 0 if the arguments are invalid. */
+size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
+                               const attn_sparse_t* sparse);
+
+/* Backward pre-pass ("34_bwd_gqa_fmha.py" cpu_bwd_gqa: D = rowsum(dO * O);
+ * Ascend formula phase 2: SoftmaxGrad(dO, O)):
+ *  - delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d] in fp32;
+ *  - zeroes the accumulated outputs: dq, dbias (if non-NULL) and, for the
+ *    sparse variant, sparse->d_ori_kv / d_cmp_kv;
+ *  - clears the workspace status record;
+ *  - when attn_bwd will take the tensor-core path, writes fp16 copies of q,
+ *    k, v and dO into the workspace (head-major [B, H, S, D] rows) for it.
+ *    Every bf16 value of magnitude in [2^-14, 65504] converts exactly; a
+ *    larger one is recorded as ATTN_ERR_RANGE.
+ * q, k, v are the same tensors later passed to attn_bwd (k, v NULL for the
+ * sparse variant). Must precede attn_bwd on the same stream with the same
+ * workspace, and the inputs must not change in between. */
+attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
+                                  const void* q, const void* k, const void* v,
+                                  const void* o, const void* dO, float* delta,
+                                  float* dq, float* dbias,
+                                  void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/* The fused backward ("34_bwd_gqa_fmha.py" docstring and cpu_bwd_gqa;
+ * "28_backward_dbias_fmha.py" cpu_attention_bwd_dbias; Ascend
+ * "sparse_flash_mla_grad" phases 1-3). P is rebuilt from lse; delta, dq and
+ * dbias / sparse gradients come from attn_bwd_preprocess (dq, dbias and the
+ * sparse gradients are accumulated into the zeroed buffers); dk and dv are
+ * written in full. dbias may be non-NULL without bias (gradient of a zero
+ * bias). Returns ATTN_ERR_UNSUPPORTED for D outside {64, 128, 512} or the
+ * sparse variant with D != 512 when no fallback kernel covers it. */
+attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
+                       const attn_sparse_t* sparse,
+                       const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* delta, const float* bias,
+                       float* dq, float* dk, float* dv, float* dbias,
+                       void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the first device-side condition
+ * recorded in the workspace status record since the last
+ * attn_bwd_preprocess (ATTN_OK if none). *detail (may be NULL) receives a
+ * condition-specific integer (e.g. the offending query row). */
+attn_status_t attn_read_device_status(const void* workspace, cudaStream_t stream,
+                                      int32_t* detail);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+/* Which backward kernel attn_bwd would launch for these arguments:
+ * 0 = none (invalid / unsupported), 1 = tcgen05 tensor-core kernel,
+ * 2 = SIMT kernels. For tests and benchmarks. */
+int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
+                      const attn_sparse_t* sparse);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_BWD_H */

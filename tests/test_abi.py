@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every function include/attn_bwd.h declares,
+and reject bad arguments with an error code before enqueuing any work (these
+calls never reach a kernel launch, so they run without a device).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ab():
+    from attention_backward_attn_gb300 import _build
+    _build.build()
+    import attention_backward_attn_gb300 as mod
+    return mod
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(attn_[a-z_0-9]+)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
+              "attn_read_device_status", "attn_status_string", "attn_bwd_path"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ab):
+    lib = ctypes.CDLL(ab._build.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(ab):
+    assert ab.status_string(0) == "ATTN_OK"
+    assert ab.status_string(5) == "ATTN_ERR_INDEX_OOB"
+    assert ab.status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def _prob(ab, B=2, Hq=8, Hk=2, Sq=256, Sk=256, D=128, scale=None):
+    p = ab.Problem()
+    p.B, p.Hq, p.Hk, p.Sq, p.Sk, p.D = B, Hq, Hk, Sq, Sk, D
+    p.scale = scale if scale is not None else D ** -0.5
+    qs = (Sq * Hq * D, Hq * D, D)
+    ks = (Sk * Hk * D, Hk * D, D)
+    p.q_stride = (ctypes.c_int64 * 3)(*qs)
+    p.o_stride = (ctypes.c_int64 * 3)(*qs)
+    p.do_stride = (ctypes.c_int64 * 3)(*qs)
+    p.k_stride = (ctypes.c_int64 * 3)(*ks)
+    p.v_stride = (ctypes.c_int64 * 3)(*ks)
+    return p
+
+
+def test_workspace_size_and_validation(ab):
+    p = _prob(ab)
+    assert ab.attn_bwd_workspace_size(p) >= 256
+    bad = _prob(ab, Hq=6, Hk=4)
+    assert ab.attn_bwd_workspace_size(bad) == 0
+    assert ab.attn_bwd_path(bad) == 0
+    assert ab.attn_bwd_path(_prob(ab, D=96)) == 0  # unsupported head dim
+    assert ab.attn_bwd_workspace_size(_prob(ab, scale=0.0)) == 0
+    assert ab.attn_bwd_workspace_size(_prob(ab, scale=float("nan"))) == 0
+    odd = _prob(ab)
+    odd.q_stride = (ctypes.c_int64 * 3)(256 * 8 * 128, 8 * 128 + 4, 128)
+    assert ab.attn_bwd_workspace_size(odd) == 0
+    assert ab.attn_bwd_path(p) in (1, 2)
+
+
+def _call_bwd(ab, p, mask=None, sparse=None, ptrs=None, ws_bytes=1 << 20):
+    fake = 1 << 20  # never dereferenced: every case below fails host validation
+    args = dict(q=fake, k=fake, v=fake, do=fake, lse=fake, delta=fake, bias=None, dq=fake,
+                dk=fake, dv=fake, dbias=None, ws=fake)
+    args.update(ptrs or {})
+    return ab.lib.attn_bwd(ctypes.byref(p), None if mask is None else ctypes.byref(mask),
+                           None if sparse is None else ctypes.byref(sparse), args["q"],
+                           args["k"], args["v"], args["do"], args["lse"], args["delta"],
+                           args["bias"], args["dq"], args["dk"], args["dv"], args["dbias"],
+                           args["ws"], ws_bytes, None)
+
+
+def test_bwd_rejects_bad_arguments_on_the_host(ab):
+    p = _prob(ab)
+    assert _call_bwd(ab, p, ptrs=dict(q=None)) == 1
+    assert _call_bwd(ab, p, ptrs=dict(dk=None)) == 1
+    assert _call_bwd(ab, p, ptrs=dict(q=(1 << 20) + 8)) == 1  # misaligned
+    assert _call_bwd(ab, p, ptrs=dict(ws=None)) == 7
+    assert _call_bwd(ab, p, ws_bytes=16) == 7
+    assert _call_bwd(ab, _prob(ab, D=80)) == 2
+    m = ab.Mask(-1, 0, -3)
+    assert _call_bwd(ab, p, mask=m) == 1
+
+
+def test_sparse_descriptor_validation(ab):
+    fake = 1 << 20
+    p = _prob(ab, B=1, Hq=16, Hk=1, Sq=128, Sk=0, D=512)
+    s = ab.Sparse()
+    s.ori_kv, s.n_ori, s.ori_win_left, s.ori_win_right = fake, 128, 31, 0
+    s.d_ori_kv = fake
+    assert ab.attn_bwd_path(p, None, s) == 2
+    # k / v must be NULL for the shared-KV variant
+    assert _call_bwd(ab, p, sparse=s) == 1
+    # compressed KV without an index list (the all-rows variant) is not built
+    s.cmp_kv, s.n_cmp, s.topk, s.d_cmp_kv = fake, 32, 8, fake
+    assert ab.attn_bwd_path(p, None, s) == 0
+    assert _call_bwd(ab, p, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None)) == 2
+    # batch must be 1
+    p2 = _prob(ab, B=2, Hq=16, Hk=1, Sq=128, Sk=0, D=512)
+    s.cmp_idx = fake
+    assert ab.attn_bwd_path(p2, None, s) == 0
+    # a mask descriptor is not allowed with the sparse window
+    assert ab.attn_bwd_path(p, ab.Mask(-1, 0, 0), s) == 0
+
+
+def test_read_status_rejects_null(ab):
+    code = ab.lib.attn_read_device_status(None, None, None)
+    assert code == 1

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA backward (through the C ABI) against the float64 oracle.
+
+Small cases compare every element; they span several 128-row tiles and a
+ragged tail. Full-size cases run the exact launch the benchmark times and
+compare complete head groups (dense) or every output (sparse).
+"""
+
+import numpy as np
+import pytest
+
+import harness as H
+from workloads import make_workload, make_dense, make_sparse
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _run_dense(w, expect_path=None):
+    torch = _torch()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    plan = H.gpu_dense_plan(w, O_b, L_f)
+    if expect_path is not None:
+        assert plan.path == expect_path
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 0, (code, detail)
+    return plan, O_b, L_f
+
+
+def _compare_dense(w, plan, O_b, L_f, batches=None, kv_heads=None):
+    ref = H.dense_reference(w, O_b, L_f, batches, kv_heads)
+    r = w.Hq // w.Hk
+    bs = batches if batches is not None else slice(0, w.B)
+    ks = kv_heads if kv_heads is not None else slice(0, w.Hk)
+    qs = slice(ks.start * r, ks.stop * r)
+    H.check_close("dq", plan.dq.cpu().numpy()[bs][:, :, qs], ref["dq"])
+    H.check_close("dk", plan.dk.cpu().numpy()[bs][:, :, ks], ref["dk"])
+    H.check_close("dv", plan.dv.cpu().numpy()[bs][:, :, ks], ref["dv"])
+    delta = plan.delta.cpu().numpy()[bs][:, qs]
+    np.testing.assert_allclose(delta, ref["delta"], rtol=1e-5, atol=1e-5 * np.abs(ref["delta"]).max())
+    if w.want_dbias:
+        assert batches is None
+        H.check_close("dbias", plan.dbias.cpu().numpy()[qs], ref["dbias"])
+
+
+SMALL_DENSE = {
+    # the exact 64-token MHA workload
+    "mha_s64_d64": lambda: make_workload("mha_s64_d64"),
+    # GQA 4:1 causal, 3 query tiles
+    "gqa4_causal_s384_d128": lambda: make_workload("gqa4_causal_s1024_d128", Hq=8, Hk=2,
+                                                   Sq=384, Sk=384),
+    # ALiBi bias + dbias, D = 64
+    "alibi_dbias_s256_d64": lambda: make_workload("mha_alibi_dbias_s2048_d64", B=3, Hq=4,
+                                                  Hk=4, Sq=256, Sk=256),
+    # window 128 + 4 sinks, GQA 4:1
+    "window128_sink4_s640_d128": lambda: make_workload("gqa4_window1024_sink4_s8192_d128",
+                                                       Hq=8, Hk=2, Sq=640, Sk=640,
+                                                       window_left=127),
+    # ragged lengths (not a multiple of the tile), causal + sinks, D = 64
+    "ragged_causal_sink_s200_d64": lambda: make_dense("r", 21, B=2, Hq=4, Hk=2, Sq=200,
+                                                      Sk=200, D=64, window_left=-1,
+                                                      window_right=0, num_sink=3),
+    # Sq != Sk, GQA 8:1, no mask
+    "gqa8_sq128_sk320_d128": lambda: make_dense("x", 22, B=1, Hq=8, Hk=1, Sq=128, Sk=320,
+                                                D=128),
+    # Sq > Sk, two-sided window, bias without dbias request
+    "window_lr_sq320_sk192_d64": lambda: make_dense("y", 23, B=2, Hq=2, Hk=1, Sq=320, Sk=192,
+                                                    D=64, window_left=40, window_right=25,
+                                                    alibi=True),
+    # MHA D = 512 through the dense path
+    "mha_s128_d512": lambda: make_dense("z", 24, B=1, Hq=2, Hk=2, Sq=128, Sk=128, D=512,
+                                        window_left=-1, window_right=0),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_DENSE))
+def test_dense_small(name):
+    w = SMALL_DENSE[name]()
+    plan, O_b, L_f = _run_dense(w)
+    _compare_dense(w, plan, O_b, L_f)
+
+
+def test_fully_masked_rows_and_empty_query():
+    # keys live only for rows 0..7 (window_right = -1 .. left 3 at Sk = 8): rows
+    # beyond see nothing -> LSE = -inf, zero gradients.
+    w = make_dense("m", 25, B=1, Hq=2, Hk=1, Sq=136, Sk=8, D=64, window_left=3,
+                   window_right=0)
+    plan, O_b, L_f = _run_dense(w)
+    assert np.all(np.isneginf(L_f[:, :, 12:]))
+    _compare_dense(w, plan, O_b, L_f)
+    # Sq = 0: nothing to differentiate; dK, dV must come back as exact zeros.
+    torch = _torch()
+    import attention_backward_attn_gb300 as ab
+    B, Sk, Hq, Hk, D = 1, 64, 2, 1, 64
+    q = torch.empty((B, 0, Hq, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.randn((B, Sk, Hk, D), device="cuda").to(torch.bfloat16)
+    lse = torch.empty((B, Hq, 0), dtype=torch.float32, device="cuda")
+    plan = ab.BackwardPlan(q, k, k.clone(), q, q, lse, D ** -0.5)
+    plan.dk.fill_(1.0)
+    plan.dv.fill_(1.0)
+    plan.run()
+    torch.cuda.synchronize()
+    assert float(plan.dk.abs().max()) == 0.0 and float(plan.dv.abs().max()) == 0.0
+
+
+def test_forward_matches_oracle():
+    torch = _torch()
+    import attention_backward_attn_gb300 as ab
+    for w in (SMALL_DENSE["window128_sink4_s640_d128"](), SMALL_DENSE["alibi_dbias_s256_d64"]()):
+        O_b, L_f, O, L = H.dense_forward_inputs(w)
+        q, k, v = (H.to_dev_bf16(x, "cuda") for x in (w.q, w.k, w.v))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+        bias = None if w.bias is None else H.to_dev_f32(w.bias, "cuda")
+        prob = ab.problem_from(q, k, v, o, o, w.scale)
+        ab.attn_fwd_lse(prob, ab.mask_from(w.window_left, w.window_right, w.num_sink), None,
+                        q, k, v, bias, o, lse)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(lse.cpu().numpy(), L, rtol=0, atol=2e-5 * max(1, np.abs(L).max()))
+        got = o.float().cpu().numpy()
+        ref = O.transpose(0, 2, 1, 3)
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+SMALL_SPARSE = {
+    "scfa_s256_h16_d512": lambda: make_sparse("s", 31, Sq=256, Hq=16, Hk=1, D=512, n_ori=256,
+                                              n_cmp=64, topk=32, cmp_ratio=4, ori_win_left=31),
+    "swa_s192_h8_d512": lambda: make_sparse("w", 32, Sq=192, Hq=8, Hk=1, D=512, n_ori=192,
+                                            n_cmp=0, topk=0, cmp_ratio=1, ori_win_left=63,
+                                            with_cmp=False),
+    "scfa_delta_hk2_d512": lambda: make_sparse("d", 33, Sq=96, Hq=8, Hk=2, D=512, n_ori=160,
+                                               n_cmp=40, topk=16, cmp_ratio=4, ori_win_left=20,
+                                               ori_win_right=3),
+}
+
+
+def _run_sparse(w):
+    torch = _torch()
+    O_b, L_f, _, _ = H.sparse_forward_inputs(w)
+    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 0, (code, detail)
+    return plan, O_b, L_f
+
+
+@pytest.mark.parametrize("name", list(SMALL_SPARSE))
+def test_sparse_small(name):
+    w = SMALL_SPARSE[name]()
+    plan, O_b, L_f = _run_sparse(w)
+    ref = H.sparse_reference(w, O_b, L_f)
+    H.check_close("dq", plan.dq.cpu().numpy()[0], ref["dq"])
+    H.check_close("d_ori", plan.d_ori.cpu().numpy(), ref["d_ori"])
+    if w.cmp_kv is not None:
+        H.check_close("d_cmp", plan.d_cmp.cpu().numpy(), ref["d_cmp"])
+
+
+def test_sparse_bad_index_is_reported_not_trapped():
+    torch = _torch()
+    w = SMALL_SPARSE["scfa_s256_h16_d512"]()
+    O_b, L_f, _, _ = H.sparse_forward_inputs(w)
+    w.cmp_idx = w.cmp_idx.copy()
+    w.cmp_idx[200, 0, 0] = w.n_cmp + 5  # out of range: must be skipped and reported
+    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 5 and detail == 200
+
+
+# ------------------------------------------------------------- full size ----
+
+def test_full_gqa4_causal_s1024_d128():
+    w = make_workload("gqa4_causal_s1024_d128")
+    plan, O_b, L_f = _run_dense(w)
+    _compare_dense(w, plan, O_b, L_f)
+
+
+def test_full_mha_alibi_dbias_s2048_d64():
+    w = make_workload("mha_alibi_dbias_s2048_d64")
+    plan, O_b, L_f = _run_dense(w)
+    for h in (0, 15):
+        ref = H.dense_reference(w, O_b, L_f, kv_heads=slice(h, h + 1))
+        H.check_close("dq", plan.dq.cpu().numpy()[:, :, h:h + 1], ref["dq"])
+        H.check_close("dk", plan.dk.cpu().numpy()[:, :, h:h + 1], ref["dk"])
+        H.check_close("dv", plan.dv.cpu().numpy()[:, :, h:h + 1], ref["dv"])
+        H.check_close("dbias", plan.dbias.cpu().numpy()[h:h + 1], ref["dbias"])
+
+
+def test_full_gqa4_window1024_sink4_s8192_d128():
+    w = make_workload("gqa4_window1024_sink4_s8192_d128")
+    plan, O_b, L_f = _run_dense(w)
+    for g in (0, 7):
+        _compare_dense(w, plan, O_b, L_f, kv_heads=slice(g, g + 1))
+
+
+def test_full_sparse_scfa_s4096_h64_d512():
+    w = make_workload("sparse_scfa_s4096_h64_d512")
+    plan, O_b, L_f = _run_sparse(w)
+    ref = H.sparse_reference(w, O_b, L_f)
+    H.check_close("dq", plan.dq.cpu().numpy()[0], ref["dq"])
+    H.check_close("d_ori", plan.d_ori.cpu().numpy(), ref["d_ori"])
+    H.check_close("d_cmp", plan.d_cmp.cpu().numpy(), ref["d_cmp"])
