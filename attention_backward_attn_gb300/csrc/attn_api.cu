@@ -246,6 +246,7 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
       return ATTN_ERR_INVALID_ARG;
   }
   const bool tc = use_tensor_cores(p);
+  if (tc && (!aligned16(lse) || !aligned16(delta))) return ATTN_ERR_INVALID_ARG;
   const WorkspaceLayout w = workspace_layout(p, tc);
   if (workspace == nullptr || workspace_bytes < w.total || !aligned16(workspace))
     return ATTN_ERR_WORKSPACE;

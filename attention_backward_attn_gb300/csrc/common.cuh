@@ -59,6 +59,30 @@ __host__ __device__ __forceinline__ void mask_col_range(const MaskSpec& m, int j
   *hi = b > n - 1 ? n - 1 : b;
 }
 
+// Tile classification over rows [m0, m1) x keys [n0, n1) for the same mask:
+// tile_any = at least one live entry, tile_full = every entry live.
+__host__ __device__ __forceinline__ bool tile_any(const MaskSpec& m, int m0, int m1, int n0,
+                                                  int n1) {
+  if (m0 >= m1 || n0 >= n1) return false;
+  if (n0 < m.sink) return true;
+  const int dmax = (n1 - 1) - m0;  // largest j - i in the tile
+  const int dmin = n0 - (m1 - 1);  // smallest j - i in the tile
+  if (m.wl >= 0 && dmax < -m.wl) return false;
+  if (m.wr >= 0 && dmin > m.wr) return false;
+  return true;
+}
+
+__host__ __device__ __forceinline__ bool tile_full(const MaskSpec& m, int m0, int m1, int n0,
+                                                   int n1) {
+  const int a = n0 > m.sink ? n0 : m.sink;  // first column not covered by the sinks
+  if (a >= n1) return true;
+  const int dmax = (n1 - 1) - m0;
+  const int dmin = a - (m1 - 1);
+  if (m.wl >= 0 && dmin < -m.wl) return false;
+  if (m.wr >= 0 && dmax > m.wr) return false;
+  return true;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -16,8 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def ab():
-    from attention_backward_attn_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import attention_backward_attn_gb300 as mod
     return mod
 

@@ -78,10 +78,42 @@ SMALL_DENSE = {
 }
 
 
+# cases whose shapes the tcgen05 kernel takes (D in {64, 128}, lengths multiples of 128)
+TC_CASES = {"gqa4_causal_s384_d128", "alibi_dbias_s256_d64", "window128_sink4_s640_d128"}
+
+
 @pytest.mark.parametrize("name", list(SMALL_DENSE))
 def test_dense_small(name):
     w = SMALL_DENSE[name]()
-    plan, O_b, L_f = _run_dense(w)
+    plan, O_b, L_f = _run_dense(w, expect_path=1 if name in TC_CASES else 2)
+    _compare_dense(w, plan, O_b, L_f)
+
+
+TC_EXTRA = {
+    # one tile, no mask: the plain five-GEMM pipeline
+    "mha_s128_d128": lambda: make_dense("a", 40, B=1, Hq=1, Hk=1, Sq=128, Sk=128, D=128),
+    "mha_s128_d64": lambda: make_dense("b", 41, B=1, Hq=1, Hk=1, Sq=128, Sk=128, D=64),
+    # Sq != Sk and GQA 8:1 (several query tiles per key tile, group sum on chip)
+    "gqa8_sq256_sk512_d128": lambda: make_dense("c", 42, B=2, Hq=8, Hk=1, Sq=256, Sk=512,
+                                                D=128),
+    # causal + 3 sinks + two-sided window at D = 64, with bias but no dbias
+    "window_sinks_bias_s512_d64": lambda: make_dense("d", 43, B=1, Hq=2, Hk=2, Sq=512, Sk=512,
+                                                     D=64, window_left=150, window_right=20,
+                                                     num_sink=3, alibi=True),
+    # dbias without bias (gradient of a zero bias), GQA 2:1
+    "dbias_only_gqa2_s256_d128": lambda: make_dense("e", 44, B=2, Hq=4, Hk=2, Sq=256, Sk=256,
+                                                    D=128, want_dbias=True),
+    # rows with no live key inside a partial tile, and a fully empty query tile
+    # (Sq > Sk, window of 11 keys: rows i >= 138 see nothing)
+    "empty_rows_sq384_sk128_d64": lambda: make_dense("f", 45, B=1, Hq=2, Hk=1, Sq=384, Sk=128,
+                                                     D=64, window_left=10, window_right=0),
+}
+
+
+@pytest.mark.parametrize("name", list(TC_EXTRA))
+def test_tensor_core_cases(name):
+    w = TC_EXTRA[name]()
+    plan, O_b, L_f = _run_dense(w, expect_path=1)
     _compare_dense(w, plan, O_b, L_f)
 
 
@@ -178,13 +210,13 @@ def test_sparse_bad_index_is_reported_not_trapped():
 
 def test_full_gqa4_causal_s1024_d128():
     w = make_workload("gqa4_causal_s1024_d128")
-    plan, O_b, L_f = _run_dense(w)
+    plan, O_b, L_f = _run_dense(w, expect_path=1)
     _compare_dense(w, plan, O_b, L_f)
 
 
 def test_full_mha_alibi_dbias_s2048_d64():
     w = make_workload("mha_alibi_dbias_s2048_d64")
-    plan, O_b, L_f = _run_dense(w)
+    plan, O_b, L_f = _run_dense(w, expect_path=1)
     for h in (0, 15):
         ref = H.dense_reference(w, O_b, L_f, kv_heads=slice(h, h + 1))
         H.check_close("dq", plan.dq.cpu().numpy()[:, :, h:h + 1], ref["dq"])
@@ -195,7 +227,7 @@ def test_full_mha_alibi_dbias_s2048_d64():
 
 def test_full_gqa4_window1024_sink4_s8192_d128():
     w = make_workload("gqa4_window1024_sink4_s8192_d128")
-    plan, O_b, L_f = _run_dense(w)
+    plan, O_b, L_f = _run_dense(w, expect_path=1)
     for g in (0, 7):
         _compare_dense(w, plan, O_b, L_f, kv_heads=slice(g, g + 1))
 
