@@ -101,7 +101,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
   WorkspaceLayout w;
-  size_t off = sizeof(DevStatus);
+  size_t off = kStatusBytes;
   if (tensor_core_path) {
     const size_t qbytes = (size_t)p.B * p.Hq * p.Sq * p.D * sizeof(__half);
     const size_t kbytes = (size_t)p.B * p.Hk * p.Sk * p.D * sizeof(__half);
@@ -211,12 +211,12 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
     return ATTN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   DevStatus* st = reinterpret_cast<DevStatus*>(ws + w.status);
-  __half* do16 = w.staged ? reinterpret_cast<__half*>(ws + w.do16) : nullptr;
-  cudaError_t e = launch_preprocess(p, o, dO, delta, dq, dbias, d_ori, d_cmp, do16, st, stream);
-  if (e != cudaSuccess || !tc) return cuda_status(e);
-  return cuda_status(launch_stage_qkv(p, q, k, v, reinterpret_cast<__half*>(ws + w.q16),
-                                      reinterpret_cast<__half*>(ws + w.k16),
-                                      reinterpret_cast<__half*>(ws + w.v16), st, stream));
+  auto staged = [&](size_t off) {
+    return w.staged ? reinterpret_cast<__half*>(ws + off) : nullptr;
+  };
+  return cuda_status(launch_preprocess(p, q, k, v, o, dO, delta, dq, dbias, d_ori, d_cmp,
+                                       staged(w.q16), staged(w.k16), staged(w.v16),
+                                       staged(w.do16), st, stream));
 }
 
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,

@@ -19,6 +19,12 @@ struct DevStatus {
 };
 static_assert(sizeof(DevStatus) == 256, "status record is 256 bytes");
 
+// Per-block flag slots of the pre-pass follow the status record: every block
+// of the pre-pass writes its slot on every call (so stale or uninitialised
+// workspace contents never leak into a report); the backward ORs them.
+constexpr int kPreMaxBlocks = 2048;
+constexpr size_t kStatusBytes = sizeof(DevStatus) + kPreMaxBlocks * sizeof(int32_t);
+
 __device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t detail) {
   if (st == nullptr) return;
   if (atomicCAS(&st->code, 0, code) == 0) {

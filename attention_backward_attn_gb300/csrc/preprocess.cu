@@ -1,18 +1,23 @@
-// Backward pre-pass and operand staging.
+// Backward pre-pass: one fused, HBM-streaming kernel.
 //
 // D = rowsum(dO * O) ("34_bwd_gqa_fmha.py" cpu_bwd_gqa; Ascend
 // "sparse_flash_mla_grad" phase 2, SoftmaxGrad(dO, O)), computed in fp32 from
-// the bf16 rows, one warp per (b, i, h) row. The same pass zeroes the row of
-// dq that the backward accumulates into and, for the tensor-core path, writes
-// dO once as an fp16 head-major copy. All of it is HBM-bound streaming.
+// the bf16 rows. The same pass zeroes the dq row that the backward accumulates
+// into, zeroes dbias / the sparse dKV buffers, clears the status record, and
+// for the tensor-core path writes fp16 head-major copies of q, k, v and dO.
 //
-// The tensor-core backward feeds fp16 operands to kind::f16 MMAs: the
-// probabilities P and the gradient dS are rounded to fp16 (11 significant
-// bits) instead of bf16 (8 bits), which keeps the rounding of the gradient
-// operands well inside the parity tolerance, and the other operand of each
-// of those MMAs must then be fp16 as well. bf16 -> fp16 is exact for every
-// bf16 value of magnitude in [2^-14, 65504]; larger magnitudes are reported as
-// ATTN_ERR_RANGE, smaller ones lose low bits (absolute error below 2^-25).
+// Why fp16 copies: the tensor-core backward feeds kind::f16 MMAs, and rounds
+// P and dS to fp16 (11 significant bits) instead of bf16 (8), which keeps the
+// rounding of the gradient operands well inside the parity tolerance; the
+// other operand of each of those MMAs must then be fp16 as well. bf16 -> fp16
+// is exact for every bf16 value of magnitude in [2^-14, 65504]; larger ones
+// set a range flag that attn_bwd turns into ATTN_ERR_RANGE, smaller ones lose
+// low bits (absolute error below 2^-25).
+//
+// Layout of the work: a row of D elements is split into 16-byte chunks of 8
+// values; LPR = min(D / 8, 32) lanes cover a row, so a warp streams
+// 32 / LPR rows at once with 16-byte loads and stores; a grid-stride loop
+// keeps every SM's memory pipe full.
 
 #include "internal.h"
 
@@ -20,168 +25,212 @@ namespace attn {
 namespace {
 
 using bf16 = __nv_bfloat16;
-constexpr int kWarps = 8;
+constexpr int kThreads = 256;
+
+struct PreParams {
+  int B, Hq, Hk, Sq, Sk;
+  int64_t o0, o1, o2, d0, d1, d2, q0, q1, q2, k0, k1, k2, v0, v1, v2;
+  const bf16* o;
+  const bf16* dO;
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  float* delta;
+  float* dq;
+  __half* q16;
+  __half* k16;
+  __half* v16;
+  __half* do16;  // nullptr: no staging (SIMT path)
+  float* zero_a;
+  int64_t zero_na;
+  float* zero_b;
+  int64_t zero_nb;
+  float* zero_c;
+  int64_t zero_nc;
+  DevStatus* st;
+};
+
+__device__ __forceinline__ void load8(const bf16* p, float* f) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 x = __bfloat1622float2(h[t]);
+    f[2 * t] = x.x;
+    f[2 * t + 1] = x.y;
+  }
+}
+
+// fp16 copy of 8 values; returns true if one of them overflowed to inf.
+__device__ __forceinline__ bool store8_half(__half* p, const float* f) {
+  uint4 raw;
+  __half2* h = reinterpret_cast<__half2*>(&raw);
+  bool bad = false;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    h[t] = __floats2half2_rn(f[2 * t], f[2 * t + 1]);
+    bad |= __hisinf(__low2half(h[t])) | __hisinf(__high2half(h[t]));
+  }
+  *reinterpret_cast<uint4*>(p) = raw;
+  return bad;
+}
 
 __device__ __forceinline__ void zero_range(float* a, int64_t n, int64_t tid, int64_t stride) {
-  // a is 16-byte aligned (checked on the host); float4 body, scalar tail.
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   float4* a4 = reinterpret_cast<float4*>(a);
   for (int64_t t = tid; t < n / 4; t += stride) a4[t] = z;
   for (int64_t t = (n / 4) * 4 + tid; t < n; t += stride) a[t] = 0.f;
 }
 
-__global__ void clear_kernel(DevStatus* st, float* a, int64_t na, float* b, int64_t nb,
-                             float* c, int64_t nc) {
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+preprocess_kernel(const PreParams p) {
+  constexpr int CH = D / 8;                 // 16-byte chunks per row
+  constexpr int LPR = CH < 32 ? CH : 32;    // lanes per row
+  constexpr int CPL = CH / LPR;             // chunks per lane
+  constexpr int RPW = 32 / LPR;             // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR;               // row slot within the warp
+  const int cl = lane % LPR;                // lane within the row
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  if (tid == 0 && st != nullptr) {
-    st->code = 0;
-    st->detail = 0;
-  }
-  zero_range(a, na, tid, stride);
-  zero_range(b, nb, tid, stride);
-  zero_range(c, nc, tid, stride);
-}
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
 
-template <int EPL>
-__device__ __forceinline__ bool store_half_checked(__half* dst, const float* x) {
-  bool bad = false;
-#pragma unroll
-  for (int e = 0; e < EPL; e += 2) {
-    __half2 h = __floats2half2_rn(x[e], x[e + 1]);
-    bad |= __hisinf(__low2half(h)) | __hisinf(__high2half(h));
-    *reinterpret_cast<__half2*>(dst + e) = h;
+  if (tid == 0) {
+    p.st->code = 0;
+    p.st->detail = 0;
+    p.st->reserved[1] = (int32_t)gridDim.x;  // number of flag slots written below
   }
-  return bad;
-}
+  int range_bits = 0;
 
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32)
-preprocess_kernel(int B, int Hq, int Sq, int64_t o0, int64_t o1, int64_t o2, int64_t d0,
-                  int64_t d1, int64_t d2, const bf16* __restrict__ o,
-                  const bf16* __restrict__ dO, float* __restrict__ delta,
-                  float* __restrict__ dq, __half* __restrict__ do16, DevStatus* st) {
-  constexpr int EPL = D / 32;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= (int64_t)B * Hq * Sq) return;
-  // Rows in memory order of dq ([B, Sq, Hq, D]) so the zeroing streams.
-  const int h = (int)(warp % Hq);
-  const int i = (int)((warp / Hq) % Sq);
-  const int b = (int)(warp / ((int64_t)Hq * Sq));
-  float ov[EPL], dv[EPL];
-  load_bf16<EPL>(o + b * o0 + i * o1 + h * o2 + lane * EPL, ov);
-  load_bf16<EPL>(dO + b * d0 + i * d1 + h * d2 + lane * EPL, dv);
-  float s = 0.f;
+  // ---- query-side rows (b, i, h) in memory order: delta, dq = 0, staging ----
+  const int64_t nq = (int64_t)p.B * p.Sq * p.Hq;
+  for (int64_t r0 = warp0 * RPW; r0 < nq; r0 += nwarps * RPW) {
+    const int64_t row = r0 + sub;
+    const bool valid = row < nq;
+    float s = 0.f;
+    if (valid) {
+      const int h = (int)(row % p.Hq);
+      const int i = (int)((row / p.Hq) % p.Sq);
+      const int b = (int)(row / ((int64_t)p.Hq * p.Sq));
+      const bf16* orow = p.o + b * p.o0 + i * p.o1 + h * p.o2;
+      const bf16* drow = p.dO + b * p.d0 + i * p.d1 + h * p.d2;
+      const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) s = fmaf(ov[e], dv[e], s);
-  s = warp_sum(s);
-  const int64_t r = ((int64_t)b * Hq + h) * Sq + i;
-  if (lane == 0) delta[r] = s;
-  float z[EPL];
+      for (int c = 0; c < CPL; ++c) {
+        const int e0 = (cl + c * LPR) * 8;
+        float of[8], df[8];
+        load8(orow + e0, of);
+        load8(drow + e0, df);
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) z[e] = 0.f;
-  store_f32<EPL>(dq + warp * D + lane * EPL, z);
-  if (do16 != nullptr) {
-    if (store_half_checked<EPL>(do16 + r * D + lane * EPL, dv)) report(st, ATTN_ERR_RANGE, 3);
-  }
-}
-
-// fp16 head-major copies of q (which = 0), k (1), v (2): warp per source row.
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32)
-stage_kernel(int B, int Hq, int Hk, int Sq, int Sk, int64_t q0, int64_t q1, int64_t q2, int64_t k0, int64_t k1, int64_t k2,
-             int64_t v0, int64_t v1, int64_t v2, const bf16* __restrict__ q,
-             const bf16* __restrict__ k, const bf16* __restrict__ v, __half* __restrict__ q16,
-             __half* __restrict__ k16, __half* __restrict__ v16, DevStatus* st) {
-  constexpr int EPL = D / 32;
-  int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t nq = (int64_t)B * Hq * Sq;
-  const int64_t nk = (int64_t)B * Hk * Sk;
-  const bf16* src;
-  __half* dst;
-  int which;
-  if (warp < nq) {
-    // destination order [B, Hq, Sq]
-    const int i = (int)(warp % Sq);
-    const int h = (int)((warp / Sq) % Hq);
-    const int b = (int)(warp / ((int64_t)Sq * Hq));
-    src = q + b * q0 + i * q1 + h * q2;
-    dst = q16 + warp * D;
-    which = 0;
-  } else {
-    warp -= nq;
-    which = 1;
-    if (warp >= nk) {
-      warp -= nk;
-      which = 2;
-      if (warp >= nk) return;
+        for (int t = 0; t < 8; ++t) s = fmaf(of[t], df[t], s);
+        float4* z = reinterpret_cast<float4*>(p.dq + row * D + e0);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.do16 != nullptr) {
+          float qf[8];
+          load8(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0, qf);
+          if (store8_half(p.do16 + hm * D + e0, df)) range_bits |= 8;
+          if (store8_half(p.q16 + hm * D + e0, qf)) range_bits |= 1;
+        }
+      }
     }
-    const int j = (int)(warp % Sk);
-    const int g = (int)((warp / Sk) % Hk);
-    const int b = (int)(warp / ((int64_t)Sk * Hk));
-    src = (which == 1) ? k + b * k0 + j * k1 + g * k2 : v + b * v0 + j * v1 + g * v2;
-    dst = ((which == 1) ? k16 : v16) + warp * D;
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (valid && cl == 0) {
+      const int h = (int)(row % p.Hq);
+      const int i = (int)((row / p.Hq) % p.Sq);
+      const int b = (int)(row / ((int64_t)p.Hq * p.Sq));
+      p.delta[((int64_t)b * p.Hq + h) * p.Sq + i] = s;
+    }
   }
-  float x[EPL];
-  load_bf16<EPL>(src + lane * EPL, x);
-  if (store_half_checked<EPL>(dst + lane * EPL, x)) report(st, ATTN_ERR_RANGE, which);
-}
 
-inline unsigned blocks_for(int64_t warps) { return (unsigned)((warps + kWarps - 1) / kWarps); }
+  // ---- key-side rows (k then v), staged head-major ----
+  if (p.do16 != nullptr) {
+    const int64_t nk = (int64_t)p.B * p.Sk * p.Hk;
+    for (int64_t r0 = warp0 * RPW; r0 < 2 * nk; r0 += nwarps * RPW) {
+      const int64_t rr = r0 + sub;
+      if (rr >= 2 * nk) continue;
+      const bool is_v = rr >= nk;
+      const int64_t row = is_v ? rr - nk : rr;
+      const int g = (int)(row % p.Hk);
+      const int j = (int)((row / p.Hk) % p.Sk);
+      const int b = (int)(row / ((int64_t)p.Hk * p.Sk));
+      const bf16* src = is_v ? p.v + b * p.v0 + j * p.v1 + g * p.v2
+                             : p.k + b * p.k0 + j * p.k1 + g * p.k2;
+      __half* dst = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk + j) * D;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int e0 = (cl + c * LPR) * 8;
+        float f[8];
+        load8(src + e0, f);
+        if (store8_half(dst + e0, f)) range_bits |= is_v ? 4 : 2;
+      }
+    }
+  }
+
+  // ---- buffers accumulated with atomics: dbias, sparse dKV ----
+  zero_range(p.zero_a, p.zero_na, tid, nthreads);
+  zero_range(p.zero_b, p.zero_nb, tid, nthreads);
+  zero_range(p.zero_c, p.zero_nc, tid, nthreads);
+
+  // Range overflow is handed to attn_bwd through this block's flag slot: a
+  // report straight into the status record could race with the reset above.
+  __shared__ int block_bits;
+  if (threadIdx.x == 0) block_bits = 0;
+  __syncthreads();
+  if (range_bits) atomicOr(&block_bits, range_bits);
+  __syncthreads();
+  if (threadIdx.x == 0) reinterpret_cast<int32_t*>(p.st + 1)[blockIdx.x] = block_bits;
+}
 
 }  // namespace
 
-cudaError_t launch_preprocess(const Problem& p, const void* o, const void* dO, float* delta,
-                              float* dq, float* dbias, float* d_ori, float* d_cmp,
-                              __half* do16, DevStatus* st, cudaStream_t stream) {
-  // 1) status record + buffers accumulated with atomics
-  const int64_t nbias = dbias ? (int64_t)p.Hq * p.Sq * p.Sk : 0;
-  const int64_t nori = d_ori ? (int64_t)p.n_ori * p.Hk * p.D : 0;
-  const int64_t ncmp = d_cmp ? (int64_t)p.n_cmp * p.Hk * p.D : 0;
-  const int64_t work = (nbias + nori + ncmp) / 4;
-  int64_t g = (work + 255) / 256;
-  g = g < 1 ? 1 : (g > 152 * 16 ? 152 * 16 : g);
-  clear_kernel<<<(unsigned)g, 256, 0, stream>>>(st, dbias, nbias, d_ori, nori, d_cmp, ncmp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // 2) delta, dq zeroing, dO staging
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq;
-  if (rows == 0) return cudaSuccess;
-  const bf16* ob = static_cast<const bf16*>(o);
-  const bf16* db = static_cast<const bf16*>(dO);
-#define ATTN_PRE(DD)                                                                        \
-  preprocess_kernel<DD><<<blocks_for(rows), kWarps * 32, 0, stream>>>(                      \
-      p.B, p.Hq, p.Sq, p.os[0], p.os[1], p.os[2], p.dos[0], p.dos[1], p.dos[2], ob, db, delta, \
-      dq, do16, st)
-  switch (p.D) {
-    case 64: ATTN_PRE(64); break;
-    case 128: ATTN_PRE(128); break;
-    case 512: ATTN_PRE(512); break;
+cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, const void* v,
+                              const void* o, const void* dO, float* delta, float* dq,
+                              float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
+                              __half* v16, __half* do16, DevStatus* st, cudaStream_t stream) {
+  PreParams p;
+  p.B = pr.B;
+  p.Hq = pr.Hq;
+  p.Hk = pr.Hk;
+  p.Sq = pr.Sq;
+  p.Sk = pr.Sk;
+  p.o0 = pr.os[0]; p.o1 = pr.os[1]; p.o2 = pr.os[2];
+  p.d0 = pr.dos[0]; p.d1 = pr.dos[1]; p.d2 = pr.dos[2];
+  p.q0 = pr.qs[0]; p.q1 = pr.qs[1]; p.q2 = pr.qs[2];
+  p.k0 = pr.ks[0]; p.k1 = pr.ks[1]; p.k2 = pr.ks[2];
+  p.v0 = pr.vs[0]; p.v1 = pr.vs[1]; p.v2 = pr.vs[2];
+  p.o = static_cast<const bf16*>(o);
+  p.dO = static_cast<const bf16*>(dO);
+  p.q = static_cast<const bf16*>(q);
+  p.k = static_cast<const bf16*>(k);
+  p.v = static_cast<const bf16*>(v);
+  p.delta = delta;
+  p.dq = dq;
+  p.q16 = q16;
+  p.k16 = k16;
+  p.v16 = v16;
+  p.do16 = do16;
+  p.zero_a = dbias;
+  p.zero_na = dbias ? (int64_t)pr.Hq * pr.Sq * pr.Sk : 0;
+  p.zero_b = d_ori;
+  p.zero_nb = d_ori ? (int64_t)pr.n_ori * pr.Hk * pr.D : 0;
+  p.zero_c = d_cmp;
+  p.zero_nc = d_cmp ? (int64_t)pr.n_cmp * pr.Hk * pr.D : 0;
+  p.st = st;
+  // Enough resident warps to keep HBM busy; the loops stride over the rest.
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned grid = (unsigned)(sms * 8 < kPreMaxBlocks ? sms * 8 : kPreMaxBlocks);
+  switch (pr.D) {
+    case 64: preprocess_kernel<64><<<grid, kThreads, 0, stream>>>(p); break;
+    case 128: preprocess_kernel<128><<<grid, kThreads, 0, stream>>>(p); break;
+    case 512: preprocess_kernel<512><<<grid, kThreads, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
-#undef ATTN_PRE
-  return cudaGetLastError();
-}
-
-cudaError_t launch_stage_qkv(const Problem& p, const void* q, const void* k, const void* v,
-                             __half* q16, __half* k16, __half* v16, DevStatus* st,
-                             cudaStream_t stream) {
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Sq + 2 * (int64_t)p.B * p.Hk * p.Sk;
-  if (rows == 0) return cudaSuccess;
-#define ATTN_STAGE(DD)                                                                      \
-  stage_kernel<DD><<<blocks_for(rows), kWarps * 32, 0, stream>>>(                           \
-      p.B, p.Hq, p.Hk, p.Sq, p.Sk, p.qs[0], p.qs[1], p.qs[2], p.ks[0], p.ks[1],     \
-      p.ks[2], p.vs[0], p.vs[1], p.vs[2], static_cast<const bf16*>(q),                      \
-      static_cast<const bf16*>(k), static_cast<const bf16*>(v), q16, k16, v16, st)
-  switch (p.D) {
-    case 64: ATTN_STAGE(64); break;
-    case 128: ATTN_STAGE(128); break;
-    case 512: ATTN_STAGE(512); break;
-    default: return cudaErrorInvalidValue;
-  }
-#undef ATTN_STAGE
   return cudaGetLastError();
 }
 

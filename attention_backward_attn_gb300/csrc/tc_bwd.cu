@@ -7,35 +7,39 @@
 //   dV = P^T dO, dK / dV summed over the query heads of a KV head,
 //   dbias = sum over the batch of dS.
 //
-// Tiling: one CTA owns a 128-row key tile of one (batch, KV head) and loops
-// over every query head of the group and every 128-row query tile that has a
-// live entry (fully masked tiles are skipped, partial ones get the per-element
-// mask). Per tile pair, in a key-major ("transposed") formulation so that the
-// softmax warps own one key row each:
-//   MMA1  S^T  = K  Q^T      (M = 128 keys,    N = 128 queries, K = D)
-//   MMA2  dP^T = V  dO^T     (M = 128 keys,    N = 128 queries, K = D)
-//   SFU   P^T = exp2(S^T * scale*log2e + bias*log2e - LSE*log2e),
-//         dS^T = P^T (dP^T - D)           -> P^T fp16 into TMEM, dS^T fp16 into SMEM
-//   MMA3  dV  += P^T  dO     (A = P^T from TMEM, B = dO  MN-major)
-//   MMA4  dK  += dS^T Q      (A = dS^T K-major,  B = Q   MN-major)
-//   MMA5  dQ_t = dS   K      (A = dS^T read MN-major, B = K MN-major)
-// dK / dV stay in TMEM for the whole group (the GQA reduction happens on
-// chip); dQ_t is drained by a second warpgroup with fp32 vector atomics.
+// Work decomposition: a thread-block cluster of `cs` CTAs owns one 128-row
+// key tile of one (batch, KV head); CTA `rank` of the cluster takes r / cs of
+// the r query heads that share the KV head, and loops over every 128-row query
+// tile with a live entry (fully masked tiles are skipped, partial tiles get a
+// per-element mask). At the end the cs partial dK / dV tiles are summed
+// through distributed shared memory, so the GQA group reduction never leaves
+// the chip. Per (query head, query tile), key-major so that one thread owns
+// one key row of the softmax:
+//   MMA1  S^T  = K  Q^T                      (M = 128 keys, N = 128 queries, K = D)
+//   MMA2  dP^T = V  dO^T                     (M = 128 keys, N = 128 queries, K = D)
+//   SFU   P^T = exp2(S^T scale log2e + bias log2e - LSE log2e), dS^T = P^T (dP^T - D)
+//         -> P^T fp16 back into TMEM (A operand of MMA3), dS^T fp16 into SMEM
+//   MMA5  D = 128: dQ^T = K^T dS^T  (M = d, N = queries; coalesced atomics)
+//         D =  64: dQ   = dS  K     (M = queries, N = d)
+//   MMA3  dV += P^T dO     (A = P^T in TMEM, B = dO MN-major)
+//   MMA4  dK += dS^T Q     (A = dS^T K-major, B = Q MN-major)
+// MMA5 is issued first so that draining dQ overlaps MMA3 / MMA4 and the next
+// tile's MMA1.
 //
 // TMEM (512 columns x 128 lanes x 32 bit): [0, D) dK, [D, 2D) dV,
-// [2D, 2D+128) S^T (P^T fp16 packed into its first 64 columns),
-// [2D+128, 2D+256) dP^T, reused for dQ_t once dS^T exists.
+// [2D, 2D+128) S^T (P^T fp16 pairs of queries 0-63 in its columns 0-31,
+// queries 64-127 in columns 64-95), [2D+128, 2D+256) dP^T, then dQ.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
-// owner), warps 4-7 softmax / dS, warps 8-11 dQ drain; warps 4-7 also write
-// dK / dV at the end. Every mbarrier wait is bounded: after ~2 s a wait
-// records ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, and the CTA
-// drains its in-flight copies / MMAs, frees TMEM and exits.
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 4-7 and 8-11 two softmax warpgroups (queries 0-63 / 64-127 of
+// the tile), which also drain dQ and, at the end, write dK (first group) and
+// dV (second group). Every mbarrier wait is bounded: after ~2 s it records
+// ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, and the CTA drains
+// its copies / MMAs, frees TMEM and exits through the same cluster barriers.
 //
 // Operands are fp16 (exact copies of the bf16 inputs, staged by the
-// pre-pass): with fp16 P and dS the rounding of the gradient GEMM operands
-// has 3 more mantissa bits than bf16, and kind::f16 needs A and B of the same
-// type.
+// pre-pass): P and dS rounded to fp16 keep 3 more mantissa bits than bf16,
+// and kind::f16 needs A and B of the same type.
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -64,13 +68,20 @@ struct Smem {
   static constexpr int BAR = DLT + 1024;     // mbarriers
   static constexpr int MISC = BAR + 128;     // TMEM base, abort flag
   static constexpr int TOTAL = MISC + 16;
+  // end-of-kernel staging of dK / dV for the cluster reduction (reuses Q..dS)
+  static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
+  static constexpr int STAGE = Q;
+  static_assert(2 * 128 * kStageRow <= 4 * kTile + 2 * kSlab, "staging fits");
 };
 
-enum Bar { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kPFull = 6, kDqFull = 7,
-           kDqEmpty = 8, kAccFull = 9, kNumBars = 10 };
+enum Bar {
+  kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kPFull = 6, kDqFull = 7, kDqEmpty = 8,
+  kAccFull = 9, kMma3 = 10, kNumBars = 11
+};
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
+  int cs;  // CTAs per cluster (query-head split)
   float scale;
   float scale_log2;
   MaskSpec mask;
@@ -85,8 +96,8 @@ struct TcParams {
 };
 
 struct Ctx {
-  uint32_t bars;       // shared address of barrier 0
-  volatile int* abort; // CTA-wide abort flag
+  uint32_t bars;        // shared address of barrier 0
+  volatile int* abort;  // CTA-wide abort flag
   DevStatus* status;
   __device__ uint32_t bar(int i) const { return bars + 8u * i; }
 };
@@ -129,14 +140,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 // Iterates the live (query head, query tile) pairs of this CTA's key tile.
 struct TileIter {
-  int r, nmt, n0, hl, mt;
+  int hpc, nmt, n0, hl, mt;
   MaskSpec mask;
-  __device__ TileIter(int r_, int nmt_, int n0_, MaskSpec m) : r(r_), nmt(nmt_), n0(n0_), hl(0), mt(-1), mask(m) {}
+  __device__ TileIter(int hpc_, int nmt_, int n0_, MaskSpec m)
+      : hpc(hpc_), nmt(nmt_), n0(n0_), hl(0), mt(-1), mask(m) {}
   __device__ bool next() {
     for (;;) {
       if (++mt >= nmt) {
         mt = 0;
-        if (++hl >= r) return false;
+        if (++hl >= hpc) return false;
       }
       if (tile_any(mask, mt * BM, mt * BM + BM, n0, n0 + BN)) return true;
     }
@@ -153,24 +165,40 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const uint32_t sbase = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (sbase & 1023u) {  // the 128B-swizzle atoms need 1 KiB alignment
+  // 1 KiB alignment of the 128B-swizzle atoms; uniform over the cluster (same
+  // kernel, same layout), so an early return cannot strand a cluster barrier.
+  if (sbase & 1023u) {
     if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 1);
     return;
   }
-  const int nnt = p.Sk / BN;
-  const int nt = blockIdx.x % nnt;
-  const int g = (blockIdx.x / nnt) % p.Hk;
-  const int b = blockIdx.x / (nnt * p.Hk);
+  const int cs = p.cs;
+  const int rank = (int)(blockIdx.x % cs);
+  const int ci = (int)(blockIdx.x / cs);
+  const int bg = ci % (p.B * p.Hk);  // (batch, KV head), key tile slowest
+  const int nt = ci / (p.B * p.Hk);
+  const int g = bg % p.Hk;
+  const int b = bg / p.Hk;
   const int n0 = nt * BN;
   const int r = p.Hq / p.Hk;
+  const int hpc = r / cs;
+  const int h_first = g * r + rank * hpc;
   const int nmt = p.Sq / BM;
 
   Ctx c;
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC);
 
+  if (blockIdx.x == 0) {
+    // fp16 overflow found while staging the operands: OR of the pre-pass's
+    // per-block flag slots
+    const int nslots = min(max(p.status->reserved[1], 0), kPreMaxBlocks);
+    const int32_t* slots = reinterpret_cast<const int32_t*>(p.status + 1);
+    int bits = 0;
+    for (int i = threadIdx.x; i < nslots; i += blockDim.x) bits |= slots[i];
+    bits = __reduce_or_sync(0xffffffffu, bits);
+    if (bits && lane == 0) report(p.status, ATTN_ERR_RANGE, bits);
+  }
   if (threadIdx.x == 0) {
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
@@ -182,10 +210,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     ptx::mbar_init(c.bar(kQEmpty0), 1);
     ptx::mbar_init(c.bar(kQEmpty0 + 1), 1);
     ptx::mbar_init(c.bar(kSFull), 1);
-    ptx::mbar_init(c.bar(kPFull), 128);
+    ptx::mbar_init(c.bar(kPFull), 256);
     ptx::mbar_init(c.bar(kDqFull), 1);
-    ptx::mbar_init(c.bar(kDqEmpty), 128);
+    ptx::mbar_init(c.bar(kDqEmpty), 256);
     ptx::mbar_init(c.bar(kAccFull), 1);
+    ptx::mbar_init(c.bar(kMma3), 1);
     *c.abort = 0;
     ptx::fence_mbar_init();
   }
@@ -196,13 +225,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
   const uint32_t t_S = tmem + 2 * D;
   const uint32_t t_dP = tmem + 2 * D + 128;
 
   const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::dS;
+  bool epi_ok = false;
   int n_iters = 0;
 
   if (warp == 0) {
@@ -215,16 +245,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         ptx::tma_load_2d(sK + hf * kSlab, &tmK, c.bar(kKvFull), hf * 64, krow);
         ptx::tma_load_2d(sV + hf * kSlab, &tmV, c.bar(kKvFull), hf * 64, krow);
       }
-      TileIter it(r, nmt, n0, p.mask);
+      TileIter it(hpc, nmt, n0, p.mask);
       int t = 0;
       int issued[2] = {0, 0};
       while (it.next()) {
         const int st = t & 1;
         const int use = t >> 1;
         if (use > 0 && !wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1)) break;
-        const int h = g * r + it.hl;
-        const int m0 = it.mt * BM;
-        const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + m0;
+        const int h = h_first + it.hl;
+        const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + it.mt * BM;
         const uint32_t full = c.bar(kQFull0 + st);
         ptx::mbar_arrive_expect_tx(full, 2 * L::kTile + 2 * 512);
 #pragma unroll
@@ -237,7 +266,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         issued[st] = use + 1;
         ++t;
       }
-      // make sure no copy is still landing in shared memory when the CTA ends
+      // no copy may still be landing in shared memory when the CTA ends
       drain_bar(c, kKvFull, 0);
       for (int st = 0; st < 2; ++st)
         if (issued[st] > 0) drain_bar(c, kQFull0 + st, (issued[st] - 1) & 1);
@@ -247,123 +276,163 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
-      constexpr uint32_t id_dKV = ptx::idesc_f16_f32(128, D, false, true);
-      constexpr uint32_t id_dQ = ptx::idesc_f16_f32(128, D, true, true);
-      bool ok = wait_bar(c, kKvFull, 0, 2);
-      TileIter it(r, nmt, n0, p.mask);
-      int t = 0;
-      while (ok && it.next()) {
-        const int st = t & 1;
+      constexpr uint32_t id_KV = ptx::idesc_f16_f32(128, D, false, true);
+      constexpr uint32_t id_Q = ptx::idesc_f16_f32(128, D == 128 ? 128 : D, true, true);
+      auto issue_S = [&](int st) {  // MMA1 S^T = K Q^T (both K-major over d)
         const uint32_t sQ = sbase + L::Q + st * L::kTile;
-        const uint32_t sdO = sbase + L::dO + st * L::kTile;
-        if (!wait_bar(c, kQFull0 + st, (t >> 1) & 1, 3)) break;
-        if (t > 0 && !wait_bar(c, kDqEmpty, (t - 1) & 1, 4)) break;
-        ptx::tc_fence_after();
-        // MMA1 S^T = K Q^T and MMA2 dP^T = V dO^T (both operands K-major over d)
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(t_S, ptx::smem_desc_sw128(sK + off, 16, 1024),
                       ptx::smem_desc_sw128(sQ + off, 16, 1024), id_S, s > 0);
         }
+      };
+      auto issue_dP = [&](int st) {  // MMA2 dP^T = V dO^T
+        const uint32_t sdO = sbase + L::dO + st * L::kTile;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(t_dP, ptx::smem_desc_sw128(sV + off, 16, 1024),
                       ptx::smem_desc_sw128(sdO + off, 16, 1024), id_S, s > 0);
         }
-        ptx::mma_commit(c.bar(kSFull));
-        if (!wait_bar(c, kPFull, t & 1, 5)) break;
+      };
+      bool ok = wait_bar(c, kKvFull, 0, 2);
+      TileIter it(hpc, nmt, n0, p.mask);
+      bool have = ok && it.next();
+      if (have) {
+        ok = wait_bar(c, kQFull0, 0, 3);
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_S(0);
+          issue_dP(0);
+          ptx::mma_commit(c.bar(kSFull));
+        }
+        have = ok;
+      }
+      int t = 0;
+      while (have) {
+        const int st = t & 1;
+        const uint32_t sQ = sbase + L::Q + st * L::kTile;
+        const uint32_t sdO = sbase + L::dO + st * L::kTile;
+        if (!wait_bar(c, kPFull, t & 1, 4)) break;
         ptx::tc_fence_after();
-        // MMA3 dV += P^T dO : A = P^T (TMEM, fp16 pairs), B = dO MN-major over d
+        // MMA5: dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64), into the dP columns
+#pragma unroll
+        for (int s = 0; s < BN / 16; ++s) {
+          const uint64_t dk_desc = ptx::smem_desc_sw128(sK + s * 2048, kSlab, 1024);
+          const uint64_t ds_desc = ptx::smem_desc_sw128(sDS + s * 2048, kSlab, 1024);
+          if constexpr (D == 128)
+            ptx::mma_ss(t_dP, dk_desc, ds_desc, id_Q, s > 0);
+          else
+            ptx::mma_ss(t_dP, ds_desc, dk_desc, id_Q, s > 0);
+        }
+        ptx::mma_commit(c.bar(kDqFull));
+        // MMA3 dV += P^T dO : A = P^T (TMEM fp16 pairs), B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
-          ptx::mma_ts(t_dV, t_S + s * 8, ptx::smem_desc_sw128(sdO + s * 2048, kSlab, 1024),
-                      id_dKV, (t > 0 || s > 0) ? 1u : 0u);
+          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_dV, a_col, ptx::smem_desc_sw128(sdO + s * 2048, kSlab, 1024), id_KV,
+                      (t > 0 || s > 0) ? 1u : 0u);
         }
+        ptx::mma_commit(c.bar(kMma3));
         // MMA4 dK += dS^T Q : A = dS^T K-major over queries, B = Q MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(t_dK, ptx::smem_desc_sw128(sDS + off, 16, 1024),
-                      ptx::smem_desc_sw128(sQ + s * 2048, kSlab, 1024), id_dKV,
+                      ptx::smem_desc_sw128(sQ + s * 2048, kSlab, 1024), id_KV,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
-        // MMA5 dQ_t = dS K : A = dS^T read MN-major over queries, B = K MN-major over d
-#pragma unroll
-        for (int s = 0; s < BN / 16; ++s) {
-          ptx::mma_ss(t_dP, ptx::smem_desc_sw128(sDS + s * 2048, kSlab, 1024),
-                      ptx::smem_desc_sw128(sK + s * 2048, kSlab, 1024), id_dQ, s > 0);
-        }
-        ptx::mma_commit(c.bar(kDqFull));
         ptx::mma_commit(c.bar(kQEmpty0 + st));
+        have = it.next();
+        if (have) {
+          const int st1 = (t + 1) & 1;
+          // next tile: S^T once its operands landed and MMA3 released the S columns,
+          // dP^T once the drain released the dP columns
+          if (!wait_bar(c, kQFull0 + st1, ((t + 1) >> 1) & 1, 5) || !wait_bar(c, kMma3, t & 1, 6))
+            break;
+          ptx::tc_fence_after();
+          issue_S(st1);
+          if (!wait_bar(c, kDqEmpty, t & 1, 7)) break;
+          ptx::tc_fence_after();
+          issue_dP(st1);
+          ptx::mma_commit(c.bar(kSFull));
+        }
         ++t;
       }
       ptx::mma_commit(c.bar(kAccFull));
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------- softmax / dS warpgroup --
-    const int tw = threadIdx.x - 128;          // key row within the tile == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int j = n0 + tw;
-    TileIter it(r, nmt, n0, p.mask);
+  } else if (warp >= 4) {
+    // ------------------------------------- softmax / dS / dQ warpgroups --
+    const int wg = (warp - 4) >> 2;                  // 0: queries 0-63, 1: 64-127
+    const int lg = warp & 3;                         // TMEM lane quarter
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int jl = lg * 32 + lane;                   // key row within the tile
+    const int j = n0 + jl;
+    TileIter it(hpc, nmt, n0, p.mask);
     int t = 0;
     bool ok = true;
     while (it.next()) {
       const int st = t & 1;
-      if (!wait_bar(c, kQFull0 + st, (t >> 1) & 1, 6)) { ok = false; break; }
-      // A row without live keys has LSE = -inf; it can only sit in a partial
-      // tile, where the per-element mask below zeroes its probabilities.
+      if (!wait_bar(c, kQFull0 + st, (t >> 1) & 1, 8)) { ok = false; break; }
       const float* lse_s = reinterpret_cast<const float*>(smem + L::LSE + st * 512);
       const float* dl_s = reinterpret_cast<const float*>(smem + L::DLT + st * 512);
-      if (!wait_bar(c, kSFull, t & 1, 7)) { ok = false; break; }
+      if (!wait_bar(c, kSFull, t & 1, 9)) { ok = false; break; }
       ptx::tc_fence_after();
-      const int h = g * r + it.hl;
+      const int h = h_first + it.hl;
       const int m0 = it.mt * BM;
+      // A row without live keys has LSE = -inf; it can only sit in a partial
+      // tile, where the per-element mask zeroes its probabilities.
       const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
       const float* brow = nullptr;
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       float* dbrow = nullptr;
       if constexpr (DBIAS) dbrow = p.dbias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
-      const uint32_t ds_row = sDS + tw * 128;
+      const uint32_t ds_row = sDS + wg * kSlab + jl * 128;
 #pragma unroll 1
-      for (int cc = 0; cc < BM / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
         uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(t_S + lane_off + cc * 32, sr);
-        ptx::tmem_ld32(t_dP + lane_off + cc * 32, dr);
+        ptx::tmem_ld32(t_S + lane_off + q0, sr);
+        ptx::tmem_ld32(t_dP + lane_off + q0, dr);
         float bv[32];
         if constexpr (BIAS) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) bv[e] = __ldg(brow + (int64_t)(cc * 32 + e) * p.Sk);
+          for (int e = 0; e < 32; ++e) bv[e] = __ldg(brow + (int64_t)(q0 + e) * p.Sk);
         }
         ptx::tmem_wait_ld();
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pe[2], de[2];
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + e4);
+          const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pe[4], de[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int il = cc * 32 + e + u;
-            float x = fmaf(__uint_as_float(sr[e + u]), p.scale_log2, lse_s[il] * -kLog2e);
-            if constexpr (BIAS) x = fmaf(bv[e + u], kLog2e, x);
+          for (int u = 0; u < 4; ++u) {
+            const int e = e4 + u;
+            float x = fmaf(__uint_as_float(sr[e]), p.scale_log2, lv[u] * -kLog2e);
+            if constexpr (BIAS) x = fmaf(bv[e], kLog2e, x);
             float pv = ptx::ex2(x);
-            if (partial && !mask_live(p.mask, m0 + il, j)) pv = 0.f;
+            if (partial && !mask_live(p.mask, m0 + q0 + e, j)) pv = 0.f;
             pe[u] = pv;
-            de[u] = pv * (__uint_as_float(dr[e + u]) - dl_s[il]);
-            if constexpr (DBIAS) atomicAdd(dbrow + (int64_t)il * p.Sk, de[u]);
+            de[u] = pv * (__uint_as_float(dr[e]) - dv[u]);
+            if constexpr (DBIAS) atomicAdd(dbrow + (int64_t)(q0 + e) * p.Sk, de[u]);
           }
-          pk[e / 2] = pack_half2(pe[0], pe[1]);
-          dk[e / 2] = pack_half2(de[0], de[1]);
+          pk[e4 / 2] = pack_half2(pe[0], pe[1]);
+          pk[e4 / 2 + 1] = pack_half2(pe[2], pe[3]);
+          dk[e4 / 2] = pack_half2(de[0], de[1]);
+          dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
         }
-        // P^T fp16 into the (already read) front of the S^T columns
-        ptx::tmem_st16(t_S + lane_off + cc * 16, pk);
+        // P^T fp16 pairs over the (already read) front half of this group's S^T columns
+        ptx::tmem_st16(t_S + lane_off + wg * 64 + cc * 16, pk);
         // dS^T fp16 into shared memory, 128B-swizzled K-major rows (one key row per thread)
-        const uint32_t slab = ds_row + (cc >> 1) * kSlab;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = (uint32_t)((cc & 1) * 4 + q4) ^ (uint32_t)(tw & 7);
-          ptx::st_shared_v4(slab + chunk * 16, dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2],
+          const uint32_t chunk = (uint32_t)(cc * 4 + q4) ^ (uint32_t)(jl & 7);
+          ptx::st_shared_v4(ds_row + chunk * 16, dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2],
                             dk[4 * q4 + 3]);
         }
       }
@@ -371,65 +440,109 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::fence_async_shared();
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(kPFull));
-      ++t;
-    }
-    n_iters = t;
-    // ------------------------------------------------ dK / dV epilogue --
-    if (ok && wait_bar(c, kAccFull, 0, 8)) {
+      // ---- drain dQ of this tile (scale applied here) ----
+      if (!wait_bar(c, kDqFull, t & 1, 10)) { ok = false; break; }
       ptx::tc_fence_after();
-      float* dkrow = p.dk + (((int64_t)b * p.Sk + j) * p.Hk + g) * D;
-      float* dvrow = p.dv + (((int64_t)b * p.Sk + j) * p.Hk + g) * D;
+      if constexpr (D == 128) {
+        // dQ^T: TMEM lane = d, column = query; a warp writes 32 consecutive d
+        const int d = jl;
+        float* base = p.dq + (((int64_t)b * p.Sq + m0) * p.Hq + h) * D + d;
+        const int64_t qstride = (int64_t)p.Hq * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t kr[32], vr[32];
-        if (n_iters > 0) {
-          ptx::tmem_ld32(t_dK + lane_off + cc * 32, kr);
-          ptx::tmem_ld32(t_dV + lane_off + cc * 32, vr);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int q0 = wg * 64 + cc * 32;
+          uint32_t v[32];
+          ptx::tmem_ld32(t_dP + lane_off + q0, v);
           ptx::tmem_wait_ld();
-        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) kr[e] = vr[e] = 0u;
+          for (int e = 0; e < 32; ++e)
+            ptx::red_add_f32(base + (int64_t)(q0 + e) * qstride, __uint_as_float(v[e]) * p.scale);
         }
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          *reinterpret_cast<float4*>(dkrow + cc * 32 + e) =
-              make_float4(__uint_as_float(kr[e]) * p.scale, __uint_as_float(kr[e + 1]) * p.scale,
-                          __uint_as_float(kr[e + 2]) * p.scale, __uint_as_float(kr[e + 3]) * p.scale);
-          *reinterpret_cast<float4*>(dvrow + cc * 32 + e) =
-              make_float4(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]),
-                          __uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
-        }
-      }
-    }
-  } else if (warp >= 8) {
-    // ---------------------------------------------------- dQ drain group --
-    const int tq = threadIdx.x - 256;  // query row within the tile == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
-    TileIter it(r, nmt, n0, p.mask);
-    int t = 0;
-    while (it.next()) {
-      if (!wait_bar(c, kDqFull, t & 1, 9)) break;
-      ptx::tc_fence_after();
-      const int h = g * r + it.hl;
-      const int i = it.mt * BM + tq;
-      float* dst = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      } else {
+        // dQ: TMEM lane = query, column = d; this group takes d in [32 wg, 32 wg + 32)
+        float* dst = p.dq + (((int64_t)b * p.Sq + m0 + jl) * p.Hq + h) * D + wg * 32;
         uint32_t v[32];
-        ptx::tmem_ld32(t_dP + lane_off + cc * 32, v);
+        ptx::tmem_ld32(t_dP + lane_off + wg * 32, v);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          atomicAdd(reinterpret_cast<float4*>(dst + cc * 32 + e),
+        for (int e = 0; e < 32; e += 4)
+          atomicAdd(reinterpret_cast<float4*>(dst + e),
                     make_float4(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
                                 __uint_as_float(v[e + 2]) * p.scale,
                                 __uint_as_float(v[e + 3]) * p.scale));
-        }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(kDqEmpty));
       ++t;
     }
+    n_iters = t;
+    epi_ok = ok && wait_bar(c, kAccFull, 0, 11);
+  }
+
+  // ------------------------------------------------- dK / dV epilogue --
+  // Warpgroup 0 owns dK (scaled), warpgroup 1 dV; thread = key row.
+  ptx::tc_fence_before();
+  __syncthreads();
+  const bool epi_thread = warp >= 4;
+  const int ewg = (warp - 4) >> 2;
+  const int ejl = (warp & 3) * 32 + lane;
+  if (epi_thread) {
+    ptx::tc_fence_after();
+    const uint32_t t_acc = ewg == 0 ? t_dK : t_dV;
+    const float mul = ewg == 0 ? p.scale : 1.f;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float* grow = (ewg == 0 ? p.dk : p.dv) + (((int64_t)b * p.Sk + n0 + ejl) * p.Hk + g) * D;
+    const uint32_t srow = sbase + L::STAGE + (ewg * 128 + ejl) * L::kStageRow;
+    if (epi_ok) {
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t v[32];
+        if (n_iters > 0) {
+          ptx::tmem_ld32(t_acc + lane_off + cc * 32, v);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float a0 = __uint_as_float(v[e]) * mul, a1 = __uint_as_float(v[e + 1]) * mul;
+          const float a2 = __uint_as_float(v[e + 2]) * mul, a3 = __uint_as_float(v[e + 3]) * mul;
+          if (cs == 1)
+            *reinterpret_cast<float4*>(grow + cc * 32 + e) = make_float4(a0, a1, a2, a3);
+          else
+            ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
+        }
+      }
+    }
+  }
+  if (cs > 1) {
+    // Sum the cs partial tiles through distributed shared memory: CTA `rank`
+    // finalises rows [rank R, rank R + R) of both dK and dV (R = 128 / cs).
+    ptx::cluster_sync();
+    if (epi_thread && !*c.abort) {
+      const int R = BN / cs;
+      const int per_mat = R * (D / 4);
+      const int tid = threadIdx.x - 128;
+      for (int item = tid; item < 2 * per_mat; item += 256) {
+        const int mat = item / per_mat;
+        const int rem = item % per_mat;
+        const int row = rank * R + rem / (D / 4);
+        const int d4 = rem % (D / 4);
+        const uint32_t local = sbase + L::STAGE + (mat * 128 + row) * L::kStageRow + d4 * 16;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int rk = 0; rk < cs; ++rk) {
+          const float4 v = ptx::ld_cluster_v4(ptx::mapa(local, (uint32_t)rk));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        float* dst = (mat == 0 ? p.dk : p.dv) + (((int64_t)b * p.Sk + n0 + row) * p.Hk + g) * D;
+        *reinterpret_cast<float4*>(dst + d4 * 4) = acc;
+      }
+    }
+    ptx::cluster_sync();  // keep every CTA's staging alive until all reads finished
   }
 
   // ----------------------------------------------------------- teardown --
@@ -489,8 +602,19 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, Smem<D>::TOTAL, stream>>>(q, k, v, dO, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<D>::TOTAL;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, dO, p);
 }
 
 template <int D>
@@ -500,6 +624,14 @@ cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
   if (p.bias) return launch_variant<D, true, false>(q, k, v, dO, p, grid, stream);
   if (p.dbias) return launch_variant<D, false, true>(q, k, v, dO, p, grid, stream);
   return launch_variant<D, false, false>(q, k, v, dO, p, grid, stream);
+}
+
+// Query heads per KV head are split over a cluster of cs CTAs: the largest
+// divisor of the group size that is at most 8 (the portable cluster size).
+int cluster_size(int ratio) {
+  for (int c = 8; c > 1; --c)
+    if (ratio % c == 0) return c;
+  return 1;
 }
 
 }  // namespace
@@ -525,6 +657,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Hk = pr.Hk;
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
+  p.cs = cluster_size(pr.Hq / pr.Hk);
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.mask = pr.mask;
@@ -536,7 +669,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dv = dv;
   p.dbias = dbias;
   p.status = st;
-  const int grid = pr.B * pr.Hk * (pr.Sk / BN);
+  const int grid = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
   if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
   return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);
 }

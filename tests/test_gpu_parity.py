@@ -206,6 +206,29 @@ def test_sparse_bad_index_is_reported_not_trapped():
     assert code == 5 and detail == 200
 
 
+def test_fp16_range_overflow_is_reported():
+    # The tensor-core path works on exact fp16 copies of the bf16 inputs; a
+    # value beyond the fp16 range must surface as ATTN_ERR_RANGE, not as a trap.
+    torch = _torch()
+    w = TC_EXTRA["mha_s128_d64"]()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    w.k = w.k.copy()
+    w.k[0, 5, 0, 3] = 1.0e5  # representable in bf16, not in fp16
+    plan = H.gpu_dense_plan(w, O_b, L_f)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 6 and detail & 2  # ATTN_ERR_RANGE, flag of k
+    # the next clean call clears the condition
+    w2 = TC_EXTRA["mha_s128_d64"]()
+    plan2 = H.gpu_dense_plan(w2, O_b, L_f)
+    plan2.workspace = plan.workspace
+    plan2.run()
+    torch.cuda.synchronize()
+    assert plan2.device_status()[0] == 0
+
+
 # ------------------------------------------------------------- full size ----
 
 def test_full_gqa4_causal_s1024_d128():
