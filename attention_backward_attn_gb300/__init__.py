@@ -19,7 +19,7 @@ __all__ = [
     "AttnError", "Problem", "Mask", "Sparse", "lib", "status_string",
     "problem_from", "mask_from", "sparse_from",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
-    "attn_read_device_status", "attn_bwd_path", "BackwardPlan",
+    "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
 ]
 
 ATTN_OK = 0
@@ -86,6 +86,9 @@ def _load():
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_bwd_path.argtypes = [P(Problem), P(Mask), P(Sparse)]
     L.attn_bwd_path.restype = ctypes.c_int32
+    L.attn_bwd_noalloc.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp,
+                                   vp, vp, vp, vp, vp, vp, P(ctypes.c_int32)]
+    L.attn_bwd_noalloc.restype = st
     return L
 
 
@@ -196,6 +199,23 @@ def attn_bwd(prob, mask, sparse, q, k, v, do, lse, delta, bias, dq, dk, dv, dbia
                         _ptr(dv), _ptr(dbias), _ptr(workspace), workspace_bytes,
                         _stream(stream)),
            "attn_bwd")
+
+
+def attn_bwd_noalloc(prob, mask, sparse, q, k, v, o, do, lse, bias, delta, dq, dk, dv, dbias,
+                     stream=None, read_status=False):
+    """Pre-pass + backward with the library's fixed device workspace (no allocation).
+
+    For callers that cannot allocate device memory; see include/attn_bwd.h.
+    With read_status=True the call synchronises the stream and returns the
+    device status (code, detail); otherwise it returns None.
+    """
+    status = (ctypes.c_int32 * 2)() if read_status else None
+    _check(lib.attn_bwd_noalloc(ctypes.byref(prob), _ref(mask), _ref(sparse), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(bias), _ptr(delta),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _stream(stream),
+                                status),
+           "attn_bwd_noalloc")
+    return (int(status[0]), int(status[1])) if read_status else None
 
 
 def attn_read_device_status(workspace, stream=None):

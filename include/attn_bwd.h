@@ -173,6 +173,37 @@ attn_status_t attn_read_device_status(const void* workspace, cudaStream_t stream
 /* Static, human-readable name of a status code. */
 const char* attn_status_string(attn_status_t status);
 
+/* Backward without any device allocation by the caller or the library.
+ * The source pages have no counterpart of this entry point: it exists for
+ * callers that cannot call cudaMalloc -- code running inside a framework hook
+ * that must not re-enter the framework's allocator, deployments whose device
+ * memory is fixed at start-up, or paths that must not stall other streams
+ * (cudaMalloc can synchronise the device).
+ *
+ * It runs attn_bwd_preprocess and attn_bwd (same arguments and results as
+ * those two calls) with their workspace placed in a fixed 32 MiB array that
+ * the library keeps in the device memory of every GPU it is used on, for as
+ * long as the library is loaded. Inputs and outputs stay caller-owned device
+ * memory; delta is an output here (the pre-pass's rowsum(dO * O)).
+ * - Returns ATTN_ERR_WORKSPACE, before enqueuing anything, when the problem
+ *   needs more than 32 MiB of workspace (attn_bwd_workspace_size).
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the array and it keeps the last call's contents (the
+ *   pre-pass rewrites everything the backward reads). Calls whose work
+ *   overlaps on the GPU race on it: order them on one stream or synchronise.
+ * - device_status may be NULL. Otherwise the call synchronises `stream` and
+ *   stores the device-side status code in device_status[0] and its detail in
+ *   device_status[1] (as attn_read_device_status would). */
+attn_status_t attn_bwd_noalloc(const attn_problem_t* prob, const attn_mask_t* mask,
+                               const attn_sparse_t* sparse,
+                               const void* q, const void* k, const void* v,
+                               const void* o, const void* dO, const float* lse,
+                               const float* bias, float* delta,
+                               float* dq, float* dk, float* dv, float* dbias,
+                               cudaStream_t stream, int32_t* device_status);
+
 /* Which backward kernel attn_bwd would launch for these arguments:
  * 0 = none (invalid / unsupported), 1 = tcgen05 tensor-core kernel,
  * 2 = SIMT kernels. For tests and benchmarks. */
