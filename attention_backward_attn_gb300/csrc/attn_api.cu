@@ -182,17 +182,15 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
 
 attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
                                   const void* q, const void* k, const void* v,
-                                  const void* o, const void* dO, float* delta, float* dq,
+                                  const void* o, const void* dO, float* delta,
                                   float* dbias, void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream) {
   Problem p;
   attn_status_t s = make_problem(prob, nullptr, sparse, &p);
   if (s != ATTN_OK) return s;
   const Sizes n = sizes_of(p);
-  if (!need(o, n.q) || !need(dO, n.q) || !need(delta, n.rows) || !need(dq, n.q))
-    return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(dq) || !aligned16(dbias))
-    return ATTN_ERR_INVALID_ARG;
+  if (!need(o, n.q) || !need(dO, n.q) || !need(delta, n.rows)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(dbias)) return ATTN_ERR_INVALID_ARG;
   float* d_ori = nullptr;
   float* d_cmp = nullptr;
   if (p.sparse) {
@@ -214,7 +212,7 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
   auto staged = [&](size_t off) {
     return w.staged ? reinterpret_cast<__half*>(ws + off) : nullptr;
   };
-  return cuda_status(launch_preprocess(p, q, k, v, o, dO, delta, dq, dbias, d_ori, d_cmp,
+  return cuda_status(launch_preprocess(p, q, k, v, o, dO, delta, dbias, d_ori, d_cmp,
                                        staged(w.q16), staged(w.k16), staged(w.v16),
                                        staged(w.do16), st, stream));
 }

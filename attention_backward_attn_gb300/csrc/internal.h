@@ -34,13 +34,13 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
                             float* d_ori, float* d_cmp, DevStatus* st, cudaStream_t stream);
 
 // ---- preprocess.cu ----
-// One fused kernel: clears the status record, zeroes dq / dbias / the sparse
-// dKV buffers, computes delta, and (if do16 != nullptr) writes fp16
+// One fused kernel: clears the status record, zeroes dbias / the sparse dKV
+// buffers, computes delta, and (if do16 != nullptr) writes fp16
 // head-major copies of q, k, v and dO. An fp16 overflow sets bits (1 q, 2 k,
 // 4 v, 8 dO) in the block's flag slot after the status record; the
 // tensor-core backward ORs the slots and reports ATTN_ERR_RANGE.
 cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, const void* v,
-                              const void* o, const void* dO, float* delta, float* dq,
+                              const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, DevStatus* st, cudaStream_t stream);
 

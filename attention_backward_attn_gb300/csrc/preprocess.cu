@@ -2,8 +2,8 @@
 //
 // D = rowsum(dO * O) ("34_bwd_gqa_fmha.py" cpu_bwd_gqa; Ascend
 // "sparse_flash_mla_grad" phase 2, SoftmaxGrad(dO, O)), computed in fp32 from
-// the bf16 rows. The same pass zeroes the dq row that the backward accumulates
-// into, zeroes dbias / the sparse dKV buffers, clears the status record, and
+// the bf16 rows. The same pass zeroes dbias / the sparse dKV buffers that the
+// backward accumulates into, clears the status record, and
 // for the tensor-core path writes fp16 head-major copies of q, k, v and dO.
 //
 // Why fp16 copies: the tensor-core backward feeds kind::f16 MMAs, and rounds
@@ -36,7 +36,6 @@ struct PreParams {
   const bf16* k;
   const bf16* v;
   float* delta;
-  float* dq;
   __half* q16;
   __half* k16;
   __half* v16;
@@ -104,7 +103,7 @@ preprocess_kernel(const PreParams p) {
   }
   int range_bits = 0;
 
-  // ---- query-side rows (b, i, h) in memory order: delta, dq = 0, staging ----
+  // ---- query-side rows (b, i, h) in memory order: delta, staging ----
   const int64_t nq = (int64_t)p.B * p.Sq * p.Hq;
   for (int64_t r0 = warp0 * RPW; r0 < nq; r0 += nwarps * RPW) {
     const int64_t row = r0 + sub;
@@ -125,9 +124,6 @@ preprocess_kernel(const PreParams p) {
         load8(drow + e0, df);
 #pragma unroll
         for (int t = 0; t < 8; ++t) s = fmaf(of[t], df[t], s);
-        float4* z = reinterpret_cast<float4*>(p.dq + row * D + e0);
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.do16 != nullptr) {
           float qf[8];
           load8(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0, qf);
@@ -188,7 +184,7 @@ preprocess_kernel(const PreParams p) {
 }  // namespace
 
 cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, const void* v,
-                              const void* o, const void* dO, float* delta, float* dq,
+                              const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, DevStatus* st, cudaStream_t stream) {
   PreParams p;
@@ -208,7 +204,6 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.k = static_cast<const bf16*>(k);
   p.v = static_cast<const bf16*>(v);
   p.delta = delta;
-  p.dq = dq;
   p.q16 = q16;
   p.k16 = k16;
   p.v16 = v16;

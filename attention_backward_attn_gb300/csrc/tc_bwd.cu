@@ -7,35 +7,39 @@
 //   dV = P^T dO, dK / dV summed over the query heads of a KV head,
 //   dbias = sum over the batch of dS.
 //
-// Work decomposition: a thread-block cluster of `cs` CTAs owns one 128-row
-// key tile of one (batch, KV head); CTA `rank` of the cluster takes r / cs of
-// the r query heads that share the KV head, and loops over every 128-row query
-// tile with a live entry (fully masked tiles are skipped, partial tiles get a
-// per-element mask). At the end the cs partial dK / dV tiles are summed
-// through distributed shared memory, so the GQA group reduction never leaves
-// the chip. Per (query head, query tile), key-major so that one thread owns
-// one key row of the softmax:
-//   MMA1  S^T  = K  Q^T                      (M = 128 keys, N = 128 queries, K = D)
-//   MMA2  dP^T = V  dO^T                     (M = 128 keys, N = 128 queries, K = D)
-//   SFU   P^T = exp2(S^T scale log2e + bias log2e - LSE log2e), dS^T = P^T (dP^T - D)
-//         -> P^T fp16 back into TMEM (A operand of MMA3), dS^T fp16 into SMEM
-//   MMA5  D = 128: dQ^T = K^T dS^T  (M = d, N = queries; coalesced atomics)
-//         D =  64: dQ   = dS  K     (M = queries, N = d)
-//   MMA3  dV += P^T dO     (A = P^T in TMEM, B = dO MN-major)
-//   MMA4  dK += dS^T Q     (A = dS^T K-major, B = Q MN-major)
-// MMA5 is issued first so that draining dQ overlaps MMA3 / MMA4 and the next
-// tile's MMA1.
+// One launch, two kinds of CTA (all tiles 128 x 128, fp16 operands, fp32
+// accumulators in TMEM; fully masked tiles are skipped and partial tiles get
+// a per-element mask):
 //
-// TMEM (512 columns x 128 lanes x 32 bit): [0, D) dK, [D, 2D) dV,
-// [2D, 2D+128) S^T (P^T fp16 pairs of queries 0-63 in its columns 0-31,
-// queries 64-127 in columns 64-95), [2D+128, 2D+256) dP^T, then dQ.
+// Key-major CTAs (dK, dV, dbias). A cluster of cs CTAs owns one 128-row key
+// tile of one (batch, KV head); CTA `rank` takes r / cs of the r query heads
+// that share the KV head and loops over their live query tiles. The cs partial
+// dK / dV tiles are summed through distributed shared memory at the end, so
+// the GQA group reduction never leaves the chip. Per tile, so that one thread
+// owns one key row of the softmax:
+//   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
+//   MMA2  dP^T = V  dO^T
+//   SFU   P^T = exp2(S^T scale log2e + bias log2e - LSE log2e), dS^T = P^T (dP^T - D)
+//         P^T fp16 back into TMEM (A operand of MMA3), dS^T fp16 into SMEM
+//   MMA3  dV += P^T dO       (A = P^T in TMEM, B = dO MN-major)
+//   MMA4  dK += dS^T Q       (A = dS^T K-major, B = Q MN-major)
+//
+// Query-major CTAs (dQ): one CTA per (batch, query head, 128-row query tile)
+// loops over the live key tiles of its KV head, recomputing S and dP:
+//   MMA1' S  = Q  K^T        (M = queries, N = keys)
+//   MMA2' dP = dO V^T
+//   SFU   dS = exp2(...) (dP - D), fp16 into TMEM over S
+//   MMA3' dQ += dS K         (A = dS in TMEM, B = K MN-major)
+// dQ accumulates in TMEM over all key tiles and is written once: no atomics
+// and no zero-filled accumulation buffer. S is double-buffered so that the
+// next tile's MMA1' runs during this tile's softmax.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 4-7 and 8-11 two softmax warpgroups (queries 0-63 / 64-127 of
-// the tile), which also drain dQ and, at the end, write dK (first group) and
-// dV (second group). Every mbarrier wait is bounded: after ~2 s it records
-// ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort flag, and the CTA drains
-// its copies / MMAs, frees TMEM and exits through the same cluster barriers.
+// owner, warps 4-7 and 8-11 two softmax warpgroups (columns 0-63 / 64-127 of
+// the tile), which also run the epilogue. Every mbarrier wait is bounded:
+// after ~2 s it records ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort
+// flag, and the CTA drains its copies / MMAs, frees TMEM and exits through
+// the same cluster barriers.
 //
 // Operands are fp16 (exact copies of the bf16 inputs, staged by the
 // pre-pass): P and dS rounded to fp16 keep 3 more mantissa bits than bf16,
@@ -50,13 +54,14 @@ namespace attn {
 namespace {
 
 constexpr int BM = 128;  // query rows per tile
-constexpr int BN = 128;  // key rows per CTA
+constexpr int BN = 128;  // key rows per tile
 constexpr int kThreads = 384;
 constexpr int kSlab = 128 * 128;  // one [128 rows][64 fp16] 128B-swizzled slab, bytes
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
+// Shared memory of a key-major CTA.
 template <int D>
-struct Smem {
+struct SmemKV {
   static constexpr int kTile = (D / 64) * kSlab;  // a [128][D] fp16 operand tile
   static constexpr int K = 0;
   static constexpr int V = K + kTile;
@@ -74,14 +79,35 @@ struct Smem {
   static_assert(2 * 128 * kStageRow <= 4 * kTile + 2 * kSlab, "staging fits");
 };
 
-enum Bar {
-  kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kPFull = 6, kDqFull = 7, kDqEmpty = 8,
-  kAccFull = 9, kMma3 = 10, kNumBars = 11
+// Shared memory of a query-major CTA.
+template <int D>
+struct SmemQ {
+  static constexpr int kTile = (D / 64) * kSlab;
+  static constexpr int Q = 0;
+  static constexpr int dO = Q + kTile;
+  static constexpr int K = dO + kTile;      // 2 stages
+  static constexpr int V = K + 2 * kTile;   // 2 stages
+  static constexpr int BAR = V + 2 * kTile;
+  static constexpr int MISC = BAR + 128;
+  static constexpr int TOTAL = MISC + 16;
 };
+
+template <int D>
+constexpr int smem_total() {
+  return SmemKV<D>::TOTAL > SmemQ<D>::TOTAL ? SmemKV<D>::TOTAL : SmemQ<D>::TOTAL;
+}
+
+// barrier indices, key-major CTA
+enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kPFull = 6, kAccFull = 7,
+             kMma3 = 8 };
+// barrier indices, query-major CTA
+enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, qAccFull = 7,
+            qMma3 = 8 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
-  int cs;  // CTAs per cluster (query-head split)
+  int cs;          // CTAs per cluster (query-head split of the key-major CTAs)
+  int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
   float scale;
   float scale_log2;
   MaskSpec mask;
@@ -133,16 +159,25 @@ __device__ __noinline__ void drain_bar(const Ctx& c, int which, uint32_t parity)
   }
 }
 
+// Bits [a, b) of a 32-bit mask, clipped to [0, 32).
+__device__ __forceinline__ uint32_t bits_between(int a, int b) {
+  a = a < 0 ? 0 : a;
+  b = b > 32 ? 32 : b;
+  if (b <= a) return 0u;
+  const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+  return below_b & ~((1u << a) - 1u);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Iterates the live (query head, query tile) pairs of this CTA's key tile.
-struct TileIter {
+// Live (query head, query tile) pairs of a key tile.
+struct QTileIter {
   int hpc, nmt, n0, hl, mt;
   MaskSpec mask;
-  __device__ TileIter(int hpc_, int nmt_, int n0_, MaskSpec m)
+  __device__ QTileIter(int hpc_, int nmt_, int n0_, MaskSpec m)
       : hpc(hpc_), nmt(nmt_), n0(n0_), hl(0), mt(-1), mask(m) {}
   __device__ bool next() {
     for (;;) {
@@ -155,26 +190,46 @@ struct TileIter {
   }
 };
 
+// Live key tiles of a query tile.
+struct KTileIter {
+  int nnt, m0, nt;
+  MaskSpec mask;
+  __device__ KTileIter(int nnt_, int m0_, MaskSpec m) : nnt(nnt_), m0(m0_), nt(-1), mask(m) {}
+  __device__ bool next() {
+    while (++nt < nnt)
+      if (tile_any(mask, m0, m0 + BM, nt * BN, nt * BN + BN)) return true;
+    return false;
+  }
+};
+
+__device__ __forceinline__ void init_common(const Ctx& c, uint32_t tmem_slot_addr, int nbars,
+                                            const uint32_t* counts, int warp) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nbars; ++i) ptx::mbar_init(c.bar(i), counts[i]);
+    *c.abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot_addr, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+}
+
+// ======================================================= key-major CTA ====
 template <int D, bool BIAS, bool DBIAS>
-__global__ void __launch_bounds__(kThreads, 1)
-attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                   const TcParams p) {
-  using L = Smem<D>;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t sbase = ptx::smem_u32(smem);
+__device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                       const CUtensorMap* tmV, const CUtensorMap* tmdO,
+                                       const TcParams& p, uint8_t* smem, uint32_t sbase) {
+  using L = SmemKV<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // 1 KiB alignment of the 128B-swizzle atoms; uniform over the cluster (same
-  // kernel, same layout), so an early return cannot strand a cluster barrier.
-  if (sbase & 1023u) {
-    if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 1);
-    return;
-  }
   const int cs = p.cs;
   const int rank = (int)(blockIdx.x % cs);
   const int ci = (int)(blockIdx.x / cs);
-  const int bg = ci % (p.B * p.Hk);  // (batch, KV head), key tile slowest
+  const int bg = ci % (p.B * p.Hk);  // (batch, KV head); key tile slowest = heaviest first
   const int nt = ci / (p.B * p.Hk);
   const int g = bg % p.Hk;
   const int b = bg / p.Hk;
@@ -188,49 +243,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-
-  if (blockIdx.x == 0) {
-    // fp16 overflow found while staging the operands: OR of the pre-pass's
-    // per-block flag slots
-    const int nslots = min(max(p.status->reserved[1], 0), kPreMaxBlocks);
-    const int32_t* slots = reinterpret_cast<const int32_t*>(p.status + 1);
-    int bits = 0;
-    for (int i = threadIdx.x; i < nslots; i += blockDim.x) bits |= slots[i];
-    bits = __reduce_or_sync(0xffffffffu, bits);
-    if (bits && lane == 0) report(p.status, ATTN_ERR_RANGE, bits);
-  }
-  if (threadIdx.x == 0) {
-    ptx::prefetch_tmap(&tmQ);
-    ptx::prefetch_tmap(&tmK);
-    ptx::prefetch_tmap(&tmV);
-    ptx::prefetch_tmap(&tmdO);
-    ptx::mbar_init(c.bar(kKvFull), 1);
-    ptx::mbar_init(c.bar(kQFull0), 1);
-    ptx::mbar_init(c.bar(kQFull0 + 1), 1);
-    ptx::mbar_init(c.bar(kQEmpty0), 1);
-    ptx::mbar_init(c.bar(kQEmpty0 + 1), 1);
-    ptx::mbar_init(c.bar(kSFull), 1);
-    ptx::mbar_init(c.bar(kPFull), 256);
-    ptx::mbar_init(c.bar(kDqFull), 1);
-    ptx::mbar_init(c.bar(kDqEmpty), 256);
-    ptx::mbar_init(c.bar(kAccFull), 1);
-    ptx::mbar_init(c.bar(kMma3), 1);
-    *c.abort = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(sbase + L::MISC, 512);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
+  const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, 256, 1, 1};
+  init_common(c, sbase + L::MISC, 9, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
   const uint32_t t_S = tmem + 2 * D;
   const uint32_t t_dP = tmem + 2 * D + 128;
-
   const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::dS;
   bool epi_ok = false;
   int n_iters = 0;
@@ -242,10 +261,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::mbar_arrive_expect_tx(c.bar(kKvFull), 2 * L::kTile);
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
-        ptx::tma_load_2d(sK + hf * kSlab, &tmK, c.bar(kKvFull), hf * 64, krow);
-        ptx::tma_load_2d(sV + hf * kSlab, &tmV, c.bar(kKvFull), hf * 64, krow);
+        ptx::tma_load_2d(sK + hf * kSlab, tmK, c.bar(kKvFull), hf * 64, krow);
+        ptx::tma_load_2d(sV + hf * kSlab, tmV, c.bar(kKvFull), hf * 64, krow);
       }
-      TileIter it(hpc, nmt, n0, p.mask);
+      QTileIter it(hpc, nmt, n0, p.mask);
       int t = 0;
       int issued[2] = {0, 0};
       while (it.next()) {
@@ -258,8 +277,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         ptx::mbar_arrive_expect_tx(full, 2 * L::kTile + 2 * 512);
 #pragma unroll
         for (int hf = 0; hf < D / 64; ++hf) {
-          ptx::tma_load_2d(sbase + L::Q + st * L::kTile + hf * kSlab, &tmQ, full, hf * 64, (int)row);
-          ptx::tma_load_2d(sbase + L::dO + st * L::kTile + hf * kSlab, &tmdO, full, hf * 64, (int)row);
+          ptx::tma_load_2d(sbase + L::Q + st * L::kTile + hf * kSlab, tmQ, full, hf * 64, (int)row);
+          ptx::tma_load_2d(sbase + L::dO + st * L::kTile + hf * kSlab, tmdO, full, hf * 64, (int)row);
         }
         ptx::bulk_load(sbase + L::LSE + st * 512, p.lse + row, 512, full);
         ptx::bulk_load(sbase + L::DLT + st * 512, p.delta + row, 512, full);
@@ -277,7 +296,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t id_KV = ptx::idesc_f16_f32(128, D, false, true);
-      constexpr uint32_t id_Q = ptx::idesc_f16_f32(128, D == 128 ? 128 : D, true, true);
       auto issue_S = [&](int st) {  // MMA1 S^T = K Q^T (both K-major over d)
         const uint32_t sQ = sbase + L::Q + st * L::kTile;
 #pragma unroll
@@ -297,17 +315,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
       };
       bool ok = wait_bar(c, kKvFull, 0, 2);
-      TileIter it(hpc, nmt, n0, p.mask);
+      QTileIter it(hpc, nmt, n0, p.mask);
       bool have = ok && it.next();
       if (have) {
-        ok = wait_bar(c, kQFull0, 0, 3);
-        if (ok) {
+        have = wait_bar(c, kQFull0, 0, 3);
+        if (have) {
           ptx::tc_fence_after();
           issue_S(0);
           issue_dP(0);
           ptx::mma_commit(c.bar(kSFull));
         }
-        have = ok;
       }
       int t = 0;
       while (have) {
@@ -316,17 +333,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const uint32_t sdO = sbase + L::dO + st * L::kTile;
         if (!wait_bar(c, kPFull, t & 1, 4)) break;
         ptx::tc_fence_after();
-        // MMA5: dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64), into the dP columns
-#pragma unroll
-        for (int s = 0; s < BN / 16; ++s) {
-          const uint64_t dk_desc = ptx::smem_desc_sw128(sK + s * 2048, kSlab, 1024);
-          const uint64_t ds_desc = ptx::smem_desc_sw128(sDS + s * 2048, kSlab, 1024);
-          if constexpr (D == 128)
-            ptx::mma_ss(t_dP, dk_desc, ds_desc, id_Q, s > 0);
-          else
-            ptx::mma_ss(t_dP, ds_desc, dk_desc, id_Q, s > 0);
-        }
-        ptx::mma_commit(c.bar(kDqFull));
         // MMA3 dV += P^T dO : A = P^T (TMEM fp16 pairs), B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
@@ -347,15 +353,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         have = it.next();
         if (have) {
           const int st1 = (t + 1) & 1;
-          // next tile: S^T once its operands landed and MMA3 released the S columns,
-          // dP^T once the drain released the dP columns
-          if (!wait_bar(c, kQFull0 + st1, ((t + 1) >> 1) & 1, 5) || !wait_bar(c, kMma3, t & 1, 6))
-            break;
-          ptx::tc_fence_after();
-          issue_S(st1);
-          if (!wait_bar(c, kDqEmpty, t & 1, 7)) break;
+          // next tile: dP^T as soon as its operands landed (the softmax already
+          // read this tile's dP^T), S^T once MMA3 released the P^T columns
+          if (!wait_bar(c, kQFull0 + st1, ((t + 1) >> 1) & 1, 5)) break;
           ptx::tc_fence_after();
           issue_dP(st1);
+          if (!wait_bar(c, kMma3, t & 1, 6)) break;
+          ptx::tc_fence_after();
+          issue_S(st1);
           ptx::mma_commit(c.bar(kSFull));
         }
         ++t;
@@ -364,13 +369,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------- softmax / dS / dQ warpgroups --
+    // ------------------------------------------- softmax / dS warpgroups --
     const int wg = (warp - 4) >> 2;                  // 0: queries 0-63, 1: 64-127
     const int lg = warp & 3;                         // TMEM lane quarter
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int jl = lg * 32 + lane;                   // key row within the tile
     const int j = n0 + jl;
-    TileIter it(hpc, nmt, n0, p.mask);
+    QTileIter it(hpc, nmt, n0, p.mask);
     int t = 0;
     bool ok = true;
     while (it.next()) {
@@ -382,26 +387,31 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::tc_fence_after();
       const int h = h_first + it.hl;
       const int m0 = it.mt * BM;
-      // A row without live keys has LSE = -inf; it can only sit in a partial
-      // tile, where the per-element mask zeroes its probabilities.
+      // Live queries of this key row within the tile, [qlo, qhi]. A row
+      // without live keys has LSE = -inf; it can only sit in a partial tile,
+      // where this mask zeroes its probabilities.
       const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      int qlo = 0, qhi = BM - 1;
+      if (partial && j >= p.mask.sink) {
+        qlo = p.mask.wr >= 0 ? j - p.mask.wr - m0 : 0;
+        qhi = p.mask.wl >= 0 ? j + p.mask.wl - m0 : BM - 1;
+      }
       const float* brow = nullptr;
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       float* dbrow = nullptr;
       if constexpr (DBIAS) dbrow = p.dbias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       const uint32_t ds_row = sDS + wg * kSlab + jl * 128;
-#pragma unroll 1
+      // all 64 columns of S^T and dP^T of this group in one round trip
+      uint32_t sr[64], dr[64];
+      ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
+      ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
+      ptx::tmem_ld32(t_dP + lane_off + wg * 64, dr);
+      ptx::tmem_ld32(t_dP + lane_off + wg * 64 + 32, dr + 32);
+      ptx::tmem_wait_ld();
+#pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld32(t_S + lane_off + q0, sr);
-        ptx::tmem_ld32(t_dP + lane_off + q0, dr);
-        float bv[32];
-        if constexpr (BIAS) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) bv[e] = __ldg(brow + (int64_t)(q0 + e) * p.Sk);
-        }
-        ptx::tmem_wait_ld();
+        const uint32_t live = bits_between(qlo - q0, qhi - q0 + 1);
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
@@ -409,16 +419,20 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + e4);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float bv[4];
+          if constexpr (BIAS) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
+          }
           float pe[4], de[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int e = e4 + u;
-            float x = fmaf(__uint_as_float(sr[e]), p.scale_log2, lv[u] * -kLog2e);
-            if constexpr (BIAS) x = fmaf(bv[e], kLog2e, x);
-            float pv = ptx::ex2(x);
-            if (partial && !mask_live(p.mask, m0 + q0 + e, j)) pv = 0.f;
+            float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, lv[u] * -kLog2e);
+            if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
+            const float pv = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
             pe[u] = pv;
-            de[u] = pv * (__uint_as_float(dr[e]) - dv[u]);
+            de[u] = pv * (__uint_as_float(dr[cc * 32 + e]) - dv[u]);
             if constexpr (DBIAS) atomicAdd(dbrow + (int64_t)(q0 + e) * p.Sk, de[u]);
           }
           pk[e4 / 2] = pack_half2(pe[0], pe[1]);
@@ -440,39 +454,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::fence_async_shared();
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(kPFull));
-      // ---- drain dQ of this tile (scale applied here) ----
-      if (!wait_bar(c, kDqFull, t & 1, 10)) { ok = false; break; }
-      ptx::tc_fence_after();
-      if constexpr (D == 128) {
-        // dQ^T: TMEM lane = d, column = query; a warp writes 32 consecutive d
-        const int d = jl;
-        float* base = p.dq + (((int64_t)b * p.Sq + m0) * p.Hq + h) * D + d;
-        const int64_t qstride = (int64_t)p.Hq * D;
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int q0 = wg * 64 + cc * 32;
-          uint32_t v[32];
-          ptx::tmem_ld32(t_dP + lane_off + q0, v);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            ptx::red_add_f32(base + (int64_t)(q0 + e) * qstride, __uint_as_float(v[e]) * p.scale);
-        }
-      } else {
-        // dQ: TMEM lane = query, column = d; this group takes d in [32 wg, 32 wg + 32)
-        float* dst = p.dq + (((int64_t)b * p.Sq + m0 + jl) * p.Hq + h) * D + wg * 32;
-        uint32_t v[32];
-        ptx::tmem_ld32(t_dP + lane_off + wg * 32, v);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          atomicAdd(reinterpret_cast<float4*>(dst + e),
-                    make_float4(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
-                                __uint_as_float(v[e + 2]) * p.scale,
-                                __uint_as_float(v[e + 3]) * p.scale));
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(kDqEmpty));
       ++t;
     }
     n_iters = t;
@@ -556,6 +537,287 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
+// ===================================================== query-major CTA ====
+template <int D, bool BIAS>
+__device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                      const CUtensorMap* tmV, const CUtensorMap* tmdO,
+                                      const TcParams& p, uint8_t* smem, uint32_t sbase, int qi) {
+  using L = SmemQ<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nmt = p.Sq / BM;
+  const int nnt = p.Sk / BN;
+  const int bh = qi % (p.B * p.Hq);
+  const int mt = nmt - 1 - qi / (p.B * p.Hq);  // later query tiles first (heavier when causal)
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
+  const int g = h / (p.Hq / p.Hk);
+  const int m0 = mt * BM;
+
+  Ctx c;
+  c.bars = sbase + L::BAR;
+  c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+  c.status = p.status;
+  const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, 256, 1, 1};
+  init_common(c, sbase + L::MISC, 9, counts, warp);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
+  // TMEM: [0, D) dQ, then S buffers 0 / 1 and dP (128 columns each)
+  const uint32_t t_dQ = tmem;
+  const uint32_t t_S0 = tmem + 128;
+  const uint32_t t_dP = tmem + 384;
+  const uint32_t sQ = sbase + L::Q, sdO = sbase + L::dO;
+  bool epi_ok = false;
+  int n_iters = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      const int qrow = (b * p.Hq + h) * p.Sq + m0;
+      ptx::mbar_arrive_expect_tx(c.bar(qQdoFull), 2 * L::kTile);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
+        ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
+        ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
+      }
+      KTileIter it(nnt, m0, p.mask);
+      int t = 0;
+      int issued[2] = {0, 0};
+      while (it.next()) {
+        const int st = t & 1;
+        const int use = t >> 1;
+        if (use > 0 && !wait_bar(c, qKvEmpty0 + st, (use - 1) & 1, 21)) break;
+        const int krow = (b * p.Hk + g) * p.Sk + it.nt * BN;
+        const uint32_t full = c.bar(qKvFull0 + st);
+        ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          ptx::tma_load_2d(sbase + L::K + st * L::kTile + hf * kSlab, tmK, full, hf * 64, krow);
+          ptx::tma_load_2d(sbase + L::V + st * L::kTile + hf * kSlab, tmV, full, hf * 64, krow);
+        }
+        issued[st] = use + 1;
+        ++t;
+      }
+      drain_bar(c, qQdoFull, 0);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] > 0) drain_bar(c, qKvFull0 + st, (issued[st] - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
+      constexpr uint32_t id_dQ = ptx::idesc_f16_f32(128, D, false, true);
+      auto issue_S = [&](int t) {  // MMA1' S = Q K^T into S buffer t & 1
+        const uint32_t sK = sbase + L::K + (t & 1) * L::kTile;
+        const uint32_t dst = t_S0 + (t & 1) * 128;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
+          ptx::mma_ss(dst, ptx::smem_desc_sw128(sQ + off, 16, 1024),
+                      ptx::smem_desc_sw128(sK + off, 16, 1024), id_S, s > 0);
+        }
+      };
+      auto issue_dP = [&](int t) {  // MMA2' dP = dO V^T
+        const uint32_t sV = sbase + L::V + (t & 1) * L::kTile;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
+          ptx::mma_ss(t_dP, ptx::smem_desc_sw128(sdO + off, 16, 1024),
+                      ptx::smem_desc_sw128(sV + off, 16, 1024), id_S, s > 0);
+        }
+      };
+      bool ok = wait_bar(c, qQdoFull, 0, 22);
+      KTileIter it(nnt, m0, p.mask);
+      bool have = ok && it.next();
+      if (have) {
+        have = wait_bar(c, qKvFull0, 0, 23);
+        if (have) {
+          ptx::tc_fence_after();
+          issue_S(0);
+          issue_dP(0);
+          ptx::mma_commit(c.bar(qSFull));
+        }
+      }
+      int t = 0;
+      while (have) {
+        const int st = t & 1;
+        have = it.next();
+        // next tile's S into the other buffer while this tile's softmax runs;
+        // that buffer held dS of tile t - 1, read by MMA3'(t - 1)
+        if (have) {
+          if (!wait_bar(c, qKvFull0 + ((t + 1) & 1), ((t + 1) >> 1) & 1, 24)) break;
+          if (t > 0 && !wait_bar(c, qMma3, (t - 1) & 1, 25)) break;
+          ptx::tc_fence_after();
+          issue_S(t + 1);
+        }
+        if (!wait_bar(c, qDsFull, t & 1, 26)) break;
+        ptx::tc_fence_after();
+        // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major over d
+        const uint32_t sK = sbase + L::K + st * L::kTile;
+        const uint32_t t_S = t_S0 + st * 128;
+#pragma unroll
+        for (int s = 0; s < BN / 16; ++s) {
+          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_dQ, a_col, ptx::smem_desc_sw128(sK + s * 2048, kSlab, 1024), id_dQ,
+                      (t > 0 || s > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(c.bar(qMma3));
+        ptx::mma_commit(c.bar(qKvEmpty0 + st));
+        if (have) {
+          ptx::tc_fence_after();
+          issue_dP(t + 1);  // the softmax already read this tile's dP
+          ptx::mma_commit(c.bar(qSFull));
+        }
+        ++t;
+      }
+      ptx::mma_commit(c.bar(qAccFull));
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax / dS groups --
+    const int wg = (warp - 4) >> 2;                  // 0: keys 0-63, 1: keys 64-127
+    const int lg = warp & 3;
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int il = lg * 32 + lane;                   // query row within the tile
+    const int i = m0 + il;
+    const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + i;
+    const float nl = p.lse[row] * -kLog2e;           // -inf rows: see the partial-tile mask
+    const float dl = p.delta[row];
+    const float* brow = nullptr;
+    if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + i) * p.Sk;
+    KTileIter it(nnt, m0, p.mask);
+    int t = 0;
+    bool ok = true;
+    while (it.next()) {
+      if (!wait_bar(c, qSFull, t & 1, 27)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const int n0 = it.nt * BN;
+      const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      // live keys of this query row within the tile: [klo, khi] plus the sinks
+      int klo = 0, khi = BN - 1, ksink = 0;
+      if (partial) {
+        klo = p.mask.wl >= 0 ? i - p.mask.wl - n0 : 0;
+        khi = p.mask.wr >= 0 ? i + p.mask.wr - n0 : BN - 1;
+        ksink = p.mask.sink - n0;
+      }
+      const uint32_t t_S = t_S0 + (t & 1) * 128;
+      uint32_t sr[64], dr[64];
+      ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
+      ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
+      ptx::tmem_ld32(t_dP + lane_off + wg * 64, dr);
+      ptx::tmem_ld32(t_dP + lane_off + wg * 64 + 32, dr + 32);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int k0 = wg * 64 + cc * 32;  // first key of this chunk within the tile
+        const uint32_t live =
+            bits_between(klo - k0, khi - k0 + 1) | bits_between(-k0, ksink - k0);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          float bv[4];
+          if constexpr (BIAS) {
+            const float4 b4 = __ldg(reinterpret_cast<const float4*>(brow + n0 + k0 + e4));
+            bv[0] = b4.x;
+            bv[1] = b4.y;
+            bv[2] = b4.z;
+            bv[3] = b4.w;
+          }
+          float de[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e4 + u;
+            float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, nl);
+            if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
+            const float pv = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
+            de[u] = pv * (__uint_as_float(dr[cc * 32 + e]) - dl);
+          }
+          dk[e4 / 2] = pack_half2(de[0], de[1]);
+          dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
+        }
+        // dS fp16 pairs over the (already read) front half of this group's S columns
+        ptx::tmem_st16(t_S + lane_off + wg * 64 + cc * 16, dk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(qDsFull));
+      ++t;
+    }
+    n_iters = t;
+    epi_ok = ok && wait_bar(c, qAccFull, 0, 28);
+    // ---------------------------------------------------- dQ epilogue --
+    // thread = query row; warpgroup wg writes columns [wg D/2, wg D/2 + D/2)
+    if (epi_ok) {
+      ptx::tc_fence_after();
+      float* grow = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D + wg * (D / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t v[32];
+        if (n_iters > 0) {
+          ptx::tmem_ld32(t_dQ + lane_off + wg * (D / 2) + cc * 32, v);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(grow + cc * 32 + e) =
+              make_float4(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
+                          __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+      }
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (lane == 0) drain_bar(c, qAccFull, 0);
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BIAS, bool DBIAS>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_u32(smem);
+  // 1 KiB alignment of the 128B-swizzle atoms; uniform over the grid, so an
+  // early return cannot strand a cluster barrier.
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 1);
+    return;
+  }
+  if (blockIdx.x == 0) {
+    // fp16 overflow found while staging the operands: OR of the pre-pass's
+    // per-block flag slots
+    const int nslots = min(max(p.status->reserved[1], 0), kPreMaxBlocks);
+    const int32_t* slots = reinterpret_cast<const int32_t*>(p.status + 1);
+    int bits = 0;
+    for (int i = threadIdx.x; i < nslots; i += blockDim.x) bits |= slots[i];
+    bits = __reduce_or_sync(0xffffffffu, bits);
+    if (bits && (threadIdx.x & 31) == 0) report(p.status, ATTN_ERR_RANGE, bits);
+  }
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmdO);
+  }
+  if ((int)blockIdx.x < p.kv_ctas) {
+    kv_cta<D, BIAS, DBIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
+  } else {
+    const int qi = (int)blockIdx.x - p.kv_ctas;
+    if (qi < p.B * p.Hq * (p.Sq / BM))  // the rest pads the grid to whole clusters
+      q_cta<D, BIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
+  }
+}
+
 // ------------------------------------------------------------------ host --
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -598,14 +860,14 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
   static bool configured = false;  // attribute set once per process and variant
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Smem<D>::TOTAL);
+                                         smem_total<D>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<D>::TOTAL;
+  cfg.dynamicSmemBytes = smem_total<D>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -658,6 +920,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
   p.cs = cluster_size(pr.Hq / pr.Hk);
+  p.kv_ctas = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.mask = pr.mask;
@@ -669,7 +932,8 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dv = dv;
   p.dbias = dbias;
   p.status = st;
-  const int grid = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
+  const int q_ctas = pr.B * pr.Hq * (pr.Sq / BM);
+  const int grid = p.kv_ctas + (q_ctas + p.cs - 1) / p.cs * p.cs;
   if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
   return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);
 }

@@ -219,7 +219,7 @@ def run_ours(args):
         torch.sum(evict, dim=0, out=scratch)
         starts[s].record(stream)
         ab.attn_bwd_preprocess(plan.prob, plan.sparse, plan.q, plan.k, plan.v, plan.o, plan.do,
-                               plan.delta, plan.dq, plan.dbias, plan.workspace, plan.ws_bytes)
+                               plan.delta, plan.dbias, plan.workspace, plan.ws_bytes)
         mids[s].record(stream)
         ab.attn_bwd(plan.prob, plan.mask, plan.sparse, plan.q, plan.k, plan.v, plan.do,
                     plan.lse, plan.delta, plan.bias, plan.dq, plan.dk, plan.dv, plan.dbias,
@@ -253,7 +253,8 @@ def run_ours(args):
         return
     peaks, peaks_src = measured_peaks()
     path = "tcgen05" if plan.path == 1 else "simt"
-    # kernels per step: the fused pre-pass, then one tcgen05 kernel or two SIMT kernels
+    # kernels per step: the fused pre-pass, then one tcgen05 kernel (key-major and
+    # query-major CTAs in one launch) or two SIMT kernels
     if path == "tcgen05":
         roof = {"bound": "tensor", "achieved": flops / (mean_bwd_ms * 1e-3) / 1e12,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}

@@ -130,8 +130,8 @@ size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* ma
 /* Backward pre-pass ("34_bwd_gqa_fmha.py" cpu_bwd_gqa: D = rowsum(dO * O);
  * Ascend formula phase 2: SoftmaxGrad(dO, O)):
  *  - delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d] in fp32;
- *  - zeroes the accumulated outputs: dq, dbias (if non-NULL) and, for the
- *    sparse variant, sparse->d_ori_kv / d_cmp_kv;
+ *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL) and,
+ *    for the sparse variant, sparse->d_ori_kv / d_cmp_kv;
  *  - clears the workspace status record;
  *  - when attn_bwd will take the tensor-core path, writes fp16 copies of q,
  *    k, v and dO into the workspace (head-major [B, H, S, D] rows) for it.
@@ -143,16 +143,15 @@ size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* ma
 attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
                                   const void* q, const void* k, const void* v,
                                   const void* o, const void* dO, float* delta,
-                                  float* dq, float* dbias,
+                                  float* dbias,
                                   void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
 
 /* The fused backward ("34_bwd_gqa_fmha.py" docstring and cpu_bwd_gqa;
  * "28_backward_dbias_fmha.py" cpu_attention_bwd_dbias; Ascend
- * "sparse_flash_mla_grad" phases 1-3). P is rebuilt from lse; delta, dq and
- * dbias / sparse gradients come from attn_bwd_preprocess (dq, dbias and the
- * sparse gradients are accumulated into the zeroed buffers); dk and dv are
- * written in full. dbias may be non-NULL without bias (gradient of a zero
+ * "sparse_flash_mla_grad" phases 1-3). P is rebuilt from lse; delta comes
+ * from attn_bwd_preprocess, which also zeroed dbias and the sparse gradients
+ * that this call accumulates into; dq, dk and dv are written in full. dbias may be non-NULL without bias (gradient of a zero
  * bias). Returns ATTN_ERR_UNSUPPORTED for D outside {64, 128, 512} or the
  * sparse variant with D != 512 when no fallback kernel covers it. */
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
