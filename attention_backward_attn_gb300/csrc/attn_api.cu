@@ -27,6 +27,10 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
   if (!strides_ok(a.q_stride) || !strides_ok(a.o_stride) || !strides_ok(a.do_stride))
     return ATTN_ERR_INVALID_ARG;
   if (a.D != 64 && a.D != 128 && a.D != 512) return ATTN_ERR_UNSUPPORTED;
+  // row counts of the [B, S, H] index spaces must fit 31 bits (32-bit index math)
+  const int64_t rows_q = (int64_t)a.B * (a.Sq + 8) * a.Hq;
+  const int64_t rows_k = (int64_t)a.B * ((a.Sk > 0 ? a.Sk : 0) + 8) * a.Hk * 2;
+  if (rows_q >= (int64_t(1) << 31) || rows_k >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   Problem p{};
   p.B = a.B;
   p.Hq = a.Hq;

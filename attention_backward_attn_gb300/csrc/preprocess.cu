@@ -17,7 +17,8 @@
 // Layout of the work: a row of D elements is split into 16-byte chunks of 8
 // values; LPR = min(D / 8, 32) lanes cover a row, so a warp streams
 // 32 / LPR rows at once with 16-byte loads and stores; a grid-stride loop
-// keeps every SM's memory pipe full.
+// keeps every SM's memory pipe full. Rows are visited in blocks of 8 per head
+// (see decompose) so that both the reads and the head-major writes stream.
 
 #include "internal.h"
 
@@ -49,8 +50,11 @@ struct PreParams {
   DevStatus* st;
 };
 
-__device__ __forceinline__ void load8(const bf16* p, float* f) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ uint4 load_raw(const bf16* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& raw, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -74,6 +78,25 @@ __device__ __forceinline__ bool store8_half(__half* p, const float* f) {
   return bad;
 }
 
+// Work order over (batch, block of kIB rows, head, row in block): a warp step
+// covers rows of one head that are contiguous in the head-major fp16 copies
+// (2 KiB runs at D = 128), and the heads of one row block together read a
+// contiguous span of the [B, S, H, D] input.
+constexpr int kIB = 8;
+
+// 32-bit index math (the host rejects problems with 2^31 or more rows): a
+// 64-bit division is a long software sequence on the GPU.
+__device__ __forceinline__ void decompose(int64_t f64, int H, int S, int* b, int* h, int* i) {
+  const uint32_t f = (uint32_t)f64;
+  const uint32_t ii = f % kIB;
+  const uint32_t g = f / kIB;
+  *h = (int)(g % (uint32_t)H);
+  const uint32_t blk = g / (uint32_t)H;
+  const uint32_t nblk = (uint32_t)(S + kIB - 1) / kIB;
+  *i = (int)((blk % nblk) * kIB + ii);
+  *b = (int)(blk / nblk);
+}
+
 __device__ __forceinline__ void zero_range(float* a, int64_t n, int64_t tid, int64_t stride) {
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   float4* a4 = reinterpret_cast<float4*>(a);
@@ -82,7 +105,7 @@ __device__ __forceinline__ void zero_range(float* a, int64_t n, int64_t tid, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 preprocess_kernel(const PreParams p) {
   constexpr int CH = D / 8;                 // 16-byte chunks per row
   constexpr int LPR = CH < 32 ? CH : 32;    // lanes per row
@@ -104,64 +127,90 @@ preprocess_kernel(const PreParams p) {
   int range_bits = 0;
 
   // ---- query-side rows (b, i, h) in memory order: delta, staging ----
-  const int64_t nq = (int64_t)p.B * p.Sq * p.Hq;
-  for (int64_t r0 = warp0 * RPW; r0 < nq; r0 += nwarps * RPW) {
-    const int64_t row = r0 + sub;
-    const bool valid = row < nq;
-    float s = 0.f;
-    if (valid) {
-      const int h = (int)(row % p.Hq);
-      const int i = (int)((row / p.Hq) % p.Sq);
-      const int b = (int)(row / ((int64_t)p.Hq * p.Sq));
-      const bf16* orow = p.o + b * p.o0 + i * p.o1 + h * p.o2;
-      const bf16* drow = p.dO + b * p.d0 + i * p.d1 + h * p.d2;
-      const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
+  // U row slots per warp step, all loads issued before any dependent work so
+  // that each thread keeps several 16-byte requests in flight.
+  constexpr int U = 2;
+  const int64_t nq = (int64_t)p.B * ((p.Sq + kIB - 1) / kIB) * kIB * p.Hq;
+  for (int64_t r0 = warp0 * RPW * U; r0 < nq; r0 += nwarps * RPW * U) {
+    uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
+    int64_t rows[U];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const int e0 = (cl + c * LPR) * 8;
-        float of[8], df[8];
-        load8(orow + e0, of);
-        load8(drow + e0, df);
+    for (int u = 0; u < U; ++u) {
+      rows[u] = r0 + u * RPW + sub;
+      int h, i, b;
+      decompose(rows[u], p.Hq, p.Sq, &b, &h, &i);
+      if (rows[u] < nq && i < p.Sq) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) s = fmaf(of[t], df[t], s);
-        if (p.do16 != nullptr) {
-          float qf[8];
-          load8(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0, qf);
-          if (store8_half(p.do16 + hm * D + e0, df)) range_bits |= 8;
-          if (store8_half(p.q16 + hm * D + e0, qf)) range_bits |= 1;
+        for (int c = 0; c < CPL; ++c) {
+          const int e0 = (cl + c * LPR) * 8;
+          of[u][c] = load_raw(p.o + b * p.o0 + i * p.o1 + h * p.o2 + e0);
+          df[u][c] = load_raw(p.dO + b * p.d0 + i * p.d1 + h * p.d2 + e0);
+          if (p.do16 != nullptr) qf[u][c] = load_raw(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0);
         }
       }
     }
 #pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (valid && cl == 0) {
-      const int h = (int)(row % p.Hq);
-      const int i = (int)((row / p.Hq) % p.Sq);
-      const int b = (int)(row / ((int64_t)p.Hq * p.Sq));
-      p.delta[((int64_t)b * p.Hq + h) * p.Sq + i] = s;
+    for (int u = 0; u < U; ++u) {
+      int h, i, b;
+      decompose(rows[u], p.Hq, p.Sq, &b, &h, &i);
+      const bool valid = rows[u] < nq && i < p.Sq;
+      float s = 0.f;
+      if (valid) {
+        const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int e0 = (cl + c * LPR) * 8;
+          float ov[8], dv[8];
+          unpack8(of[u][c], ov);
+          unpack8(df[u][c], dv);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) s = fmaf(ov[t], dv[t], s);
+          if (p.do16 != nullptr) {
+            float qv[8];
+            unpack8(qf[u][c], qv);
+            if (store8_half(p.do16 + hm * D + e0, dv)) range_bits |= 8;
+            if (store8_half(p.q16 + hm * D + e0, qv)) range_bits |= 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (valid && cl == 0) p.delta[((int64_t)b * p.Hq + h) * p.Sq + i] = s;
     }
   }
 
   // ---- key-side rows (k then v), staged head-major ----
   if (p.do16 != nullptr) {
-    const int64_t nk = (int64_t)p.B * p.Sk * p.Hk;
-    for (int64_t r0 = warp0 * RPW; r0 < 2 * nk; r0 += nwarps * RPW) {
-      const int64_t rr = r0 + sub;
-      if (rr >= 2 * nk) continue;
-      const bool is_v = rr >= nk;
-      const int64_t row = is_v ? rr - nk : rr;
-      const int g = (int)(row % p.Hk);
-      const int j = (int)((row / p.Hk) % p.Sk);
-      const int b = (int)(row / ((int64_t)p.Hk * p.Sk));
-      const bf16* src = is_v ? p.v + b * p.v0 + j * p.v1 + g * p.v2
-                             : p.k + b * p.k0 + j * p.k1 + g * p.k2;
-      __half* dst = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk + j) * D;
+    const int64_t nk = (int64_t)p.B * ((p.Sk + kIB - 1) / kIB) * kIB * p.Hk;
+    for (int64_t r0 = warp0 * RPW * U; r0 < 2 * nk; r0 += nwarps * RPW * U) {
+      uint4 f[U][CPL];
+      int64_t rows[U];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const int e0 = (cl + c * LPR) * 8;
-        float f[8];
-        load8(src + e0, f);
-        if (store8_half(dst + e0, f)) range_bits |= is_v ? 4 : 2;
+      for (int u = 0; u < U; ++u) {
+        rows[u] = r0 + u * RPW + sub;
+        const bool is_v = rows[u] >= nk;
+        int g, j, b;
+        decompose(is_v ? rows[u] - nk : rows[u], p.Hk, p.Sk, &b, &g, &j);
+        if (rows[u] < 2 * nk && j < p.Sk) {
+          const bf16* src = is_v ? p.v + b * p.v0 + j * p.v1 + g * p.v2
+                                 : p.k + b * p.k0 + j * p.k1 + g * p.k2;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src + (cl + c * LPR) * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool is_v = rows[u] >= nk;
+        int g, j, b;
+        decompose(is_v ? rows[u] - nk : rows[u], p.Hk, p.Sk, &b, &g, &j);
+        if (rows[u] >= 2 * nk || j >= p.Sk) continue;
+        __half* dst = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk + j) * D;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          float x[8];
+          unpack8(f[u][c], x);
+          if (store8_half(dst + (cl + c * LPR) * 8, x)) range_bits |= is_v ? 4 : 2;
+        }
       }
     }
   }
@@ -219,7 +268,7 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = (unsigned)(sms * 8 < kPreMaxBlocks ? sms * 8 : kPreMaxBlocks);
+  const unsigned grid = (unsigned)(sms * 4 < kPreMaxBlocks ? sms * 4 : kPreMaxBlocks);
   switch (pr.D) {
     case 64: preprocess_kernel<64><<<grid, kThreads, 0, stream>>>(p); break;
     case 128: preprocess_kernel<128><<<grid, kThreads, 0, stream>>>(p); break;
