@@ -89,6 +89,9 @@ def _load():
     L.attn_bwd_noalloc.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp, vp, P(ctypes.c_int32)]
     L.attn_bwd_noalloc.restype = st
+    L.attn_mask_tile_classes.argtypes = [P(Mask), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, vp]
+    L.attn_mask_tile_classes.restype = st
     return L
 
 
@@ -216,6 +219,16 @@ def attn_bwd_noalloc(prob, mask, sparse, q, k, v, o, do, lse, bias, delta, dq, d
                                 status),
            "attn_bwd_noalloc")
     return (int(status[0]), int(status[1])) if read_status else None
+
+
+def attn_mask_tile_classes(mask: Optional[Mask], Sq: int, Sk: int, tile_q: int = 128,
+                           tile_k: int = 128):
+    """Host-side tile classes (0 empty, 1 partial, 2 full) as a nested list."""
+    nmt, nnt = -(-Sq // tile_q), -(-Sk // tile_k)
+    buf = (ctypes.c_int8 * (nmt * nnt))()
+    _check(lib.attn_mask_tile_classes(_ref(mask), Sq, Sk, tile_q, tile_k, buf),
+           "attn_mask_tile_classes")
+    return [[buf[m * nnt + n] for n in range(nnt)] for m in range(nmt)]
 
 
 def attn_read_device_status(workspace, stream=None):

@@ -144,6 +144,28 @@ const char* attn_status_string(attn_status_t s) {
   return "ATTN_ERR_UNKNOWN";
 }
 
+attn_status_t attn_mask_tile_classes(const attn_mask_t* mask, int32_t Sq, int32_t Sk,
+                                     int32_t tile_q, int32_t tile_k, int8_t* out) {
+  if (Sq <= 0 || Sk <= 0 || tile_q <= 0 || tile_k <= 0 || out == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  MaskSpec m{-1, -1, 0};
+  if (mask != nullptr) {
+    if (mask->num_sink < 0) return ATTN_ERR_INVALID_ARG;
+    m = MaskSpec{mask->window_left < 0 ? -1 : mask->window_left,
+                 mask->window_right < 0 ? -1 : mask->window_right, mask->num_sink};
+  }
+  const int nmt = (Sq + tile_q - 1) / tile_q, nnt = (Sk + tile_k - 1) / tile_k;
+  for (int mt = 0; mt < nmt; ++mt) {
+    const int m0 = mt * tile_q, m1 = m0 + tile_q < Sq ? m0 + tile_q : Sq;
+    for (int nt = 0; nt < nnt; ++nt) {
+      const int n0 = nt * tile_k, n1 = n0 + tile_k < Sk ? n0 + tile_k : Sk;
+      out[(int64_t)mt * nnt + nt] =
+          !tile_any(m, m0, m1, n0, n1) ? 0 : (tile_full(m, m0, m1, n0, n1) ? 2 : 1);
+    }
+  }
+  return ATTN_OK;
+}
+
 int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
                       const attn_sparse_t* sparse) {
   Problem p;

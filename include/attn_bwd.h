@@ -203,6 +203,16 @@ attn_status_t attn_bwd_noalloc(const attn_problem_t* prob, const attn_mask_t* ma
                                float* dq, float* dk, float* dv, float* dbias,
                                cudaStream_t stream, int32_t* device_status);
 
+/* Tile classes of a mask ("22_sink_tokens_fmha.py" mask builders applied to
+ * tiles): out[mt * ceil(Sk / tile_k) + nt] = 0 if the tile rows
+ * [mt tile_q, ...) x keys [nt tile_k, ...) (clipped to Sq, Sk) hold no live
+ * entry, 2 if every entry is live, 1 otherwise. Host-only (the same
+ * classification the kernels use to skip tiles and to mask partial ones);
+ * out holds ceil(Sq / tile_q) * ceil(Sk / tile_k) bytes. Returns
+ * ATTN_ERR_INVALID_ARG for non-positive sizes or a NULL out. */
+attn_status_t attn_mask_tile_classes(const attn_mask_t* mask, int32_t Sq, int32_t Sk,
+                                     int32_t tile_q, int32_t tile_k, int8_t* out);
+
 /* Which backward kernel attn_bwd would launch for these arguments:
  * 0 = none (invalid / unsupported), 1 = tcgen05 tensor-core kernel,
  * 2 = SIMT kernels. For tests and benchmarks. */

@@ -129,3 +129,28 @@ def test_sparse_descriptor_validation(ab):
 def test_read_status_rejects_null(ab):
     code = ab.lib.attn_read_device_status(None, None, None)
     assert code == 1
+
+
+@pytest.mark.parametrize("spec", [
+    # (Sq, Sk, window_left, window_right, num_sink, tile_q, tile_k)
+    (1024, 1024, -1, 0, 0, 128, 128),       # the causal benchmark workload
+    (8192, 8192, 1023, 0, 4, 128, 128),     # window 1024 + 4 sinks workload
+    (2048, 2048, -1, -1, 0, 128, 128),      # no mask
+    (640, 640, 127, 0, 4, 128, 128),
+    (200, 328, 40, 25, 3, 64, 32),          # ragged tails, two-sided window
+    (384, 128, 10, 0, 0, 128, 128),         # rows without live keys
+    (97, 61, -1, 0, 70, 16, 8),             # sinks beyond the diagonal
+])
+def test_tile_classes_match_oracle_mask(ab, spec):
+    # The kernels skip tiles classed 0 and mask tiles classed 1 per element;
+    # the classes must agree bit-exactly with the oracle's element mask.
+    import numpy as np
+    import oracle
+    Sq, Sk, wl, wr, ns, tq, tk = spec
+    m = oracle.live_mask(Sq, Sk, wl, wr, ns)
+    got = ab.attn_mask_tile_classes(ab.Mask(wl, wr, ns), Sq, Sk, tq, tk)
+    for mt, row in enumerate(got):
+        for nt, cls in enumerate(row):
+            tile = m[mt * tq:(mt + 1) * tq, nt * tk:(nt + 1) * tk]
+            expect = 0 if not tile.any() else (2 if tile.all() else 1)
+            assert cls == expect, (mt, nt, cls, expect)
