@@ -95,7 +95,9 @@ Sizes sizes_of(const Problem& p) {
 
 bool need(const void* ptr, int64_t count) { return count == 0 || ptr != nullptr; }
 
-bool use_tensor_cores(const Problem& p) { return !p.sparse && tc_supported(p); }
+bool use_tensor_cores(const Problem& p) {
+  return p.sparse ? tc_sparse_supported(p) : tc_supported(p);
+}
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
@@ -106,7 +108,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
   WorkspaceLayout w;
   size_t off = kStatusBytes;
-  if (tensor_core_path) {
+  if (tensor_core_path && p.sparse) {
+    const size_t kvbytes = (size_t)(p.n_ori + p.n_cmp) * p.Hk * p.D * sizeof(__half);
+    off = align_up(off, 1024);
+    w.kv16 = off;
+    off = align_up(off + kvbytes, 1024);
+    w.staged = true;
+  } else if (tensor_core_path) {
     const size_t qbytes = (size_t)p.B * p.Hq * p.Sq * p.D * sizeof(__half);
     const size_t kbytes = (size_t)p.B * p.Hk * p.Sk * p.D * sizeof(__half);
     off = align_up(off, 1024);
@@ -227,9 +235,11 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
     if (!aligned16(d_ori) || !aligned16(d_cmp)) return ATTN_ERR_INVALID_ARG;
   }
   const bool tc = use_tensor_cores(p);
-  if (tc && (!need(q, n.q) || !need(k, n.k) || !need(v, n.k) || !aligned16(q) ||
-             !aligned16(k) || !aligned16(v)))
+  if (tc && !p.sparse &&
+      (!need(q, n.q) || !need(k, n.k) || !need(v, n.k) || !aligned16(q) || !aligned16(k) ||
+       !aligned16(v)))
     return ATTN_ERR_INVALID_ARG;
+  if (tc && p.sparse && !need(sparse->ori_kv, n.ori)) return ATTN_ERR_INVALID_ARG;
   const WorkspaceLayout w = workspace_layout(p, tc);
   if (workspace == nullptr || workspace_bytes < w.total || !aligned16(workspace))
     return ATTN_ERR_WORKSPACE;
@@ -238,9 +248,13 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
   auto staged = [&](size_t off) {
     return w.staged ? reinterpret_cast<__half*>(ws + off) : nullptr;
   };
-  return cuda_status(launch_preprocess(p, q, k, v, o, dO, delta, dbias, d_ori, d_cmp,
-                                       staged(w.q16), staged(w.k16), staged(w.v16),
-                                       staged(w.do16), st, stream));
+  const bool dense_staged = w.staged && !p.sparse;
+  return cuda_status(launch_preprocess(
+      p, q, k, v, o, dO, delta, dbias, d_ori, d_cmp, dense_staged ? staged(w.q16) : nullptr,
+      dense_staged ? staged(w.k16) : nullptr, dense_staged ? staged(w.v16) : nullptr,
+      dense_staged ? staged(w.do16) : nullptr, p.sparse ? sparse->ori_kv : nullptr,
+      p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr, st,
+      stream));
 }
 
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
@@ -276,6 +290,11 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
     return ATTN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   DevStatus* st = reinterpret_cast<DevStatus*>(ws + w.status);
+  if (tc && p.sparse) {
+    const __half* kv16 = reinterpret_cast<const __half*>(ws + w.kv16);
+    return cuda_status(launch_bwd_sparse_tc(p, q, dO, kv16, sparse->cmp_idx, lse, delta, dq,
+                                            sparse->d_ori_kv, sparse->d_cmp_kv, st, stream));
+  }
   if (tc) {
     const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16);
     const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16);

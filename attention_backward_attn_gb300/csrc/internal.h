@@ -12,9 +12,11 @@ namespace attn {
 // Workspace layout: [DevStatus (256 B)] then, for the tensor-core path, fp16
 // copies of Q, dO [B, Hq, Sq, D] and K, V [B, Hk, Sk, D] (head-major rows),
 // each region aligned to 1 KiB.
+// The sparse tensor-core path stages one fp16 copy of the shared KV rows
+// [ori rows ; cmp rows] ([(n_ori + n_cmp) * Hk][D]) instead.
 struct WorkspaceLayout {
   size_t status = 0;
-  size_t q16 = 0, k16 = 0, v16 = 0, do16 = 0;
+  size_t q16 = 0, k16 = 0, v16 = 0, do16 = 0, kv16 = 0;
   size_t total = 0;
   bool staged = false;
 };
@@ -36,13 +38,15 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
 // ---- preprocess.cu ----
 // One fused kernel: clears the status record, zeroes dbias / the sparse dKV
 // buffers, computes delta, and (if do16 != nullptr) writes fp16
-// head-major copies of q, k, v and dO. An fp16 overflow sets bits (1 q, 2 k,
-// 4 v, 8 dO) in the block's flag slot after the status record; the
-// tensor-core backward ORs the slots and reports ATTN_ERR_RANGE.
+// head-major copies of q, k, v and dO, and (if kv16 != nullptr) the fp16
+// copy of the sparse shared KV rows. An fp16 overflow sets bits (1 q, 2 k or
+// shared KV, 4 v, 8 dO) in the block's flag slot after the status record;
+// the tensor-core backward ORs the slots and reports ATTN_ERR_RANGE.
 cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, const void* v,
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
-                              __half* v16, __half* do16, DevStatus* st, cudaStream_t stream);
+                              __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
+                              __half* kv16, DevStatus* st, cudaStream_t stream);
 
 // ---- tc_bwd.cu ----
 bool tc_supported(const Problem& p);
@@ -50,5 +54,12 @@ cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16
                           const __half* v16, const __half* do16, const float* lse,
                           const float* delta, const float* bias, float* dq, float* dk,
                           float* dv, float* dbias, DevStatus* st, cudaStream_t stream);
+
+// ---- tc_sparse.cu ----
+bool tc_sparse_supported(const Problem& p);
+cudaError_t launch_bwd_sparse_tc(const Problem& p, const void* q, const void* dO,
+                                 const __half* kv16, const int32_t* idx, const float* lse,
+                                 const float* delta, float* dq, float* d_ori, float* d_cmp,
+                                 DevStatus* st, cudaStream_t stream);
 
 }  // namespace attn

@@ -4,7 +4,8 @@
 // "sparse_flash_mla_grad" phase 2, SoftmaxGrad(dO, O)), computed in fp32 from
 // the bf16 rows. The same pass zeroes dbias / the sparse dKV buffers that the
 // backward accumulates into, clears the status record, and
-// for the tensor-core path writes fp16 head-major copies of q, k, v and dO.
+// for the tensor-core path writes fp16 head-major copies of q, k, v and dO
+// (dense) or one fp16 copy of the original and compressed KV rows (sparse).
 //
 // Why fp16 copies: the tensor-core backward feeds kind::f16 MMAs, and rounds
 // P and dS to fp16 (11 significant bits) instead of bf16 (8), which keeps the
@@ -41,6 +42,10 @@ struct PreParams {
   __half* k16;
   __half* v16;
   __half* do16;  // nullptr: no staging (SIMT path)
+  const bf16* ori;  // sparse shared KV: fp16 copy [ori rows ; cmp rows] into kv16
+  const bf16* cmp;
+  int64_t kv_ori_rows, kv_cmp_rows;
+  __half* kv16;     // nullptr: no KV staging
   float* zero_a;
   int64_t zero_na;
   float* zero_b;
@@ -215,6 +220,35 @@ preprocess_kernel(const PreParams p) {
     }
   }
 
+  // ---- sparse shared KV rows, staged as one fp16 [ori ; cmp] matrix ----
+  if (p.kv16 != nullptr) {
+    const int64_t nkv = p.kv_ori_rows + p.kv_cmp_rows;
+    for (int64_t r0 = warp0 * RPW * U; r0 < nkv; r0 += nwarps * RPW * U) {
+      uint4 f[U][CPL];
+      int64_t rows[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        rows[u] = r0 + u * RPW + sub;
+        if (rows[u] < nkv) {
+          const bf16* src = rows[u] < p.kv_ori_rows ? p.ori + rows[u] * D
+                                                    : p.cmp + (rows[u] - p.kv_ori_rows) * D;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src + (cl + c * LPR) * 8);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (rows[u] >= nkv) continue;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          float x[8];
+          unpack8(f[u][c], x);
+          if (store8_half(p.kv16 + rows[u] * D + (cl + c * LPR) * 8, x)) range_bits |= 2;
+        }
+      }
+    }
+  }
+
   // ---- buffers accumulated with atomics: dbias, sparse dKV ----
   zero_range(p.zero_a, p.zero_na, tid, nthreads);
   zero_range(p.zero_b, p.zero_nb, tid, nthreads);
@@ -235,7 +269,8 @@ preprocess_kernel(const PreParams p) {
 cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, const void* v,
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
-                              __half* v16, __half* do16, DevStatus* st, cudaStream_t stream) {
+                              __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
+                              __half* kv16, DevStatus* st, cudaStream_t stream) {
   PreParams p;
   p.B = pr.B;
   p.Hq = pr.Hq;
@@ -257,6 +292,11 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.k16 = k16;
   p.v16 = v16;
   p.do16 = do16;
+  p.ori = static_cast<const bf16*>(ori_kv);
+  p.cmp = static_cast<const bf16*>(cmp_kv);
+  p.kv_ori_rows = kv16 ? (int64_t)pr.n_ori * pr.Hk : 0;
+  p.kv_cmp_rows = kv16 && cmp_kv ? (int64_t)pr.n_cmp * pr.Hk : 0;
+  p.kv16 = kv16;
   p.zero_a = dbias;
   p.zero_na = dbias ? (int64_t)pr.Hq * pr.Sq * pr.Sk : 0;
   p.zero_b = d_ori;

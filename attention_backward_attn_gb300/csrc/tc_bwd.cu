@@ -47,6 +47,7 @@
 
 #include "internal.h"
 #include "tc_ptx.cuh"
+#include "tc_util.cuh"
 
 #include <mutex>
 
@@ -57,7 +58,6 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // key rows per tile
 constexpr int kThreads = 384;
 constexpr int kSlab = 128 * 128;  // one [128 rows][64 fp16] 128B-swizzled slab, bytes
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // Shared memory of a key-major CTA.
 template <int D>
@@ -121,44 +121,6 @@ struct TcParams {
   DevStatus* status;
 };
 
-struct Ctx {
-  uint32_t bars;        // shared address of barrier 0
-  volatile int* abort;  // CTA-wide abort flag
-  DevStatus* status;
-  __device__ uint32_t bar(int i) const { return bars + 8u * i; }
-};
-
-// Bounded mbarrier wait: true when the phase with `parity` completed; false
-// if the CTA aborted or ~2 s passed (then the abort flag is raised).
-__device__ __noinline__ bool wait_bar(const Ctx& c, int which, uint32_t parity, int where) {
-  const uint32_t bar = c.bar(which);
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((n & 31u) == 0) {
-      if (*c.abort) return false;
-      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
-        *c.abort = 1;
-        report(c.status, ATTN_ERR_DEVICE_TIMEOUT, where);
-        return false;
-      }
-    }
-  }
-}
-
-// Teardown wait: ignores the abort flag, still bounded.
-__device__ __noinline__ void drain_bar(const Ctx& c, int which, uint32_t parity) {
-  const uint32_t bar = c.bar(which);
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
-      report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 100 + which);
-      return;
-    }
-  }
-}
-
 // Bits [a, b) of a 32-bit mask, clipped to [0, 32).
 __device__ __forceinline__ uint32_t bits_between(int a, int b) {
   a = a < 0 ? 0 : a;
@@ -168,10 +130,6 @@ __device__ __forceinline__ uint32_t bits_between(int a, int b) {
   return below_b & ~((1u << a) - 1u);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // Live (query head, query tile) pairs of a key tile.
 struct QTileIter {
@@ -820,25 +778,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
 // ------------------------------------------------------------------ host --
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(f);
-  });
-  return fn;
-}
-
 // Row-major [rows][D] fp16 matrix, boxes of 128 rows x 64 columns, 128B swizzle.
 bool make_map(CUtensorMap* m, const __half* base, uint64_t rows, int D) {
   EncodeFn enc = encode_fn();
@@ -897,6 +836,20 @@ int cluster_size(int ratio) {
 }
 
 }  // namespace
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+  });
+  return fn;
+}
 
 bool tc_supported(const Problem& p) {
   return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0 &&

@@ -1,0 +1,591 @@
+// Tensor-core (tcgen05 / TMEM) backward of the selected-KV sparse attention
+// with one shared latent KV per KV head (Ascend "sparse_flash_mla_grad",
+// formula section, phases 1-3):
+//   selKv(i) = original rows in the window of query i, then the compressed
+//              rows listed in topk[i] (-1 = empty slot);  K = V = selKv;
+//   P = exp(scale Q selKv^T - LSE) (the given LSE);  dP = dO selKv^T;
+//   dS = P (dP - D) with D = rowsum(dO * O);  dQ = scale dS selKv;
+//   dKV = scale dS^T Q + P^T dO, added into the rows it was gathered from.
+//
+// One CTA per (query token i, KV head g). The r = 64 query heads of the KV
+// head and their 64 dO rows are stacked into one 128-row operand
+// X = [Q_i ; dO_i] (fp16, eight 128B-swizzled slabs of 64 columns), so S and
+// dP come out of one MMA and the thread that owns a selected row sees S and
+// dP of every head for it. The selected rows are processed in tiles of 128:
+//   MMA-A  [S^T | dP^T] = KV X^T     M = 128 rows, N = 128 (64 S + 64 dP), K = 512
+//   SFU    P^T = exp2(S^T scale log2e - LSE log2e), dS^T = P^T (dP^T - D);
+//          G = [scale dS^T | P^T] as fp16 in shared memory ([128 rows][128])
+//   MMA-B  dQ^T += KV^T (scale dS^T) M = 128 d (4 chunks), N = 64 heads, K = 128 rows
+//   MMA-C  dKV^T = X^T G             M = 128 d (4 chunks) x N = 64 rows (2 halves), K = 128
+//   drain  every dKV^T block: TMEM -> registers -> red.global.add.f32 into the
+//          original / compressed gradient rows (each warp instruction adds
+//          one 128-byte run of one row)
+// dQ^T accumulates in TMEM over all tiles of the token and is written once.
+// The dKV reductions (D fp32 per selected row and token, from every token
+// that selected the row) are the bulk of the memory traffic, so the drain
+// has two warpgroups and its own TMEM buffers: the next tile's MMA-A,
+// softmax and MMA-B run while the previous tile drains.
+//
+// KV rows come from an fp16 copy of [ori_kv ; cmp_kv] made by the pre-pass.
+// Two loader warps copy them with cp.async (16 bytes per thread, written in
+// the 128-byte swizzled layout the MMAs read) into a ring of 16 KB slots.
+// Every tile streams twice: 8 slots of [128 rows x 64 d] (K-major A of
+// MMA-A), then 8 slots of [64 rows x 128 d] (MN-major A of MMA-B: two
+// 64-column halves 8 KB apart); X takes 128 KB of shared memory, which leaves
+// no room to keep a whole [128 x 512] KV tile between the two.
+//
+// TMEM (512 columns): [0, 128) S^T|dP^T, [128, 192) and [192, 256) the two
+// dKV^T buffers, [256, 512) dQ^T (chunk c of 128 d at 256 + 64 c, one column
+// per head).
+//
+// Warp roles (512 threads): warp 0 builds the selected-row list and issues
+// the TMA copies of X; warp 1 owns TMEM and lane 0 issues the MMAs; warps 2-3
+// load KV rows; warps 4-15 convert X from bf16 to fp16 in place, then warps
+// 4-7 run the softmax (thread = selected row) and warps 8-11 / 12-15 drain
+// the two dKV^T buffers and write dQ (thread = column d). Every wait is
+// bounded (tc_util.cuh).
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+#include "tc_util.cuh"
+
+#include <math.h>
+
+#include <algorithm>
+
+namespace attn {
+namespace {
+
+constexpr int kSpThreads = 512;
+constexpr int kSpD = 512;         // head dim (latent KV width)
+constexpr int kSpR = 64;          // query heads per KV head
+constexpr int kSpMaxRows = 1024;  // selected rows per (token, KV head)
+constexpr int kSpSlots = 3;       // KV ring depth
+constexpr int kSpSlot = 16384;    // bytes per slot / per X or G slab
+constexpr int kSpConvThreads = 384;  // warps 4-15 convert X
+
+struct SpSmem {
+  static constexpr int X = 0;                          // 8 slabs: rows 0-63 Q, 64-127 dO
+  static constexpr int KV = X + 8 * kSpSlot;           // ring of kSpSlots slots
+  static constexpr int G = KV + kSpSlots * kSpSlot;    // slab 0 scale dS^T, slab 1 P^T
+  static constexpr int ROWS = G + 2 * kSpSlot;         // int32 row ids into the fp16 KV copy
+  static constexpr int LSE = ROWS + 4 * kSpMaxRows;    // 64 fp32: LSE log2e, +inf if not finite
+  static constexpr int DLT = LSE + 4 * kSpR;           // 64 fp32: D
+  static constexpr int BAR = DLT + 4 * kSpR;           // mbarriers
+  static constexpr int MISC = BAR + 256;               // TMEM base, abort flag, row count
+  static constexpr int TOTAL = MISC + 16;
+};
+static_assert(SpSmem::TOTAL <= 227 * 1024, "shared memory budget");
+
+// mbarriers; the dKV^T buffers b = 0, 1 hold the row halves nh = b of a tile.
+enum SpBar {
+  sXFull = 0,       // X landed (TMA transaction count)
+  sXReady = 1,      // X converted to fp16 (kSpConvThreads arrivals)
+  sKvFull0 = 2,     // ring slot filled (x3, 64 loader arrivals)
+  sKvEmpty0 = 5,    // ring slot consumed by its MMAs (x3)
+  sStFull = 8,      // S^T | dP^T of the tile in TMEM
+  sGFull = 9,       // G written, S^T | dP^T read (128 arrivals)
+  sGFree = 10,      // the MMAs of the tile stopped reading G
+  sDkvFull0 = 11,   // a dKV^T block is in buffer b (x2)
+  sDkvEmpty0 = 13,  // the drain has read buffer b (x2, 128 arrivals)
+  sDqFull = 15,     // dQ^T complete
+  sDone = 16,       // every MMA of the CTA completed (teardown)
+  kSpBars = 17
+};
+
+struct SpParams {
+  int Sq, Hq, Hk, n_ori, n_cmp, topk, wl, wr;
+  float scale;
+  float scale_log2;
+  const __half* kv16;  // [(n_ori + n_cmp) * Hk][512] fp16 copy of [ori_kv ; cmp_kv]
+  const int32_t* idx;  // [Sq][Hk][topk] or nullptr
+  const float* lse;    // [Hq][Sq]
+  const float* delta;  // [Hq][Sq]
+  float* dq;           // [Sq][Hq][512]
+  float* d_ori;        // [n_ori][Hk][512]
+  float* d_cmp;        // [n_cmp][Hk][512]
+  DevStatus* status;
+};
+
+// Selected rows of (token i, KV head g) as row ids of the fp16 copy
+// [ori rows ; cmp rows] viewed as [(n_ori + n_cmp) * Hk][512]: the window
+// first, then the valid top-k entries in slot order. Returns the count; the
+// list is padded to a multiple of 128 with its first entry (masked later).
+// Run by one full warp.
+__device__ int build_rows(const SpParams& p, int i, int g, int32_t* rows, int lane) {
+  const int pos = (p.n_ori - p.Sq) + i;
+  int lo = p.wl >= 0 ? pos - p.wl : 0;
+  int hi = p.wr >= 0 ? pos + p.wr : p.n_ori - 1;
+  lo = max(lo, 0);
+  hi = min(hi, p.n_ori - 1);
+  const int nwin = hi >= lo ? hi - lo + 1 : 0;
+  for (int j = lane; j < nwin; j += 32) rows[j] = (lo + j) * p.Hk + g;
+  int n = nwin;
+  if (p.idx != nullptr) {
+    const int32_t* ir = p.idx + ((int64_t)i * p.Hk + g) * p.topk;
+    bool bad = false;
+    for (int t0 = 0; t0 < p.topk; t0 += 32) {
+      const int t = t0 + lane;
+      const int cidx = t < p.topk ? __ldg(ir + t) : -1;
+      bad |= cidx < -1 || cidx >= p.n_cmp;
+      const bool ok = cidx >= 0 && cidx < p.n_cmp;
+      const uint32_t m = __ballot_sync(0xffffffffu, ok);
+      if (ok) rows[n + __popc(m & ((1u << lane) - 1u))] = (p.n_ori + cidx) * p.Hk + g;
+      n += __popc(m);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, ATTN_ERR_INDEX_OOB, i);
+  }
+  __syncwarp();
+  const int padded = (n + 127) / 128 * 128;
+  const int32_t first = n > 0 ? rows[0] : 0;
+  __syncwarp();
+  for (int j = n + lane; j < padded; j += 32) rows[j] = first;
+  return n;
+}
+
+// 8 bf16 -> 8 fp16 in place; returns the largest magnitude seen (a bf16
+// value overflows fp16 exactly when its magnitude is at least 65520).
+__device__ __forceinline__ float bf16x8_to_half(uint4* v, float amax) {
+  uint32_t w[4] = {v->x, v->y, v->z, v->w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float lo = __uint_as_float(w[t] << 16);
+    const float hi = __uint_as_float(w[t] & 0xffff0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+    w[t] = pack_half2(lo, hi);
+  }
+  *v = make_uint4(w[0], w[1], w[2], w[3]);
+  return amax;
+}
+
+__global__ void __launch_bounds__(kSpThreads, 1)
+attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmdO, const SpParams p) {
+  using L = SpSmem;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_u32(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 2);
+    return;
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = (int)(blockIdx.x % p.Hk);
+  const int i = p.Sq - 1 - (int)(blockIdx.x / p.Hk);  // later tokens select more rows: first
+
+  if (blockIdx.x == 0) {
+    // fp16 overflow found while staging the KV copy: OR of the pre-pass's
+    // per-block flag slots
+    const int nslots = min(max(p.status->reserved[1], 0), kPreMaxBlocks);
+    const int32_t* slots = reinterpret_cast<const int32_t*>(p.status + 1);
+    int bits = 0;
+    for (int s = threadIdx.x; s < nslots; s += blockDim.x) bits |= slots[s];
+    bits = __reduce_or_sync(0xffffffffu, bits);
+    if (bits && lane == 0) report(p.status, ATTN_ERR_RANGE, bits);
+  }
+
+  Ctx c;
+  c.bars = sbase + L::BAR;
+  c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+  c.status = p.status;
+  int32_t* rows = reinterpret_cast<int32_t*>(smem + L::ROWS);
+  float* lse_s = reinterpret_cast<float*>(smem + L::LSE);
+  float* dlt_s = reinterpret_cast<float*>(smem + L::DLT);
+  volatile int* nrows_s = reinterpret_cast<volatile int*>(smem + L::MISC + 8);
+
+  if (threadIdx.x == 0) {
+    uint32_t counts[kSpBars];
+    for (int b = 0; b < kSpBars; ++b) counts[b] = 1;
+    counts[sXReady] = kSpConvThreads;
+    for (int s = 0; s < kSpSlots; ++s) counts[sKvFull0 + s] = 64;
+    counts[sGFull] = 128;
+    counts[sDkvEmpty0] = counts[sDkvEmpty0 + 1] = 128;
+    for (int b = 0; b < kSpBars; ++b) ptx::mbar_init(c.bar(b), counts[b]);
+    *c.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmdO);
+  }
+  if (warp == 0) {
+    const int n = build_rows(p, i, g, rows, lane);
+    if (lane == 0) *nrows_s = n;
+  } else if (warp == 1) {
+    ptx::tmem_alloc(sbase + L::MISC, 512);
+    ptx::tmem_relinquish();
+  } else if (warp == 2) {
+    for (int h = lane; h < kSpR; h += 32) {
+      const int64_t r = (int64_t)(g * kSpR + h) * p.Sq + i;
+      const float lv = p.lse[r];
+      lse_s[h] = isfinite(lv) ? lv * kLog2e : INFINITY;  // +inf: P = 0 for the head
+      dlt_s[h] = p.delta[r];
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
+  const int N = *nrows_s;
+  const int T = (N + 127) / 128;
+  const uint32_t sX = sbase + L::X, sKV = sbase + L::KV, sG = sbase + L::G;
+
+  if (warp == 0) {
+    // --------------------------------------------------- X: TMA copies --
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(c.bar(sXFull), 8 * kSpSlot);
+      for (int s = 0; s < 8; ++s) {
+        ptx::tma_load_3d(sX + s * kSpSlot, &tmQ, c.bar(sXFull), 64 * s, g * kSpR, i);
+        ptx::tma_load_3d(sX + s * kSpSlot + kSpSlot / 2, &tmdO, c.bar(sXFull), 64 * s, g * kSpR,
+                         i);
+      }
+      drain_bar(c, sXFull, 0);  // in flight until it lands, whatever else happens
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      bool ok = wait_bar(c, sXReady, 0, 40);
+      ptx::tc_fence_after();
+      constexpr uint32_t idA = ptx::idesc_f16_f32(128, 128, false, false);
+      constexpr uint32_t idB = ptx::idesc_f16_f32(128, 64, true, true);
+      constexpr uint32_t idC = ptx::idesc_f16_f32(128, 64, true, false);
+      const uint32_t tS = tmem, tQ = tmem + 256;
+      int slot = 0;
+      uint32_t ph = 0;
+      int issued[2] = {0, 0}, freed[2] = {0, 0};
+      // MMA-A of tile t: [S^T | dP^T] = KV X^T over the 8 column slabs
+      auto mma_a = [&]() {
+        for (int s = 0; s < 8 && ok; ++s) {
+          if (!wait_bar(c, sKvFull0 + slot, ph, 42)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a0 = sKV + slot * kSpSlot, b0 = sX + s * kSpSlot;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            ptx::mma_ss(tS, ptx::smem_desc_sw128(a0 + 32 * k, 16, 1024),
+                        ptx::smem_desc_sw128(b0 + 32 * k, 16, 1024), idA, (s | k) != 0);
+          ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+          if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+        }
+        if (ok) ptx::mma_commit(c.bar(sStFull));
+      };
+      if (T > 0) mma_a();
+      for (int t = 0; t < T && ok; ++t) {
+        // MMA-B: dQ^T += KV^T (scale dS^T), 16 selected rows per K step
+        if (!wait_bar(c, sGFull, (uint32_t)t & 1u, 43)) { ok = false; break; }
+        ptx::tc_fence_after();
+        for (int cc = 0; cc < 4 && ok; ++cc) {
+          for (int nh = 0; nh < 2 && ok; ++nh) {
+            if (!wait_bar(c, sKvFull0 + slot, ph, 44)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t a0 = sKV + slot * kSpSlot;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::mma_ss(tQ + 64 * cc, ptx::smem_desc_sw128(a0 + 2048 * k, kSpSlot / 2, 1024),
+                          ptx::smem_desc_sw128(sG + (64 * nh + 16 * k) * 128, kSpSlot, 1024), idB,
+                          (t | nh | k) != 0);
+            ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+            if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+          }
+        }
+        if (!ok) break;
+        // the softmax has read S^T | dP^T of tile t (sGFull): tile t + 1 may start
+        if (t + 1 < T) mma_a();
+        if (!ok) break;
+        // MMA-C: dKV^T blocks (d chunk cc, row half nh) into buffer nh
+        for (int h = 0; h < 8 && ok; ++h) {
+          const int cc = h >> 1, b = h & 1;
+          while (ok && freed[b] < issued[b]) {
+            ok = wait_bar(c, sDkvEmpty0 + b, (uint32_t)freed[b] & 1u, 45);
+            ++freed[b];
+          }
+          if (!ok) break;
+          const uint32_t a0 = sX + 2 * cc * kSpSlot;
+          const uint32_t g0 = sG + 64 * b * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            ptx::mma_ss(tmem + 128 + 64 * b, ptx::smem_desc_sw128(a0 + 2048 * k, kSpSlot, 1024),
+                        ptx::smem_desc_sw128(g0 + (k >> 2) * kSpSlot + (k & 3) * 32, 16, 1024),
+                        idC, k != 0);
+          ptx::mma_commit(c.bar(sDkvFull0 + b));
+          ++issued[b];
+        }
+        if (ok) ptx::mma_commit(c.bar(sGFree));
+      }
+      if (ok && T > 0) ptx::mma_commit(c.bar(sDqFull));
+      ptx::mma_commit(c.bar(sDone));  // completes once every MMA above has
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------- KV rows: cp.async loaders --
+    // Thread tl owns rows r0 + 8 k (k < 16) of every tile and the 16-byte
+    // chunk c8 of each 128-byte row segment; (r0 + 8 k) & 7 == r0, so the
+    // 128B-swizzle position of its chunk is the same for all of them.
+    const int tl = (int)threadIdx.x - 64;
+    const int c8 = tl & 7, r0 = tl >> 3;
+    const uint32_t swz = (uint32_t)((c8 ^ r0) << 4);
+    int slot = 0, pend = -1;
+    uint32_t ph = 0;
+    bool ok = true;
+    auto publish = [&](int next) {  // the previous fill is complete: make it visible
+      if (pend >= 0) {
+        ptx::cp_async_wait<1>();
+        ptx::fence_async_shared();
+        ptx::mbar_arrive(c.bar(sKvFull0 + pend));
+      }
+      pend = next;
+    };
+    for (int t = 0; t < T && ok; ++t) {
+      const __half* src[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        src[k] = p.kv16 + (int64_t)rows[128 * t + r0 + 8 * k] * kSpD + 8 * c8;
+      for (int s = 0; s < 8; ++s) {  // pass 1: [128 rows][64 d], columns 64 s
+        if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 31)) { ok = false; break; }
+        const uint32_t dst = sKV + slot * kSpSlot + swz;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) ptx::cp_async_16(dst + (r0 + 8 * k) * 128, src[k] + 64 * s);
+        ptx::cp_async_commit();
+        publish(slot);
+        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      }
+      for (int h = 0; h < 8 && ok; ++h) {  // pass 2: [64 rows][128 d] as two [64][64] halves
+        const int cc = h >> 1, nh = h & 1;
+        if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 32)) { ok = false; break; }
+        const uint32_t dst = sKV + slot * kSpSlot + swz;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const __half* sp = src[8 * nh + kk] + 128 * cc;
+          ptx::cp_async_16(dst + (r0 + 8 * kk) * 128, sp);
+          ptx::cp_async_16(dst + kSpSlot / 2 + (r0 + 8 * kk) * 128, sp + 64);
+        }
+        ptx::cp_async_commit();
+        publish(slot);
+        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait<0>();
+    if (pend >= 0) {
+      ptx::fence_async_shared();
+      ptx::mbar_arrive(c.bar(sKvFull0 + pend));
+    }
+  } else {
+    // ------------------------------------------- X: bf16 -> fp16 in place --
+    {
+      const bool ok = wait_bar(c, sXFull, 0, 50);
+      float amax = 0.f;
+      if (ok) {
+        // 8192 16-byte chunks over 384 threads; 4 loads in flight per thread
+        constexpr int kChunks = 8 * kSpSlot / 16;
+        for (int e0 = (int)threadIdx.x - 128; e0 < kChunks; e0 += 4 * kSpConvThreads) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e0 + u * kSpConvThreads < kChunks)
+              v[u] = ptx::ld_shared_v4_u32(sX + 16 * (e0 + u * kSpConvThreads));
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e0 + u * kSpConvThreads < kChunks) {
+              amax = bf16x8_to_half(&v[u], amax);
+              ptx::st_shared_v4(sX + 16 * (e0 + u * kSpConvThreads), v[u].x, v[u].y, v[u].z,
+                                v[u].w);
+            }
+        }
+      }
+      if (__any_sync(0xffffffffu, amax >= 65520.f) && lane == 0)
+        report(p.status, ATTN_ERR_RANGE, 16);
+      ptx::fence_async_shared();
+      ptx::mbar_arrive(c.bar(sXReady));
+    }
+    const int q4 = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    if (warp < 8) {
+      // ------------------------------------- softmax: thread = selected row --
+      const int n = 32 * q4 + lane;
+      const uint32_t grow = sG + n * 128;
+      const uint32_t sw = (uint32_t)(n & 7);
+      for (int t = 0; t < T; ++t) {
+        if (!wait_bar(c, sStFull, (uint32_t)t & 1u, 60)) break;
+        ptx::tc_fence_after();
+        const bool valid = 128 * t + n < N;
+        uint32_t pk[32], dk[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sv[32], dv[32];
+          ptx::tmem_ld32(tmem + lane_off + 32 * half, sv);
+          ptx::tmem_ld32(tmem + lane_off + 64 + 32 * half, dv);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int h = 32 * half + j;
+            float pr[2], ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float e = fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -lse_s[h + u]);
+              pr[u] = valid ? ptx::ex2(e) : 0.f;
+              ds[u] = pr[u] * (__uint_as_float(dv[j + u]) - dlt_s[h + u]) * p.scale;
+            }
+            pk[h / 2] = pack_half2(pr[0], pr[1]);
+            dk[h / 2] = pack_half2(ds[0], ds[1]);
+          }
+        }
+        ptx::tc_fence_before();
+        // G of the previous tile must be out of use
+        if (t > 0 && !wait_bar(c, sGFree, (uint32_t)(t - 1) & 1u, 61)) break;
+        // head h lives in 16-byte chunk h / 8 of the row (slab 0 dS, slab 1 P)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t off = (((uint32_t)q) ^ sw) * 16u;
+          ptx::st_shared_v4(grow + off, dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+          ptx::st_shared_v4(grow + kSpSlot + off, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                            pk[4 * q + 3]);
+        }
+        ptx::fence_async_shared();
+        ptx::mbar_arrive(c.bar(sGFull));
+      }
+    } else {
+      // ------------------------ dKV^T drain and dQ: thread = column d --
+      const int b = warp < 12 ? 0 : 1;  // buffer / row half of this warpgroup
+      const int dl = 32 * q4 + lane;
+      const int ori_rows = p.n_ori * p.Hk;
+      const uint32_t tbuf = tmem + 128 + 64 * b + lane_off;
+      bool ok = true;
+      int used = 0;
+      for (int t = 0; t < T && ok; ++t) {
+        const int nt = min(64, N - 128 * t - 64 * b);  // valid rows of this half (may be <= 0)
+        const uint32_t rt_s = sbase + L::ROWS + 512 * t + 256 * b;
+        for (int cc = 0; cc < 4; ++cc) {
+          if (!wait_bar(c, sDkvFull0 + b, (uint32_t)used & 1u, 70)) { ok = false; break; }
+          ++used;
+          ptx::tc_fence_after();
+          uint32_t v[64];
+          ptx::tmem_ld32(tbuf, v);
+          ptx::tmem_ld32(tbuf + 32, v + 32);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(c.bar(sDkvEmpty0 + b));
+          float* const ori_base = p.d_ori + 128 * cc + dl;
+          float* const cmp_base = p.d_cmp - (int64_t)ori_rows * kSpD + 128 * cc + dl;
+#pragma unroll
+          for (int n0 = 0; n0 < 64; n0 += 8) {
+            if (n0 < nt) {
+              const int4 ra = ptx::ld_shared_v4_s32(rt_s + 4 * n0);
+              const int4 rb = ptx::ld_shared_v4_s32(rt_s + 4 * n0 + 16);
+              const int r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                if (n0 + u < nt) {
+                  float* const base = r8[u] < ori_rows ? ori_base : cmp_base;
+                  ptx::red_add_f32_stream(base + (int64_t)r8[u] * kSpD,
+                                          __uint_as_float(v[n0 + u]));
+                }
+              }
+            }
+          }
+        }
+      }
+      if (ok) {
+        // dQ: this warpgroup writes d chunks 2 b and 2 b + 1
+        float* dq = p.dq + ((int64_t)i * p.Hq + g * kSpR) * kSpD;
+        if (T == 0) {
+          for (int h = 0; h < kSpR; ++h)
+#pragma unroll
+            for (int cc = 2 * b; cc < 2 * b + 2; ++cc) dq[h * kSpD + 128 * cc + dl] = 0.f;
+        } else if (wait_bar(c, sDqFull, 0, 71)) {
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int cc = 2 * b; cc < 2 * b + 2; ++cc) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t v[32];
+              ptx::tmem_ld32(tmem + lane_off + 256 + 64 * cc + 32 * half, v);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                dq[(32 * half + j) * kSpD + 128 * cc + dl] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (lane == 0) drain_bar(c, sDone, 0);
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+// [Sq][H][512] bf16 rows with element strides (token, head): 3-D map, boxes
+// of 64 heads x 64 columns, 128B swizzle.
+bool make_qmap(CUtensorMap* m, const void* base, int Sq, int H, int64_t s_tok, int64_t s_head) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kSpD, (cuuint64_t)H, (cuuint64_t)Sq};
+  cuuint64_t strides[2] = {(cuuint64_t)s_head * 2, (cuuint64_t)s_tok * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kSpR, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t max_selected_rows(const Problem& p) {
+  const int64_t win = (p.ori_wl >= 0 && p.ori_wr >= 0)
+                          ? std::min<int64_t>(p.n_ori, (int64_t)p.ori_wl + p.ori_wr + 1)
+                          : p.n_ori;
+  return win + (p.n_cmp > 0 ? p.topk : 0);
+}
+
+}  // namespace
+
+bool tc_sparse_supported(const Problem& p) {
+  return p.sparse && p.D == kSpD && p.B == 1 && p.Hq == kSpR * p.Hk && p.Sq > 0 && p.n_ori > 0 &&
+         max_selected_rows(p) <= kSpMaxRows &&
+         (int64_t)(p.n_ori + p.n_cmp) * p.Hk < (int64_t(1) << 31) && p.qs[1] > 0 &&
+         p.qs[2] > 0 && p.dos[1] > 0 && p.dos[2] > 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* dO,
+                                 const __half* kv16, const int32_t* idx, const float* lse,
+                                 const float* delta, float* dq, float* d_ori, float* d_cmp,
+                                 DevStatus* st, cudaStream_t stream) {
+  CUtensorMap mq, mdo;
+  if (!make_qmap(&mq, q, pr.Sq, pr.Hq, pr.qs[1], pr.qs[2]) ||
+      !make_qmap(&mdo, dO, pr.Sq, pr.Hq, pr.dos[1], pr.dos[2]))
+    return cudaErrorInvalidValue;
+  SpParams p;
+  p.Sq = pr.Sq;
+  p.Hq = pr.Hq;
+  p.Hk = pr.Hk;
+  p.n_ori = pr.n_ori;
+  p.n_cmp = pr.n_cmp;
+  p.topk = pr.topk;
+  p.wl = pr.ori_wl;
+  p.wr = pr.ori_wr;
+  p.scale = pr.scale;
+  p.scale_log2 = pr.scale * kLog2e;
+  p.kv16 = kv16;
+  p.idx = pr.n_cmp > 0 ? idx : nullptr;
+  p.lse = lse;
+  p.delta = delta;
+  p.dq = dq;
+  p.d_ori = d_ori;
+  p.d_cmp = d_cmp;
+  p.status = st;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_sparse_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SpSmem::TOTAL);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = (unsigned)pr.Sq * pr.Hk;
+  attn_bwd_sparse_tc_kernel<<<grid, kSpThreads, SpSmem::TOTAL, stream>>>(mq, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -171,10 +171,34 @@ SMALL_SPARSE = {
 }
 
 
-def _run_sparse(w):
+# Shapes of the tensor-core sparse path (64 query heads per KV head, D = 512).
+TC_SPARSE = {
+    # at most one ragged 128-row tile per token: window then compressed rows
+    "tc_scfa_s200_h64": lambda: make_sparse("t1", 41, Sq=200, Hq=64, Hk=1, D=512, n_ori=200,
+                                            n_cmp=50, topk=40, cmp_ratio=4, ori_win_left=127),
+    # two KV heads, a right window, queries offset by delta_s = 28
+    "tc_scfa_hk2_delta": lambda: make_sparse("t2", 42, Sq=72, Hq=128, Hk=2, D=512, n_ori=100,
+                                             n_cmp=30, topk=24, cmp_ratio=4, ori_win_left=20,
+                                             ori_win_right=3),
+    # window only, no compressed KV
+    "tc_swa_s160_h64": lambda: make_sparse("t3", 43, Sq=160, Hq=64, Hk=1, D=512, n_ori=160,
+                                           n_cmp=0, topk=0, cmp_ratio=1, ori_win_left=63,
+                                           with_cmp=False),
+    # 500 selected rows per token: four tiles, the last one ragged
+    "tc_scfa_rows500": lambda: make_sparse("t4", 44, Sq=96, Hq=64, Hk=1, D=512, n_ori=1000,
+                                           n_cmp=250, topk=200, cmp_ratio=4, ori_win_left=299),
+    # n_ori < Sq: the first 36 tokens select no row at all (dQ = 0, LSE = -inf)
+    "tc_scfa_empty_rows": lambda: make_sparse("t5", 45, Sq=100, Hq=64, Hk=1, D=512, n_ori=64,
+                                              n_cmp=16, topk=8, cmp_ratio=4, ori_win_left=15),
+}
+
+
+def _run_sparse(w, expect_path=None):
     torch = _torch()
     O_b, L_f, _, _ = H.sparse_forward_inputs(w)
     plan = H.gpu_sparse_plan(w, O_b, L_f)
+    if expect_path is not None:
+        assert plan.path == expect_path
     plan.run()
     torch.cuda.synchronize()
     code, detail = plan.device_status()
@@ -185,12 +209,58 @@ def _run_sparse(w):
 @pytest.mark.parametrize("name", list(SMALL_SPARSE))
 def test_sparse_small(name):
     w = SMALL_SPARSE[name]()
-    plan, O_b, L_f = _run_sparse(w)
+    plan, O_b, L_f = _run_sparse(w, expect_path=2)
+    _compare_sparse(w, plan, O_b, L_f)
+
+
+def _compare_sparse(w, plan, O_b, L_f):
     ref = H.sparse_reference(w, O_b, L_f)
     H.check_close("dq", plan.dq.cpu().numpy()[0], ref["dq"])
     H.check_close("d_ori", plan.d_ori.cpu().numpy(), ref["d_ori"])
     if w.cmp_kv is not None:
         H.check_close("d_cmp", plan.d_cmp.cpu().numpy(), ref["d_cmp"])
+
+
+@pytest.mark.parametrize("name", list(TC_SPARSE))
+def test_sparse_tensor_core(name):
+    w = TC_SPARSE[name]()
+    plan, O_b, L_f = _run_sparse(w, expect_path=1)
+    _compare_sparse(w, plan, O_b, L_f)
+    if name == "tc_scfa_empty_rows":
+        assert np.all(plan.dq.cpu().numpy()[0, :36] == 0)
+
+
+def test_sparse_tensor_core_bad_index_is_reported():
+    torch = _torch()
+    w = TC_SPARSE["tc_scfa_s200_h64"]()
+    O_b, L_f, _, _ = H.sparse_forward_inputs(w)
+    w.cmp_idx = w.cmp_idx.copy()
+    w.cmp_idx[150, 0, 1] = -7  # neither a row nor the empty marker: skipped and reported
+    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 5 and detail == 150
+
+
+@pytest.mark.parametrize("where", ["ori_kv", "q"])
+def test_sparse_tensor_core_fp16_range_is_reported(where):
+    torch = _torch()
+    w = TC_SPARSE["tc_swa_s160_h64"]()
+    O_b, L_f, _, _ = H.sparse_forward_inputs(w)
+    if where == "ori_kv":
+        w.ori_kv = w.ori_kv.copy()
+        w.ori_kv[7, 0, 100] = 1.0e5  # representable in bf16, not in fp16
+    else:
+        w.q = w.q.copy()
+        w.q[9, 3, 200] = -1.0e5
+    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 6 and detail & (2 if where == "ori_kv" else 16)
 
 
 def test_sparse_bad_index_is_reported_not_trapped():
@@ -200,6 +270,7 @@ def test_sparse_bad_index_is_reported_not_trapped():
     w.cmp_idx = w.cmp_idx.copy()
     w.cmp_idx[200, 0, 0] = w.n_cmp + 5  # out of range: must be skipped and reported
     plan = H.gpu_sparse_plan(w, O_b, L_f)
+    assert plan.path == 2
     plan.run()
     torch.cuda.synchronize()
     code, detail = plan.device_status()
@@ -257,8 +328,5 @@ def test_full_gqa4_window1024_sink4_s8192_d128():
 
 def test_full_sparse_scfa_s4096_h64_d512():
     w = make_workload("sparse_scfa_s4096_h64_d512")
-    plan, O_b, L_f = _run_sparse(w)
-    ref = H.sparse_reference(w, O_b, L_f)
-    H.check_close("dq", plan.dq.cpu().numpy()[0], ref["dq"])
-    H.check_close("d_ori", plan.d_ori.cpu().numpy(), ref["d_ori"])
-    H.check_close("d_cmp", plan.d_cmp.cpu().numpy(), ref["d_cmp"])
+    plan, O_b, L_f = _run_sparse(w, expect_path=1)
+    _compare_sparse(w, plan, O_b, L_f)
