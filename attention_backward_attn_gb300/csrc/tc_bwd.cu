@@ -11,18 +11,22 @@
 // accumulators in TMEM; fully masked tiles are skipped and partial tiles get
 // a per-element mask):
 //
-// Key-major CTAs (dK, dV, dbias). A cluster of cs CTAs owns one 128-row key
-// tile of one (batch, KV head); CTA `rank` takes r / cs of the r query heads
-// that share the KV head and loops over their live query tiles. The cs partial
-// dK / dV tiles are summed through distributed shared memory at the end, so
-// the GQA group reduction never leaves the chip. Per tile, so that one thread
-// owns one key row of the softmax:
+// Key-major CTAs (dK, dV, dbias). cs CTAs share one 128-row key tile of one
+// (batch, KV head); CTA `rank` takes r / cs of the r query heads that share
+// the KV head and loops over their live query tiles, accumulating its partial
+// dK / dV in TMEM over the group. At the end each CTA adds its partial rows
+// into dK / dV with TMA bulk reductions (the buffers are zeroed before the
+// launch when cs > 1), so no post-pass over per-head gradients exists. Per
+// tile, so that one thread owns one key row of the softmax:
 //   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
 //   MMA2  dP^T = V  dO^T
-//   SFU   P^T = exp2(S^T scale log2e + bias log2e - LSE log2e), dS^T = P^T (dP^T - D)
-//         P^T fp16 back into TMEM (A operand of MMA3), dS^T fp16 into SMEM
-//   MMA3  dV += P^T dO       (A = P^T in TMEM, B = dO MN-major)
-//   MMA4  dK += dS^T Q       (A = dS^T K-major, B = Q MN-major)
+//   SFU   phase 1: P^T = exp2(S^T scale log2e + bias log2e - LSE log2e),
+//                  fp16 into SMEM (A operand of MMA3)
+//         phase 2: dS^T = P^T (dP^T - D), fp16 into TMEM over dP^T (A of MMA4)
+//   MMA3  dV += P^T dO       (A = P^T K-major, B = dO MN-major)
+//   MMA4  dK += dS^T Q       (A = dS^T in TMEM, B = Q MN-major)
+// Issue order dV(t), S(t+1), dK(t), dP(t+1): phase 1 of the next tile runs
+// while dK(t) and dP(t+1) are on the tensor pipe.
 //
 // Query-major CTAs (dQ): one CTA per (batch, query head, 128-row query tile)
 // loops over the live key tiles of its KV head, recomputing S and dP:
@@ -38,8 +42,7 @@
 // owner, warps 4-7 and 8-11 two softmax warpgroups (columns 0-63 / 64-127 of
 // the tile), which also run the epilogue. Every mbarrier wait is bounded:
 // after ~2 s it records ATTN_ERR_DEVICE_TIMEOUT, raises a CTA-wide abort
-// flag, and the CTA drains its copies / MMAs, frees TMEM and exits through
-// the same cluster barriers.
+// flag, and the CTA drains its copies / MMAs, frees TMEM and exits.
 //
 // Operands are fp16 (exact copies of the bf16 inputs, staged by the
 // pre-pass): P and dS rounded to fp16 keep 3 more mantissa bits than bf16,
@@ -67,13 +70,13 @@ struct SmemKV {
   static constexpr int V = K + kTile;
   static constexpr int Q = V + kTile;        // 2 stages
   static constexpr int dO = Q + 2 * kTile;   // 2 stages
-  static constexpr int dS = dO + 2 * kTile;  // [128 keys][128 queries] fp16, 2 slabs
+  static constexpr int dS = dO + 2 * kTile;  // P^T: [128 keys][128 queries] fp16, 2 slabs
   static constexpr int LSE = dS + 2 * kSlab; // 2 stages x 128 fp32
   static constexpr int DLT = LSE + 1024;     // 2 stages x 128 fp32
   static constexpr int BAR = DLT + 1024;     // mbarriers
   static constexpr int MISC = BAR + 128;     // TMEM base, abort flag
   static constexpr int TOTAL = MISC + 16;
-  // end-of-kernel staging of dK / dV for the cluster reduction (reuses Q..dS)
+  // end-of-kernel staging of dK / dV rows for the bulk reductions (reuses Q..dS)
   static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
   static constexpr int STAGE = Q;
   static_assert(2 * 128 * kStageRow <= 4 * kTile + 2 * kSlab, "staging fits");
@@ -98,15 +101,19 @@ constexpr int smem_total() {
 }
 
 // barrier indices, key-major CTA
-enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kPFull = 6, kAccFull = 7,
-             kMma3 = 8 };
+// kSFull / kdPFull: S^T / dP^T of the tile in TMEM; kP1Full: P^T in shared
+// memory, S^T read (256 arrivals); kP2Full: dS^T written over dP^T in TMEM
+// (256 arrivals); kMma3: dV of the tile done (the P^T buffer is free again);
+// kMma4: dK of the tile done (the dP^T columns are free again).
+enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kP1Full = 6, kAccFull = 7,
+             kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kKvBars = 12 };
 // barrier indices, query-major CTA
 enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, qAccFull = 7,
             qMma3 = 8 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
-  int cs;          // CTAs per cluster (query-head split of the key-major CTAs)
+  int cs;          // key-major CTAs per key tile (query-head split)
   int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
   float scale;
   float scale_log2;
@@ -201,8 +208,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, 256, 1, 1};
-  init_common(c, sbase + L::MISC, 9, counts, warp);
+  const uint32_t counts[kKvBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1, 256, 1};
+  init_common(c, sbase + L::MISC, kKvBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
@@ -272,6 +279,10 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
                       ptx::smem_desc_sw128(sdO + off, 16, 1024), id_S, s > 0);
         }
       };
+      // Per tile t: dV(t) as soon as P^T(t) is in shared memory, then S(t+1)
+      // (the softmax has read S^T(t)); dK(t) once dS^T(t) replaced dP^T(t) in
+      // TMEM, then dP(t+1) after dK(t) released those columns. The softmax of
+      // tile t+1 overlaps dV(t), dK(t) and dP(t+1).
       bool ok = wait_bar(c, kKvFull, 0, 2);
       QTileIter it(hpc, nmt, n0, p.mask);
       bool have = ok && it.next();
@@ -280,8 +291,9 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         if (have) {
           ptx::tc_fence_after();
           issue_S(0);
-          issue_dP(0);
           ptx::mma_commit(c.bar(kSFull));
+          issue_dP(0);
+          ptx::mma_commit(c.bar(kdPFull));
         }
       }
       int t = 0;
@@ -289,37 +301,51 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         const int st = t & 1;
         const uint32_t sQ = sbase + L::Q + st * L::kTile;
         const uint32_t sdO = sbase + L::dO + st * L::kTile;
-        if (!wait_bar(c, kPFull, t & 1, 4)) break;
+        if (!wait_bar(c, kP1Full, t & 1, 4)) break;
         ptx::tc_fence_after();
-        // MMA3 dV += P^T dO : A = P^T (TMEM fp16 pairs), B = dO MN-major over d
-#pragma unroll
-        for (int s = 0; s < BM / 16; ++s) {
-          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_dV, a_col, ptx::smem_desc_sw128(sdO + s * 2048, kSlab, 1024), id_KV,
-                      (t > 0 || s > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(c.bar(kMma3));
-        // MMA4 dK += dS^T Q : A = dS^T K-major over queries, B = Q MN-major over d
+        // MMA3 dV += P^T dO : A = P^T K-major over queries, B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dK, ptx::smem_desc_sw128(sDS + off, 16, 1024),
-                      ptx::smem_desc_sw128(sQ + s * 2048, kSlab, 1024), id_KV,
+          ptx::mma_ss(t_dV, ptx::smem_desc_sw128(sDS + off, 16, 1024),
+                      ptx::smem_desc_sw128(sdO + s * 2048, kSlab, 1024), id_KV,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
-        ptx::mma_commit(c.bar(kQEmpty0 + st));
+        ptx::mma_commit(c.bar(kMma3));
         have = it.next();
-        if (have) {
-          const int st1 = (t + 1) & 1;
-          // next tile: dP^T as soon as its operands landed (the softmax already
-          // read this tile's dP^T), S^T once MMA3 released the P^T columns
-          if (!wait_bar(c, kQFull0 + st1, ((t + 1) >> 1) & 1, 5)) break;
-          ptx::tc_fence_after();
-          issue_dP(st1);
-          if (!wait_bar(c, kMma3, t & 1, 6)) break;
+        const int st1 = (t + 1) & 1;
+        const uint32_t qpar = ((t + 1) >> 1) & 1;
+        // S(t+1) ahead of dK(t) only if its operands already landed: dK(t)
+        // releases the stage the tile after next is loaded into
+        bool s_done = false;
+        if (have && ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
           ptx::tc_fence_after();
           issue_S(st1);
           ptx::mma_commit(c.bar(kSFull));
+          s_done = true;
+        }
+        if (!wait_bar(c, kP2Full, t & 1, 7)) break;
+        ptx::tc_fence_after();
+        // MMA4 dK += dS^T Q : A = dS^T (TMEM fp16 pairs), B = Q MN-major over d
+#pragma unroll
+        for (int s = 0; s < BM / 16; ++s) {
+          const uint32_t a_col = t_dP + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_dK, a_col, ptx::smem_desc_sw128(sQ + s * 2048, kSlab, 1024), id_KV,
+                      (t > 0 || s > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(c.bar(kQEmpty0 + st));
+        ptx::mma_commit(c.bar(kMma4));
+        if (have && !s_done) {
+          if (!wait_bar(c, kQFull0 + st1, qpar, 5)) break;
+          ptx::tc_fence_after();
+          issue_S(st1);
+          ptx::mma_commit(c.bar(kSFull));
+        }
+        if (have) {
+          if (!wait_bar(c, kMma4, t & 1, 6)) break;
+          ptx::tc_fence_after();
+          issue_dP(st1);
+          ptx::mma_commit(c.bar(kdPFull));
         }
         ++t;
       }
@@ -358,60 +384,83 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       float* dbrow = nullptr;
       if constexpr (DBIAS) dbrow = p.dbias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
-      const uint32_t ds_row = sDS + wg * kSlab + jl * 128;
-      // all 64 columns of S^T and dP^T of this group in one round trip
-      uint32_t sr[64], dr[64];
-      ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
-      ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
-      ptx::tmem_ld32(t_dP + lane_off + wg * 64, dr);
-      ptx::tmem_ld32(t_dP + lane_off + wg * 64 + 32, dr + 32);
-      ptx::tmem_wait_ld();
+      const uint32_t ps_row = sDS + wg * kSlab + jl * 128;
+      // phase 1: P^T from S^T as fp16 into shared memory, 128B-swizzled K-major
+      // rows (one key row per thread; A operand of dV)
+      float pv[64];
+      {
+        uint32_t sr[64];
+        ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
+        ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
+          const uint32_t live = bits_between(qlo - q0, qhi - q0 + 1);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + e4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float bv[4];
+            if constexpr (BIAS) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = e4 + u;
+              float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, lv[u] * -kLog2e);
+              if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
+              pv[cc * 32 + e] = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
+            }
+            pk[cc * 16 + e4 / 2] = pack_half2(pv[cc * 32 + e4], pv[cc * 32 + e4 + 1]);
+            pk[cc * 16 + e4 / 2 + 1] = pack_half2(pv[cc * 32 + e4 + 2], pv[cc * 32 + e4 + 3]);
+          }
+        }
+        // the previous tile's dV has finished reading the P^T buffer
+        if (t > 0 && !wait_bar(c, kMma3, (t - 1) & 1, 12)) { ok = false; break; }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const uint32_t chunk = (uint32_t)q4 ^ (uint32_t)(jl & 7);
+          ptx::st_shared_v4(ps_row + chunk * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
+                            pk[4 * q4 + 3]);
+        }
+        ptx::fence_async_shared();
+        ptx::mbar_arrive(c.bar(kP1Full));
+      }
+      // phase 2: dS^T = P^T (dP^T - D), fp16 pairs over the front half of this
+      // group's dP^T columns (A operand of dK)
+      if (!wait_bar(c, kdPFull, t & 1, 10)) { ok = false; break; }
+      ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
-        const uint32_t live = bits_between(qlo - q0, qhi - q0 + 1);
-        uint32_t pk[16], dk[16];
+        const int q0 = wg * 64 + cc * 32;
+        uint32_t dr[32];
+        ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
+        ptx::tmem_wait_ld();
+        uint32_t dk[16];
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + e4);
           const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float bv[4];
-          if constexpr (BIAS) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
-          }
-          float pe[4], de[4];
+          float de[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int e = e4 + u;
-            float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, lv[u] * -kLog2e);
-            if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
-            const float pv = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
-            pe[u] = pv;
-            de[u] = pv * (__uint_as_float(dr[cc * 32 + e]) - dv[u]);
+            de[u] = pv[cc * 32 + e] * (__uint_as_float(dr[e]) - dv[u]);
             if constexpr (DBIAS) atomicAdd(dbrow + (int64_t)(q0 + e) * p.Sk, de[u]);
           }
-          pk[e4 / 2] = pack_half2(pe[0], pe[1]);
-          pk[e4 / 2 + 1] = pack_half2(pe[2], pe[3]);
           dk[e4 / 2] = pack_half2(de[0], de[1]);
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
         }
-        // P^T fp16 pairs over the (already read) front half of this group's S^T columns
-        ptx::tmem_st16(t_S + lane_off + wg * 64 + cc * 16, pk);
-        // dS^T fp16 into shared memory, 128B-swizzled K-major rows (one key row per thread)
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t chunk = (uint32_t)(cc * 4 + q4) ^ (uint32_t)(jl & 7);
-          ptx::st_shared_v4(ds_row + chunk * 16, dk[4 * q4], dk[4 * q4 + 1], dk[4 * q4 + 2],
-                            dk[4 * q4 + 3]);
-        }
+        // columns [cc 16, cc 16 + 16) were read above (chunk 0 covers 0-31)
+        ptx::tmem_st16(t_dP + lane_off + wg * 64 + cc * 16, dk);
       }
       ptx::tmem_wait_st();
-      ptx::fence_async_shared();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(kPFull));
+      ptx::mbar_arrive(c.bar(kP2Full));
       ++t;
     }
     n_iters = t;
@@ -453,35 +502,16 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
         }
       }
-    }
-  }
-  if (cs > 1) {
-    // Sum the cs partial tiles through distributed shared memory: CTA `rank`
-    // finalises rows [rank R, rank R + R) of both dK and dV (R = 128 / cs).
-    ptx::cluster_sync();
-    if (epi_thread && !*c.abort) {
-      const int R = BN / cs;
-      const int per_mat = R * (D / 4);
-      const int tid = threadIdx.x - 128;
-      for (int item = tid; item < 2 * per_mat; item += 256) {
-        const int mat = item / per_mat;
-        const int rem = item % per_mat;
-        const int row = rank * R + rem / (D / 4);
-        const int d4 = rem % (D / 4);
-        const uint32_t local = sbase + L::STAGE + (mat * 128 + row) * L::kStageRow + d4 * 16;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int rk = 0; rk < cs; ++rk) {
-          const float4 v = ptx::ld_cluster_v4(ptx::mapa(local, (uint32_t)rk));
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
-        float* dst = (mat == 0 ? p.dk : p.dv) + (((int64_t)b * p.Sk + n0 + row) * p.Hk + g) * D;
-        *reinterpret_cast<float4*>(dst + d4 * 4) = acc;
+      if (cs > 1) {
+        // The cs head-split CTAs of this key tile add their partial rows into
+        // dK / dV (zeroed before the launch) with one TMA bulk reduction per
+        // row; the shared-memory row must stay until the copy engine read it.
+        ptx::fence_async_shared();
+        ptx::bulk_reduce_add_f32(grow, srow, D * 4);
+        ptx::bulk_commit();
+        ptx::bulk_wait_all();
       }
     }
-    ptx::cluster_sync();  // keep every CTA's staging alive until all reads finished
   }
 
   // ----------------------------------------------------------- teardown --
@@ -745,8 +775,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
-  // 1 KiB alignment of the 128B-swizzle atoms; uniform over the grid, so an
-  // early return cannot strand a cluster barrier.
+  // 1 KiB alignment of the 128B-swizzle atoms (uniform over the grid)
   if (sbase & 1023u) {
     if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 1);
     return;
@@ -771,8 +800,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     kv_cta<D, BIAS, DBIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
   } else {
     const int qi = (int)blockIdx.x - p.kv_ctas;
-    if (qi < p.B * p.Hq * (p.Sq / BM))  // the rest pads the grid to whole clusters
-      q_cta<D, BIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
+    q_cta<D, BIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
   }
 }
 
@@ -803,19 +831,8 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_total<D>();
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, dO, p);
+  kern<<<grid, kThreads, smem_total<D>(), stream>>>(q, k, v, dO, p);
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -827,9 +844,9 @@ cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
   return launch_variant<D, false, false>(q, k, v, dO, p, grid, stream);
 }
 
-// Query heads per KV head are split over a cluster of cs CTAs: the largest
-// divisor of the group size that is at most 8 (the portable cluster size).
-int cluster_size(int ratio) {
+// Query heads per KV head are split over cs key-major CTAs: the largest
+// divisor of the group size that is at most 8.
+int head_split(int ratio) {
   for (int c = 8; c > 1; --c)
     if (ratio % c == 0) return c;
   return 1;
@@ -872,7 +889,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Hk = pr.Hk;
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
-  p.cs = cluster_size(pr.Hq / pr.Hk);
+  p.cs = head_split(pr.Hq / pr.Hk);
   p.kv_ctas = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
@@ -886,7 +903,13 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dbias = dbias;
   p.status = st;
   const int q_ctas = pr.B * pr.Hq * (pr.Sq / BM);
-  const int grid = p.kv_ctas + (q_ctas + p.cs - 1) / p.cs * p.cs;
+  const int grid = p.kv_ctas + q_ctas;
+  if (p.cs > 1) {  // the head-split partials are added into dK / dV
+    const size_t bytes = (size_t)pr.B * pr.Sk * pr.Hk * pr.D * sizeof(float);
+    cudaError_t e = cudaMemsetAsync(dk, 0, bytes, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, bytes, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
   return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);
 }
