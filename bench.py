@@ -147,6 +147,14 @@ def reduce_max(values, device):
     return [float(x) for x in t.tolist()]
 
 
+def overrides_of(args):
+    out = {}
+    for kv in args.override:
+        key, _, val = kv.partition("=")
+        out[key] = int(val)
+    return out
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -164,7 +172,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, **overrides_of(args))
     sparse = w.__class__.__name__ == "SparseWorkload"
 
     def up_bf16(x):
@@ -291,7 +299,7 @@ def run_ours(args):
                 "peak": SIMT_FP32_PEAK_TFLOPS, "unit": "TFLOP/s"}
         launches_per_step = 3
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = NCU_TRAFFIC.get(args.workload) if not overrides_of(args) else None
     roof["peak_source"] = peaks_src
     roof["kernel"] = "attn_bwd (" + path + ")"
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
@@ -308,7 +316,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f16" if path == "tcgen05" else "f32",
         "data": "synthetic (seeded bf16 N(0,1); O/LSE from the library forward)",
-        "config": {"workload": args.workload, "flops_per_step": flops,
+        "config": {"workload": args.workload, "overrides": overrides_of(args) or None,
+                   "flops_per_step": flops,
                    "algorithmic_bytes_per_step": algorithmic_bytes(w),
                    "path": path, "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                    "launch": "attn_bwd_preprocess and attn_bwd captured once into CUDA graphs, replayed per step",
@@ -327,6 +336,15 @@ def run_ours(args):
     if ws > 1:
         dist.destroy_process_group()
 
+
+# dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, per launch, from
+# the ncu captures summarised in profiles/ (the sparse figure is a 1024-token capture
+# scaled by the token count: its DRAM bytes are Q, dO and dQ, all linear in Sq). An entry
+# goes back to None when its kernel changes.
+NCU_TRAFFIC = {
+    "gqa4_causal_s1024_d128": 29.72e6,
+    "sparse_scfa_s4096_h64_d512": 4 * 231.0e6,
+}
 
 # CUDA-core fp32 FMA rate for the SIMT fallback's roofline: 152 SMs x 128
 # FP32 lanes x 2 FLOP x 2.07 GHz.
@@ -477,6 +495,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", nargs="*", default=[], metavar="KEY=INT",
+                    help="shrink the workload (e.g. Sq=1024 n_ori=1024 n_cmp=256) for a "
+                         "profiler capture; the JSON line then records the overrides")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
