@@ -75,7 +75,7 @@ def _load():
     L.attn_bwd_workspace_size.argtypes = [P(Problem), P(Mask), P(Sparse)]
     L.attn_bwd_workspace_size.restype = sz
     L.attn_bwd_preprocess.argtypes = [P(Problem), P(Sparse), vp, vp, vp, vp, vp, vp, vp, vp,
-                                      sz, vp]
+                                      vp, vp, sz, vp]
     L.attn_bwd_preprocess.restype = st
     L.attn_bwd.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp,
                            vp, vp, vp, vp, vp, sz, vp]
@@ -187,11 +187,11 @@ def attn_fwd_lse(prob, mask, sparse, q, k, v, bias, o, lse, stream=None):
            "attn_fwd_lse")
 
 
-def attn_bwd_preprocess(prob, sparse, q, k, v, o, do, delta, dbias, workspace,
+def attn_bwd_preprocess(prob, sparse, q, k, v, o, do, delta, dbias, dk, dv, workspace,
                         workspace_bytes, stream=None):
     _check(lib.attn_bwd_preprocess(ctypes.byref(prob), _ref(sparse), _ptr(q), _ptr(k), _ptr(v),
-                                   _ptr(o), _ptr(do), _ptr(delta), _ptr(dbias),
-                                   _ptr(workspace), workspace_bytes, _stream(stream)),
+                                   _ptr(o), _ptr(do), _ptr(delta), _ptr(dbias), _ptr(dk),
+                                   _ptr(dv), _ptr(workspace), workspace_bytes, _stream(stream)),
            "attn_bwd_preprocess")
 
 
@@ -281,7 +281,8 @@ class BackwardPlan:
 
     def run(self, stream=None):
         attn_bwd_preprocess(self.prob, self.sparse, self.q, self.k, self.v, self.o, self.do,
-                            self.delta, self.dbias, self.workspace, self.ws_bytes, stream)
+                            self.delta, self.dbias, self.dk, self.dv, self.workspace,
+                            self.ws_bytes, stream)
         attn_bwd(self.prob, self.mask, self.sparse, self.q, self.k, self.v, self.do, self.lse,
                  self.delta, self.bias, self.dq, self.dk, self.dv, self.dbias, self.workspace,
                  self.ws_bytes, stream)

@@ -217,8 +217,8 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
 attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
                                   const void* q, const void* k, const void* v,
                                   const void* o, const void* dO, float* delta,
-                                  float* dbias, void* workspace, size_t workspace_bytes,
-                                  cudaStream_t stream) {
+                                  float* dbias, float* dk, float* dv, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
   Problem p;
   attn_status_t s = make_problem(prob, nullptr, sparse, &p);
   if (s != ATTN_OK) return s;
@@ -228,13 +228,17 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
   float* d_ori = nullptr;
   float* d_cmp = nullptr;
   if (p.sparse) {
-    if (dbias != nullptr) return ATTN_ERR_INVALID_ARG;
+    if (dbias != nullptr || dk != nullptr || dv != nullptr) return ATTN_ERR_INVALID_ARG;
     d_ori = sparse->d_ori_kv;
     d_cmp = sparse->cmp_kv ? sparse->d_cmp_kv : nullptr;
     if (!need(d_ori, n.ori) || (sparse->cmp_kv && d_cmp == nullptr)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(d_ori) || !aligned16(d_cmp)) return ATTN_ERR_INVALID_ARG;
+  } else if (!need(dk, n.k) || !need(dv, n.k) || !aligned16(dk) || !aligned16(dv)) {
+    return ATTN_ERR_INVALID_ARG;
   }
   const bool tc = use_tensor_cores(p);
+  // the head-split tensor-core kernel adds partial dK / dV sums into zeroed buffers
+  const bool zero_kv = tc && !p.sparse && tc_head_split(p) > 1;
   if (tc && !p.sparse &&
       (!need(q, n.q) || !need(k, n.k) || !need(v, n.k) || !aligned16(q) || !aligned16(k) ||
        !aligned16(v)))
@@ -253,8 +257,8 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
       p, q, k, v, o, dO, delta, dbias, d_ori, d_cmp, dense_staged ? staged(w.q16) : nullptr,
       dense_staged ? staged(w.k16) : nullptr, dense_staged ? staged(w.v16) : nullptr,
       dense_staged ? staged(w.do16) : nullptr, p.sparse ? sparse->ori_kv : nullptr,
-      p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr, st,
-      stream));
+      p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr,
+      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, dk, dv, st, stream));
 }
 
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,

@@ -39,17 +39,24 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
 // One fused kernel: clears the status record, zeroes dbias / the sparse dKV
 // buffers, computes delta, and (if do16 != nullptr) writes fp16
 // head-major copies of q, k, v and dO, and (if kv16 != nullptr) the fp16
-// copy of the sparse shared KV rows. An fp16 overflow sets bits (1 q, 2 k or
-// shared KV, 4 v, 8 dO) in the block's flag slot after the status record;
-// the tensor-core backward ORs the slots and reports ATTN_ERR_RANGE.
+// copy of the sparse shared KV rows. dk_zero / dv_zero (may be nullptr) are
+// zeroed; dk / dv are recorded in the status record (reserved[2..5]) so the
+// backward can check it received the buffers this pass prepared. An fp16
+// overflow sets bits (1 q, 2 k or shared KV, 4 v, 8 dO) in the block's flag
+// slot after the status record; the tensor-core backward ORs the slots and
+// reports ATTN_ERR_RANGE.
 cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, const void* v,
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
-                              __half* kv16, DevStatus* st, cudaStream_t stream);
+                              __half* kv16, float* dk_zero, float* dv_zero, float* dk,
+                              float* dv, DevStatus* st, cudaStream_t stream);
 
 // ---- tc_bwd.cu ----
 bool tc_supported(const Problem& p);
+// Key-major CTAs per (key tile, KV head) of the dense tensor-core kernel; when
+// above 1 they add partial dK / dV sums into buffers the pre-pass zeroed.
+int tc_head_split(const Problem& p);
 cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16,
                           const __half* v16, const __half* do16, const float* lse,
                           const float* delta, const float* bias, float* dq, float* dk,

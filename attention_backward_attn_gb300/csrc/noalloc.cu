@@ -68,7 +68,7 @@ extern "C" attn_status_t attn_bwd_noalloc(const attn_problem_t* prob, const attn
   if (need > attn::kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
   void* ws = nullptr;
   if (attn::scratch_address(&ws) != cudaSuccess) return ATTN_ERR_CUDA;
-  attn_status_t s = attn_bwd_preprocess(prob, sparse, q, k, v, o, dO, delta, dbias, ws,
+  attn_status_t s = attn_bwd_preprocess(prob, sparse, q, k, v, o, dO, delta, dbias, dk, dv, ws,
                                         attn::kNoAllocScratchBytes, stream);
   if (s != ATTN_OK) return s;
   s = attn_bwd(prob, mask, sparse, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias, ws,

@@ -52,6 +52,12 @@ struct PreParams {
   int64_t zero_nb;
   float* zero_c;
   int64_t zero_nc;
+  float* zero_d;
+  int64_t zero_nd;
+  float* zero_e;
+  int64_t zero_ne;
+  float* dk;  // recorded for the backward's check
+  float* dv;
   DevStatus* st;
 };
 
@@ -69,18 +75,19 @@ __device__ __forceinline__ void unpack8(const uint4& raw, float* f) {
   }
 }
 
-// fp16 copy of 8 values; returns true if one of them overflowed to inf.
-__device__ __forceinline__ bool store8_half(__half* p, const float* f) {
+// fp16 copy of 8 values; returns their largest magnitude (the caller checks
+// the fp16 range once at the end).
+__device__ __forceinline__ float store8_half(__half* p, const float* f) {
   uint4 raw;
   __half2* h = reinterpret_cast<__half2*>(&raw);
-  bool bad = false;
+  float m = 0.f;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     h[t] = __floats2half2_rn(f[2 * t], f[2 * t + 1]);
-    bad |= __hisinf(__low2half(h[t])) | __hisinf(__high2half(h[t]));
+    m = fmaxf(m, fmaxf(fabsf(f[2 * t]), fabsf(f[2 * t + 1])));
   }
   *reinterpret_cast<uint4*>(p) = raw;
-  return bad;
+  return m;
 }
 
 // Work order over (batch, block of kIB rows, head, row in block): a warp step
@@ -128,23 +135,29 @@ preprocess_kernel(const PreParams p) {
     p.st->code = 0;
     p.st->detail = 0;
     p.st->reserved[1] = (int32_t)gridDim.x;  // number of flag slots written below
+    uint64_t* rec = reinterpret_cast<uint64_t*>(&p.st->reserved[2]);
+    rec[0] = reinterpret_cast<uint64_t>(p.dk);
+    rec[1] = reinterpret_cast<uint64_t>(p.dv);
   }
   int range_bits = 0;
 
   // ---- query-side rows (b, i, h) in memory order: delta, staging ----
   // U row slots per warp step, all loads issued before any dependent work so
-  // that each thread keeps several 16-byte requests in flight.
-  constexpr int U = 2;
+  // that each thread keeps several 16-byte requests in flight. The RPW * U
+  // rows of a step (a divisor of kIB, aligned) lie in one block of kIB rows of
+  // one head, so the index split is done once per step.
+  constexpr int U = D >= 512 ? 1 : 2;  // D = 512 rows are 1 KiB: one slot keeps registers in budget
+  static_assert(kIB % (RPW * U) == 0, "a warp step stays inside one row block");
+  float amax_q = 0.f, amax_do = 0.f, amax_k = 0.f, amax_v = 0.f;
   const int64_t nq = (int64_t)p.B * ((p.Sq + kIB - 1) / kIB) * kIB * p.Hq;
   for (int64_t r0 = warp0 * RPW * U; r0 < nq; r0 += nwarps * RPW * U) {
+    int h, i0, b;
+    decompose(r0, p.Hq, p.Sq, &b, &h, &i0);
     uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
-    int64_t rows[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      rows[u] = r0 + u * RPW + sub;
-      int h, i, b;
-      decompose(rows[u], p.Hq, p.Sq, &b, &h, &i);
-      if (rows[u] < nq && i < p.Sq) {
+      const int i = i0 + u * RPW + sub;
+      if (i < p.Sq) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           const int e0 = (cl + c * LPR) * 8;
@@ -156,9 +169,8 @@ preprocess_kernel(const PreParams p) {
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      int h, i, b;
-      decompose(rows[u], p.Hq, p.Sq, &b, &h, &i);
-      const bool valid = rows[u] < nq && i < p.Sq;
+      const int i = i0 + u * RPW + sub;
+      const bool valid = i < p.Sq;
       float s = 0.f;
       if (valid) {
         const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
@@ -173,8 +185,8 @@ preprocess_kernel(const PreParams p) {
           if (p.do16 != nullptr) {
             float qv[8];
             unpack8(qf[u][c], qv);
-            if (store8_half(p.do16 + hm * D + e0, dv)) range_bits |= 8;
-            if (store8_half(p.q16 + hm * D + e0, qv)) range_bits |= 1;
+            amax_do = fmaxf(amax_do, store8_half(p.do16 + hm * D + e0, dv));
+            amax_q = fmaxf(amax_q, store8_half(p.q16 + hm * D + e0, qv));
           }
         }
       }
@@ -187,39 +199,37 @@ preprocess_kernel(const PreParams p) {
   // ---- key-side rows (k then v), staged head-major ----
   if (p.do16 != nullptr) {
     const int64_t nk = (int64_t)p.B * ((p.Sk + kIB - 1) / kIB) * kIB * p.Hk;
+    // nk is a multiple of kIB, so a warp step never straddles the k / v boundary
     for (int64_t r0 = warp0 * RPW * U; r0 < 2 * nk; r0 += nwarps * RPW * U) {
+      const bool is_v = r0 >= nk;
+      int g, j0, b;
+      decompose(is_v ? r0 - nk : r0, p.Hk, p.Sk, &b, &g, &j0);
+      const bf16* src0 = is_v ? p.v + b * p.v0 + g * p.v2 : p.k + b * p.k0 + g * p.k2;
+      const int64_t s1 = is_v ? p.v1 : p.k1;
+      __half* dst0 = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk) * D;
       uint4 f[U][CPL];
-      int64_t rows[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        rows[u] = r0 + u * RPW + sub;
-        const bool is_v = rows[u] >= nk;
-        int g, j, b;
-        decompose(is_v ? rows[u] - nk : rows[u], p.Hk, p.Sk, &b, &g, &j);
-        if (rows[u] < 2 * nk && j < p.Sk) {
-          const bf16* src = is_v ? p.v + b * p.v0 + j * p.v1 + g * p.v2
-                                 : p.k + b * p.k0 + j * p.k1 + g * p.k2;
+        const int j = j0 + u * RPW + sub;
+        if (j < p.Sk) {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src + (cl + c * LPR) * 8);
+          for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src0 + j * s1 + (cl + c * LPR) * 8);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const bool is_v = rows[u] >= nk;
-        int g, j, b;
-        decompose(is_v ? rows[u] - nk : rows[u], p.Hk, p.Sk, &b, &g, &j);
-        if (rows[u] >= 2 * nk || j >= p.Sk) continue;
-        __half* dst = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk + j) * D;
+        const int j = j0 + u * RPW + sub;
+        if (j >= p.Sk) continue;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float x[8];
           unpack8(f[u][c], x);
-          if (store8_half(dst + (cl + c * LPR) * 8, x)) range_bits |= is_v ? 4 : 2;
+          const float m = store8_half(dst0 + (int64_t)j * D + (cl + c * LPR) * 8, x);
+          if (is_v) amax_v = fmaxf(amax_v, m); else amax_k = fmaxf(amax_k, m);
         }
       }
     }
   }
-
   // ---- sparse shared KV rows, staged as one fp16 [ori ; cmp] matrix ----
   if (p.kv16 != nullptr) {
     const int64_t nkv = p.kv_ori_rows + p.kv_cmp_rows;
@@ -243,16 +253,22 @@ preprocess_kernel(const PreParams p) {
         for (int c = 0; c < CPL; ++c) {
           float x[8];
           unpack8(f[u][c], x);
-          if (store8_half(p.kv16 + rows[u] * D + (cl + c * LPR) * 8, x)) range_bits |= 2;
+          amax_k = fmaxf(amax_k, store8_half(p.kv16 + rows[u] * D + (cl + c * LPR) * 8, x));
         }
       }
     }
   }
 
+  // a bf16 value overflows fp16 exactly when its magnitude is at least 65520
+  range_bits |= (amax_q >= 65520.f ? 1 : 0) | (amax_k >= 65520.f ? 2 : 0) |
+                (amax_v >= 65520.f ? 4 : 0) | (amax_do >= 65520.f ? 8 : 0);
+
   // ---- buffers accumulated with atomics: dbias, sparse dKV ----
   zero_range(p.zero_a, p.zero_na, tid, nthreads);
   zero_range(p.zero_b, p.zero_nb, tid, nthreads);
   zero_range(p.zero_c, p.zero_nc, tid, nthreads);
+  zero_range(p.zero_d, p.zero_nd, tid, nthreads);
+  zero_range(p.zero_e, p.zero_ne, tid, nthreads);
 
   // Range overflow is handed to attn_bwd through this block's flag slot: a
   // report straight into the status record could race with the reset above.
@@ -270,7 +286,8 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
-                              __half* kv16, DevStatus* st, cudaStream_t stream) {
+                              __half* kv16, float* dk_zero, float* dv_zero, float* dk,
+                              float* dv, DevStatus* st, cudaStream_t stream) {
   PreParams p;
   p.B = pr.B;
   p.Hq = pr.Hq;
@@ -303,6 +320,13 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.zero_nb = d_ori ? (int64_t)pr.n_ori * pr.Hk * pr.D : 0;
   p.zero_c = d_cmp;
   p.zero_nc = d_cmp ? (int64_t)pr.n_cmp * pr.Hk * pr.D : 0;
+  const int64_t nkd = (int64_t)pr.B * pr.Sk * pr.Hk * pr.D;
+  p.zero_d = dk_zero;
+  p.zero_nd = dk_zero ? nkd : 0;
+  p.zero_e = dv_zero;
+  p.zero_ne = dv_zero ? nkd : 0;
+  p.dk = dk;
+  p.dv = dv;
   p.st = st;
   // Enough resident warps to keep HBM busy; the loops stride over the rest.
   int dev = 0, sms = 152;

@@ -15,8 +15,8 @@
 // (batch, KV head); CTA `rank` takes r / cs of the r query heads that share
 // the KV head and loops over their live query tiles, accumulating its partial
 // dK / dV in TMEM over the group. At the end each CTA adds its partial rows
-// into dK / dV with TMA bulk reductions (the buffers are zeroed before the
-// launch when cs > 1), so no post-pass over per-head gradients exists. Per
+// into dK / dV with TMA bulk reductions (the pre-pass zeroes the buffers when
+// cs > 1), so no post-pass over per-head gradients exists. Per
 // tile, so that one thread owns one key row of the softmax:
 //   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
 //   MMA2  dP^T = V  dO^T
@@ -504,12 +504,19 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       }
       if (cs > 1) {
         // The cs head-split CTAs of this key tile add their partial rows into
-        // dK / dV (zeroed before the launch) with one TMA bulk reduction per
-        // row; the shared-memory row must stay until the copy engine read it.
-        ptx::fence_async_shared();
-        ptx::bulk_reduce_add_f32(grow, srow, D * 4);
-        ptx::bulk_commit();
-        ptx::bulk_wait_all();
+        // dK / dV (zeroed by the pre-pass, which recorded which buffers) with
+        // one TMA bulk reduction per row; the shared-memory row must stay
+        // until the copy engine read it.
+        const uint64_t* rec = reinterpret_cast<const uint64_t*>(&p.status->reserved[2]);
+        if (rec[0] == reinterpret_cast<uint64_t>(p.dk) &&
+            rec[1] == reinterpret_cast<uint64_t>(p.dv)) {
+          ptx::fence_async_shared();
+          ptx::bulk_reduce_add_f32(grow, srow, D * 4);
+          ptx::bulk_commit();
+          ptx::bulk_wait_all();
+        } else if (ejl == 0) {
+          report(p.status, ATTN_ERR_INVALID_ARG, 3);  // dk / dv not prepared by the pre-pass
+        }
       }
     }
   }
@@ -878,6 +885,10 @@ EncodeFn encode_fn() {
   return fn;
 }
 
+int tc_head_split(const Problem& p) {
+  return head_split(p.Hq / p.Hk, p.B * p.Hk * (p.Sk / BN), sm_count());
+}
+
 bool tc_supported(const Problem& p) {
   return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0 &&
          p.Sq % BM == 0 && p.Sk % BN == 0 && encode_fn() != nullptr;
@@ -899,7 +910,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Hk = pr.Hk;
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
-  p.cs = head_split(pr.Hq / pr.Hk, pr.B * pr.Hk * (pr.Sk / BN), sm_count());
+  p.cs = tc_head_split(pr);
   p.kv_ctas = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
@@ -914,12 +925,6 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.status = st;
   const int q_ctas = pr.B * pr.Hq * (pr.Sq / BM);
   const int grid = p.kv_ctas + q_ctas;
-  if (p.cs > 1) {  // the head-split partials are added into dK / dV
-    const size_t bytes = (size_t)pr.B * pr.Sk * pr.Hk * pr.D * sizeof(float);
-    cudaError_t e = cudaMemsetAsync(dk, 0, bytes, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, bytes, stream);
-    if (e != cudaSuccess) return e;
-  }
   if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
   return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);
 }

@@ -224,7 +224,8 @@ def run_ours(args):
     # never shows up as GPU idle time inside the timed events.
     def call_pre():
         ab.attn_bwd_preprocess(plan.prob, plan.sparse, plan.q, plan.k, plan.v, plan.o, plan.do,
-                               plan.delta, plan.dbias, plan.workspace, plan.ws_bytes)
+                               plan.delta, plan.dbias, plan.dk, plan.dv, plan.workspace,
+                               plan.ws_bytes)
 
     def call_bwd():
         ab.attn_bwd(plan.prob, plan.mask, plan.sparse, plan.q, plan.k, plan.v, plan.do,

@@ -130,28 +130,35 @@ size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* ma
 /* Backward pre-pass ("34_bwd_gqa_fmha.py" cpu_bwd_gqa: D = rowsum(dO * O);
  * Ascend formula phase 2: SoftmaxGrad(dO, O)):
  *  - delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d] in fp32;
- *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL) and,
- *    for the sparse variant, sparse->d_ori_kv / d_cmp_kv;
+ *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL), for
+ *    the sparse variant sparse->d_ori_kv / d_cmp_kv, and dk / dv when the
+ *    tensor-core path splits a KV head's query-head group over several CTAs
+ *    that add their partial sums (small problems);
  *  - clears the workspace status record;
  *  - when attn_bwd will take the tensor-core path, writes fp16 copies of q,
  *    k, v and dO into the workspace (head-major [B, H, S, D] rows) for it.
  *    Every bf16 value of magnitude in [2^-14, 65504] converts exactly; a
  *    larger one is recorded as ATTN_ERR_RANGE.
- * q, k, v are the same tensors later passed to attn_bwd (k, v NULL for the
- * sparse variant). Must precede attn_bwd on the same stream with the same
- * workspace, and the inputs must not change in between. */
+ * q, k, v, dbias, dk and dv are the same tensors later passed to attn_bwd
+ * (k, v, dk, dv NULL for the sparse variant; for a dense problem dk and dv
+ * must be given, fp32 [B, Sk, Hk, D] contiguous, 16-byte aligned). Must
+ * precede attn_bwd on the same stream with the same workspace, and the inputs
+ * must not change in between; attn_bwd reports ATTN_ERR_INVALID_ARG through
+ * the status record (and leaves dk / dv unwritten) if it receives dk / dv
+ * buffers other than the ones this call prepared. */
 attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_t* sparse,
                                   const void* q, const void* k, const void* v,
                                   const void* o, const void* dO, float* delta,
-                                  float* dbias,
+                                  float* dbias, float* dk, float* dv,
                                   void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
 
 /* The fused backward ("34_bwd_gqa_fmha.py" docstring and cpu_bwd_gqa;
  * "28_backward_dbias_fmha.py" cpu_attention_bwd_dbias; Ascend
  * "sparse_flash_mla_grad" phases 1-3). P is rebuilt from lse; delta comes
- * from attn_bwd_preprocess, which also zeroed dbias and the sparse gradients
- * that this call accumulates into; dq, dk and dv are written in full. dbias may be non-NULL without bias (gradient of a zero
+ * from attn_bwd_preprocess, which also zeroed dbias, the sparse gradients
+ * and (when needed) dk / dv that this call accumulates into; dq, dk and dv
+ * hold the complete gradients afterwards. dbias may be non-NULL without bias (gradient of a zero
  * bias). Returns ATTN_ERR_UNSUPPORTED for D outside {64, 128, 512} or the
  * sparse variant with D != 512 when no fallback kernel covers it. */
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,

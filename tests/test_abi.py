@@ -105,6 +105,35 @@ def test_bwd_rejects_bad_arguments_on_the_host(ab):
     assert _call_bwd(ab, p, mask=m) == 1
 
 
+def _call_pre(ab, p, sparse=None, ptrs=None, ws_bytes=1 << 20):
+    fake = 1 << 20  # never dereferenced: every case below fails host validation
+    args = dict(q=fake, k=fake, v=fake, o=fake, do=fake, delta=fake, dbias=None, dk=fake,
+                dv=fake, ws=fake)
+    args.update(ptrs or {})
+    return ab.lib.attn_bwd_preprocess(ctypes.byref(p),
+                                      None if sparse is None else ctypes.byref(sparse),
+                                      args["q"], args["k"], args["v"], args["o"], args["do"],
+                                      args["delta"], args["dbias"], args["dk"], args["dv"],
+                                      args["ws"], ws_bytes, None)
+
+
+def test_preprocess_validates_dk_dv(ab):
+    # dense problems hand dk / dv to the pre-pass (it zeroes them when the
+    # head-split kernel adds partial sums into them); the sparse variant has none
+    p = _prob(ab)
+    assert _call_pre(ab, p, ptrs=dict(dk=None)) == 1
+    assert _call_pre(ab, p, ptrs=dict(dv=None)) == 1
+    assert _call_pre(ab, p, ptrs=dict(dv=(1 << 20) + 4)) == 1  # misaligned
+    assert _call_pre(ab, p, ptrs=dict(ws=None)) == 7
+    fake = 1 << 20
+    sp = _prob(ab, B=1, Hq=16, Hk=1, Sq=128, Sk=0, D=512)
+    s = ab.Sparse()
+    s.ori_kv, s.n_ori, s.ori_win_left, s.ori_win_right = fake, 128, 31, 0
+    s.d_ori_kv = fake
+    assert _call_pre(ab, sp, sparse=s, ptrs=dict(k=None, v=None)) == 1
+    assert _call_pre(ab, sp, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None, ws=None)) == 7
+
+
 def test_sparse_descriptor_validation(ab):
     fake = 1 << 20
     p = _prob(ab, B=1, Hq=16, Hk=1, Sq=128, Sk=0, D=512)

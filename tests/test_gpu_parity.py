@@ -117,6 +117,34 @@ def test_tensor_core_cases(name):
     _compare_dense(w, plan, O_b, L_f)
 
 
+def test_head_split_needs_the_prepared_dk_dv():
+    # GQA 8:1 on a small problem splits each key tile's query heads over
+    # several CTAs that add partial sums into dk / dv; the pre-pass zeroes the
+    # buffers it was given, so attn_bwd with other buffers must refuse them
+    torch = _torch()
+    import attention_backward_attn_gb300 as ab
+    w = TC_EXTRA["gqa8_sq256_sk512_d128"]()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    plan = H.gpu_dense_plan(w, O_b, L_f)
+    assert plan.path == 1
+    other_dk = torch.full_like(plan.dk, float("nan"))
+    ab.attn_bwd_preprocess(plan.prob, plan.sparse, plan.q, plan.k, plan.v, plan.o, plan.do,
+                           plan.delta, plan.dbias, plan.dk, plan.dv, plan.workspace,
+                           plan.ws_bytes)
+    ab.attn_bwd(plan.prob, plan.mask, plan.sparse, plan.q, plan.k, plan.v, plan.do, plan.lse,
+                plan.delta, plan.bias, plan.dq, other_dk, plan.dv, plan.dbias, plan.workspace,
+                plan.ws_bytes)
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 1 and detail == 3
+    assert torch.isnan(other_dk).all()  # left unwritten
+    # the regular pairing still works afterwards
+    plan.run()
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+    _compare_dense(w, plan, O_b, L_f)
+
+
 def test_fully_masked_rows_and_empty_query():
     # keys live only for rows 0..7 (window_right = -1 .. left 3 at Sk = 8): rows
     # beyond see nothing -> LSE = -inf, zero gradients.
