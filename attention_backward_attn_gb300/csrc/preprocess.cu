@@ -22,6 +22,7 @@
 // (see decompose) so that both the reads and the head-major writes stream.
 
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -131,6 +132,9 @@ preprocess_kernel(const PreParams p) {
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
 
+  // the backward launched after this kernel may start its set-up now; it waits
+  // for this grid's completion before it reads anything written here
+  ptx::grid_launch_dependents();
   if (tid == 0) {
     p.st->code = 0;
     p.st->detail = 0;

@@ -787,6 +787,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (threadIdx.x == 0) report(p.status, ATTN_ERR_UNSUPPORTED, 1);
     return;
   }
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmdO);
+  }
+  // everything below reads what the pre-pass wrote (launched as its
+  // programmatic dependent, this grid may start before the pre-pass ends)
+  ptx::grid_dependency_wait();
   if (blockIdx.x == 0) {
     // fp16 overflow found while staging the operands: OR of the pre-pass's
     // per-block flag slots
@@ -796,12 +805,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     for (int i = threadIdx.x; i < nslots; i += blockDim.x) bits |= slots[i];
     bits = __reduce_or_sync(0xffffffffu, bits);
     if (bits && (threadIdx.x & 31) == 0) report(p.status, ATTN_ERR_RANGE, bits);
-  }
-  if (threadIdx.x == 0) {
-    ptx::prefetch_tmap(&tmQ);
-    ptx::prefetch_tmap(&tmK);
-    ptx::prefetch_tmap(&tmV);
-    ptx::prefetch_tmap(&tmdO);
   }
   if ((int)blockIdx.x < p.kv_ctas) {
     kv_cta<D, BIAS, DBIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
@@ -838,8 +841,8 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, smem_total<D>(), stream>>>(q, k, v, dO, p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), (size_t)smem_total<D>(), stream, q,
+                          k, v, dO, p);
 }
 
 template <int D>

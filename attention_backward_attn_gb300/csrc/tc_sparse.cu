@@ -173,6 +173,9 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const int g = (int)(blockIdx.x % p.Hk);
   const int i = p.Sq - 1 - (int)(blockIdx.x / p.Hk);  // later tokens select more rows: first
 
+  // everything below reads what the pre-pass wrote (launched as its
+  // programmatic dependent, this grid may start before the pre-pass ends)
+  ptx::grid_dependency_wait();
   if (blockIdx.x == 0) {
     // fp16 overflow found while staging the KV copy: OR of the pre-pass's
     // per-block flag slots
@@ -584,8 +587,8 @@ cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* d
     configured = true;
   }
   const unsigned grid = (unsigned)pr.Sq * pr.Hk;
-  attn_bwd_sparse_tc_kernel<<<grid, kSpThreads, SpSmem::TOTAL, stream>>>(mq, mdo, p);
-  return cudaGetLastError();
+  return launch_dependent(attn_bwd_sparse_tc_kernel, dim3(grid), dim3(kSpThreads),
+                          (size_t)SpSmem::TOTAL, stream, mq, mdo, p);
 }
 
 }  // namespace attn

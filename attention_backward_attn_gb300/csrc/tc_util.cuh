@@ -66,4 +66,23 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeFn encode_fn();
 
+// Launches `kern` as a programmatic dependent of the previous kernel in the
+// stream (the pre-pass): its CTAs may be scheduled while that kernel drains,
+// and they call grid_dependency_wait() before reading its outputs.
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace attn
