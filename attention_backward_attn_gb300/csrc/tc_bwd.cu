@@ -93,6 +93,10 @@ struct SmemQ {
   static constexpr int BAR = V + 2 * kTile;
   static constexpr int MISC = BAR + 128;
   static constexpr int TOTAL = MISC + 16;
+  // end-of-kernel staging of dQ rows for the copy-engine stores (reuses K, V)
+  static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
+  static constexpr int STAGE = K;
+  static_assert(128 * kStageRow <= 4 * kTile, "staging fits");
 };
 
 template <int D>
@@ -496,13 +500,16 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         for (int e = 0; e < 32; e += 4) {
           const float a0 = __uint_as_float(v[e]) * mul, a1 = __uint_as_float(v[e + 1]) * mul;
           const float a2 = __uint_as_float(v[e + 2]) * mul, a3 = __uint_as_float(v[e + 3]) * mul;
-          if (cs == 1)
-            *reinterpret_cast<float4*>(grow + cc * 32 + e) = make_float4(a0, a1, a2, a3);
-          else
-            ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
+          ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
         }
       }
-      if (cs > 1) {
+      if (cs == 1) {
+        // the whole row goes out as one copy-engine store
+        ptx::fence_async_shared();
+        ptx::bulk_store(grow, srow, D * 4);
+        ptx::bulk_commit();
+        ptx::bulk_wait_all();
+      } else {
         // The cs head-split CTAs of this key tile add their partial rows into
         // dK / dV (zeroed by the pre-pass, which recorded which buffers) with
         // one TMA bulk reduction per row; the shared-memory row must stay
@@ -744,7 +751,9 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     // thread = query row; warpgroup wg writes columns [wg D/2, wg D/2 + D/2)
     if (epi_ok) {
       ptx::tc_fence_after();
+      // staged in the (idle) K / V stages, then one copy-engine store per half row
       float* grow = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D + wg * (D / 2);
+      const uint32_t srow = sbase + L::STAGE + il * L::kStageRow + wg * (D / 2) * 4;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t v[32];
@@ -757,10 +766,15 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(grow + cc * 32 + e) =
-              make_float4(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
-                          __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+          ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, __uint_as_float(v[e]) * p.scale,
+                             __uint_as_float(v[e + 1]) * p.scale,
+                             __uint_as_float(v[e + 2]) * p.scale,
+                             __uint_as_float(v[e + 3]) * p.scale);
       }
+      ptx::fence_async_shared();
+      ptx::bulk_store(grow, srow, D / 2 * 4);
+      ptx::bulk_commit();
+      ptx::bulk_wait_all();
     }
   }
 
