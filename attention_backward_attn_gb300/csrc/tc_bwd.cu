@@ -112,8 +112,10 @@ constexpr int smem_total() {
 enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kP1Full = 6, kAccFull = 7,
              kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kKvBars = 12 };
 // barrier indices, query-major CTA
+// qSFull / qdPFull: S / dP of the tile in TMEM; qDsFull: dS written over S
+// (256 arrivals; dP read); qMma3: dQ of the tile done (its S buffer free).
 enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, qAccFull = 7,
-            qMma3 = 8 };
+            qMma3 = 8, qdPFull = 9, kQBars = 10 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
@@ -560,8 +562,8 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, 256, 1, 1};
-  init_common(c, sbase + L::MISC, 9, counts, warp);
+  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1};
+  init_common(c, sbase + L::MISC, kQBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   // TMEM: [0, D) dQ, then S buffers 0 / 1 and dP (128 columns each)
   const uint32_t t_dQ = tmem;
@@ -628,30 +630,36 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
                       ptx::smem_desc_sw128(sV + off, 16, 1024), id_S, s > 0);
         }
       };
+      // Per tile t: dQ(t) once dS(t) replaced S(t) in TMEM, dP(t+1) (the
+      // softmax read dP(t)), then S(t+2) into the buffer dQ(t) released. S is
+      // one tile ahead, so the softmax computes P(t+1) while dQ(t) and
+      // dP(t+1) are on the tensor pipe; only its dS half waits for dP.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
       KTileIter it(nnt, m0, p.mask);
       bool have = ok && it.next();
+      bool have1 = false;
       if (have) {
         have = wait_bar(c, qKvFull0, 0, 23);
         if (have) {
           ptx::tc_fence_after();
           issue_S(0);
-          issue_dP(0);
           ptx::mma_commit(c.bar(qSFull));
+          issue_dP(0);
+          ptx::mma_commit(c.bar(qdPFull));
+          have1 = it.next();
+          if (have1) {
+            if (!wait_bar(c, qKvFull0 + 1, 0, 24)) { have = have1 = false; }
+            if (have1) {
+              ptx::tc_fence_after();
+              issue_S(1);
+              ptx::mma_commit(c.bar(qSFull));
+            }
+          }
         }
       }
       int t = 0;
       while (have) {
         const int st = t & 1;
-        have = it.next();
-        // next tile's S into the other buffer while this tile's softmax runs;
-        // that buffer held dS of tile t - 1, read by MMA3'(t - 1)
-        if (have) {
-          if (!wait_bar(c, qKvFull0 + ((t + 1) & 1), ((t + 1) >> 1) & 1, 24)) break;
-          if (t > 0 && !wait_bar(c, qMma3, (t - 1) & 1, 25)) break;
-          ptx::tc_fence_after();
-          issue_S(t + 1);
-        }
         if (!wait_bar(c, qDsFull, t & 1, 26)) break;
         ptx::tc_fence_after();
         // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major over d
@@ -665,11 +673,20 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         }
         ptx::mma_commit(c.bar(qMma3));
         ptx::mma_commit(c.bar(qKvEmpty0 + st));
-        if (have) {
+        if (!have1) break;  // tile t was the last one
+        ptx::tc_fence_after();
+        issue_dP(t + 1);  // the softmax already read dP(t)
+        ptx::mma_commit(c.bar(qdPFull));
+        const bool have2 = it.next();
+        if (have2) {
+          // S(t+2) into buffer t & 1 once dQ(t) has read dS(t) from it
+          if (!wait_bar(c, qKvFull0 + st, ((t + 2) >> 1) & 1, 24)) break;
+          if (!wait_bar(c, qMma3, t & 1, 25)) break;
           ptx::tc_fence_after();
-          issue_dP(t + 1);  // the softmax already read this tile's dP
+          issue_S(t + 2);
           ptx::mma_commit(c.bar(qSFull));
         }
+        have1 = have2;
         ++t;
       }
       ptx::mma_commit(c.bar(qAccFull));
@@ -703,41 +720,57 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ksink = p.mask.sink - n0;
       }
       const uint32_t t_S = t_S0 + (t & 1) * 128;
-      uint32_t sr[64], dr[64];
-      ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
-      ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
-      ptx::tmem_ld32(t_dP + lane_off + wg * 64, dr);
-      ptx::tmem_ld32(t_dP + lane_off + wg * 64 + 32, dr + 32);
-      ptx::tmem_wait_ld();
+      // phase 1: P from S (registers)
+      float pv[64];
+      {
+        uint32_t sr[64];
+        ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
+        ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int k0 = wg * 64 + cc * 32;  // first key of this chunk within the tile
+          const uint32_t live =
+              bits_between(klo - k0, khi - k0 + 1) | bits_between(-k0, ksink - k0);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            float bv[4];
+            if constexpr (BIAS) {
+              const float4 b4 = __ldg(reinterpret_cast<const float4*>(brow + n0 + k0 + e4));
+              bv[0] = b4.x;
+              bv[1] = b4.y;
+              bv[2] = b4.z;
+              bv[3] = b4.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = e4 + u;
+              float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, nl);
+              if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
+              pv[cc * 32 + e] = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
+            }
+          }
+        }
+      }
+      // phase 2: dS = P (dP - D), fp16 pairs over the (already read) front
+      // half of this group's S columns (A operand of dQ)
+      if (!wait_bar(c, qdPFull, t & 1, 29)) { ok = false; break; }
+      ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int k0 = wg * 64 + cc * 32;  // first key of this chunk within the tile
-        const uint32_t live =
-            bits_between(klo - k0, khi - k0 + 1) | bits_between(-k0, ksink - k0);
+        uint32_t dr[32];
+        ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
+        ptx::tmem_wait_ld();
         uint32_t dk[16];
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
-          float bv[4];
-          if constexpr (BIAS) {
-            const float4 b4 = __ldg(reinterpret_cast<const float4*>(brow + n0 + k0 + e4));
-            bv[0] = b4.x;
-            bv[1] = b4.y;
-            bv[2] = b4.z;
-            bv[3] = b4.w;
-          }
           float de[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e4 + u;
-            float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, nl);
-            if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
-            const float pv = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
-            de[u] = pv * (__uint_as_float(dr[cc * 32 + e]) - dl);
-          }
+          for (int u = 0; u < 4; ++u)
+            de[u] = pv[cc * 32 + e4 + u] * (__uint_as_float(dr[e4 + u]) - dl);
           dk[e4 / 2] = pack_half2(de[0], de[1]);
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
         }
-        // dS fp16 pairs over the (already read) front half of this group's S columns
         ptx::tmem_st16(t_S + lane_off + wg * 64 + cc * 16, dk);
       }
       ptx::tmem_wait_st();
