@@ -414,12 +414,24 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 #pragma unroll
               for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
             }
+            // x = S scale log2e - LSE log2e (+ bias log2e), two queries per instruction
+            float x[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = e4 + u;
-              float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, lv[u] * -kLog2e);
-              if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
-              pv[cc * 32 + e] = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
+            for (int u = 0; u < 4; u += 2) {
+              float n0, n1;
+              ptx::mul2(n0, n1, lv[u], lv[u + 1], -kLog2e, -kLog2e);
+              ptx::fma2(x[u], x[u + 1], __uint_as_float(sr[cc * 32 + e4 + u]),
+                        __uint_as_float(sr[cc * 32 + e4 + u + 1]), p.scale_log2, p.scale_log2,
+                        n0, n1);
+              if constexpr (BIAS)
+                ptx::fma2(x[u], x[u + 1], bv[u], bv[u + 1], kLog2e, kLog2e, x[u], x[u + 1]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[cc * 32 + e4 + u] = ptx::ex2(x[u]);
+            if (partial) {  // warp-uniform: only tiles the mask cuts need the per-query test
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (!((live >> (e4 + u)) & 1u)) pv[cc * 32 + e4 + u] = 0.f;
             }
             pk[cc * 16 + e4 / 2] = pack_half2(pv[cc * 32 + e4], pv[cc * 32 + e4 + 1]);
             pk[cc * 16 + e4 / 2 + 1] = pack_half2(pv[cc * 32 + e4 + 2], pv[cc * 32 + e4 + 3]);
@@ -453,10 +465,15 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float de[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = e4 + u;
-            de[u] = pv[cc * 32 + e] * (__uint_as_float(dr[e]) - dv[u]);
-            if constexpr (DBIAS) atomicAdd(dbrow + (int64_t)(q0 + e) * p.Sk, de[u]);
+          for (int u = 0; u < 4; u += 2) {
+            float t0, t1;
+            ptx::sub2(t0, t1, __uint_as_float(dr[e4 + u]), __uint_as_float(dr[e4 + u + 1]), dv[u],
+                      dv[u + 1]);
+            ptx::mul2(de[u], de[u + 1], pv[cc * 32 + e4 + u], pv[cc * 32 + e4 + u + 1], t0, t1);
+          }
+          if constexpr (DBIAS) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) atomicAdd(dbrow + (int64_t)(q0 + e4 + u) * p.Sk, de[u]);
           }
           dk[e4 / 2] = pack_half2(de[0], de[1]);
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
@@ -742,12 +759,21 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
               bv[2] = b4.z;
               bv[3] = b4.w;
             }
+            float x[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = e4 + u;
-              float x = fmaf(__uint_as_float(sr[cc * 32 + e]), p.scale_log2, nl);
-              if constexpr (BIAS) x = fmaf(bv[u], kLog2e, x);
-              pv[cc * 32 + e] = ((live >> e) & 1u) ? ptx::ex2(x) : 0.f;
+            for (int u = 0; u < 4; u += 2) {
+              ptx::fma2(x[u], x[u + 1], __uint_as_float(sr[cc * 32 + e4 + u]),
+                        __uint_as_float(sr[cc * 32 + e4 + u + 1]), p.scale_log2, p.scale_log2,
+                        nl, nl);
+              if constexpr (BIAS)
+                ptx::fma2(x[u], x[u + 1], bv[u], bv[u + 1], kLog2e, kLog2e, x[u], x[u + 1]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[cc * 32 + e4 + u] = ptx::ex2(x[u]);
+            if (partial) {  // warp-uniform: only tiles the mask cuts need the per-key test
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (!((live >> (e4 + u)) & 1u)) pv[cc * 32 + e4 + u] = 0.f;
             }
           }
         }
@@ -766,8 +792,12 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         for (int e4 = 0; e4 < 32; e4 += 4) {
           float de[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            de[u] = pv[cc * 32 + e4 + u] * (__uint_as_float(dr[e4 + u]) - dl);
+          for (int u = 0; u < 4; u += 2) {
+            float t0, t1;
+            ptx::sub2(t0, t1, __uint_as_float(dr[e4 + u]), __uint_as_float(dr[e4 + u + 1]), dl,
+                      dl);
+            ptx::mul2(de[u], de[u + 1], pv[cc * 32 + e4 + u], pv[cc * 32 + e4 + u + 1], t0, t1);
+          }
           dk[e4 / 2] = pack_half2(de[0], de[1]);
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
         }
