@@ -99,6 +99,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Arrives on the mbarrier once every cp.async this thread issued so far has
+// landed; .noinc: the arrival counts against the barrier's expected count.
+// A consumer that reads the data through the async proxy (tcgen05.mma)
+// issues fence_async_shared() after its wait.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(

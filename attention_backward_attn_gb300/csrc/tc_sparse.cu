@@ -7,7 +7,8 @@
 //   dS = P (dP - D) with D = rowsum(dO * O);  dQ = scale dS selKv;
 //   dKV = scale dS^T Q + P^T dO, added into the rows it was gathered from.
 //
-// One CTA per (query token i, KV head g). The r = 64 query heads of the KV
+// One work item per (query token i, KV head g); a persistent CTA per SM takes
+// items in a fixed stride. The r = 64 query heads of the KV
 // head and their 64 dO rows are stacked into one 128-row operand
 // X = [Q_i ; dO_i] (fp16, eight 128B-swizzled slabs of 64 columns), so S and
 // dP come out of one MMA and the thread that owns a selected row sees S and
@@ -38,12 +39,15 @@
 // dKV^T buffers, [256, 512) dQ^T (chunk c of 128 d at 256 + 64 c, one column
 // per head).
 //
-// Warp roles (512 threads): warp 0 builds the selected-row list and issues
-// the TMA copies of X; warp 1 owns TMEM and lane 0 issues the MMAs; warps 2-3
-// load KV rows; warps 4-15 convert X from bf16 to fp16 in place, then warps
-// 4-7 run the softmax (thread = selected row) and warps 8-11 / 12-15 drain
-// the two dKV^T buffers and write dQ (thread = column d). Every wait is
-// bounded (tc_util.cuh).
+// Warp roles (512 threads): warp 0 builds the selected-row list of each
+// token (two buffers, so the list of the next token is ready early) and
+// issues the TMA copies of X; warp 1 owns TMEM and lane 0 issues the MMAs;
+// warps 2-3 load KV rows (they run on into the next token's tiles while the
+// current one finishes); warps 4-7 convert X from bf16 to fp16 in place and
+// run the softmax (thread = selected row); warps 8-11 / 12-15 drain the two
+// dKV^T buffers and write dQ (thread = column d). Between tokens the drain
+// is still reducing the last tile while X of the next token loads and
+// converts. Every wait is bounded (tc_util.cuh).
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -62,35 +66,41 @@ constexpr int kSpR = 64;          // query heads per KV head
 constexpr int kSpMaxRows = 1024;  // selected rows per (token, KV head)
 constexpr int kSpSlots = 3;       // KV ring depth
 constexpr int kSpSlot = 16384;    // bytes per slot / per X or G slab
-constexpr int kSpConvThreads = 384;  // warps 4-15 convert X
 
 struct SpSmem {
   static constexpr int X = 0;                          // 8 slabs: rows 0-63 Q, 64-127 dO
   static constexpr int KV = X + 8 * kSpSlot;           // ring of kSpSlots slots
   static constexpr int G = KV + kSpSlots * kSpSlot;    // slab 0 scale dS^T, slab 1 P^T
-  static constexpr int ROWS = G + 2 * kSpSlot;         // int32 row ids into the fp16 KV copy
-  static constexpr int LSE = ROWS + 4 * kSpMaxRows;    // 64 fp32: LSE log2e, +inf if not finite
-  static constexpr int DLT = LSE + 4 * kSpR;           // 64 fp32: D
-  static constexpr int BAR = DLT + 4 * kSpR;           // mbarriers
-  static constexpr int MISC = BAR + 256;               // TMEM base, abort flag, row count
+  static constexpr int ROWS = G + 2 * kSpSlot;         // 2 buffers: int32 row ids of a token
+  static constexpr int LSE = ROWS + 2 * 4 * kSpMaxRows;  // 2 x 64 fp32: LSE log2e (+inf if not finite)
+  static constexpr int DLT = LSE + 2 * 4 * kSpR;       // 2 x 64 fp32: D
+  static constexpr int BAR = DLT + 2 * 4 * kSpR;       // mbarriers
+  static constexpr int MISC = BAR + 256;               // TMEM base, abort flag, 2 row counts
   static constexpr int TOTAL = MISC + 16;
 };
 static_assert(SpSmem::TOTAL <= 227 * 1024, "shared memory budget");
 
-// mbarriers; the dKV^T buffers b = 0, 1 hold the row halves nh = b of a tile.
+// mbarriers. Per token: sXFull, sXReady, sXFree, sRowsReady/sRowsFree (one
+// pair per row-list buffer, tokens alternate), sDqFull, sDqFree. Per tile
+// (running counters across the tokens of the CTA): the ring, sStFull, sGFull,
+// sGFree, and the two dKV^T buffers (b = 0, 1 hold the row halves nh = b).
 enum SpBar {
-  sXFull = 0,       // X landed (TMA transaction count)
-  sXReady = 1,      // X converted to fp16 (kSpConvThreads arrivals)
-  sKvFull0 = 2,     // ring slot filled (x3, 64 loader arrivals)
-  sKvEmpty0 = 5,    // ring slot consumed by its MMAs (x3)
-  sStFull = 8,      // S^T | dP^T of the tile in TMEM
-  sGFull = 9,       // G written, S^T | dP^T read (128 arrivals)
-  sGFree = 10,      // the MMAs of the tile stopped reading G
-  sDkvFull0 = 11,   // a dKV^T block is in buffer b (x2)
-  sDkvEmpty0 = 13,  // the drain has read buffer b (x2, 128 arrivals)
-  sDqFull = 15,     // dQ^T complete
-  sDone = 16,       // every MMA of the CTA completed (teardown)
-  kSpBars = 17
+  sXFull = 0,        // X landed (TMA transaction count)
+  sXReady = 1,       // X converted to fp16 (128 softmax threads)
+  sXFree = 2,        // the MMAs of the token stopped reading X
+  sRowsReady0 = 3,   // row list, N, LSE and D of a token written (x2, 32 lanes)
+  sRowsFree0 = 5,    // every role is done with the token's row list (x2, 449 arrivals)
+  sKvFull0 = 7,      // ring slot filled (x3, 64 loader arrivals)
+  sKvEmpty0 = 10,    // ring slot consumed by its MMAs (x3)
+  sStFull = 13,      // S^T | dP^T of the tile in TMEM
+  sGFull = 14,       // G written, S^T | dP^T read (128 arrivals)
+  sGFree = 15,       // the MMAs of the tile stopped reading G
+  sDkvFull0 = 16,    // a dKV^T block is in buffer b (x2)
+  sDkvEmpty0 = 18,   // the drain has read buffer b (x2, 128 arrivals)
+  sDqFull = 20,      // dQ^T of the token complete
+  sDqFree = 21,      // the drain has read dQ^T (256 arrivals)
+  sDone = 22,        // every MMA of the CTA completed (teardown)
+  kSpBars = 23
 };
 
 struct SpParams {
@@ -170,8 +180,15 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = (int)(blockIdx.x % p.Hk);
-  const int i = p.Sq - 1 - (int)(blockIdx.x / p.Hk);  // later tokens select more rows: first
+  // Persistent: this CTA takes work items u = blockIdx.x + k gridDim.x, item
+  // u = (token Sq - 1 - u / Hk, KV head u % Hk): later tokens select more rows
+  // and go first, and a strided share keeps the CTAs balanced.
+  const int n_items = p.Sq * p.Hk;
+  const int n_tok = ((int)blockIdx.x < n_items)
+                        ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                        : 0;
+  auto item_i = [&](int k) { return p.Sq - 1 - ((int)blockIdx.x + k * (int)gridDim.x) / p.Hk; };
+  auto item_g = [&](int k) { return ((int)blockIdx.x + k * (int)gridDim.x) % p.Hk; };
 
   // everything below reads what the pre-pass wrote (launched as its
   // programmatic dependent, this grid may start before the pre-pass ends)
@@ -191,128 +208,173 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  int32_t* rows = reinterpret_cast<int32_t*>(smem + L::ROWS);
-  float* lse_s = reinterpret_cast<float*>(smem + L::LSE);
-  float* dlt_s = reinterpret_cast<float*>(smem + L::DLT);
-  volatile int* nrows_s = reinterpret_cast<volatile int*>(smem + L::MISC + 8);
+  volatile int* nrows_s = reinterpret_cast<volatile int*>(smem + L::MISC + 8);  // [2]
 
   if (threadIdx.x == 0) {
     uint32_t counts[kSpBars];
     for (int b = 0; b < kSpBars; ++b) counts[b] = 1;
-    counts[sXReady] = kSpConvThreads;
+    counts[sXReady] = 128;
+    counts[sRowsReady0] = counts[sRowsReady0 + 1] = 32;
+    // drain 256 + loaders 64 + softmax 128 + MMA thread 1: once all of them
+    // arrived, every role has also passed the token's sRowsReady phase
+    counts[sRowsFree0] = counts[sRowsFree0 + 1] = 449;
     for (int s = 0; s < kSpSlots; ++s) counts[sKvFull0 + s] = 64;
     counts[sGFull] = 128;
     counts[sDkvEmpty0] = counts[sDkvEmpty0 + 1] = 128;
+    counts[sDqFree] = 256;
     for (int b = 0; b < kSpBars; ++b) ptx::mbar_init(c.bar(b), counts[b]);
     *c.abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmdO);
   }
-  if (warp == 0) {
-    const int n = build_rows(p, i, g, rows, lane);
-    if (lane == 0) *nrows_s = n;
-  } else if (warp == 1) {
+  if (warp == 1) {
     ptx::tmem_alloc(sbase + L::MISC, 512);
     ptx::tmem_relinquish();
-  } else if (warp == 2) {
-    for (int h = lane; h < kSpR; h += 32) {
-      const int64_t r = (int64_t)(g * kSpR + h) * p.Sq + i;
-      const float lv = p.lse[r];
-      lse_s[h] = isfinite(lv) ? lv * kLog2e : INFINITY;  // +inf: P = 0 for the head
-      dlt_s[h] = p.delta[r];
-    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
-  const int N = *nrows_s;
-  const int T = (N + 127) / 128;
   const uint32_t sX = sbase + L::X, sKV = sbase + L::KV, sG = sbase + L::G;
+  auto rows_of = [&](int b) { return reinterpret_cast<int32_t*>(smem + L::ROWS + b * 4 * kSpMaxRows); };
+  auto rows_addr = [&](int b) { return sbase + L::ROWS + b * 4 * kSpMaxRows; };
+  auto lse_of = [&](int b) { return reinterpret_cast<float*>(smem + L::LSE + b * 4 * kSpR); };
+  auto dlt_of = [&](int b) { return reinterpret_cast<float*>(smem + L::DLT + b * 4 * kSpR); };
 
   if (warp == 0) {
-    // --------------------------------------------------- X: TMA copies --
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(c.bar(sXFull), 8 * kSpSlot);
-      for (int s = 0; s < 8; ++s) {
-        ptx::tma_load_3d(sX + s * kSpSlot, &tmQ, c.bar(sXFull), 64 * s, g * kSpR, i);
-        ptx::tma_load_3d(sX + s * kSpSlot + kSpSlot / 2, &tmdO, c.bar(sXFull), 64 * s, g * kSpR,
-                         i);
+    // ------------------------- per token: row list, LSE / D, X TMA copies --
+    int x_issued = 0;
+    for (int k = 0; k < n_tok; ++k) {
+      const int b = k & 1, i = item_i(k), g = item_g(k);
+      if (k >= 2 && !wait_bar(c, sRowsFree0 + b, (uint32_t)((k - 2) >> 1) & 1u, 30)) break;
+      const int n = build_rows(p, i, g, rows_of(b), lane);
+      for (int h = lane; h < kSpR; h += 32) {
+        const int64_t r = (int64_t)(g * kSpR + h) * p.Sq + i;
+        const float lv = p.lse[r];
+        lse_of(b)[h] = isfinite(lv) ? lv * kLog2e : INFINITY;  // +inf: P = 0 for the head
+        dlt_of(b)[h] = p.delta[r];
       }
-      drain_bar(c, sXFull, 0);  // in flight until it lands, whatever else happens
+      if (lane == 0) nrows_s[b] = n;
+      __syncwarp();
+      ptx::mbar_arrive(c.bar(sRowsReady0 + b));
+      // X of this token once the previous token's MMAs stopped reading X
+      if (k >= 1 && !wait_bar(c, sXFree, (uint32_t)(k - 1) & 1u, 31)) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(c.bar(sXFull), 8 * kSpSlot);
+        for (int s = 0; s < 8; ++s) {
+          ptx::tma_load_3d(sX + s * kSpSlot, &tmQ, c.bar(sXFull), 64 * s, g * kSpR, i);
+          ptx::tma_load_3d(sX + s * kSpSlot + kSpSlot / 2, &tmdO, c.bar(sXFull), 64 * s,
+                           g * kSpR, i);
+        }
+      }
+      ++x_issued;
     }
+    // the last X copy lands before the CTA moves on, whatever else happened
+    if (lane == 0 && x_issued > 0) drain_bar(c, sXFull, (uint32_t)(x_issued - 1) & 1u);
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      bool ok = wait_bar(c, sXReady, 0, 40);
-      ptx::tc_fence_after();
       constexpr uint32_t idA = ptx::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t idB = ptx::idesc_f16_f32(128, 64, true, true);
       constexpr uint32_t idC = ptx::idesc_f16_f32(128, 64, true, false);
       const uint32_t tS = tmem, tQ = tmem + 256;
+      bool ok = true;
       int slot = 0;
       uint32_t ph = 0;
       int issued[2] = {0, 0}, freed[2] = {0, 0};
-      // MMA-A of tile t: [S^T | dP^T] = KV X^T over the 8 column slabs
-      auto mma_a = [&]() {
-        for (int s = 0; s < 8 && ok; ++s) {
-          if (!wait_bar(c, sKvFull0 + slot, ph, 42)) { ok = false; break; }
-          ptx::tc_fence_after();
-          const uint32_t a0 = sKV + slot * kSpSlot, b0 = sX + s * kSpSlot;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            ptx::mma_ss(tS, ptx::smem_desc_sw128(a0 + 32 * k, 16, 1024),
-                        ptx::smem_desc_sw128(b0 + 32 * k, 16, 1024), idA, (s | k) != 0);
-          ptx::mma_commit(c.bar(sKvEmpty0 + slot));
-          if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
-        }
-        if (ok) ptx::mma_commit(c.bar(sStFull));
-      };
-      if (T > 0) mma_a();
-      for (int t = 0; t < T && ok; ++t) {
-        // MMA-B: dQ^T += KV^T (scale dS^T), 16 selected rows per K step
-        if (!wait_bar(c, sGFull, (uint32_t)t & 1u, 43)) { ok = false; break; }
+      int gt = 0;  // tiles of this CTA so far (all tokens)
+      // One ring slot of MMA-A: [S^T | dP^T] (+)= KV X^T over column slab s.
+      auto a_slab = [&](int s) {
+        if (!wait_bar(c, sKvFull0 + slot, ph, 42)) return false;
+        ptx::fence_async_shared();  // cp.async data -> async proxy
         ptx::tc_fence_after();
-        for (int cc = 0; cc < 4 && ok; ++cc) {
-          for (int nh = 0; nh < 2 && ok; ++nh) {
-            if (!wait_bar(c, sKvFull0 + slot, ph, 44)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t a0 = sKV + slot * kSpSlot;
+        const uint32_t a0 = sKV + slot * kSpSlot, b0 = sX + s * kSpSlot;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              ptx::mma_ss(tQ + 64 * cc, ptx::smem_desc_sw128(a0 + 2048 * k, kSpSlot / 2, 1024),
-                          ptx::smem_desc_sw128(sG + (64 * nh + 16 * k) * 128, kSpSlot, 1024), idB,
-                          (t | nh | k) != 0);
-            ptx::mma_commit(c.bar(sKvEmpty0 + slot));
-            if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
-          }
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_ss(tS, ptx::smem_desc_sw128(a0 + 32 * k, 16, 1024),
+                      ptx::smem_desc_sw128(b0 + 32 * k, 16, 1024), idA, (s | k) != 0);
+        ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+        return true;
+      };
+      // One ring slot of MMA-B: dQ^T (d chunk j / 2) += KV^T (scale dS^T) over
+      // the 64 selected rows of half j % 2, 16 per K step.
+      auto b_slot = [&](int t, int j) {
+        const int cc = j >> 1, nh = j & 1;
+        if (!wait_bar(c, sKvFull0 + slot, ph, 44)) return false;
+        ptx::fence_async_shared();  // cp.async data -> async proxy
+        ptx::tc_fence_after();
+        const uint32_t a0 = sKV + slot * kSpSlot;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::mma_ss(tQ + 64 * cc, ptx::smem_desc_sw128(a0 + 2048 * kk, kSpSlot / 2, 1024),
+                      ptx::smem_desc_sw128(sG + (64 * nh + 16 * kk) * 128, kSpSlot, 1024), idB,
+                      (t | nh | kk) != 0);
+        ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+        return true;
+      };
+      // One MMA-C block: dKV^T (d chunk h / 2, row half h % 2) = X^T G into
+      // buffer h % 2, once the drain has read that buffer's previous block.
+      auto c_block = [&](int h) {
+        const int cc = h >> 1, bb = h & 1;
+        while (freed[bb] < issued[bb]) {
+          if (!wait_bar(c, sDkvEmpty0 + bb, (uint32_t)freed[bb] & 1u, 45)) return false;
+          ++freed[bb];
         }
-        if (!ok) break;
-        // the softmax has read S^T | dP^T of tile t (sGFull): tile t + 1 may start
-        if (t + 1 < T) mma_a();
-        if (!ok) break;
-        // MMA-C: dKV^T blocks (d chunk cc, row half nh) into buffer nh
-        for (int h = 0; h < 8 && ok; ++h) {
-          const int cc = h >> 1, b = h & 1;
-          while (ok && freed[b] < issued[b]) {
-            ok = wait_bar(c, sDkvEmpty0 + b, (uint32_t)freed[b] & 1u, 45);
-            ++freed[b];
+        ptx::tc_fence_after();
+        const uint32_t a0 = sX + 2 * cc * kSpSlot;
+        const uint32_t g0 = sG + 64 * bb * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_ss(tmem + 128 + 64 * bb, ptx::smem_desc_sw128(a0 + 2048 * kk, kSpSlot, 1024),
+                      ptx::smem_desc_sw128(g0 + (kk >> 2) * kSpSlot + (kk & 3) * 32, 16, 1024),
+                      idC, kk != 0);
+        ptx::mma_commit(c.bar(sDkvFull0 + bb));
+        ++issued[bb];
+        return true;
+      };
+      for (int k = 0; k < n_tok && ok; ++k) {
+        const int b = k & 1;
+        if (!wait_bar(c, sRowsReady0 + b, (uint32_t)(k >> 1) & 1u, 40)) break;
+        const int T = (nrows_s[b] + 127) / 128;
+        ptx::mbar_arrive(c.bar(sRowsFree0 + b));
+        if (!wait_bar(c, sXReady, (uint32_t)k & 1u, 41)) break;
+        ptx::tc_fence_after();
+        if (T > 0) {
+          for (int s = 0; s < 8 && ok; ++s) ok = a_slab(s);
+          if (!ok) break;
+          ptx::mma_commit(c.bar(sStFull));
+        }
+        for (int t = 0; t < T && ok; ++t, ++gt) {
+          if (!wait_bar(c, sGFull, (uint32_t)gt & 1u, 43)) { ok = false; break; }
+          // the first dQ^T MMA of a token overwrites what the drain read last token
+          if (t == 0 && k > 0 && !wait_bar(c, sDqFree, (uint32_t)(k - 1) & 1u, 46)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          // The drain paces the MMA-C blocks; between two of them the ring
+          // slots of this tile's MMA-B and of the next tile's MMA-A are
+          // consumed, so the KV loads stream while the drain works. (The
+          // softmax read S^T | dP^T of this tile before sGFull: MMA-A of the
+          // next tile may overwrite it.)
+          const bool next = t + 1 < T;
+          for (int j = 0; j < 8 && ok; ++j) {
+            ok = c_block(j) && b_slot(t, j) && (!next || a_slab(j));
           }
           if (!ok) break;
-          const uint32_t a0 = sX + 2 * cc * kSpSlot;
-          const uint32_t g0 = sG + 64 * b * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            ptx::mma_ss(tmem + 128 + 64 * b, ptx::smem_desc_sw128(a0 + 2048 * k, kSpSlot, 1024),
-                        ptx::smem_desc_sw128(g0 + (k >> 2) * kSpSlot + (k & 3) * 32, 16, 1024),
-                        idC, k != 0);
-          ptx::mma_commit(c.bar(sDkvFull0 + b));
-          ++issued[b];
+          ptx::mma_commit(c.bar(sGFree));
+          if (next) ptx::mma_commit(c.bar(sStFull));
         }
-        if (ok) ptx::mma_commit(c.bar(sGFree));
+        if (!ok) break;
+        // with no tiles, dQ^T was not touched, but sDqFull of this token must not
+        // complete before the drain consumed the previous one
+        if (T == 0 && k > 0 && !wait_bar(c, sDqFree, (uint32_t)(k - 1) & 1u, 47)) break;
+        ptx::mma_commit(c.bar(sXFree));   // completes when every MMA reading X did
+        ptx::mma_commit(c.bar(sDqFull));  // dQ^T of the token (T = 0: nothing to wait for)
       }
-      if (ok && T > 0) ptx::mma_commit(c.bar(sDqFull));
       ptx::mma_commit(c.bar(sDone));  // completes once every MMA above has
     }
   } else if (warp < 4) {
@@ -323,88 +385,96 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int tl = (int)threadIdx.x - 64;
     const int c8 = tl & 7, r0 = tl >> 3;
     const uint32_t swz = (uint32_t)((c8 ^ r0) << 4);
-    int slot = 0, pend = -1;
+    int slot = 0;
     uint32_t ph = 0;
     bool ok = true;
-    auto publish = [&](int next) {  // the previous fill is complete: make it visible
-      if (pend >= 0) {
-        ptx::cp_async_wait<1>();
-        ptx::fence_async_shared();
-        ptx::mbar_arrive(c.bar(sKvFull0 + pend));
-      }
-      pend = next;
+    // Each fill arrives on its slot's sKvFull when its own copies land (the
+    // MMA thread fences the async proxy after the wait), so all three slots
+    // can be in flight and no fill waits on the loader's next step.
+    // MMA-A slot: [128 rows][64 d], columns 64 s of the tile's rows rt[0, 128)
+    auto fill_a = [&](const int32_t* rt, int s) {
+      if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 31)) return false;
+      const uint32_t dst = sKV + slot * kSpSlot + swz;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk)
+        ptx::cp_async_16(dst + (r0 + 8 * kk) * 128,
+                         p.kv16 + (int64_t)rt[r0 + 8 * kk] * kSpD + 8 * c8 + 64 * s);
+      ptx::cp_async_arrive_noinc(c.bar(sKvFull0 + slot));
+      if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      return true;
     };
-    for (int t = 0; t < T && ok; ++t) {
-      const __half* src[16];
+    // MMA-B slot j: [64 rows][128 d] (rows 64 (j % 2) on, d chunk j / 2) as two
+    // [64][64] halves 8 KB apart
+    auto fill_b = [&](const int32_t* rt, int j) {
+      const int cc = j >> 1, nh = j & 1;
+      if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 32)) return false;
+      const uint32_t dst = sKV + slot * kSpSlot + swz;
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        src[k] = p.kv16 + (int64_t)rows[128 * t + r0 + 8 * k] * kSpD + 8 * c8;
-      for (int s = 0; s < 8; ++s) {  // pass 1: [128 rows][64 d], columns 64 s
-        if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 31)) { ok = false; break; }
-        const uint32_t dst = sKV + slot * kSpSlot + swz;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) ptx::cp_async_16(dst + (r0 + 8 * k) * 128, src[k] + 64 * s);
-        ptx::cp_async_commit();
-        publish(slot);
-        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      for (int kk = 0; kk < 8; ++kk) {
+        const __half* sp = p.kv16 + (int64_t)rt[64 * nh + r0 + 8 * kk] * kSpD + 8 * c8 + 128 * cc;
+        ptx::cp_async_16(dst + (r0 + 8 * kk) * 128, sp);
+        ptx::cp_async_16(dst + kSpSlot / 2 + (r0 + 8 * kk) * 128, sp + 64);
       }
-      for (int h = 0; h < 8 && ok; ++h) {  // pass 2: [64 rows][128 d] as two [64][64] halves
-        const int cc = h >> 1, nh = h & 1;
-        if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 32)) { ok = false; break; }
-        const uint32_t dst = sKV + slot * kSpSlot + swz;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const __half* sp = src[8 * nh + kk] + 128 * cc;
-          ptx::cp_async_16(dst + (r0 + 8 * kk) * 128, sp);
-          ptx::cp_async_16(dst + kSpSlot / 2 + (r0 + 8 * kk) * 128, sp + 64);
-        }
-        ptx::cp_async_commit();
-        publish(slot);
-        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      ptx::cp_async_arrive_noinc(c.bar(sKvFull0 + slot));
+      if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+      return true;
+    };
+    for (int k = 0; k < n_tok && ok; ++k) {
+      const int b = k & 1;
+      const uint32_t rph = (uint32_t)(k >> 1) & 1u;
+      if (!wait_bar(c, sRowsReady0 + b, rph, 35)) break;
+      const int T = (nrows_s[b] + 127) / 128;
+      const int32_t* rows = rows_of(b);
+      // the order in which the MMA thread consumes the ring
+      if (T > 0)
+        for (int s = 0; s < 8 && ok; ++s) ok = fill_a(rows, s);
+      for (int t = 0; t < T && ok; ++t) {
+        const bool next = t + 1 < T;
+        for (int j = 0; j < 8 && ok; ++j)
+          ok = fill_b(rows + 128 * t, j) && (!next || fill_a(rows + 128 * (t + 1), j));
       }
+      if (ok) ptx::mbar_arrive(c.bar(sRowsFree0 + b));  // row ids no longer read
     }
-    ptx::cp_async_wait<0>();
-    if (pend >= 0) {
-      ptx::fence_async_shared();
-      ptx::mbar_arrive(c.bar(sKvFull0 + pend));
-    }
-  } else {
-    // ------------------------------------------- X: bf16 -> fp16 in place --
-    {
-      const bool ok = wait_bar(c, sXFull, 0, 50);
+    ptx::cp_async_commit();
+    ptx::cp_async_wait<0>();  // no copy may still write shared memory at exit
+  } else if (warp < 8) {
+    // ------------- per token: X bf16 -> fp16 in place, then the softmax --
+    const int q4 = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    const int n = 32 * q4 + lane;  // selected row of a tile
+    const uint32_t grow = sG + n * 128;
+    const uint32_t sw = (uint32_t)(n & 7);
+    int gt = 0;
+    bool ok = true;
+    for (int k = 0; k < n_tok && ok; ++k) {
+      const int b = k & 1;
+      if (!wait_bar(c, sXFull, (uint32_t)k & 1u, 50)) break;
       float amax = 0.f;
-      if (ok) {
-        // 8192 16-byte chunks over 384 threads; 4 loads in flight per thread
+      {
+        // 8192 16-byte chunks over 128 threads; 4 loads in flight per thread
         constexpr int kChunks = 8 * kSpSlot / 16;
-        for (int e0 = (int)threadIdx.x - 128; e0 < kChunks; e0 += 4 * kSpConvThreads) {
+        for (int e0 = (int)threadIdx.x - 128; e0 < kChunks; e0 += 4 * 128) {
           uint4 v[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (e0 + u * kSpConvThreads < kChunks)
-              v[u] = ptx::ld_shared_v4_u32(sX + 16 * (e0 + u * kSpConvThreads));
+          for (int u = 0; u < 4; ++u) v[u] = ptx::ld_shared_v4_u32(sX + 16 * (e0 + u * 128));
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (e0 + u * kSpConvThreads < kChunks) {
-              amax = bf16x8_to_half(&v[u], amax);
-              ptx::st_shared_v4(sX + 16 * (e0 + u * kSpConvThreads), v[u].x, v[u].y, v[u].z,
-                                v[u].w);
-            }
+          for (int u = 0; u < 4; ++u) {
+            amax = bf16x8_to_half(&v[u], amax);
+            ptx::st_shared_v4(sX + 16 * (e0 + u * 128), v[u].x, v[u].y, v[u].z, v[u].w);
+          }
         }
       }
       if (__any_sync(0xffffffffu, amax >= 65520.f) && lane == 0)
         report(p.status, ATTN_ERR_RANGE, 16);
       ptx::fence_async_shared();
       ptx::mbar_arrive(c.bar(sXReady));
-    }
-    const int q4 = warp & 3;
-    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    if (warp < 8) {
-      // ------------------------------------- softmax: thread = selected row --
-      const int n = 32 * q4 + lane;
-      const uint32_t grow = sG + n * 128;
-      const uint32_t sw = (uint32_t)(n & 7);
-      for (int t = 0; t < T; ++t) {
-        if (!wait_bar(c, sStFull, (uint32_t)t & 1u, 60)) break;
+      if (!wait_bar(c, sRowsReady0 + b, (uint32_t)(k >> 1) & 1u, 51)) break;
+      const int N = nrows_s[b];
+      const int T = (N + 127) / 128;
+      const float* lse_s = lse_of(b);
+      const float* dlt_s = dlt_of(b);
+      for (int t = 0; t < T; ++t, ++gt) {
+        if (!wait_bar(c, sStFull, (uint32_t)gt & 1u, 60)) { ok = false; break; }
         ptx::tc_fence_after();
         const bool valid = 128 * t + n < N;
         uint32_t pk[32], dk[32];
@@ -417,20 +487,22 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const int h = 32 * half + j;
-            float pr[2], ds[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float e = fmaf(__uint_as_float(sv[j + u]), p.scale_log2, -lse_s[h + u]);
-              pr[u] = valid ? ptx::ex2(e) : 0.f;
-              ds[u] = pr[u] * (__uint_as_float(dv[j + u]) - dlt_s[h + u]) * p.scale;
-            }
-            pk[h / 2] = pack_half2(pr[0], pr[1]);
-            dk[h / 2] = pack_half2(ds[0], ds[1]);
+            float x0, x1, pr0, pr1, t0, t1, d0, d1;
+            ptx::fma2(x0, x1, __uint_as_float(sv[j]), __uint_as_float(sv[j + 1]), p.scale_log2,
+                      p.scale_log2, -lse_s[h], -lse_s[h + 1]);
+            pr0 = valid ? ptx::ex2(x0) : 0.f;
+            pr1 = valid ? ptx::ex2(x1) : 0.f;
+            ptx::sub2(t0, t1, __uint_as_float(dv[j]), __uint_as_float(dv[j + 1]), dlt_s[h],
+                      dlt_s[h + 1]);
+            ptx::mul2(d0, d1, pr0, pr1, t0, t1);
+            ptx::mul2(d0, d1, d0, d1, p.scale, p.scale);
+            pk[h / 2] = pack_half2(pr0, pr1);
+            dk[h / 2] = pack_half2(d0, d1);
           }
         }
         ptx::tc_fence_before();
         // G of the previous tile must be out of use
-        if (t > 0 && !wait_bar(c, sGFree, (uint32_t)(t - 1) & 1u, 61)) break;
+        if (gt > 0 && !wait_bar(c, sGFree, (uint32_t)(gt - 1) & 1u, 61)) { ok = false; break; }
         // head h lives in 16-byte chunk h / 8 of the row (slab 0 dS, slab 1 P)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -442,19 +514,28 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         ptx::fence_async_shared();
         ptx::mbar_arrive(c.bar(sGFull));
       }
-    } else {
-      // ------------------------ dKV^T drain and dQ: thread = column d --
-      const int b = warp < 12 ? 0 : 1;  // buffer / row half of this warpgroup
-      const int dl = 32 * q4 + lane;
-      const int ori_rows = p.n_ori * p.Hk;
-      const uint32_t tbuf = tmem + 128 + 64 * b + lane_off;
-      bool ok = true;
-      int used = 0;
+      if (ok) ptx::mbar_arrive(c.bar(sRowsFree0 + b));
+    }
+  } else {
+    // -------------------- per token: dKV^T drain, then dQ: thread = column d --
+    const int q4 = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    const int bb = warp < 12 ? 0 : 1;  // buffer / row half of this warpgroup
+    const int dl = 32 * q4 + lane;
+    const int ori_rows = p.n_ori * p.Hk;
+    const uint32_t tbuf = tmem + 128 + 64 * bb + lane_off;
+    bool ok = true;
+    int used = 0;
+    for (int k = 0; k < n_tok && ok; ++k) {
+      const int b = k & 1, i = item_i(k), g = item_g(k);
+      if (!wait_bar(c, sRowsReady0 + b, (uint32_t)(k >> 1) & 1u, 70)) break;
+      const int N = nrows_s[b];
+      const int T = (N + 127) / 128;
       for (int t = 0; t < T && ok; ++t) {
-        const int nt = min(64, N - 128 * t - 64 * b);  // valid rows of this half (may be <= 0)
-        const uint32_t rt_s = sbase + L::ROWS + 512 * t + 256 * b;
+        const int nt = min(64, N - 128 * t - 64 * bb);  // valid rows of this half (may be <= 0)
+        const uint32_t rt_s = rows_addr(b) + 512 * t + 256 * bb;
         for (int cc = 0; cc < 4; ++cc) {
-          if (!wait_bar(c, sDkvFull0 + b, (uint32_t)used & 1u, 70)) { ok = false; break; }
+          if (!wait_bar(c, sDkvFull0 + bb, (uint32_t)used & 1u, 71)) { ok = false; break; }
           ++used;
           ptx::tc_fence_after();
           uint32_t v[64];
@@ -462,7 +543,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           ptx::tmem_ld32(tbuf + 32, v + 32);
           ptx::tmem_wait_ld();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(c.bar(sDkvEmpty0 + b));
+          ptx::mbar_arrive(c.bar(sDkvEmpty0 + bb));
           float* const ori_base = p.d_ori + 128 * cc + dl;
           float* const cmp_base = p.d_cmp - (int64_t)ori_rows * kSpD + 128 * cc + dl;
 #pragma unroll
@@ -483,29 +564,34 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
         }
       }
-      if (ok) {
-        // dQ: this warpgroup writes d chunks 2 b and 2 b + 1
-        float* dq = p.dq + ((int64_t)i * p.Hq + g * kSpR) * kSpD;
-        if (T == 0) {
-          for (int h = 0; h < kSpR; ++h)
+      if (!ok) break;
+      // dQ of the token: this warpgroup writes d chunks 2 bb and 2 bb + 1
+      if (!wait_bar(c, sDqFull, (uint32_t)k & 1u, 72)) break;
+      ptx::tc_fence_after();
+      float* dq = p.dq + ((int64_t)i * p.Hq + g * kSpR) * kSpD;
+      if (T == 0) {
+        for (int h = 0; h < kSpR; ++h)
 #pragma unroll
-            for (int cc = 2 * b; cc < 2 * b + 2; ++cc) dq[h * kSpD + 128 * cc + dl] = 0.f;
-        } else if (wait_bar(c, sDqFull, 0, 71)) {
-          ptx::tc_fence_after();
+          for (int cc = 2 * bb; cc < 2 * bb + 2; ++cc) dq[h * kSpD + 128 * cc + dl] = 0.f;
+      } else {
 #pragma unroll 1
-          for (int cc = 2 * b; cc < 2 * b + 2; ++cc) {
+        for (int cc = 2 * bb; cc < 2 * bb + 2; ++cc) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t v[32];
-              ptx::tmem_ld32(tmem + lane_off + 256 + 64 * cc + 32 * half, v);
-              ptx::tmem_wait_ld();
+          for (int half = 0; half < 2; ++half) {
+            uint32_t v[32];
+            ptx::tmem_ld32(tmem + lane_off + 256 + 64 * cc + 32 * half, v);
+            ptx::tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                dq[(32 * half + j) * kSpD + 128 * cc + dl] = __uint_as_float(v[j]);
-            }
+            for (int j = 0; j < 32; ++j)
+              dq[(32 * half + j) * kSpD + 128 * cc + dl] = __uint_as_float(v[j]);
           }
         }
       }
+      // dQ^T read: the next token's MMA-B may overwrite it
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(sDqFree));
+      // this token's row list, N, LSE and D are no longer read by anyone
+      ptx::mbar_arrive(c.bar(sRowsFree0 + b));
     }
   }
 
@@ -586,7 +672,15 @@ cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* d
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned grid = (unsigned)pr.Sq * pr.Hk;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int64_t items = (int64_t)pr.Sq * pr.Hk;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);  // persistent: one CTA per SM
   return launch_dependent(attn_bwd_sparse_tc_kernel, dim3(grid), dim3(kSpThreads),
                           (size_t)SpSmem::TOTAL, stream, mq, mdo, p);
 }

@@ -215,6 +215,11 @@ TC_SPARSE = {
     # 500 selected rows per token: four tiles, the last one ragged
     "tc_scfa_rows500": lambda: make_sparse("t4", 44, Sq=96, Hq=64, Hk=1, D=512, n_ori=1000,
                                            n_cmp=250, topk=200, cmp_ratio=4, ori_win_left=299),
+    # about eight work items per persistent CTA: row counts from 0 to two tiles
+    # vary between a CTA's items, and each CTA ends on items with no row
+    "tc_scfa_persistent_mix": lambda: make_sparse("t6", 46, Sq=600, Hq=128, Hk=2, D=512,
+                                                  n_ori=360, n_cmp=90, topk=40, cmp_ratio=4,
+                                                  ori_win_left=200),
     # n_ori < Sq: the first 36 tokens select no row at all (dQ = 0, LSE = -inf)
     "tc_scfa_empty_rows": lambda: make_sparse("t5", 45, Sq=100, Hq=64, Hk=1, D=512, n_ori=64,
                                               n_cmp=16, topk=8, cmp_ratio=4, ori_win_left=15),
