@@ -267,22 +267,29 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     if (lane == 0) {
       constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t id_KV = ptx::idesc_f16_f32(128, D, false, true);
+      // operand descriptors, built once (K steps add their offsets)
+      const uint64_t dK = ptx::smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dV = ptx::smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dDS = ptx::smem_desc_sw128(sDS, 16, 1024);
+      // stage 0 of Q / dO in K-major and MN-major views (stage st: + st kTile)
+      const uint64_t dQk = ptx::smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t ddOk = ptx::smem_desc_sw128(sbase + L::dO, 16, 1024);
+      const uint64_t dQmn = ptx::smem_desc_sw128(sbase + L::Q, kSlab, 1024);
+      const uint64_t ddOmn = ptx::smem_desc_sw128(sbase + L::dO, kSlab, 1024);
       auto issue_S = [&](int st) {  // MMA1 S^T = K Q^T (both K-major over d)
-        const uint32_t sQ = sbase + L::Q + st * L::kTile;
+        const uint64_t dq = ptx::desc_add(dQk, st * L::kTile);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_S, ptx::smem_desc_sw128(sK + off, 16, 1024),
-                      ptx::smem_desc_sw128(sQ + off, 16, 1024), id_S, s > 0);
+          ptx::mma_ss(t_S, ptx::desc_add(dK, off), ptx::desc_add(dq, off), id_S, s > 0);
         }
       };
       auto issue_dP = [&](int st) {  // MMA2 dP^T = V dO^T
-        const uint32_t sdO = sbase + L::dO + st * L::kTile;
+        const uint64_t ddo = ptx::desc_add(ddOk, st * L::kTile);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dP, ptx::smem_desc_sw128(sV + off, 16, 1024),
-                      ptx::smem_desc_sw128(sdO + off, 16, 1024), id_S, s > 0);
+          ptx::mma_ss(t_dP, ptx::desc_add(dV, off), ptx::desc_add(ddo, off), id_S, s > 0);
         }
       };
       // Per tile t: dV(t) as soon as P^T(t) is in shared memory, then S(t+1)
@@ -305,16 +312,15 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       int t = 0;
       while (have) {
         const int st = t & 1;
-        const uint32_t sQ = sbase + L::Q + st * L::kTile;
-        const uint32_t sdO = sbase + L::dO + st * L::kTile;
+        const uint64_t dq_mn = ptx::desc_add(dQmn, st * L::kTile);
+        const uint64_t ddo_mn = ptx::desc_add(ddOmn, st * L::kTile);
         if (!wait_bar(c, kP1Full, t & 1, 4)) break;
         ptx::tc_fence_after();
         // MMA3 dV += P^T dO : A = P^T K-major over queries, B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dV, ptx::smem_desc_sw128(sDS + off, 16, 1024),
-                      ptx::smem_desc_sw128(sdO + s * 2048, kSlab, 1024), id_KV,
+          ptx::mma_ss(t_dV, ptx::desc_add(dDS, off), ptx::desc_add(ddo_mn, s * 2048), id_KV,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(kMma3));
@@ -336,7 +342,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
           const uint32_t a_col = t_dP + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_dK, a_col, ptx::smem_desc_sw128(sQ + s * 2048, kSlab, 1024), id_KV,
+          ptx::mma_ts(t_dK, a_col, ptx::desc_add(dq_mn, s * 2048), id_KV,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(kQEmpty0 + st));
@@ -628,23 +634,28 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     if (lane == 0) {
       constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t id_dQ = ptx::idesc_f16_f32(128, D, false, true);
+      // operand descriptors, built once (K steps add their offsets)
+      const uint64_t dQ = ptx::smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t ddO = ptx::smem_desc_sw128(sdO, 16, 1024);
+      // stage 0 of K / V (stage st: + st kTile)
+      const uint64_t dKk = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
+      const uint64_t dVk = ptx::smem_desc_sw128(sbase + L::V, 16, 1024);
+      const uint64_t dKmn = ptx::smem_desc_sw128(sbase + L::K, kSlab, 1024);
       auto issue_S = [&](int t) {  // MMA1' S = Q K^T into S buffer t & 1
-        const uint32_t sK = sbase + L::K + (t & 1) * L::kTile;
+        const uint64_t dk = ptx::desc_add(dKk, (t & 1) * L::kTile);
         const uint32_t dst = t_S0 + (t & 1) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(dst, ptx::smem_desc_sw128(sQ + off, 16, 1024),
-                      ptx::smem_desc_sw128(sK + off, 16, 1024), id_S, s > 0);
+          ptx::mma_ss(dst, ptx::desc_add(dQ, off), ptx::desc_add(dk, off), id_S, s > 0);
         }
       };
       auto issue_dP = [&](int t) {  // MMA2' dP = dO V^T
-        const uint32_t sV = sbase + L::V + (t & 1) * L::kTile;
+        const uint64_t dv = ptx::desc_add(dVk, (t & 1) * L::kTile);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dP, ptx::smem_desc_sw128(sdO + off, 16, 1024),
-                      ptx::smem_desc_sw128(sV + off, 16, 1024), id_S, s > 0);
+          ptx::mma_ss(t_dP, ptx::desc_add(ddO, off), ptx::desc_add(dv, off), id_S, s > 0);
         }
       };
       // Per tile t: dQ(t) once dS(t) replaced S(t) in TMEM, dP(t+1) (the
@@ -680,12 +691,12 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         if (!wait_bar(c, qDsFull, t & 1, 26)) break;
         ptx::tc_fence_after();
         // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major over d
-        const uint32_t sK = sbase + L::K + st * L::kTile;
+        const uint64_t dk = ptx::desc_add(dKmn, st * L::kTile);
         const uint32_t t_S = t_S0 + st * 128;
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
           const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_dQ, a_col, ptx::smem_desc_sw128(sK + s * 2048, kSlab, 1024), id_dQ,
+          ptx::mma_ts(t_dQ, a_col, ptx::desc_add(dk, s * 2048), id_dQ,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(qMma3));

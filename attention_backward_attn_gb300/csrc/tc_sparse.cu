@@ -284,55 +284,103 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       uint32_t ph = 0;
       int issued[2] = {0, 0}, freed[2] = {0, 0};
       int gt = 0;  // tiles of this CTA so far (all tokens)
+      // operand descriptors, built once (slots and K steps add their offsets)
+      const uint64_t dKV = ptx::smem_desc_sw128(sKV, 16, 1024);               // K-major
+      const uint64_t dKVmn = ptx::smem_desc_sw128(sKV, kSpSlot / 2, 1024);    // MN-major
+      const uint64_t dX = ptx::smem_desc_sw128(sX, 16, 1024);                 // K-major
+      const uint64_t dXmn = ptx::smem_desc_sw128(sX, kSpSlot, 1024);          // MN-major
+      const uint64_t dG = ptx::smem_desc_sw128(sG, 16, 1024);                 // K-major
+      const uint64_t dGmn = ptx::smem_desc_sw128(sG, kSpSlot, 1024);          // MN-major
       // One ring slot of MMA-A: [S^T | dP^T] (+)= KV X^T over column slab s.
       auto a_slab = [&](int s) {
         if (!wait_bar(c, sKvFull0 + slot, ph, 42)) return false;
         ptx::fence_async_shared();  // cp.async data -> async proxy
         ptx::tc_fence_after();
-        const uint32_t a0 = sKV + slot * kSpSlot, b0 = sX + s * kSpSlot;
+        const uint64_t a0 = ptx::desc_add(dKV, slot * kSpSlot);
+        const uint64_t b0 = ptx::desc_add(dX, s * kSpSlot);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          ptx::mma_ss(tS, ptx::smem_desc_sw128(a0 + 32 * k, 16, 1024),
-                      ptx::smem_desc_sw128(b0 + 32 * k, 16, 1024), idA, (s | k) != 0);
+          ptx::mma_ss(tS, ptx::desc_add(a0, 32 * k), ptx::desc_add(b0, 32 * k), idA, (s | k) != 0);
         ptx::mma_commit(c.bar(sKvEmpty0 + slot));
         if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
         return true;
       };
       // One ring slot of MMA-B: dQ^T (d chunk j / 2) += KV^T (scale dS^T) over
-      // the 64 selected rows of half j % 2, 16 per K step.
+      // the 64 selected rows of half j % 2, 16 per K step (slot data landed).
       auto b_slot = [&](int t, int j) {
         const int cc = j >> 1, nh = j & 1;
-        if (!wait_bar(c, sKvFull0 + slot, ph, 44)) return false;
-        ptx::fence_async_shared();  // cp.async data -> async proxy
-        ptx::tc_fence_after();
-        const uint32_t a0 = sKV + slot * kSpSlot;
+        const uint64_t a0 = ptx::desc_add(dKVmn, slot * kSpSlot);
+        const uint64_t b0 = ptx::desc_add(dGmn, 64 * nh * 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::mma_ss(tQ + 64 * cc, ptx::smem_desc_sw128(a0 + 2048 * kk, kSpSlot / 2, 1024),
-                      ptx::smem_desc_sw128(sG + (64 * nh + 16 * kk) * 128, kSpSlot, 1024), idB,
-                      (t | nh | kk) != 0);
-        ptx::mma_commit(c.bar(sKvEmpty0 + slot));
-        if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
-        return true;
+          ptx::mma_ss(tQ + 64 * cc, ptx::desc_add(a0, 2048 * kk), ptx::desc_add(b0, 2048 * kk),
+                      idB, (t | nh | kk) != 0);
+      };
+      // One ring slot of MMA-A for the next tile (slot data landed).
+      auto a_next = [&](int s) {
+        const uint64_t a0 = ptx::desc_add(dKV, slot * kSpSlot);
+        const uint64_t b0 = ptx::desc_add(dX, s * kSpSlot);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          ptx::mma_ss(tS, ptx::desc_add(a0, 32 * k), ptx::desc_add(b0, 32 * k), idA, (s | k) != 0);
       };
       // One MMA-C block: dKV^T (d chunk h / 2, row half h % 2) = X^T G into
-      // buffer h % 2, once the drain has read that buffer's previous block.
+      // buffer h % 2 (the drain has read that buffer's previous block).
       auto c_block = [&](int h) {
         const int cc = h >> 1, bb = h & 1;
-        while (freed[bb] < issued[bb]) {
-          if (!wait_bar(c, sDkvEmpty0 + bb, (uint32_t)freed[bb] & 1u, 45)) return false;
-          ++freed[bb];
-        }
-        ptx::tc_fence_after();
-        const uint32_t a0 = sX + 2 * cc * kSpSlot;
-        const uint32_t g0 = sG + 64 * bb * 128;
+        const uint64_t a0 = ptx::desc_add(dXmn, 2 * cc * kSpSlot);
+        const uint64_t g0 = ptx::desc_add(dG, 64 * bb * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_ss(tmem + 128 + 64 * bb, ptx::smem_desc_sw128(a0 + 2048 * kk, kSpSlot, 1024),
-                      ptx::smem_desc_sw128(g0 + (kk >> 2) * kSpSlot + (kk & 3) * 32, 16, 1024),
-                      idC, kk != 0);
+          ptx::mma_ss(tmem + 128 + 64 * bb, ptx::desc_add(a0, 2048 * kk),
+                      ptx::desc_add(g0, (kk >> 2) * kSpSlot + (kk & 3) * 32), idC, kk != 0);
         ptx::mma_commit(c.bar(sDkvFull0 + bb));
         ++issued[bb];
+      };
+      // After sGFull of tile t: two independent streams. The MMA-C blocks go
+      // out as the drain frees a dKV^T buffer; the ring slots (MMA-B of this
+      // tile interleaved with MMA-A of the next, in fill order) as their data
+      // lands. Neither waits for the other: the thread polls both.
+      auto tile_streams = [&](int t, bool next) {
+        const int nr = next ? 16 : 8;
+        int r = 0, cb = 0;
+        uint64_t t0 = 0;
+        for (uint32_t idle = 0; r < nr || cb < 8;) {
+          bool did = false;
+          if (cb < 8) {
+            const int bb = cb & 1;
+            if (freed[bb] < issued[bb] &&
+                ptx::mbar_test_wait(c.bar(sDkvEmpty0 + bb), (uint32_t)freed[bb] & 1u))
+              ++freed[bb];
+            if (freed[bb] >= issued[bb]) {
+              ptx::tc_fence_after();
+              c_block(cb++);
+              did = true;
+            }
+          }
+          if (r < nr && ptx::mbar_test_wait(c.bar(sKvFull0 + slot), ph)) {
+            ptx::fence_async_shared();  // cp.async data -> async proxy
+            ptx::tc_fence_after();
+            if (!next || (r & 1) == 0) b_slot(t, next ? r >> 1 : r);
+            else a_next(r >> 1);
+            ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+            if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+            ++r;
+            did = true;
+          }
+          if (did) {
+            idle = 0;
+          } else if ((++idle & 63u) == 0) {
+            if (*c.abort) return false;
+            const uint64_t now = ptx::globaltimer_ns();
+            if (t0 == 0 || idle == 64) t0 = now;
+            if (now - t0 > kTimeoutNs) {
+              *c.abort = 1;
+              report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 48);
+              return false;
+            }
+          }
+        }
         return true;
       };
       for (int k = 0; k < n_tok && ok; ++k) {
@@ -355,16 +403,10 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             break;
           }
           ptx::tc_fence_after();
-          // The drain paces the MMA-C blocks; between two of them the ring
-          // slots of this tile's MMA-B and of the next tile's MMA-A are
-          // consumed, so the KV loads stream while the drain works. (The
-          // softmax read S^T | dP^T of this tile before sGFull: MMA-A of the
-          // next tile may overwrite it.)
+          // (the softmax read S^T | dP^T of this tile before sGFull: MMA-A of
+          // the next tile may overwrite it)
           const bool next = t + 1 < T;
-          for (int j = 0; j < 8 && ok; ++j) {
-            ok = c_block(j) && b_slot(t, j) && (!next || a_slab(j));
-          }
-          if (!ok) break;
+          if (!(ok = tile_streams(t, next))) break;
           ptx::mma_commit(c.bar(sGFree));
           if (next) ptx::mma_commit(c.bar(sStFull));
         }
