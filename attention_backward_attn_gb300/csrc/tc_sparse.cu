@@ -347,6 +347,18 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         uint64_t t0 = 0;
         for (uint32_t idle = 0; r < nr || cb < 8;) {
           bool did = false;
+          // ring slots first: a slot returns to the loaders only once its MMAs
+          // complete, and the next tile's MMA-A and softmax wait on the ring
+          if (r < nr && ptx::mbar_test_wait(c.bar(sKvFull0 + slot), ph)) {
+            ptx::fence_async_shared();  // cp.async data -> async proxy
+            ptx::tc_fence_after();
+            if (!next || (r & 1) == 0) b_slot(t, next ? r >> 1 : r);
+            else a_next(r >> 1);
+            ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+            if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
+            ++r;
+            did = true;
+          }
           if (cb < 8) {
             const int bb = cb & 1;
             if (freed[bb] < issued[bb] &&
@@ -357,16 +369,6 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
               c_block(cb++);
               did = true;
             }
-          }
-          if (r < nr && ptx::mbar_test_wait(c.bar(sKvFull0 + slot), ph)) {
-            ptx::fence_async_shared();  // cp.async data -> async proxy
-            ptx::tc_fence_after();
-            if (!next || (r & 1) == 0) b_slot(t, next ? r >> 1 : r);
-            else a_next(r >> 1);
-            ptx::mma_commit(c.bar(sKvEmpty0 + slot));
-            if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
-            ++r;
-            did = true;
           }
           if (did) {
             idle = 0;
@@ -433,27 +435,35 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // Each fill arrives on its slot's sKvFull when its own copies land (the
     // MMA thread fences the async proxy after the wait), so all three slots
     // can be in flight and no fill waits on the loader's next step.
-    // MMA-A slot: [128 rows][64 d], columns 64 s of the tile's rows rt[0, 128)
-    auto fill_a = [&](const int32_t* rt, int s) {
+    // Row ids live in registers (this thread's 16 rows r0 + 8 k of a tile):
+    // shared-memory loads wait behind the MMAs' operand reads, and a fill
+    // must not wait on them.
+    auto load_ids = [&](const int32_t* rt, int32_t (&ids)[16]) {
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) ids[kk] = rt[r0 + 8 * kk];
+    };
+    // MMA-A slot: [128 rows][64 d], columns 64 s of the tile's rows
+    auto fill_a = [&](const int32_t (&ids)[16], int s) {
       if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 31)) return false;
       const uint32_t dst = sKV + slot * kSpSlot + swz;
+      const __half* src = p.kv16 + 8 * c8 + 64 * s;
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk)
-        ptx::cp_async_16(dst + (r0 + 8 * kk) * 128,
-                         p.kv16 + (int64_t)rt[r0 + 8 * kk] * kSpD + 8 * c8 + 64 * s);
+        ptx::cp_async_16(dst + (r0 + 8 * kk) * 128, src + (int64_t)ids[kk] * kSpD);
       ptx::cp_async_arrive_noinc(c.bar(sKvFull0 + slot));
       if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
       return true;
     };
     // MMA-B slot j: [64 rows][128 d] (rows 64 (j % 2) on, d chunk j / 2) as two
     // [64][64] halves 8 KB apart
-    auto fill_b = [&](const int32_t* rt, int j) {
+    auto fill_b = [&](const int32_t (&ids)[16], int j) {
       const int cc = j >> 1, nh = j & 1;
       if (!wait_bar(c, sKvEmpty0 + slot, ph ^ 1u, 32)) return false;
       const uint32_t dst = sKV + slot * kSpSlot + swz;
+      const __half* src = p.kv16 + 8 * c8 + 128 * cc;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const __half* sp = p.kv16 + (int64_t)rt[64 * nh + r0 + 8 * kk] * kSpD + 8 * c8 + 128 * cc;
+        const __half* sp = src + (int64_t)(nh ? ids[8 + kk] : ids[kk]) * kSpD;
         ptx::cp_async_16(dst + (r0 + 8 * kk) * 128, sp);
         ptx::cp_async_16(dst + kSpSlot / 2 + (r0 + 8 * kk) * 128, sp + 64);
       }
@@ -461,6 +471,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
       return true;
     };
+    int32_t cur[16], nxt[16];
     for (int k = 0; k < n_tok && ok; ++k) {
       const int b = k & 1;
       const uint32_t rph = (uint32_t)(k >> 1) & 1u;
@@ -468,12 +479,17 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const int T = (nrows_s[b] + 127) / 128;
       const int32_t* rows = rows_of(b);
       // the order in which the MMA thread consumes the ring
-      if (T > 0)
-        for (int s = 0; s < 8 && ok; ++s) ok = fill_a(rows, s);
+      if (T > 0) {
+        load_ids(rows, cur);
+        for (int s = 0; s < 8 && ok; ++s) ok = fill_a(cur, s);
+      }
       for (int t = 0; t < T && ok; ++t) {
         const bool next = t + 1 < T;
+        if (next) load_ids(rows + 128 * (t + 1), nxt);
         for (int j = 0; j < 8 && ok; ++j)
-          ok = fill_b(rows + 128 * t, j) && (!next || fill_a(rows + 128 * (t + 1), j));
+          ok = fill_b(cur, j) && (!next || fill_a(nxt, j));
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) cur[kk] = nxt[kk];
       }
       if (ok) ptx::mbar_arrive(c.bar(sRowsFree0 + b));  // row ids no longer read
     }
