@@ -316,6 +316,22 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         const uint64_t ddo_mn = ptx::desc_add(ddOmn, st * L::kTile);
         if (!wait_bar(c, kP1Full, t & 1, 4)) break;
         ptx::tc_fence_after();
+        // The softmax has read S^T(t): S(t+1) goes first (the softmax's next
+        // step waits on it), then dV(t). S(t+1) needs its Q stage, which dK(t-1)
+        // released; if that load has not landed yet, dV(t) goes first.
+        have = it.next();
+        const int st1 = (t + 1) & 1;
+        const uint32_t qpar = ((t + 1) >> 1) & 1;
+        bool s_done = false;
+        auto try_S = [&]() {
+          if (have && !s_done && ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
+            ptx::tc_fence_after();
+            issue_S(st1);
+            ptx::mma_commit(c.bar(kSFull));
+            s_done = true;
+          }
+        };
+        try_S();
         // MMA3 dV += P^T dO : A = P^T K-major over queries, B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
@@ -324,18 +340,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(kMma3));
-        have = it.next();
-        const int st1 = (t + 1) & 1;
-        const uint32_t qpar = ((t + 1) >> 1) & 1;
-        // S(t+1) ahead of dK(t) only if its operands already landed: dK(t)
-        // releases the stage the tile after next is loaded into
-        bool s_done = false;
-        if (have && ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
-          ptx::tc_fence_after();
-          issue_S(st1);
-          ptx::mma_commit(c.bar(kSFull));
-          s_done = true;
-        }
+        try_S();
         if (!wait_bar(c, kP2Full, t & 1, 7)) break;
         ptx::tc_fence_after();
         // MMA4 dK += dS^T Q : A = dS^T (TMEM fp16 pairs), B = Q MN-major over d

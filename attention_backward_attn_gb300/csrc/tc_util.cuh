@@ -21,12 +21,11 @@ struct Ctx {
   __device__ uint32_t bar(int i) const { return bars + 8u * i; }
 };
 
-// Bounded mbarrier wait: true when the phase with `parity` completed; false
-// if the CTA aborted or ~2 s passed (then the abort flag is raised).
-static __device__ __noinline__ bool wait_bar(const Ctx& c, int which, uint32_t parity,
-                                             int where) {
+// Slow path of wait_bar (out of line: the caller's registers are saved only
+// when the barrier was not already complete).
+static __device__ __noinline__ bool wait_bar_slow(const Ctx& c, int which, uint32_t parity,
+                                                  int where) {
   const uint32_t bar = c.bar(which);
-  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -39,6 +38,14 @@ static __device__ __noinline__ bool wait_bar(const Ctx& c, int which, uint32_t p
       }
     }
   }
+}
+
+// Bounded mbarrier wait: true when the phase with `parity` completed; false
+// if the CTA aborted or ~2 s passed (then the abort flag is raised).
+static __device__ __forceinline__ bool wait_bar(const Ctx& c, int which, uint32_t parity,
+                                                int where) {
+  if (ptx::mbar_try_wait(c.bar(which), parity)) return true;
+  return wait_bar_slow(c, which, parity, where);
 }
 
 // Teardown wait: ignores the abort flag, still bounded.
