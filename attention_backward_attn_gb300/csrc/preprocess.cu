@@ -29,6 +29,8 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int kThreads = 256;
+// Resident blocks per SM (32 warps) for the HBM latency.
+constexpr int kPreBlocksPerSM = 4;
 
 struct PreParams {
   int B, Hq, Hk, Sq, Sk;
@@ -118,7 +120,7 @@ __device__ __forceinline__ void zero_range(float* a, int64_t n, int64_t tid, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, kPreBlocksPerSM)
 preprocess_kernel(const PreParams p) {
   constexpr int CH = D / 8;                 // 16-byte chunks per row
   constexpr int LPR = CH < 32 ? CH : 32;    // lanes per row
@@ -145,66 +147,67 @@ preprocess_kernel(const PreParams p) {
   }
   int range_bits = 0;
 
-  // ---- query-side rows (b, i, h) in memory order: delta, staging ----
-  // U row slots per warp step, all loads issued before any dependent work so
-  // that each thread keeps several 16-byte requests in flight. The RPW * U
-  // rows of a step (a divisor of kIB, aligned) lie in one block of kIB rows of
-  // one head, so the index split is done once per step.
+  // ---- query-side rows (b, i, h): delta, staging; key-side rows (k, v) ----
+  // One loop over the steps of both kinds, so that each warp waits for about
+  // one round of loads. A step covers RPW * U rows (a divisor of kIB, aligned)
+  // of one head inside one block of kIB rows: the index split is done once per
+  // step, and all of the step's loads are issued before any dependent work.
   constexpr int U = D >= 512 ? 1 : 2;  // D = 512 rows are 1 KiB: one slot keeps registers in budget
   static_assert(kIB % (RPW * U) == 0, "a warp step stays inside one row block");
   float amax_q = 0.f, amax_do = 0.f, amax_k = 0.f, amax_v = 0.f;
   const int64_t nq = (int64_t)p.B * ((p.Sq + kIB - 1) / kIB) * kIB * p.Hq;
-  for (int64_t r0 = warp0 * RPW * U; r0 < nq; r0 += nwarps * RPW * U) {
-    int h, i0, b;
-    decompose(r0, p.Hq, p.Sq, &b, &h, &i0);
-    uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
+  const int64_t nk = (int64_t)p.B * ((p.Sk + kIB - 1) / kIB) * kIB * p.Hk;
+  const int64_t nq_steps = nq / (RPW * U);
+  const int64_t n_steps = nq_steps + (p.do16 != nullptr ? 2 * nk / (RPW * U) : 0);
+  for (int64_t step = warp0; step < n_steps; step += nwarps) {
+    if (step < nq_steps) {
+      const int64_t r0 = step * RPW * U;
+      int h, i0, b;
+      decompose(r0, p.Hq, p.Sq, &b, &h, &i0);
+      uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * RPW + sub;
-      if (i < p.Sq) {
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * RPW + sub;
+        if (i < p.Sq) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const int e0 = (cl + c * LPR) * 8;
-          of[u][c] = load_raw(p.o + b * p.o0 + i * p.o1 + h * p.o2 + e0);
-          df[u][c] = load_raw(p.dO + b * p.d0 + i * p.d1 + h * p.d2 + e0);
-          if (p.do16 != nullptr) qf[u][c] = load_raw(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * RPW + sub;
-      const bool valid = i < p.Sq;
-      float s = 0.f;
-      if (valid) {
-        const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const int e0 = (cl + c * LPR) * 8;
-          float ov[8], dv[8];
-          unpack8(of[u][c], ov);
-          unpack8(df[u][c], dv);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) s = fmaf(ov[t], dv[t], s);
-          if (p.do16 != nullptr) {
-            float qv[8];
-            unpack8(qf[u][c], qv);
-            amax_do = fmaxf(amax_do, store8_half(p.do16 + hm * D + e0, dv));
-            amax_q = fmaxf(amax_q, store8_half(p.q16 + hm * D + e0, qv));
+          for (int c = 0; c < CPL; ++c) {
+            const int e0 = (cl + c * LPR) * 8;
+            of[u][c] = load_raw(p.o + b * p.o0 + i * p.o1 + h * p.o2 + e0);
+            df[u][c] = load_raw(p.dO + b * p.d0 + i * p.d1 + h * p.d2 + e0);
+            if (p.do16 != nullptr) qf[u][c] = load_raw(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0);
           }
         }
       }
 #pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (valid && cl == 0) p.delta[((int64_t)b * p.Hq + h) * p.Sq + i] = s;
-    }
-  }
-
-  // ---- key-side rows (k then v), staged head-major ----
-  if (p.do16 != nullptr) {
-    const int64_t nk = (int64_t)p.B * ((p.Sk + kIB - 1) / kIB) * kIB * p.Hk;
-    // nk is a multiple of kIB, so a warp step never straddles the k / v boundary
-    for (int64_t r0 = warp0 * RPW * U; r0 < 2 * nk; r0 += nwarps * RPW * U) {
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * RPW + sub;
+        const bool valid = i < p.Sq;
+        float s = 0.f;
+        if (valid) {
+          const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const int e0 = (cl + c * LPR) * 8;
+            float ov[8], dv[8];
+            unpack8(of[u][c], ov);
+            unpack8(df[u][c], dv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) s = fmaf(ov[t], dv[t], s);
+            if (p.do16 != nullptr) {
+              float qv[8];
+              unpack8(qf[u][c], qv);
+              amax_do = fmaxf(amax_do, store8_half(p.do16 + hm * D + e0, dv));
+              amax_q = fmaxf(amax_q, store8_half(p.q16 + hm * D + e0, qv));
+            }
+          }
+        }
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (valid && cl == 0) p.delta[((int64_t)b * p.Hq + h) * p.Sq + i] = s;
+      }
+    } else {
+      // nk is a multiple of kIB, so a step never straddles the k / v boundary
+      const int64_t r0 = (step - nq_steps) * RPW * U;
       const bool is_v = r0 >= nk;
       int g, j0, b;
       decompose(is_v ? r0 - nk : r0, p.Hk, p.Sk, &b, &g, &j0);
@@ -336,7 +339,8 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = (unsigned)(sms * 4 < kPreMaxBlocks ? sms * 4 : kPreMaxBlocks);
+  const int want = sms * kPreBlocksPerSM;
+  const unsigned grid = (unsigned)(want < kPreMaxBlocks ? want : kPreMaxBlocks);
   switch (pr.D) {
     case 64: preprocess_kernel<64><<<grid, kThreads, 0, stream>>>(p); break;
     case 128: preprocess_kernel<128><<<grid, kThreads, 0, stream>>>(p); break;
