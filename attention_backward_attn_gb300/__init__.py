@@ -58,6 +58,7 @@ class Sparse(ctypes.Structure):
         ("n_ori", ctypes.c_int32), ("n_cmp", ctypes.c_int32), ("topk", ctypes.c_int32),
         ("ori_win_left", ctypes.c_int32), ("ori_win_right", ctypes.c_int32),
         ("d_ori_kv", ctypes.c_void_p), ("d_cmp_kv", ctypes.c_void_p),
+        ("cmp_ratio", ctypes.c_int32),
     ]
 
 
@@ -157,7 +158,10 @@ def mask_from(window_left: int = -1, window_right: int = -1, num_sink: int = 0) 
 
 
 def sparse_from(ori_kv, cmp_kv=None, cmp_idx=None, ori_win_left=-1, ori_win_right=-1,
-                d_ori_kv=None, d_cmp_kv=None) -> Sparse:
+                d_ori_kv=None, d_cmp_kv=None, cmp_ratio=0) -> Sparse:
+    """cmp_kv with cmp_idx: SCFA (listed rows); cmp_kv without cmp_idx: CFA
+    (every compressed row whose block of cmp_ratio positions ends by the query);
+    neither: SWA."""
     s = Sparse()
     s.ori_kv = _ptr(ori_kv)
     s.cmp_kv = _ptr(cmp_kv)
@@ -168,6 +172,7 @@ def sparse_from(ori_kv, cmp_kv=None, cmp_idx=None, ori_win_left=-1, ori_win_righ
     s.ori_win_left, s.ori_win_right = ori_win_left, ori_win_right
     s.d_ori_kv = _ptr(d_ori_kv)
     s.d_cmp_kv = _ptr(d_cmp_kv)
+    s.cmp_ratio = cmp_ratio
     return s
 
 
@@ -247,7 +252,7 @@ class BackwardPlan:
 
     def __init__(self, q, k, v, o, do, lse, scale, mask: Optional[Mask] = None, bias=None,
                  want_dbias=False, ori_kv=None, cmp_kv=None, cmp_idx=None,
-                 ori_win_left=-1, ori_win_right=-1):
+                 ori_win_left=-1, ori_win_right=-1, cmp_ratio=0):
         import torch
         dev = q.device
         self.q, self.k, self.v, self.o, self.do, self.lse, self.bias = q, k, v, o, do, lse, bias
@@ -259,7 +264,7 @@ class BackwardPlan:
             self.d_cmp = (torch.empty(cmp_kv.shape, dtype=torch.float32, device=dev)
                           if cmp_kv is not None else None)
             self.sparse = sparse_from(ori_kv, cmp_kv, cmp_idx, ori_win_left, ori_win_right,
-                                      self.d_ori, self.d_cmp)
+                                      self.d_ori, self.d_cmp, cmp_ratio)
             self._keep = (ori_kv, cmp_kv, cmp_idx)
             self.prob = problem_from(q, None, None, o, do, scale, Sk=0, Hk=Hk)
             self.dk = self.dv = None

@@ -58,15 +58,17 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
     if (a.B != 1) return ATTN_ERR_INVALID_ARG;
     if (sp->n_ori < 0) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(sp->ori_kv) || !aligned16(sp->cmp_kv)) return ATTN_ERR_INVALID_ARG;
+    const bool cfa = sp->cmp_kv != nullptr && sp->cmp_idx == nullptr;
     if (sp->cmp_kv != nullptr) {
-      if (sp->cmp_idx == nullptr) return ATTN_ERR_UNSUPPORTED;  // all-rows CFA variant
-      if (sp->n_cmp < 1 || sp->topk < 1) return ATTN_ERR_INVALID_ARG;
+      if (sp->n_cmp < 1) return ATTN_ERR_INVALID_ARG;
+      if (cfa ? sp->cmp_ratio < 1 : sp->topk < 1) return ATTN_ERR_INVALID_ARG;
     } else if (sp->cmp_idx != nullptr) {
       return ATTN_ERR_INVALID_ARG;
     }
     p.n_ori = sp->n_ori;
     p.n_cmp = sp->cmp_kv ? sp->n_cmp : 0;
-    p.topk = sp->cmp_kv ? sp->topk : 0;
+    p.topk = sp->cmp_kv && !cfa ? sp->topk : 0;
+    p.cmp_ratio = cfa ? sp->cmp_ratio : 0;
     p.ori_wl = sp->ori_win_left < 0 ? -1 : sp->ori_win_left;
     p.ori_wr = sp->ori_win_right < 0 ? -1 : sp->ori_win_right;
     p.Sk = 0;

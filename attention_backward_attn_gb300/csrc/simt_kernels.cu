@@ -102,7 +102,7 @@ struct SparseSel {
   const bf16* ori;
   const bf16* cmp;
   const int32_t* idx;
-  int Sq, Hk, D, n_ori, n_cmp, topk, wl, wr;
+  int Sq, Hk, D, n_ori, n_cmp, topk, wl, wr, ratio;  // ratio > 0: CFA (no index list)
 };
 
 template <typename F>
@@ -115,6 +115,11 @@ __device__ __forceinline__ void for_each_selected(const SparseSel& s, int i, int
   hi = min(hi, s.n_ori - 1);
   for (int j = lo; j <= hi; ++j) f(s.ori + ((int64_t)j * s.Hk + g) * s.D, 0, j);
   if (s.cmp == nullptr) return;
+  if (s.ratio > 0) {  // CFA: every compressed row whose block ends at or before pos
+    const int nc = min(s.n_cmp, max(pos + 1, 0) / s.ratio);
+    for (int c = 0; c < nc; ++c) f(s.cmp + ((int64_t)c * s.Hk + g) * s.D, 1, c);
+    return;
+  }
   const int32_t* row = s.idx + ((int64_t)i * s.Hk + g) * s.topk;
   for (int t = 0; t < s.topk; ++t) {
     const int c = __ldg(row + t);
@@ -405,6 +410,7 @@ SparseSel sel_of(const Problem& p, const void* ori, const void* cmp, const int32
   s.topk = p.topk;
   s.wl = p.ori_wl;
   s.wr = p.ori_wr;
+  s.ratio = p.cmp_ratio;
   return s;
 }
 

@@ -105,6 +105,7 @@ enum SpBar {
 
 struct SpParams {
   int Sq, Hq, Hk, n_ori, n_cmp, topk, wl, wr;
+  int ratio;  // > 0: CFA (no index list; every compressed row whose block ends by the query)
   float scale;
   float scale_log2;
   const __half* kv16;  // [(n_ori + n_cmp) * Hk][512] fp16 copy of [ori_kv ; cmp_kv]
@@ -119,7 +120,8 @@ struct SpParams {
 
 // Selected rows of (token i, KV head g) as row ids of the fp16 copy
 // [ori rows ; cmp rows] viewed as [(n_ori + n_cmp) * Hk][512]: the window
-// first, then the valid top-k entries in slot order. Returns the count; the
+// first, then the valid top-k entries in slot order (SCFA) or every compressed
+// row whose block ends at or before the query (CFA). Returns the count; the
 // list is padded to a multiple of 128 with its first entry (masked later).
 // Run by one full warp.
 __device__ int build_rows(const SpParams& p, int i, int g, int32_t* rows, int lane) {
@@ -131,7 +133,11 @@ __device__ int build_rows(const SpParams& p, int i, int g, int32_t* rows, int la
   const int nwin = hi >= lo ? hi - lo + 1 : 0;
   for (int j = lane; j < nwin; j += 32) rows[j] = (lo + j) * p.Hk + g;
   int n = nwin;
-  if (p.idx != nullptr) {
+  if (p.ratio > 0) {  // CFA
+    const int nc = min(p.n_cmp, max(pos + 1, 0) / p.ratio);
+    for (int c = lane; c < nc; c += 32) rows[n + c] = (p.n_ori + c) * p.Hk + g;
+    n += nc;
+  } else if (p.idx != nullptr) {
     const int32_t* ir = p.idx + ((int64_t)i * p.Hk + g) * p.topk;
     bool bad = false;
     for (int t0 = 0; t0 < p.topk; t0 += 32) {
@@ -684,7 +690,7 @@ int64_t max_selected_rows(const Problem& p) {
   const int64_t win = (p.ori_wl >= 0 && p.ori_wr >= 0)
                           ? std::min<int64_t>(p.n_ori, (int64_t)p.ori_wl + p.ori_wr + 1)
                           : p.n_ori;
-  return win + (p.n_cmp > 0 ? p.topk : 0);
+  return win + (p.n_cmp > 0 ? (p.cmp_ratio > 0 ? p.n_cmp : p.topk) : 0);
 }
 
 }  // namespace
@@ -711,12 +717,13 @@ cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* d
   p.n_ori = pr.n_ori;
   p.n_cmp = pr.n_cmp;
   p.topk = pr.topk;
+  p.ratio = pr.cmp_ratio;
   p.wl = pr.ori_wl;
   p.wr = pr.ori_wr;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.kv16 = kv16;
-  p.idx = pr.n_cmp > 0 ? idx : nullptr;
+  p.idx = pr.n_cmp > 0 && pr.cmp_ratio == 0 ? idx : nullptr;
   p.lse = lse;
   p.delta = delta;
   p.dq = dq;

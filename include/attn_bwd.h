@@ -88,14 +88,21 @@ typedef struct attn_mask {
 } attn_mask_t;
 
 /* Selected-KV sparse attention with shared latent KV (Ascend
- * "sparse_flash_mla_grad": selectedKv = concat(oriKv window,
- * Gather(cmpKv, topkIndices[i])), K = V = selectedKv).
+ * "sparse_flash_mla_grad" formula, phase 1: selectedKv = concat(oriKv
+ * window, Gather(cmpKv, topkIndices[i])) in the SCFA case, concat(oriKv
+ * window, cmpKv) in the CFA case, oriKv window alone in the SWA case;
+ * K = V = selectedKv).
  * One sequence: the problem's B must be 1, its Sk is ignored, k / v / bias /
  * dk / dv / dbias must be NULL. Query i sits at position p = (n_ori - Sq) + i
  * and selects original rows [p - ori_win_left, p + ori_win_right] clipped to
- * [0, n_ori) (negative bound = unbounded) plus the compressed rows listed in
- * cmp_idx[i, g, :] (-1 = unused slot; indices may repeat and then count
- * twice). cmp_kv == NULL means no compressed rows (the sliding-window case).
+ * [0, n_ori) (negative bound = unbounded) plus compressed rows:
+ *   SCFA (cmp_kv and cmp_idx given): the rows listed in cmp_idx[i, g, :]
+ *     (-1 = unused slot; indices may repeat and then count twice);
+ *   CFA (cmp_kv given, cmp_idx == NULL): every compressed row c whose block
+ *     of cmp_ratio original positions ends at or before p, i.e.
+ *     c < min(n_cmp, (p + 1) / cmp_ratio) (cmp_ratio >= 1 required; topk is
+ *     ignored);
+ *   SWA (cmp_kv == NULL, cmp_idx == NULL): none.
  * All arrays contiguous: ori_kv bf16 [n_ori, Hk, D], cmp_kv bf16
  * [n_cmp, Hk, D], cmp_idx int32 [Sq, Hk, topk]; gradients d_ori_kv fp32
  * [n_ori, Hk, D] and d_cmp_kv fp32 [n_cmp, Hk, D] receive dKV = dK + dV,
@@ -108,6 +115,7 @@ typedef struct attn_sparse {
   int32_t ori_win_left, ori_win_right;
   float* d_ori_kv;
   float* d_cmp_kv;
+  int32_t cmp_ratio; /* CFA only: original positions per compressed row */
 } attn_sparse_t;
 
 /* Forward with log-sum-exp, used to produce the backward's O and LSE inputs

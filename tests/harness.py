@@ -60,11 +60,17 @@ def dense_reference(w, O_b, L_f, batches=None, kv_heads=None):
     return dict(dq=t(dQ), dk=t(dK), dv=t(dV), dbias=dB, delta=oracle.preprocess(O, dO))
 
 
+def cfa_ratio(w):
+    """cmp_ratio for the CFA case (compressed KV without an index list), else None."""
+    return w.cmp_ratio if (w.cmp_kv is not None and w.cmp_idx is None) else None
+
+
 def sparse_forward_inputs(w):
     q = np.asarray(w.q, np.float64)
     okv = np.asarray(w.ori_kv, np.float64)
     ckv = None if w.cmp_kv is None else np.asarray(w.cmp_kv, np.float64)
-    O, L = oracle.sparse_forward(q, okv, ckv, w.cmp_idx, w.scale, w.ori_win_left, w.ori_win_right)
+    O, L = oracle.sparse_forward(q, okv, ckv, w.cmp_idx, w.scale, w.ori_win_left, w.ori_win_right,
+                                 cfa_ratio(w))
     return np.ascontiguousarray(bf16_round(O.astype(np.float32))), L.astype(np.float32), O, L
 
 
@@ -75,7 +81,7 @@ def sparse_reference(w, O_b, L_f):
     dq, dori, dcmp = oracle.sparse_backward(q, okv, ckv, w.cmp_idx, np.asarray(O_b, np.float64),
                                             np.asarray(w.do, np.float64),
                                             np.asarray(L_f, np.float64), w.scale,
-                                            w.ori_win_left, w.ori_win_right)
+                                            w.ori_win_left, w.ori_win_right, cfa_ratio(w))
     return dict(dq=dq, d_ori=dori, d_cmp=dcmp)
 
 
@@ -131,4 +137,4 @@ def gpu_sparse_plan(w, O_b, L_f, dev="cuda"):
     idx = None if w.cmp_idx is None else torch.from_numpy(w.cmp_idx).to(dev)
     return ab.BackwardPlan(q, None, None, o, do, lse, w.scale, ori_kv=okv, cmp_kv=ckv,
                            cmp_idx=idx, ori_win_left=w.ori_win_left,
-                           ori_win_right=w.ori_win_right)
+                           ori_win_right=w.ori_win_right, cmp_ratio=cfa_ratio(w) or 0)

@@ -143,10 +143,16 @@ def test_sparse_descriptor_validation(ab):
     assert ab.attn_bwd_path(p, None, s) == 2
     # k / v must be NULL for the shared-KV variant
     assert _call_bwd(ab, p, sparse=s) == 1
-    # compressed KV without an index list (the all-rows variant) is not built
+    # compressed KV without an index list is the CFA case: it needs cmp_ratio >= 1
     s.cmp_kv, s.n_cmp, s.topk, s.d_cmp_kv = fake, 32, 8, fake
+    s.cmp_ratio = 0
     assert ab.attn_bwd_path(p, None, s) == 0
-    assert _call_bwd(ab, p, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None)) == 2
+    assert _call_bwd(ab, p, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None)) == 1
+    s.cmp_ratio = 4
+    assert ab.attn_bwd_path(p, None, s) == 2  # 16 query heads per KV head: SIMT kernels
+    s.n_cmp = 0
+    assert ab.attn_bwd_path(p, None, s) == 0  # compressed KV needs rows
+    s.n_cmp = 32
     # batch must be 1
     p2 = _prob(ab, B=2, Hq=16, Hk=1, Sq=128, Sk=0, D=512)
     s.cmp_idx = fake

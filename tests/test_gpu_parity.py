@@ -193,6 +193,9 @@ SMALL_SPARSE = {
     "swa_s192_h8_d512": lambda: make_sparse("w", 32, Sq=192, Hq=8, Hk=1, D=512, n_ori=192,
                                             n_cmp=0, topk=0, cmp_ratio=1, ori_win_left=63,
                                             with_cmp=False),
+    "cfa_hk2_d512": lambda: make_sparse("c", 34, Sq=96, Hq=8, Hk=2, D=512, n_ori=160,
+                                        n_cmp=40, topk=1, cmp_ratio=4, ori_win_left=20,
+                                        cfa=True),
     "scfa_delta_hk2_d512": lambda: make_sparse("d", 33, Sq=96, Hq=8, Hk=2, D=512, n_ori=160,
                                                n_cmp=40, topk=16, cmp_ratio=4, ori_win_left=20,
                                                ori_win_right=3),
@@ -215,6 +218,14 @@ TC_SPARSE = {
     # 500 selected rows per token: four tiles, the last one ragged
     "tc_scfa_rows500": lambda: make_sparse("t4", 44, Sq=96, Hq=64, Hk=1, D=512, n_ori=1000,
                                            n_cmp=250, topk=200, cmp_ratio=4, ori_win_left=299),
+    # CFA: compressed KV without an index list (every block that ended by the query)
+    "tc_cfa_s200_h64": lambda: make_sparse("t7", 47, Sq=200, Hq=64, Hk=1, D=512, n_ori=200,
+                                           n_cmp=50, topk=1, cmp_ratio=4, ori_win_left=127,
+                                           cfa=True),
+    # CFA, two KV heads, queries offset by delta_s = 60, two 128-row tiles per token
+    "tc_cfa_hk2_delta": lambda: make_sparse("t8", 48, Sq=100, Hq=128, Hk=2, D=512, n_ori=160,
+                                            n_cmp=40, topk=1, cmp_ratio=4, ori_win_left=99,
+                                            cfa=True),
     # about eight work items per persistent CTA: row counts from 0 to two tiles
     # vary between a CTA's items, and each CTA ends on items with no row
     "tc_scfa_persistent_mix": lambda: make_sparse("t6", 46, Sq=600, Hq=128, Hk=2, D=512,

@@ -179,3 +179,70 @@ def test_hand_derived_sparse_example():
     got = dict(O=O, LSE=L, dQ=dq, d_ori_kv=dori)
     for key, val in ex["expect"].items():
         np.testing.assert_allclose(got[key], np.array(_ev(val)), rtol=0, atol=1e-14, err_msg=key)
+
+
+def _small_cfa(Sq, n_ori, n_cmp, ratio, left, Hq, Hk, D=4, seed=7):
+    return make_sparse("cfa", seed, Sq=Sq, Hq=Hq, Hk=Hk, D=D, n_ori=n_ori, n_cmp=n_cmp, topk=1,
+                       cmp_ratio=ratio, ori_win_left=left, cfa=True)
+
+
+def test_cfa_selects_every_block_that_ends_by_the_query():
+    # Compressed row c covers positions [c * ratio, (c + 1) * ratio): it is live
+    # for position p once that block has ended, c < (p + 1) // ratio.
+    _, cmp = oracle.selected_rows(0, 12, 12, 2, 0, None, n_cmp=4, cmp_ratio=3)
+    assert cmp.size == 0                                  # p = 0: block 0 not complete
+    _, cmp = oracle.selected_rows(2, 12, 12, 2, 0, None, n_cmp=4, cmp_ratio=3)
+    assert list(cmp) == [0]                               # p = 2 ends block 0
+    _, cmp = oracle.selected_rows(11, 12, 12, 2, 0, None, n_cmp=3, cmp_ratio=3)
+    assert list(cmp) == [0, 1, 2]                         # clipped to n_cmp
+    _, cmp = oracle.selected_rows(1, 4, 8, 2, 0, None, n_cmp=4, cmp_ratio=2)
+    assert list(cmp) == [0, 1, 2]                         # bottom-right: p = 5 ends block 2
+
+
+def test_cfa_reduces_to_dense_mask_over_concatenated_kv():
+    # CFA == a dense mask over [ori_kv ; cmp_kv] with the window plus every
+    # compressed block that ended by the query.
+    w = _small_cfa(Sq=12, n_ori=12, n_cmp=4, ratio=3, left=2, Hq=2, Hk=1)
+    assert w.cmp_idx is None and w.cmp_kv is not None
+    q, okv, ckv, do = _f64(w.q), _f64(w.ori_kv), _f64(w.cmp_kv), _f64(w.do)
+    O, L = oracle.sparse_forward(q, okv, ckv, None, w.scale, 2, 0, cmp_ratio=3)
+    dq, dori, dcmp = oracle.sparse_backward(q, okv, ckv, None, O, do, L, w.scale, 2, 0,
+                                            cmp_ratio=3)
+    kv = np.concatenate([okv, ckv], axis=0)
+    m = np.zeros((12, 16), dtype=bool)
+    for i in range(12):
+        m[i, max(0, i - 2):i + 1] = True
+        for c in range(4):
+            if (c + 1) * 3 <= i + 1:
+                m[i, 12 + c] = True
+    Q, KV, dO = q.transpose(1, 0, 2)[None], kv.transpose(1, 0, 2)[None], do.transpose(1, 0, 2)[None]
+    Od, Ld = oracle.forward(Q, KV, KV, w.scale, m)
+    np.testing.assert_allclose(Od[0].transpose(1, 0, 2), O, atol=1e-13)
+    dQd, dKd, dVd, _ = oracle.backward(Q, KV, KV, Od, dO, Ld, w.scale, m)
+    dkv = (dKd + dVd)[0].transpose(1, 0, 2)
+    np.testing.assert_allclose(dQd[0].transpose(1, 0, 2), dq, atol=1e-12)
+    np.testing.assert_allclose(dkv[:12], dori, atol=1e-12)
+    np.testing.assert_allclose(dkv[12:], dcmp, atol=1e-12)
+
+
+def test_cfa_matches_brute_force_with_the_explicit_row_list():
+    # The pure-Python brute force takes index lists: give it the eligible rows.
+    w = _small_cfa(Sq=6, n_ori=8, n_cmp=3, ratio=2, left=1, Hq=2, Hk=1, D=3)
+    q, okv, ckv, do = _f64(w.q), _f64(w.ori_kv), _f64(w.cmp_kv), _f64(w.do)
+    O, L = oracle.sparse_forward(q, okv, ckv, None, w.scale, 1, 0, cmp_ratio=2)
+    got = oracle.sparse_backward(q, okv, ckv, None, O, do, L, w.scale, 1, 0, cmp_ratio=2)
+    idx = np.full((6, 1, 3), -1, dtype=np.int32)
+    for i in range(6):
+        p = (8 - 6) + i
+        n = min(3, (p + 1) // 2)
+        idx[i, 0, :n] = np.arange(n)
+    ref = brute.sparse_backward(q.tolist(), okv.tolist(), ckv.tolist(), idx.tolist(), O.tolist(),
+                                do.tolist(), L.tolist(), w.scale, 1, 0)
+    for g_, r_ in zip(got, ref):
+        np.testing.assert_allclose(g_, np.asarray(r_), atol=1e-12)
+
+
+def test_cfa_without_a_ratio_is_rejected():
+    w = _small_cfa(Sq=4, n_ori=4, n_cmp=2, ratio=2, left=1, Hq=1, Hk=1)
+    with pytest.raises(ValueError):
+        oracle.sparse_forward(_f64(w.q), _f64(w.ori_kv), _f64(w.cmp_kv), None, w.scale, 1, 0)

@@ -219,15 +219,20 @@ def make_sparse(
     ori_win_right: int = 0,
     mult: float = 0.5,
     with_cmp: bool = True,
+    cfa: bool = False,
 ) -> SparseWorkload:
-    """Draw q, ori_kv, cmp_kv, dO (in that order), then the top-k indices."""
+    """Draw q, ori_kv, cmp_kv, dO (in that order), then the top-k indices.
+
+    cfa=True keeps cmp_kv but draws no index list: every compressed row whose
+    block of cmp_ratio positions ends at or before the query is selected.
+    """
     rng = np.random.default_rng(seed)
     q = _normal_bf16(rng, (Sq, Hq, D), mult)
     ori_kv = _normal_bf16(rng, (n_ori, Hk, D), mult)
     cmp_kv = _normal_bf16(rng, (n_cmp, Hk, D), mult) if with_cmp else None
     do = _normal_bf16(rng, (Sq, Hq, D), mult)
     idx = (topk_compressed_indices(rng, Sq, n_ori, n_cmp, cmp_ratio, topk, Hk)
-           if with_cmp else None)
+           if with_cmp and not cfa else None)
     return SparseWorkload(
         name=name, Sq=Sq, Hq=Hq, Hk=Hk, D=D, n_ori=n_ori,
         n_cmp=n_cmp if with_cmp else 0, topk=topk if with_cmp else 0,
