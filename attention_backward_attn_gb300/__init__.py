@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "AttnError", "Problem", "Mask", "Sparse", "lib", "status_string",
-    "problem_from", "mask_from", "sparse_from",
+    "problem_from", "mask_from", "sparse_from", "ATTN_FLAG_DETERMINISTIC",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
 ]
@@ -44,6 +44,7 @@ class Problem(ctypes.Structure):
         ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
         ("do_stride", ctypes.c_int64 * 3),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -134,8 +135,12 @@ def _strides(t):
     return (ctypes.c_int64 * 3)(s[0], s[1], s[2])
 
 
+ATTN_FLAG_DETERMINISTIC = 1
+
+
 def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = None,
-                 Sk: Optional[int] = None, Hk: Optional[int] = None) -> Problem:
+                 Sk: Optional[int] = None, Hk: Optional[int] = None,
+                 deterministic: bool = False) -> Problem:
     """Problem descriptor from BSHD tensors (q [B, Sq, Hq, D], k / v [B, Sk, Hk, D])."""
     B, Sq, Hq, D = q.shape
     p = Problem()
@@ -148,6 +153,7 @@ def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = No
     p.v_stride = _strides(v if v is not None else (k if k is not None else q))
     p.o_stride = _strides(o if o is not None else q)
     p.do_stride = _strides(do if do is not None else (o if o is not None else q))
+    p.flags = ATTN_FLAG_DETERMINISTIC if deterministic else 0
     return p
 
 
@@ -252,7 +258,7 @@ class BackwardPlan:
 
     def __init__(self, q, k, v, o, do, lse, scale, mask: Optional[Mask] = None, bias=None,
                  want_dbias=False, ori_kv=None, cmp_kv=None, cmp_idx=None,
-                 ori_win_left=-1, ori_win_right=-1, cmp_ratio=0):
+                 ori_win_left=-1, ori_win_right=-1, cmp_ratio=0, deterministic=False):
         import torch
         dev = q.device
         self.q, self.k, self.v, self.o, self.do, self.lse, self.bias = q, k, v, o, do, lse, bias
@@ -266,10 +272,11 @@ class BackwardPlan:
             self.sparse = sparse_from(ori_kv, cmp_kv, cmp_idx, ori_win_left, ori_win_right,
                                       self.d_ori, self.d_cmp, cmp_ratio)
             self._keep = (ori_kv, cmp_kv, cmp_idx)
-            self.prob = problem_from(q, None, None, o, do, scale, Sk=0, Hk=Hk)
+            self.prob = problem_from(q, None, None, o, do, scale, Sk=0, Hk=Hk,
+                                     deterministic=deterministic)
             self.dk = self.dv = None
         else:
-            self.prob = problem_from(q, k, v, o, do, scale)
+            self.prob = problem_from(q, k, v, o, do, scale, deterministic=deterministic)
             self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
             self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
         self.mask = mask

@@ -46,6 +46,8 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
     p.os[t] = a.o_stride[t];
     p.dos[t] = a.do_stride[t];
   }
+  if (a.flags & ~ATTN_FLAG_DETERMINISTIC) return ATTN_ERR_INVALID_ARG;
+  p.deterministic = (a.flags & ATTN_FLAG_DETERMINISTIC) != 0;
   p.mask = MaskSpec{-1, -1, 0};
   if (mask != nullptr) {
     if (mask->num_sink < 0) return ATTN_ERR_INVALID_ARG;
@@ -53,6 +55,7 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
                       mask->window_right < 0 ? -1 : mask->window_right, mask->num_sink};
   }
   p.sparse = sp != nullptr;
+  if (p.sparse && p.deterministic) return ATTN_ERR_UNSUPPORTED;  // dKV: reduction over tokens
   if (p.sparse) {
     if (mask != nullptr) return ATTN_ERR_INVALID_ARG;  // the sparse window replaces it
     if (a.B != 1) return ATTN_ERR_INVALID_ARG;
@@ -260,7 +263,10 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
       dense_staged ? staged(w.k16) : nullptr, dense_staged ? staged(w.v16) : nullptr,
       dense_staged ? staged(w.do16) : nullptr, p.sparse ? sparse->ori_kv : nullptr,
       p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr,
-      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, dk, dv, st, stream));
+      // dk / dv are recorded (for attn_bwd's check) only when zeroed here:
+      // only then may the head-split kernel add partial sums into them
+      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, zero_kv ? dk : nullptr,
+      zero_kv ? dv : nullptr, st, stream));
 }
 
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
@@ -301,20 +307,47 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
     return cuda_status(launch_bwd_sparse_tc(p, q, dO, kv16, sparse->cmp_idx, lse, delta, dq,
                                             sparse->d_ori_kv, sparse->d_cmp_kv, st, stream));
   }
-  if (tc) {
-    const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16);
-    const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16);
-    const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16);
-    const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16);
-    return cuda_status(launch_bwd_tc(p, q16, k16, v16, do16, lse, delta, bias, dq, dk, dv,
-                                     dbias, st, stream));
+  if (p.sparse) {
+    return cuda_status(launch_bwd_simt(p, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias,
+                                       sparse->ori_kv, sparse->cmp_kv, sparse->cmp_idx,
+                                       sparse->d_ori_kv, sparse->d_cmp_kv, st, stream));
   }
-  return cuda_status(launch_bwd_simt(p, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias,
-                                     sparse ? sparse->ori_kv : nullptr,
-                                     sparse ? sparse->cmp_kv : nullptr,
-                                     sparse ? sparse->cmp_idx : nullptr,
-                                     sparse ? sparse->d_ori_kv : nullptr,
-                                     sparse ? sparse->d_cmp_kv : nullptr, st, stream));
+  // Deterministic dbias over several batches: one launch per batch (B = 1
+  // sub-problems on offset pointers), so that every dbias element receives its
+  // per-batch terms in batch order; within one batch each element has one
+  // writer. bias and dbias are shared by the batches.
+  const int n_launch = (p.deterministic && dbias != nullptr) ? p.B : 1;
+  Problem pb = p;
+  if (n_launch > 1) pb.B = 1;
+  const int64_t rows_q = (int64_t)p.Hq * p.Sq, rows_k = (int64_t)p.Hk * p.Sk;
+  for (int b = 0; b < n_launch; ++b) {
+    const int64_t bq = b;  // 0 when there is a single launch
+    const float* lse_b = lse + bq * rows_q;
+    const float* delta_b = delta + bq * rows_q;
+    float* dq_b = dq + bq * rows_q * p.D;
+    float* dk_b = dk + bq * rows_k * p.D;
+    float* dv_b = dv + bq * rows_k * p.D;
+    cudaError_t e;
+    if (tc) {
+      // staged fp16 copies are head-major [B, H, S, D]
+      const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16) + bq * rows_q * p.D;
+      const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16) + bq * rows_k * p.D;
+      const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16) + bq * rows_k * p.D;
+      const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16) + bq * rows_q * p.D;
+      e = launch_bwd_tc(pb, q16, k16, v16, do16, lse_b, delta_b, bias, dq_b, dk_b, dv_b, dbias,
+                        st, stream);
+    } else {
+      // bf16 inputs: batch stride in elements, 2 bytes each
+      const char* qb = static_cast<const char*>(q) + bq * p.qs[0] * 2;
+      const char* kb = static_cast<const char*>(k) + bq * p.ks[0] * 2;
+      const char* vb = static_cast<const char*>(v) + bq * p.vs[0] * 2;
+      const char* dob = static_cast<const char*>(dO) + bq * p.dos[0] * 2;
+      e = launch_bwd_simt(pb, qb, kb, vb, dob, lse_b, delta_b, bias, dq_b, dk_b, dv_b, dbias,
+                          nullptr, nullptr, nullptr, nullptr, nullptr, st, stream);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return ATTN_OK;
 }
 
 attn_status_t attn_read_device_status(const void* workspace, cudaStream_t stream,

@@ -153,6 +153,7 @@ struct Problem {
   int64_t qs[3], ks[3], vs[3], os[3], dos[3];
   MaskSpec mask;
   bool sparse;
+  bool deterministic;  // ATTN_FLAG_DETERMINISTIC
   // sparse fields (cmp_ratio > 0 only in the CFA case: no index list, every
   // compressed row whose block ends at or before the query is selected)
   int n_ori, n_cmp, topk, ori_wl, ori_wr, cmp_ratio;

@@ -982,6 +982,9 @@ EncodeFn encode_fn() {
 }
 
 int tc_head_split(const Problem& p) {
+  // deterministic: one CTA per key tile writes dK / dV (no partial sums added
+  // in arrival order)
+  if (p.deterministic) return 1;
   return head_split(p.Hq / p.Hk, p.B * p.Hk * (p.Sk / BN), sm_count());
 }
 

@@ -73,7 +73,22 @@ typedef struct attn_problem {
   int64_t v_stride[3];
   int64_t o_stride[3];    /* o (written by attn_fwd_lse, read by preprocess) */
   int64_t do_stride[3];
+  int32_t flags;          /* ATTN_FLAG_* bits; 0 = defaults. Pass the same value to
+                             attn_bwd_preprocess and attn_bwd. */
 } attn_problem_t;
+
+/* Deterministic dense backward: dq, dk, dv and dbias are bitwise the same on
+ * every run. dk / dv are then written by one CTA per key tile (no split of a
+ * key tile's query heads over CTAs, whose partial sums would be added in
+ * arrival order), and with dbias and B > 1 attn_bwd runs one launch per batch
+ * so that each dbias element receives its per-batch terms in batch order.
+ * Slower than the default. The sparse path's dKV is a reduction over tokens
+ * in arrival order: a sparse problem with this flag returns
+ * ATTN_ERR_UNSUPPORTED. (Composable_kernel "34_bwd_gqa_fmha.py" names
+ * atomics vs a deterministic reduction for dK / dV; the Ascend
+ * "sparse_flash_mla_grad" page notes its operator is not deterministic by
+ * default.) */
+#define ATTN_FLAG_DETERMINISTIC 1
 
 /* Key mask, positions aligned top-left ("22_sink_tokens_fmha.py"):
  *   live(i, j) = (j < num_sink) || (i - window_left <= j && j <= i + window_right)

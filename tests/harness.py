@@ -115,14 +115,14 @@ def to_dev_f32(x, dev):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
 
 
-def gpu_dense_plan(w, O_b, L_f, dev="cuda"):
+def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False):
     import attention_backward_attn_gb300 as ab
     q, k, v, o, do = (to_dev_bf16(x, dev) for x in (w.q, w.k, w.v, O_b, w.do))
     lse = to_dev_f32(L_f, dev)
     bias = None if w.bias is None else to_dev_f32(w.bias, dev)
     mask = ab.mask_from(w.window_left, w.window_right, w.num_sink)
     return ab.BackwardPlan(q, k, v, o, do, lse, w.scale, mask=mask, bias=bias,
-                           want_dbias=w.want_dbias)
+                           want_dbias=w.want_dbias, deterministic=deterministic)
 
 
 def gpu_sparse_plan(w, O_b, L_f, dev="cuda"):

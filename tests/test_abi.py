@@ -159,6 +159,21 @@ def test_sparse_descriptor_validation(ab):
     assert ab.attn_bwd_path(p2, None, s) == 0
     # a mask descriptor is not allowed with the sparse window
     assert ab.attn_bwd_path(p, ab.Mask(-1, 0, 0), s) == 0
+    # the deterministic mode covers the dense path only (sparse dKV is a
+    # reduction over tokens in arrival order)
+    p.flags = ab.ATTN_FLAG_DETERMINISTIC
+    assert ab.attn_bwd_path(p, None, s) == 0
+    assert _call_bwd(ab, p, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None)) == 2
+    p.flags = 0
+
+
+def test_problem_flags(ab):
+    p = _prob(ab)
+    assert ab.attn_bwd_path(p, None, None) in (1, 2)
+    p.flags = ab.ATTN_FLAG_DETERMINISTIC
+    assert ab.attn_bwd_path(p, None, None) in (1, 2)
+    p.flags = 2  # unknown bit
+    assert ab.attn_bwd_path(p, None, None) == 0
 
 
 def test_read_status_rejects_null(ab):

@@ -117,6 +117,44 @@ def test_tensor_core_cases(name):
     _compare_dense(w, plan, O_b, L_f)
 
 
+# Deterministic mode (ATTN_FLAG_DETERMINISTIC): bitwise-identical outputs over
+# repeated runs, and the usual oracle parity.
+DETERMINISTIC = {
+    # dbias over 3 batches on the tensor-core path: one launch per batch
+    "alibi_dbias_s256_d64": (lambda: SMALL_DENSE["alibi_dbias_s256_d64"](), 1),
+    # GQA 8:1 on two key tiles: by default each query head of a key tile gets its
+    # own CTA and the 8 partial dK / dV sums are added in arrival order
+    "gqa8_s256_d128": (lambda: make_dense("det", 25, B=1, Hq=8, Hk=1, Sq=256, Sk=256, D=128,
+                                          window_left=-1, window_right=0), 1),
+    # SIMT kernels (ragged lengths), dbias over 3 batches
+    "ragged_alibi_dbias_s200_d64": (lambda: make_dense("detr", 26, B=3, Hq=2, Hk=2, Sq=200,
+                                                       Sk=200, D=64, alibi=True,
+                                                       want_dbias=True), 2),
+}
+
+
+@pytest.mark.parametrize("name", list(DETERMINISTIC))
+def test_deterministic_mode(name):
+    torch = _torch()
+    make, path = DETERMINISTIC[name]
+    w = make()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    plan = H.gpu_dense_plan(w, O_b, L_f, deterministic=True)
+    assert plan.path == path
+    runs = []
+    for _ in range(3):
+        plan.run()
+        torch.cuda.synchronize()
+        code, detail = plan.device_status()
+        assert code == 0, (code, detail)
+        outs = [plan.dq, plan.dk, plan.dv] + ([plan.dbias] if w.want_dbias else [])
+        runs.append([t.cpu().numpy().copy() for t in outs])
+    for later in runs[1:]:
+        for a, b in zip(runs[0], later):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    _compare_dense(w, plan, O_b, L_f)
+
+
 def test_head_split_needs_the_prepared_dk_dv():
     # GQA 8:1 on a small problem splits each key tile's query heads over
     # several CTAs that add partial sums into dk / dv; the pre-pass zeroes the
