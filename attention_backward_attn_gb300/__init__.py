@@ -50,7 +50,7 @@ class Problem(ctypes.Structure):
 
 class Mask(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
-                ("num_sink", ctypes.c_int32)]
+                ("num_sink", ctypes.c_int32), ("bottom_right", ctypes.c_int32)]
 
 
 class Sparse(ctypes.Structure):
@@ -157,10 +157,13 @@ def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = No
     return p
 
 
-def mask_from(window_left: int = -1, window_right: int = -1, num_sink: int = 0) -> Optional[Mask]:
+def mask_from(window_left: int = -1, window_right: int = -1, num_sink: int = 0,
+              bottom_right: bool = False) -> Optional[Mask]:
+    """(window_left, window_right) around the diagonal j = i (top-left) or
+    j = i + Sk - Sq (bottom_right); negative = unbounded; plus num_sink keys."""
     if window_left < 0 and window_right < 0 and num_sink == 0:
         return None
-    return Mask(window_left, window_right, num_sink)
+    return Mask(window_left, window_right, num_sink, 1 if bottom_right else 0)
 
 
 def sparse_from(ori_kv, cmp_kv=None, cmp_idx=None, ori_win_left=-1, ori_win_right=-1,

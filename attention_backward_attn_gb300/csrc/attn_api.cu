@@ -16,6 +16,25 @@ bool strides_ok(const int64_t* s) {
   return true;
 }
 
+// The mask descriptor as window bounds around the diagonal (MaskSpec): a
+// negative window bound means unbounded; bounds beyond any sequence are
+// unbounded too; bottom-right alignment shifts both bounds by Sk - Sq.
+attn_status_t mask_spec_of(const attn_mask_t* mask, int Sq, int Sk, MaskSpec* out) {
+  MaskSpec m{kMaskUnbounded, kMaskUnbounded, 0};
+  if (mask != nullptr) {
+    if (mask->num_sink < 0 || (mask->bottom_right != 0 && mask->bottom_right != 1))
+      return ATTN_ERR_INVALID_ARG;
+    const bool open_l = mask->window_left < 0 || mask->window_left >= kMaskMaxBound;
+    const bool open_r = mask->window_right < 0 || mask->window_right >= kMaskMaxBound;
+    const int off = mask->bottom_right ? Sk - Sq : 0;
+    m.wl = open_l ? kMaskUnbounded : mask->window_left - off;
+    m.wr = open_r ? kMaskUnbounded : mask->window_right + off;
+    m.sink = mask->num_sink;
+  }
+  *out = m;
+  return ATTN_OK;
+}
+
 // Validates the shared problem / mask / sparse descriptors and fills `out`.
 attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
                            const attn_sparse_t* sp, Problem* out) {
@@ -48,12 +67,9 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
   }
   if (a.flags & ~ATTN_FLAG_DETERMINISTIC) return ATTN_ERR_INVALID_ARG;
   p.deterministic = (a.flags & ATTN_FLAG_DETERMINISTIC) != 0;
-  p.mask = MaskSpec{-1, -1, 0};
-  if (mask != nullptr) {
-    if (mask->num_sink < 0) return ATTN_ERR_INVALID_ARG;
-    p.mask = MaskSpec{mask->window_left < 0 ? -1 : mask->window_left,
-                      mask->window_right < 0 ? -1 : mask->window_right, mask->num_sink};
-  }
+  if (a.Sq > kMaxMaskedLen || a.Sk > kMaxMaskedLen) return ATTN_ERR_UNSUPPORTED;
+  const attn_status_t ms = mask_spec_of(mask, a.Sq, a.Sk, &p.mask);
+  if (ms != ATTN_OK) return ms;
   p.sparse = sp != nullptr;
   if (p.sparse && p.deterministic) return ATTN_ERR_UNSUPPORTED;  // dKV: reduction over tokens
   if (p.sparse) {
@@ -161,12 +177,10 @@ attn_status_t attn_mask_tile_classes(const attn_mask_t* mask, int32_t Sq, int32_
                                      int32_t tile_q, int32_t tile_k, int8_t* out) {
   if (Sq <= 0 || Sk <= 0 || tile_q <= 0 || tile_k <= 0 || out == nullptr)
     return ATTN_ERR_INVALID_ARG;
-  MaskSpec m{-1, -1, 0};
-  if (mask != nullptr) {
-    if (mask->num_sink < 0) return ATTN_ERR_INVALID_ARG;
-    m = MaskSpec{mask->window_left < 0 ? -1 : mask->window_left,
-                 mask->window_right < 0 ? -1 : mask->window_right, mask->num_sink};
-  }
+  if (Sq > kMaxMaskedLen || Sk > kMaxMaskedLen) return ATTN_ERR_UNSUPPORTED;
+  MaskSpec m;
+  const attn_status_t ms = mask_spec_of(mask, Sq, Sk, &m);
+  if (ms != ATTN_OK) return ms;
   const int nmt = (Sq + tile_q - 1) / tile_q, nnt = (Sk + tile_k - 1) / tile_k;
   for (int mt = 0; mt < nmt; ++mt) {
     const int m0 = mt * tile_q, m1 = m0 + tile_q < Sq ? m0 + tile_q : Sq;

@@ -34,6 +34,15 @@ __device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t deta
 
 // live(i, j) = j < sink || (i - wl <= j <= i + wr); negative bound = unbounded
 // ("22_sink_tokens_fmha.py" mask builders, top-left aligned).
+// Key mask over (query i, key j): live when j < sink or -wl <= j - i <= wr.
+// The bounds are relative to the diagonal j = i; kMaskUnbounded leaves that
+// side open. They may be negative: a bottom-right aligned mask is a top-left
+// one with both bounds shifted by Sk - Sq. Bounds are clamped to
+// [-kMaskMaxBound, kMaskMaxBound] and lengths to kMaxMaskedLen, so i +- bound
+// stays inside int.
+constexpr int kMaskUnbounded = 1 << 29;
+constexpr int kMaskMaxBound = 1 << 28;
+constexpr int kMaxMaskedLen = 1 << 28;
 struct MaskSpec {
   int wl;
   int wr;
@@ -42,16 +51,14 @@ struct MaskSpec {
 
 __host__ __device__ __forceinline__ bool mask_live(const MaskSpec& m, int i, int j) {
   if (j < m.sink) return true;
-  if (m.wl >= 0 && j < i - m.wl) return false;
-  if (m.wr >= 0 && j > i + m.wr) return false;
-  return true;
+  return j >= i - m.wl && j <= i + m.wr;
 }
 
-// Non-sink key range [lo, hi] (inclusive, clipped to [0, n)) live for row i.
+// Non-sink key range [lo, hi] (inclusive, clipped to [0, n); empty when
+// lo > hi) live for row i.
 __host__ __device__ __forceinline__ void mask_row_range(const MaskSpec& m, int i, int n,
                                                         int* lo, int* hi) {
-  int a = (m.wl >= 0) ? i - m.wl : 0;
-  int b = (m.wr >= 0) ? i + m.wr : n - 1;
+  const int a = i - m.wl, b = i + m.wr;
   *lo = a < 0 ? 0 : a;
   *hi = b > n - 1 ? n - 1 : b;
 }
@@ -59,8 +66,7 @@ __host__ __device__ __forceinline__ void mask_row_range(const MaskSpec& m, int i
 // Non-sink query range [lo, hi] live for key j (j >= sink), clipped to [0, n).
 __host__ __device__ __forceinline__ void mask_col_range(const MaskSpec& m, int j, int n,
                                                         int* lo, int* hi) {
-  int a = (m.wr >= 0) ? j - m.wr : 0;
-  int b = (m.wl >= 0) ? j + m.wl : n - 1;
+  const int a = j - m.wr, b = j + m.wl;
   *lo = a < 0 ? 0 : a;
   *hi = b > n - 1 ? n - 1 : b;
 }
@@ -73,9 +79,7 @@ __host__ __device__ __forceinline__ bool tile_any(const MaskSpec& m, int m0, int
   if (n0 < m.sink) return true;
   const int dmax = (n1 - 1) - m0;  // largest j - i in the tile
   const int dmin = n0 - (m1 - 1);  // smallest j - i in the tile
-  if (m.wl >= 0 && dmax < -m.wl) return false;
-  if (m.wr >= 0 && dmin > m.wr) return false;
-  return true;
+  return dmax >= -m.wl && dmin <= m.wr;
 }
 
 __host__ __device__ __forceinline__ bool tile_full(const MaskSpec& m, int m0, int m1, int n0,
@@ -84,9 +88,7 @@ __host__ __device__ __forceinline__ bool tile_full(const MaskSpec& m, int m0, in
   if (a >= n1) return true;
   const int dmax = (n1 - 1) - m0;
   const int dmin = a - (m1 - 1);
-  if (m.wl >= 0 && dmin < -m.wl) return false;
-  if (m.wr >= 0 && dmax > m.wr) return false;
-  return true;
+  return dmin >= -m.wl && dmax <= m.wr;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

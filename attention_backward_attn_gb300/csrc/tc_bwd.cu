@@ -394,8 +394,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
       int qlo = 0, qhi = BM - 1;
       if (partial && j >= p.mask.sink) {
-        qlo = p.mask.wr >= 0 ? j - p.mask.wr - m0 : 0;
-        qhi = p.mask.wl >= 0 ? j + p.mask.wl - m0 : BM - 1;
+        qlo = j - p.mask.wr - m0;  // bits_between clamps to the tile
+        qhi = j + p.mask.wl - m0;
       }
       const float* brow = nullptr;
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
@@ -748,8 +748,8 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // live keys of this query row within the tile: [klo, khi] plus the sinks
       int klo = 0, khi = BN - 1, ksink = 0;
       if (partial) {
-        klo = p.mask.wl >= 0 ? i - p.mask.wl - n0 : 0;
-        khi = p.mask.wr >= 0 ? i + p.mask.wr - n0 : BN - 1;
+        klo = i - p.mask.wl - n0;  // bits_between clamps to the tile
+        khi = i + p.mask.wr - n0;
         ksink = p.mask.sink - n0;
       }
       const uint32_t t_S = t_S0 + (t & 1) * 128;

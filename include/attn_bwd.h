@@ -100,6 +100,12 @@ typedef struct attn_mask {
   int32_t window_left;
   int32_t window_right;
   int32_t num_sink;
+  int32_t bottom_right; /* 0: top-left as above; 1: bottom-right, i.e. i is
+                           replaced by i + (Sk - Sq) in the window test (the
+                           diagonal ends in the last query / key corner; with
+                           Sk < Sq the first Sq - Sk queries of a causal mask
+                           then have no live key). Equal to top-left when
+                           Sq == Sk. Sinks are unaffected. */
 } attn_mask_t;
 
 /* Selected-KV sparse attention with shared latent KV (Ascend

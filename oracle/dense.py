@@ -55,15 +55,21 @@ def window_sink_mask(seqlen_q: int, seqlen_k: int, window: int, num_sink: int) -
 
 
 def live_mask(seqlen_q: int, seqlen_k: int, window_left: int = -1,
-              window_right: int = -1, num_sink: int = 0) -> np.ndarray:
-    """The library's mask parametrisation, positions aligned top-left.
+              window_right: int = -1, num_sink: int = 0,
+              bottom_right: bool = False) -> np.ndarray:
+    """The library's mask parametrisation.
 
-    live(i, j) = (j < num_sink) or (i - window_left <= j <= i + window_right),
+    live(i, j) = (j < num_sink) or (i' - window_left <= j <= i' + window_right),
     where a negative window bound means that side is unbounded. So causal is
     (-1, 0, 0), causal + n sinks is (-1, 0, n) and a window of w keys plus n
-    sinks is (w - 1, 0, n).
+    sinks is (w - 1, 0, n). Positions are aligned top-left (i' = i) or, with
+    bottom_right, so that the diagonal ends in the last query / key corner
+    (i' = i + seqlen_k - seqlen_q: the "22_sink_tokens_fmha.py" mask format
+    names both alignments for the causal mask).
     """
     i, j = _grid(seqlen_q, seqlen_k)
+    if bottom_right:
+        i = i + (seqlen_k - seqlen_q)
     inside = np.ones((seqlen_q, seqlen_k), dtype=bool)
     if window_left >= 0:
         inside &= j >= i - window_left

@@ -24,7 +24,8 @@ def bhsd(x):
 def mask_of(w):
     if w.window_left < 0 and w.window_right < 0 and w.num_sink == 0:
         return None
-    return oracle.live_mask(w.Sq, w.Sk, w.window_left, w.window_right, w.num_sink)
+    return oracle.live_mask(w.Sq, w.Sk, w.window_left, w.window_right, w.num_sink,
+                            getattr(w, "bottom_right", False))
 
 
 def dense_forward_inputs(w):
@@ -120,7 +121,8 @@ def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False):
     q, k, v, o, do = (to_dev_bf16(x, dev) for x in (w.q, w.k, w.v, O_b, w.do))
     lse = to_dev_f32(L_f, dev)
     bias = None if w.bias is None else to_dev_f32(w.bias, dev)
-    mask = ab.mask_from(w.window_left, w.window_right, w.num_sink)
+    mask = ab.mask_from(w.window_left, w.window_right, w.num_sink,
+                        getattr(w, "bottom_right", False))
     return ab.BackwardPlan(q, k, v, o, do, lse, w.scale, mask=mask, bias=bias,
                            want_dbias=w.want_dbias, deterministic=deterministic)
 

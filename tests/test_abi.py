@@ -190,15 +190,21 @@ def test_read_status_rejects_null(ab):
     (200, 328, 40, 25, 3, 64, 32),          # ragged tails, two-sided window
     (384, 128, 10, 0, 0, 128, 128),         # rows without live keys
     (97, 61, -1, 0, 70, 16, 8),             # sinks beyond the diagonal
+    # bottom-right alignment (last column: 1)
+    (128, 384, -1, 0, 0, 128, 128, 1),      # causal, Sq < Sk
+    (384, 128, -1, 0, 0, 128, 128, 1),      # causal, Sq > Sk: rows without keys
+    (200, 328, 40, 25, 3, 64, 32, 1),       # ragged, two-sided window + sinks
+    (97, 61, 5, 0, 2, 16, 8, 1),
 ])
 def test_tile_classes_match_oracle_mask(ab, spec):
     # The kernels skip tiles classed 0 and mask tiles classed 1 per element;
     # the classes must agree bit-exactly with the oracle's element mask.
     import numpy as np
     import oracle
-    Sq, Sk, wl, wr, ns, tq, tk = spec
-    m = oracle.live_mask(Sq, Sk, wl, wr, ns)
-    got = ab.attn_mask_tile_classes(ab.Mask(wl, wr, ns), Sq, Sk, tq, tk)
+    Sq, Sk, wl, wr, ns, tq, tk = spec[:7]
+    br = spec[7] if len(spec) > 7 else 0
+    m = oracle.live_mask(Sq, Sk, wl, wr, ns, bottom_right=bool(br))
+    got = ab.attn_mask_tile_classes(ab.Mask(wl, wr, ns, br), Sq, Sk, tq, tk)
     for mt, row in enumerate(got):
         for nt, cls in enumerate(row):
             tile = m[mt * tq:(mt + 1) * tq, nt * tk:(nt + 1) * tk]

@@ -72,6 +72,19 @@ SMALL_DENSE = {
     "window_lr_sq320_sk192_d64": lambda: make_dense("y", 23, B=2, Hq=2, Hk=1, Sq=320, Sk=192,
                                                     D=64, window_left=40, window_right=25,
                                                     alibi=True),
+    # bottom-right causal, Sq < Sk (tensor-core path), GQA 4:1
+    "br_causal_sq128_sk384_d128": lambda: make_dense("br1", 27, B=1, Hq=8, Hk=2, Sq=128,
+                                                     Sk=384, D=128, window_left=-1,
+                                                     window_right=0, bottom_right=True),
+    # bottom-right causal, Sq > Sk: the first 256 queries have no key
+    "br_causal_sq384_sk128_d64": lambda: make_dense("br2", 28, B=2, Hq=4, Hk=4, Sq=384,
+                                                    Sk=128, D=64, window_left=-1,
+                                                    window_right=0, bottom_right=True),
+    # bottom-right window + sinks, ragged lengths (SIMT kernels), bias
+    "br_window_sink_sq150_sk230_d64": lambda: make_dense("br3", 29, B=1, Hq=4, Hk=2, Sq=150,
+                                                         Sk=230, D=64, window_left=31,
+                                                         window_right=0, num_sink=3,
+                                                         alibi=True, bottom_right=True),
     # MHA D = 512 through the dense path
     "mha_s128_d512": lambda: make_dense("z", 24, B=1, Hq=2, Hk=2, Sq=128, Sk=128, D=512,
                                         window_left=-1, window_right=0),
@@ -79,7 +92,8 @@ SMALL_DENSE = {
 
 
 # cases whose shapes the tcgen05 kernel takes (D in {64, 128}, lengths multiples of 128)
-TC_CASES = {"gqa4_causal_s384_d128", "alibi_dbias_s256_d64", "window128_sink4_s640_d128"}
+TC_CASES = {"gqa4_causal_s384_d128", "alibi_dbias_s256_d64", "window128_sink4_s640_d128",
+            "br_causal_sq128_sk384_d128", "br_causal_sq384_sk128_d64"}
 
 
 @pytest.mark.parametrize("name", list(SMALL_DENSE))

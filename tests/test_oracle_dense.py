@@ -59,6 +59,32 @@ def test_masks_equal_page_definitions(sq, sk, sink, window):
     assert oracle.live_mask(sq, sk, -1, -1, 0).all()
 
 
+@pytest.mark.parametrize("sq,sk", [(5, 5), (5, 9), (9, 5), (1, 6), (6, 1)])
+@pytest.mark.parametrize("left,right,sink", [(-1, 0, 0), (-1, 0, 2), (2, 0, 1), (1, 2, 0)])
+def test_bottom_right_alignment(sq, sk, left, right, sink):
+    # Bottom-right: the diagonal ends in the last query / key corner, i.e. the
+    # window test uses i + (sk - sq); checked as a scalar loop.
+    off = sk - sq
+
+    def live(i, j):
+        if j < sink:
+            return True
+        ii = i + off
+        return (left < 0 or j >= ii - left) and (right < 0 or j <= ii + right)
+
+    got = oracle.live_mask(sq, sk, left, right, sink, bottom_right=True)
+    assert np.array_equal(got, _loop_mask(sq, sk, live))
+    if sq == sk:  # the two alignments coincide
+        assert np.array_equal(got, oracle.live_mask(sq, sk, left, right, sink))
+    if left < 0 and right == 0 and sink == 0:
+        # causal: sk >= sq is top-left causal widened by sk - sq; sk < sq leaves
+        # the first sq - sk queries without a key
+        if sk >= sq:
+            assert np.array_equal(got, oracle.live_mask(sq, sk, -1, sk - sq, 0))
+        else:
+            assert not got[:sq - sk].any() and got[sq - sk:].any(axis=1).all()
+
+
 def test_live_entry_counts_closed_form():
     # Causal S=1024: sum_{i} (i + 1) = S (S + 1) / 2.
     assert oracle.live_mask(1024, 1024, -1, 0, 0).sum() == 1024 * 1025 // 2

@@ -109,7 +109,8 @@ class DenseWorkload:
     Tensors are float32 holding bf16-exact values, in the library's BSHD
     layout: q, do [B, Sq, Hq, D]; k, v [B, Sk, Hk, D]. bias is float32
     [Hq, Sq, Sk] or None. The mask is (window_left, window_right, num_sink)
-    with -1 meaning unbounded, positions aligned top-left.
+    with -1 meaning unbounded, positions aligned top-left (bottom_right=True:
+    the window is taken around j = i + Sk - Sq).
     """
 
     name: str
@@ -129,6 +130,7 @@ class DenseWorkload:
     window_right: int = -1
     num_sink: int = 0
     want_dbias: bool = False
+    bottom_right: bool = False
 
     @property
     def masked(self) -> bool:
@@ -187,6 +189,7 @@ def make_dense(
     want_dbias: bool = False,
     scale: Optional[float] = None,
     mult: float = 1.0,
+    bottom_right: bool = False,
 ) -> DenseWorkload:
     """Draw q, k, v, dO (in that order) from default_rng(seed), N(0,1)*mult, bf16."""
     rng = np.random.default_rng(seed)
@@ -200,7 +203,7 @@ def make_dense(
         scale=float(1.0 / np.sqrt(D)) if scale is None else float(scale),
         q=q, k=k, v=v, do=do, bias=bias,
         window_left=window_left, window_right=window_right, num_sink=num_sink,
-        want_dbias=want_dbias,
+        want_dbias=want_dbias, bottom_right=bottom_right,
     )
 
 
