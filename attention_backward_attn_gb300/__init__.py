@@ -20,6 +20,7 @@ __all__ = [
     "problem_from", "mask_from", "sparse_from", "ATTN_FLAG_DETERMINISTIC",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
+    "attn_bwd_dsinks",
 ]
 
 ATTN_OK = 0
@@ -82,6 +83,8 @@ def _load():
     L.attn_bwd.argtypes = [P(Problem), P(Mask), P(Sparse), vp, vp, vp, vp, vp, vp, vp,
                            vp, vp, vp, vp, vp, sz, vp]
     L.attn_bwd.restype = st
+    L.attn_bwd_dsinks.argtypes = [P(Problem), vp, vp, vp, vp, vp]
+    L.attn_bwd_dsinks.restype = st
     L.attn_read_device_status.argtypes = [vp, vp, P(ctypes.c_int32)]
     L.attn_read_device_status.restype = st
     L.attn_status_string.argtypes = [st]
@@ -216,6 +219,13 @@ def attn_bwd(prob, mask, sparse, q, k, v, do, lse, delta, bias, dq, dk, dv, dbia
                         _ptr(dv), _ptr(dbias), _ptr(workspace), workspace_bytes,
                         _stream(stream)),
            "attn_bwd")
+
+
+def attn_bwd_dsinks(prob, sinks, lse, delta, dsinks, stream=None):
+    """dsinks [Hq] = -sum_{b,i} exp(sinks - lse) * delta (see include/attn_bwd.h)."""
+    _check(lib.attn_bwd_dsinks(ctypes.byref(prob), _ptr(sinks), _ptr(lse), _ptr(delta),
+                               _ptr(dsinks), _stream(stream)),
+           "attn_bwd_dsinks")
 
 
 def attn_bwd_noalloc(prob, mask, sparse, q, k, v, o, do, lse, bias, delta, dq, dk, dv, dbias,

@@ -364,6 +364,20 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
   return ATTN_OK;
 }
 
+attn_status_t attn_bwd_dsinks(const attn_problem_t* prob, const float* sinks,
+                              const float* lse, const float* delta, float* dsinks,
+                              cudaStream_t stream) {
+  if (prob == nullptr || sinks == nullptr || lse == nullptr || delta == nullptr ||
+      dsinks == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (prob->B <= 0 || prob->Hq <= 0 || prob->Sq <= 0) return ATTN_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(sinks) | reinterpret_cast<uintptr_t>(lse) |
+                        reinterpret_cast<uintptr_t>(delta) | reinterpret_cast<uintptr_t>(dsinks);
+  if (mis & 3u) return ATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_dsinks(prob->B, prob->Hq, prob->Sq, sinks, lse, delta, dsinks,
+                                   stream));
+}
+
 attn_status_t attn_read_device_status(const void* workspace, cudaStream_t stream,
                                       int32_t* detail) {
   if (workspace == nullptr) return ATTN_ERR_INVALID_ARG;

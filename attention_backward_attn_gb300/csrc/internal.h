@@ -52,6 +52,11 @@ cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, co
                               __half* kv16, float* dk_zero, float* dv_zero, float* dk,
                               float* dv, DevStatus* st, cudaStream_t stream);
 
+// dsinks[h] = -sum_{b, i} exp(sinks[h] - lse[b, h, i]) delta[b, h, i], one
+// CTA per head, fixed-order reduction.
+cudaError_t launch_dsinks(int B, int Hq, int Sq, const float* sinks, const float* lse,
+                          const float* delta, float* dsinks, cudaStream_t stream);
+
 // ---- tc_bwd.cu ----
 bool tc_supported(const Problem& p);
 // Key-major CTAs per (key tile, KV head) of the dense tensor-core kernel; when

@@ -287,7 +287,41 @@ preprocess_kernel(const PreParams p) {
   if (threadIdx.x == 0) reinterpret_cast<int32_t*>(p.st + 1)[blockIdx.x] = block_bits;
 }
 
+// Sink-logit gradient: one CTA per query head; each thread sums its strided
+// share of the (batch, query) rows in double, then a fixed tree over the
+// block, so the result does not depend on scheduling.
+constexpr int kSinkThreads = 256;
+__global__ void __launch_bounds__(kSinkThreads)
+dsinks_kernel(int B, int Hq, int Sq, const float* __restrict__ sinks,
+              const float* __restrict__ lse, const float* __restrict__ delta,
+              float* __restrict__ dsinks) {
+  const int h = blockIdx.x;
+  const float s = sinks[h];
+  const int64_t n = (int64_t)B * Sq;
+  double acc = 0.0;
+  for (int64_t r = threadIdx.x; r < n; r += kSinkThreads) {
+    const int64_t b = r / Sq, i = r % Sq;
+    const int64_t row = (b * Hq + h) * Sq + i;
+    const float L = lse[row];
+    if (L != -INFINITY) acc -= (double)expf(s - L) * (double)delta[row];
+  }
+  __shared__ double part[kSinkThreads];
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = kSinkThreads / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsinks[h] = (float)part[0];
+}
+
 }  // namespace
+
+cudaError_t launch_dsinks(int B, int Hq, int Sq, const float* sinks, const float* lse,
+                          const float* delta, float* dsinks, cudaStream_t stream) {
+  dsinks_kernel<<<Hq, kSinkThreads, 0, stream>>>(B, Hq, Sq, sinks, lse, delta, dsinks);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, const void* v,
                               const void* o, const void* dO, float* delta,

@@ -198,6 +198,23 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
                        void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Gradient of learnable sink logits (one per query head): a sink logit s_h
+ * joins every softmax denominator of head h without a value vector, so it is
+ * already inside the LSE the forward returned, and P, dS, dq, dk, dv of
+ * attn_bwd are unchanged by it. Its own gradient (Ascend
+ * "sparse_flash_mla_grad" formula, phase 3: dSinks = ReduceSum(-P x dP x
+ * SimpleSoftmax(sinks, lse))) is
+ *   dsinks[h] = -sum over b, i of exp(sinks[h] - lse[b, h, i]) * delta[b, h, i]
+ * with delta the attn_bwd_preprocess output; rows with lse = -inf add nothing.
+ * sinks, dsinks fp32 [Hq]; lse, delta fp32 [B, Hq, Sq] (B = 1 for the sparse
+ * variant); all device memory, 4-byte aligned. dsinks is overwritten. One CTA
+ * per head sums in a fixed order: the result is bitwise reproducible.
+ * Call after attn_bwd_preprocess on the same stream. Returns
+ * ATTN_ERR_INVALID_ARG for null pointers or non-positive B, Hq, Sq. */
+attn_status_t attn_bwd_dsinks(const attn_problem_t* prob, const float* sinks,
+                              const float* lse, const float* delta, float* dsinks,
+                              cudaStream_t stream);
+
 /* Synchronises `stream`, then returns the first device-side condition
  * recorded in the workspace status record since the last
  * attn_bwd_preprocess (ATTN_OK if none). *detail (may be NULL) receives a

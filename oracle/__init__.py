@@ -30,6 +30,7 @@ from .dense import (
     live_mask,
     forward,
     preprocess,
+    dsinks,
     backward,
 )
 from .sparse import (
@@ -45,6 +46,7 @@ __all__ = [
     "live_mask",
     "forward",
     "preprocess",
+    "dsinks",
     "backward",
     "selected_rows",
     "sparse_forward",

@@ -99,8 +99,14 @@ def _block_cols(mask: Optional[np.ndarray], r0: int, r1: int, seqlen_k: int):
 
 def forward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
             mask: Optional[np.ndarray] = None,
-            bias: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+            bias: Optional[np.ndarray] = None,
+            sinks: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
     """O = softmax(scale Q K^T + bias, masked) V and LSE = natural log-sum-exp.
+
+    sinks (float [Hq], optional): a learnable logit per query head that joins
+    every row's softmax denominator without a value vector (the Ascend
+    "sparse_flash_mla_grad" sinks input): LSE = log(sum_j exp(S_ij) +
+    exp(sink_h)), O = sum_j exp(S_ij - LSE) V_j.
 
     Returns (O [B, Hq, Sq, Dv] float64, LSE [B, Hq, Sq] float64).
     """
@@ -112,22 +118,25 @@ def forward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
     ratio = Hq // Hk
     O = np.zeros((B, Hq, Sq, Dv))
     LSE = np.full((B, Hq, Sq), -np.inf)
+    sk = None if sinks is None else np.asarray(sinks, np.float64)
     for b in range(B):
         for h in range(Hq):
             g = h // ratio
+            sink = -np.inf if sk is None else sk[h]
             for r0, r1 in _blocks(Sq):
                 cols, m = _block_cols(mask, r0, r1, Sk)
                 if cols.size == 0:
+                    LSE[b, h, r0:r1] = sink  # only the sink (or nothing) in the row
                     continue
                 S = scale * (Q[b, h, r0:r1] @ K[b, g, cols].T)
                 if bias is not None:
                     S = S + np.asarray(bias[h, r0:r1][:, cols], np.float64)
                 if m is not None:
                     S = np.where(m, S, -np.inf)
-                row_max = S.max(axis=1)
+                row_max = np.maximum(S.max(axis=1), sink)
                 shift = np.where(np.isfinite(row_max), row_max, 0.0)
                 E = np.exp(S - shift[:, None])
-                denom = E.sum(axis=1)
+                denom = E.sum(axis=1) + np.exp(sink - shift)
                 live = denom > 0
                 P = np.zeros_like(E)
                 P[live] = E[live] / denom[live, None]
@@ -145,6 +154,22 @@ def forward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
 def preprocess(O: np.ndarray, dO: np.ndarray) -> np.ndarray:
     """D = rowsum(dO * O) over the value dimension, [B, Hq, Sq]."""
     return (np.asarray(dO, np.float64) * np.asarray(O, np.float64)).sum(axis=-1)
+
+
+def dsinks(LSE: np.ndarray, Dlt: np.ndarray, sinks: np.ndarray) -> np.ndarray:
+    """Gradient of the sink logits, float [Hq] (Ascend "sparse_flash_mla_grad"
+    formula, phase 3: dSinks = ReduceSum(-P x dP x SimpleSoftmax(sinks, lse))).
+
+    The sink's probability in row (b, h, i) is p = exp(sink_h - LSE[b, h, i]);
+    sum_j P_ij dP_ij = D[b, h, i]; so dsink_h = -sum_{b, i} p D[b, h, i]. A row
+    with LSE = -inf (no live key and no sink) contributes nothing.
+    """
+    LSE = np.asarray(LSE, np.float64)
+    Dlt = np.asarray(Dlt, np.float64)
+    s = np.asarray(sinks, np.float64)[None, :, None]
+    with np.errstate(invalid="ignore", over="ignore"):
+        p = np.where(np.isfinite(LSE), np.exp(s - LSE), 0.0)
+    return -(p * Dlt).sum(axis=(0, 2))
 
 
 def backward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, O: np.ndarray,

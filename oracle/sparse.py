@@ -76,8 +76,12 @@ def _check_case(cmp_kv, cmp_idx, cmp_ratio):
 
 def sparse_forward(q: np.ndarray, ori_kv: np.ndarray, cmp_kv: Optional[np.ndarray],
                    cmp_idx: Optional[np.ndarray], scale: float, win_left: int,
-                   win_right: int, cmp_ratio: Optional[int] = None):
-    """O [Sq, Hq, D] and LSE [Hq, Sq] (natural log) over the selected rows."""
+                   win_right: int, cmp_ratio: Optional[int] = None,
+                   sinks: Optional[np.ndarray] = None):
+    """O [Sq, Hq, D] and LSE [Hq, Sq] (natural log) over the selected rows.
+
+    sinks (float [Hq], optional): per-head logits that join the softmax
+    denominator without a value vector (the page's sinks input)."""
     _check_case(cmp_kv, cmp_idx, cmp_ratio)
     q = np.asarray(q, np.float64)
     ori_kv = np.asarray(ori_kv, np.float64)
@@ -87,17 +91,19 @@ def sparse_forward(q: np.ndarray, ori_kv: np.ndarray, cmp_kv: Optional[np.ndarra
     ratio = Hq // Hk
     O = np.zeros((Sq, Hq, D))
     LSE = np.full((Hq, Sq), -np.inf)
+    sk = np.full(Hq, -np.inf) if sinks is None else np.asarray(sinks, np.float64)
     for i in range(Sq):
         for g in range(Hk):
             _, _, sel = _gather(i, g, ori_kv, cmp_kv, cmp_idx, Sq, win_left, win_right,
                                 cmp_ratio)
-            if sel.shape[0] == 0:
-                continue
             hs = slice(g * ratio, (g + 1) * ratio)
+            if sel.shape[0] == 0:
+                LSE[hs, i] = sk[hs]  # only the sink (or nothing)
+                continue
             S = scale * (q[i, hs] @ sel.T)
-            row_max = S.max(axis=1)
+            row_max = np.maximum(S.max(axis=1), sk[hs])
             E = np.exp(S - row_max[:, None])
-            denom = E.sum(axis=1)
+            denom = E.sum(axis=1) + np.exp(sk[hs] - row_max)
             O[i, hs] = (E / denom[:, None]) @ sel
             LSE[hs, i] = row_max + np.log(denom)
     return O, LSE

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import harness as H
+import oracle
 from workloads import make_workload, make_dense, make_sparse
 
 pytestmark = pytest.mark.gpu
@@ -426,3 +427,61 @@ def test_full_sparse_scfa_s4096_h64_d512():
     w = make_workload("sparse_scfa_s4096_h64_d512")
     plan, O_b, L_f = _run_sparse(w, expect_path=1)
     _compare_sparse(w, plan, O_b, L_f)
+
+
+SINK_CASES = {
+    # dense, tensor-core path, GQA 4:1 causal
+    "dense_tc": lambda: make_workload("gqa4_causal_s1024_d128", Hq=8, Hk=2, Sq=256, Sk=256),
+    # dense, SIMT path (ragged), window + sinks tokens
+    "dense_simt": lambda: SMALL_DENSE["ragged_causal_sink_s200_d64"](),
+    # sparse, tensor-core path
+    "sparse_tc": lambda: TC_SPARSE["tc_scfa_hk2_delta"](),
+}
+
+
+@pytest.mark.parametrize("name", list(SINK_CASES))
+def test_sink_logits(name):
+    # Learnable sink logits: the forward's LSE contains them, attn_bwd is
+    # unchanged, and attn_bwd_dsinks gives their gradient.
+    torch = _torch()
+    import attention_backward_attn_gb300 as ab
+    w = SINK_CASES[name]()
+    rng = np.random.default_rng(90)
+    sinks = rng.standard_normal(w.Hq).astype(np.float32)
+    sparse = w.__class__.__name__ == "SparseWorkload"
+    if sparse:
+        q = np.asarray(w.q, np.float64)
+        okv = np.asarray(w.ori_kv, np.float64)
+        ckv = None if w.cmp_kv is None else np.asarray(w.cmp_kv, np.float64)
+        O, L = oracle.sparse_forward(q, okv, ckv, w.cmp_idx, w.scale, w.ori_win_left,
+                                     w.ori_win_right, H.cfa_ratio(w), sinks=sinks)
+        O_b = np.ascontiguousarray(H.bf16_round(O.astype(np.float32)))
+        L_f = L.astype(np.float32)
+        plan = H.gpu_sparse_plan(w, O_b, L_f)
+    else:
+        O, L = oracle.forward(H.bhsd(w.q), H.bhsd(w.k), H.bhsd(w.v), w.scale, H.mask_of(w),
+                              None if w.bias is None else w.bias.astype(np.float64), sinks)
+        O_b = np.ascontiguousarray(H.bf16_round(O.transpose(0, 2, 1, 3).astype(np.float32)))
+        L_f = L.astype(np.float32)
+        plan = H.gpu_dense_plan(w, O_b, L_f)
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 0, (code, detail)
+    if sparse:
+        _compare_sparse(w, plan, O_b, L_f)
+        lse3 = L_f[None].astype(np.float64)
+        dlt = (np.asarray(w.do, np.float64) * O_b.astype(np.float64)).sum(-1).T[None]
+    else:
+        _compare_dense(w, plan, O_b, L_f)
+        lse3 = L_f.astype(np.float64)
+        dlt = oracle.preprocess(H.bhsd(O_b), H.bhsd(w.do))
+    ref = oracle.dsinks(lse3, dlt, sinks.astype(np.float64))
+    sk = torch.from_numpy(sinks).cuda()
+    got = torch.empty(w.Hq, dtype=torch.float32, device="cuda")
+    ab.attn_bwd_dsinks(plan.prob, sk, plan.lse, plan.delta, got)
+    got2 = torch.empty_like(got)
+    ab.attn_bwd_dsinks(plan.prob, sk, plan.lse, plan.delta, got2)
+    torch.cuda.synchronize()
+    H.check_close("dsinks", got.cpu().numpy(), ref)
+    assert torch.equal(got, got2)  # fixed-order reduction

@@ -296,3 +296,67 @@ def test_alibi_generator_matches_formula():
     assert b[3, 4, 1] == np.float32(-(2.0 ** -8) * 3)
     sq = alibi_bias(3, 7, 7)
     assert np.array_equal(sq, sq.transpose(0, 2, 1))  # |i - j| is symmetric
+
+
+def _sink_case(seed=11, B=2, Hq=4, Hk=2, Sq=6, Sk=7, D=3):
+    rng = np.random.default_rng(seed)
+    Q = rng.standard_normal((B, Hq, Sq, D))
+    K = rng.standard_normal((B, Hk, Sk, D))
+    V = rng.standard_normal((B, Hk, Sk, D))
+    dO = rng.standard_normal((B, Hq, Sq, D))
+    sinks = rng.standard_normal(Hq)
+    return Q, K, V, dO, sinks
+
+
+def test_sink_logit_equals_an_extra_key_with_zero_value():
+    # A sink logit s_h behaves as one more key, live for every query, with a
+    # zero key and value vector and bias s_h: the same O and LSE, and dsink_h
+    # is that column's bias gradient summed over the queries.
+    Q, K, V, dO, sinks = _sink_case()
+    B, Hq, Sq, D = Q.shape
+    Hk, Sk = K.shape[1], K.shape[2]
+    m = oracle.live_mask(Sq, Sk, 1, 0, 1)
+    O, L = oracle.forward(Q, K, V, 0.7, m, None, sinks)
+    Kx = np.concatenate([K, np.zeros((B, Hk, 1, D))], axis=2)
+    Vx = np.concatenate([V, np.zeros((B, Hk, 1, D))], axis=2)
+    mx = np.concatenate([m, np.ones((Sq, 1), dtype=bool)], axis=1)
+    bx = np.zeros((Hq, Sq, Sk + 1))
+    bx[:, :, Sk] = sinks[:, None]
+    Ox, Lx = oracle.forward(Q, Kx, Vx, 0.7, mx, bx)
+    np.testing.assert_allclose(O, Ox, atol=1e-13)
+    np.testing.assert_allclose(L, Lx, atol=1e-13)
+    dQ, dK, dV, _ = oracle.backward(Q, K, V, O, dO, L, 0.7, m)
+    dQx, dKx, dVx, dbx = oracle.backward(Q, Kx, Vx, Ox, dO, Lx, 0.7, mx, bx)
+    np.testing.assert_allclose(dQ, dQx, atol=1e-12)
+    np.testing.assert_allclose(dK, dKx[:, :, :Sk], atol=1e-12)
+    np.testing.assert_allclose(dV, dVx[:, :, :Sk], atol=1e-12)
+    ds = oracle.dsinks(L, oracle.preprocess(O, dO), sinks)
+    np.testing.assert_allclose(ds, dbx[:, :, Sk].sum(axis=1), atol=1e-12)
+
+
+def test_dsinks_finite_differences():
+    Q, K, V, dO, sinks = _sink_case(seed=12)
+    m = oracle.live_mask(Q.shape[2], K.shape[2], -1, 0, 0)
+    O, L = oracle.forward(Q, K, V, 0.5, m, None, sinks)
+    ds = oracle.dsinks(L, oracle.preprocess(O, dO), sinks)
+    eps = 1e-6
+    for h in range(len(sinks)):
+        vals = []
+        for sgn in (1, -1):
+            s2 = sinks.copy()
+            s2[h] += sgn * eps
+            O2, _ = oracle.forward(Q, K, V, 0.5, m, None, s2)
+            vals.append(float((O2 * dO).sum()))
+        num = (vals[0] - vals[1]) / (2 * eps)
+        assert abs(num - ds[h]) <= 1e-6 * max(1.0, abs(num)), (h, num, ds[h])
+
+
+def test_sinks_at_minus_infinity_change_nothing():
+    Q, K, V, dO, _ = _sink_case(seed=13)
+    m = oracle.live_mask(Q.shape[2], K.shape[2], -1, 0, 0)
+    off = np.full(Q.shape[1], -np.inf)
+    O, L = oracle.forward(Q, K, V, 0.5, m)
+    O2, L2 = oracle.forward(Q, K, V, 0.5, m, None, off)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(L, L2)
+    assert np.all(oracle.dsinks(L2, oracle.preprocess(O2, dO), off) == 0)

@@ -246,3 +246,26 @@ def test_cfa_without_a_ratio_is_rejected():
     w = _small_cfa(Sq=4, n_ori=4, n_cmp=2, ratio=2, left=1, Hq=1, Hk=1)
     with pytest.raises(ValueError):
         oracle.sparse_forward(_f64(w.q), _f64(w.ori_kv), _f64(w.cmp_kv), None, w.scale, 1, 0)
+
+
+def test_sparse_sinks_match_the_dense_extra_key():
+    # With sinks the sparse forward equals the dense one over the concatenated
+    # selected rows plus a zero key carrying the sink as its bias.
+    w = _small(Sq=8, n_ori=8, n_cmp=3, topk=2, ratio=2, left=2, Hq=2, Hk=1, D=3)
+    q, okv, ckv = _f64(w.q), _f64(w.ori_kv), _f64(w.cmp_kv)
+    sinks = np.array([0.3, -1.2])
+    O, L = oracle.sparse_forward(q, okv, ckv, w.cmp_idx, w.scale, 2, 0, sinks=sinks)
+    kv = np.concatenate([okv, ckv, np.zeros((1, 1, 3))], axis=0)
+    m = np.zeros((8, 12), dtype=bool)
+    for i in range(8):
+        m[i, max(0, i - 2):i + 1] = True
+        for c in w.cmp_idx[i, 0]:
+            if c >= 0:
+                m[i, 8 + c] = True
+    m[:, 11] = True
+    bias = np.zeros((2, 8, 12))
+    bias[:, :, 11] = sinks[:, None]
+    KV = kv.transpose(1, 0, 2)[None]
+    Od, Ld = oracle.forward(q.transpose(1, 0, 2)[None], KV, KV, w.scale, m, bias)
+    np.testing.assert_allclose(Od[0].transpose(1, 0, 2), O, atol=1e-13)
+    np.testing.assert_allclose(Ld[0], L, atol=1e-13)
