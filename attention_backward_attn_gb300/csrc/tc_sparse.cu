@@ -17,15 +17,17 @@
 //   SFU    P^T = exp2(S^T scale log2e - LSE log2e), dS^T = P^T (dP^T - D);
 //          G = [scale dS^T | P^T] as fp16 in shared memory ([128 rows][128])
 //   MMA-B  dQ^T += KV^T (scale dS^T) M = 128 d (4 chunks), N = 64 heads, K = 128 rows
-//   MMA-C  dKV^T = X^T G             M = 128 d (4 chunks) x N = 64 rows (2 halves), K = 128
+//   MMA-C  dKV^T = X^T G             M = 128 d (4 chunks), N = 128 rows, K = 128
 //   drain  every dKV^T block: TMEM -> registers -> red.global.add.f32 into the
 //          original / compressed gradient rows (each warp instruction adds
 //          one 128-byte run of one row)
 // dQ^T accumulates in TMEM over all tiles of the token and is written once.
 // The dKV reductions (D fp32 per selected row and token, from every token
 // that selected the row) are the bulk of the memory traffic, so the drain
-// has two warpgroups and its own TMEM buffers: the next tile's MMA-A,
-// softmax and MMA-B run while the previous tile drains.
+// has two warpgroups (one per 64-row half) and its own TMEM columns: a drain
+// warpgroup copies its half of a block into registers and releases it at
+// once, so the next block's MMAs run while it reduces, and the next tile's
+// MMA-A, softmax and MMA-B run while the previous tile drains.
 //
 // KV rows come from an fp16 copy of [ori_kv ; cmp_kv] made by the pre-pass.
 // Two loader warps copy them with cp.async (16 bytes per thread, written in
@@ -35,17 +37,17 @@
 // 64-column halves 8 KB apart); X takes 128 KB of shared memory, which leaves
 // no room to keep a whole [128 x 512] KV tile between the two.
 //
-// TMEM (512 columns): [0, 128) S^T|dP^T, [128, 192) and [192, 256) the two
-// dKV^T buffers, [256, 512) dQ^T (chunk c of 128 d at 256 + 64 c, one column
-// per head).
+// TMEM (512 columns): [0, 128) S^T|dP^T, [128, 256) a dKV^T block (column n =
+// row n of the tile), [256, 512) dQ^T (chunk c of 128 d at 256 + 64 c, one
+// column per head).
 //
 // Warp roles (512 threads): warp 0 builds the selected-row list of each
 // token (two buffers, so the list of the next token is ready early) and
 // issues the TMA copies of X; warp 1 owns TMEM and lane 0 issues the MMAs;
 // warps 2-3 load KV rows (they run on into the next token's tiles while the
 // current one finishes); warps 4-7 convert X from bf16 to fp16 in place and
-// run the softmax (thread = selected row); warps 8-11 / 12-15 drain the two
-// dKV^T buffers and write dQ (thread = column d). Between tokens the drain
+// run the softmax (thread = selected row); warps 8-11 / 12-15 drain rows
+// 0-63 / 64-127 of each dKV^T block and write dQ (thread = column d). Between tokens the drain
 // is still reducing the last tile while X of the next token loads and
 // converts. Every wait is bounded (tc_util.cuh).
 
@@ -83,7 +85,7 @@ static_assert(SpSmem::TOTAL <= 227 * 1024, "shared memory budget");
 // mbarriers. Per token: sXFull, sXReady, sXFree, sRowsReady/sRowsFree (one
 // pair per row-list buffer, tokens alternate), sDqFull, sDqFree. Per tile
 // (running counters across the tokens of the CTA): the ring, sStFull, sGFull,
-// sGFree, and the two dKV^T buffers (b = 0, 1 hold the row halves nh = b).
+// sGFree, sDkvFull / sDkvEmpty (four dKV^T blocks per tile).
 enum SpBar {
   sXFull = 0,        // X landed (TMA transaction count)
   sXReady = 1,       // X converted to fp16 (128 softmax threads)
@@ -95,12 +97,12 @@ enum SpBar {
   sStFull = 13,      // S^T | dP^T of the tile in TMEM
   sGFull = 14,       // G written, S^T | dP^T read (128 arrivals)
   sGFree = 15,       // the MMAs of the tile stopped reading G
-  sDkvFull0 = 16,    // a dKV^T block is in buffer b (x2)
-  sDkvEmpty0 = 18,   // the drain has read buffer b (x2, 128 arrivals)
-  sDqFull = 20,      // dQ^T of the token complete
-  sDqFree = 21,      // the drain has read dQ^T (256 arrivals)
-  sDone = 22,        // every MMA of the CTA completed (teardown)
-  kSpBars = 23
+  sDkvFull = 16,     // a dKV^T block (one d chunk, all 128 rows) is in TMEM
+  sDkvEmpty = 17,    // both drain warpgroups have read it (256 arrivals)
+  sDqFull = 18,      // dQ^T of the token complete
+  sDqFree = 19,      // the drain has read dQ^T (256 arrivals)
+  sDone = 20,        // every MMA of the CTA completed (teardown)
+  kSpBars = 21
 };
 
 struct SpParams {
@@ -226,7 +228,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     counts[sRowsFree0] = counts[sRowsFree0 + 1] = 449;
     for (int s = 0; s < kSpSlots; ++s) counts[sKvFull0 + s] = 64;
     counts[sGFull] = 128;
-    counts[sDkvEmpty0] = counts[sDkvEmpty0 + 1] = 128;
+    counts[sDkvEmpty] = 256;
     counts[sDqFree] = 256;
     for (int b = 0; b < kSpBars; ++b) ptx::mbar_init(c.bar(b), counts[b]);
     *c.abort = 0;
@@ -283,12 +285,12 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (lane == 0) {
       constexpr uint32_t idA = ptx::idesc_f16_f32(128, 128, false, false);
       constexpr uint32_t idB = ptx::idesc_f16_f32(128, 64, true, true);
-      constexpr uint32_t idC = ptx::idesc_f16_f32(128, 64, true, false);
+      constexpr uint32_t idC = ptx::idesc_f16_f32(128, 128, true, false);
       const uint32_t tS = tmem, tQ = tmem + 256;
       bool ok = true;
       int slot = 0;
       uint32_t ph = 0;
-      int issued[2] = {0, 0}, freed[2] = {0, 0};
+      int issued = 0, freed = 0;  // dKV^T blocks issued / read by the drain
       int gt = 0;  // tiles of this CTA so far (all tokens)
       // operand descriptors, built once (slots and K steps add their offsets)
       const uint64_t dKV = ptx::smem_desc_sw128(sKV, 16, 1024);               // K-major
@@ -330,18 +332,16 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 4; ++k)
           ptx::mma_ss(tS, ptx::desc_add(a0, 32 * k), ptx::desc_add(b0, 32 * k), idA, (s | k) != 0);
       };
-      // One MMA-C block: dKV^T (d chunk h / 2, row half h % 2) = X^T G into
-      // buffer h % 2 (the drain has read that buffer's previous block).
-      auto c_block = [&](int h) {
-        const int cc = h >> 1, bb = h & 1;
+      // One MMA-C block: dKV^T (d chunk cc, all 128 rows of the tile) =
+      // X^T G (the drain has read the previous block).
+      auto c_block = [&](int cc) {
         const uint64_t a0 = ptx::desc_add(dXmn, 2 * cc * kSpSlot);
-        const uint64_t g0 = ptx::desc_add(dG, 64 * bb * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_ss(tmem + 128 + 64 * bb, ptx::desc_add(a0, 2048 * kk),
-                      ptx::desc_add(g0, (kk >> 2) * kSpSlot + (kk & 3) * 32), idC, kk != 0);
-        ptx::mma_commit(c.bar(sDkvFull0 + bb));
-        ++issued[bb];
+          ptx::mma_ss(tmem + 128, ptx::desc_add(a0, 2048 * kk),
+                      ptx::desc_add(dG, (kk >> 2) * kSpSlot + (kk & 3) * 32), idC, kk != 0);
+        ptx::mma_commit(c.bar(sDkvFull));
+        ++issued;
       };
       // After sGFull of tile t: two independent streams. The MMA-C blocks go
       // out as the drain frees a dKV^T buffer; the ring slots (MMA-B of this
@@ -351,7 +351,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int nr = next ? 16 : 8;
         int r = 0, cb = 0;
         uint64_t t0 = 0;
-        for (uint32_t idle = 0; r < nr || cb < 8;) {
+        for (uint32_t idle = 0; r < nr || cb < 4;) {
           bool did = false;
           // ring slots first: a slot returns to the loaders only once its MMAs
           // complete, and the next tile's MMA-A and softmax wait on the ring
@@ -365,12 +365,11 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             ++r;
             did = true;
           }
-          if (cb < 8) {
-            const int bb = cb & 1;
-            if (freed[bb] < issued[bb] &&
-                ptx::mbar_test_wait(c.bar(sDkvEmpty0 + bb), (uint32_t)freed[bb] & 1u))
-              ++freed[bb];
-            if (freed[bb] >= issued[bb]) {
+          if (cb < 4) {
+            if (freed < issued &&
+                ptx::mbar_test_wait(c.bar(sDkvEmpty), (uint32_t)freed & 1u))
+              ++freed;
+            if (freed >= issued) {
               ptx::tc_fence_after();
               c_block(cb++);
               did = true;
@@ -584,7 +583,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // -------------------- per token: dKV^T drain, then dQ: thread = column d --
     const int q4 = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    const int bb = warp < 12 ? 0 : 1;  // buffer / row half of this warpgroup
+    const int bb = warp < 12 ? 0 : 1;  // row half of this warpgroup (columns 64 bb of a block)
     const int dl = 32 * q4 + lane;
     const int ori_rows = p.n_ori * p.Hk;
     const uint32_t tbuf = tmem + 128 + 64 * bb + lane_off;
@@ -599,7 +598,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int nt = min(64, N - 128 * t - 64 * bb);  // valid rows of this half (may be <= 0)
         const uint32_t rt_s = rows_addr(b) + 512 * t + 256 * bb;
         for (int cc = 0; cc < 4; ++cc) {
-          if (!wait_bar(c, sDkvFull0 + bb, (uint32_t)used & 1u, 71)) { ok = false; break; }
+          if (!wait_bar(c, sDkvFull, (uint32_t)used & 1u, 71)) { ok = false; break; }
           ++used;
           ptx::tc_fence_after();
           uint32_t v[64];
@@ -607,7 +606,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           ptx::tmem_ld32(tbuf + 32, v + 32);
           ptx::tmem_wait_ld();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(c.bar(sDkvEmpty0 + bb));
+          ptx::mbar_arrive(c.bar(sDkvEmpty));
           float* const ori_base = p.d_ori + 128 * cc + dl;
           float* const cmp_base = p.d_cmp - (int64_t)ori_rows * kSpD + 128 * cc + dl;
 #pragma unroll
