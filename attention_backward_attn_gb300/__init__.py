@@ -18,6 +18,7 @@ from . import _build
 __all__ = [
     "AttnError", "Problem", "Mask", "Sparse", "lib", "status_string",
     "problem_from", "mask_from", "sparse_from", "ATTN_FLAG_DETERMINISTIC",
+    "ATTN_FLAG_CUDA_CORES",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
     "attn_bwd_dsinks",
@@ -139,11 +140,12 @@ def _strides(t):
 
 
 ATTN_FLAG_DETERMINISTIC = 1
+ATTN_FLAG_CUDA_CORES = 2
 
 
 def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = None,
                  Sk: Optional[int] = None, Hk: Optional[int] = None,
-                 deterministic: bool = False) -> Problem:
+                 deterministic: bool = False, cuda_cores: bool = False) -> Problem:
     """Problem descriptor from BSHD tensors (q [B, Sq, Hq, D], k / v [B, Sk, Hk, D])."""
     B, Sq, Hq, D = q.shape
     p = Problem()
@@ -156,7 +158,8 @@ def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = No
     p.v_stride = _strides(v if v is not None else (k if k is not None else q))
     p.o_stride = _strides(o if o is not None else q)
     p.do_stride = _strides(do if do is not None else (o if o is not None else q))
-    p.flags = ATTN_FLAG_DETERMINISTIC if deterministic else 0
+    p.flags = ((ATTN_FLAG_DETERMINISTIC if deterministic else 0) |
+               (ATTN_FLAG_CUDA_CORES if cuda_cores else 0))
     return p
 
 
@@ -271,7 +274,8 @@ class BackwardPlan:
 
     def __init__(self, q, k, v, o, do, lse, scale, mask: Optional[Mask] = None, bias=None,
                  want_dbias=False, ori_kv=None, cmp_kv=None, cmp_idx=None,
-                 ori_win_left=-1, ori_win_right=-1, cmp_ratio=0, deterministic=False):
+                 ori_win_left=-1, ori_win_right=-1, cmp_ratio=0, deterministic=False,
+                 cuda_cores=False):
         import torch
         dev = q.device
         self.q, self.k, self.v, self.o, self.do, self.lse, self.bias = q, k, v, o, do, lse, bias
@@ -286,10 +290,11 @@ class BackwardPlan:
                                       self.d_ori, self.d_cmp, cmp_ratio)
             self._keep = (ori_kv, cmp_kv, cmp_idx)
             self.prob = problem_from(q, None, None, o, do, scale, Sk=0, Hk=Hk,
-                                     deterministic=deterministic)
+                                     deterministic=deterministic, cuda_cores=cuda_cores)
             self.dk = self.dv = None
         else:
-            self.prob = problem_from(q, k, v, o, do, scale, deterministic=deterministic)
+            self.prob = problem_from(q, k, v, o, do, scale, deterministic=deterministic,
+                                     cuda_cores=cuda_cores)
             self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
             self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
         self.mask = mask

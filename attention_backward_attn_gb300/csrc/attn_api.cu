@@ -46,9 +46,10 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
   if (!strides_ok(a.q_stride) || !strides_ok(a.o_stride) || !strides_ok(a.do_stride))
     return ATTN_ERR_INVALID_ARG;
   if (a.D != 64 && a.D != 128 && a.D != 512) return ATTN_ERR_UNSUPPORTED;
-  // row counts of the [B, S, H] index spaces must fit 31 bits (32-bit index math)
-  const int64_t rows_q = (int64_t)a.B * (a.Sq + 8) * a.Hq;
-  const int64_t rows_k = (int64_t)a.B * ((a.Sk > 0 ? a.Sk : 0) + 8) * a.Hk * 2;
+  // row counts of the [B, S, H] index spaces, staged rows included (a length
+  // rounded up to whole tiles), must fit 31 bits (32-bit index math)
+  const int64_t rows_q = (int64_t)a.B * (a.Sq + 128) * a.Hq;
+  const int64_t rows_k = (int64_t)a.B * ((a.Sk > 0 ? a.Sk : 0) + 128) * a.Hk * 2;
   if (rows_q >= (int64_t(1) << 31) || rows_k >= (int64_t(1) << 31)) return ATTN_ERR_UNSUPPORTED;
   Problem p{};
   p.B = a.B;
@@ -65,8 +66,9 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
     p.os[t] = a.o_stride[t];
     p.dos[t] = a.do_stride[t];
   }
-  if (a.flags & ~ATTN_FLAG_DETERMINISTIC) return ATTN_ERR_INVALID_ARG;
+  if (a.flags & ~(ATTN_FLAG_DETERMINISTIC | ATTN_FLAG_CUDA_CORES)) return ATTN_ERR_INVALID_ARG;
   p.deterministic = (a.flags & ATTN_FLAG_DETERMINISTIC) != 0;
+  p.cuda_cores = (a.flags & ATTN_FLAG_CUDA_CORES) != 0;
   if (a.Sq > kMaxMaskedLen || a.Sk > kMaxMaskedLen) return ATTN_ERR_UNSUPPORTED;
   const attn_status_t ms = mask_spec_of(mask, a.Sq, a.Sk, &p.mask);
   if (ms != ATTN_OK) return ms;
@@ -117,6 +119,7 @@ Sizes sizes_of(const Problem& p) {
 bool need(const void* ptr, int64_t count) { return count == 0 || ptr != nullptr; }
 
 bool use_tensor_cores(const Problem& p) {
+  if (p.cuda_cores) return false;
   return p.sparse ? tc_sparse_supported(p) : tc_supported(p);
 }
 
@@ -136,8 +139,8 @@ WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
     off = align_up(off + kvbytes, 1024);
     w.staged = true;
   } else if (tensor_core_path) {
-    const size_t qbytes = (size_t)p.B * p.Hq * p.Sq * p.D * sizeof(__half);
-    const size_t kbytes = (size_t)p.B * p.Hk * p.Sk * p.D * sizeof(__half);
+    const size_t qbytes = (size_t)p.B * p.Hq * tc_rows(p.Sq) * p.D * sizeof(__half);
+    const size_t kbytes = (size_t)p.B * p.Hk * tc_rows(p.Sk) * p.D * sizeof(__half);
     off = align_up(off, 1024);
     w.q16 = off;
     off = align_up(off + qbytes, 1024);
@@ -343,11 +346,12 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
     float* dv_b = dv + bq * rows_k * p.D;
     cudaError_t e;
     if (tc) {
-      // staged fp16 copies are head-major [B, H, S, D]
-      const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16) + bq * rows_q * p.D;
-      const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16) + bq * rows_k * p.D;
-      const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16) + bq * rows_k * p.D;
-      const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16) + bq * rows_q * p.D;
+      // staged fp16 copies are head-major [B, H, tc_rows(S), D]
+      const int64_t sq16 = bq * p.Hq * tc_rows(p.Sq) * p.D, sk16 = bq * p.Hk * tc_rows(p.Sk) * p.D;
+      const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16) + sq16;
+      const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16) + sk16;
+      const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16) + sk16;
+      const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16) + sq16;
       e = launch_bwd_tc(pb, q16, k16, v16, do16, lse_b, delta_b, bias, dq_b, dk_b, dv_b, dbias,
                         st, stream);
     } else {

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "attn_bwd.h"
+#include "mask.h"
 
 namespace attn {
 
@@ -30,65 +31,6 @@ __device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t deta
   if (atomicCAS(&st->code, 0, code) == 0) {
     atomicExch(&st->detail, detail);
   }
-}
-
-// live(i, j) = j < sink || (i - wl <= j <= i + wr); negative bound = unbounded
-// ("22_sink_tokens_fmha.py" mask builders, top-left aligned).
-// Key mask over (query i, key j): live when j < sink or -wl <= j - i <= wr.
-// The bounds are relative to the diagonal j = i; kMaskUnbounded leaves that
-// side open. They may be negative: a bottom-right aligned mask is a top-left
-// one with both bounds shifted by Sk - Sq. Bounds are clamped to
-// [-kMaskMaxBound, kMaskMaxBound] and lengths to kMaxMaskedLen, so i +- bound
-// stays inside int.
-constexpr int kMaskUnbounded = 1 << 29;
-constexpr int kMaskMaxBound = 1 << 28;
-constexpr int kMaxMaskedLen = 1 << 28;
-struct MaskSpec {
-  int wl;
-  int wr;
-  int sink;
-};
-
-__host__ __device__ __forceinline__ bool mask_live(const MaskSpec& m, int i, int j) {
-  if (j < m.sink) return true;
-  return j >= i - m.wl && j <= i + m.wr;
-}
-
-// Non-sink key range [lo, hi] (inclusive, clipped to [0, n); empty when
-// lo > hi) live for row i.
-__host__ __device__ __forceinline__ void mask_row_range(const MaskSpec& m, int i, int n,
-                                                        int* lo, int* hi) {
-  const int a = i - m.wl, b = i + m.wr;
-  *lo = a < 0 ? 0 : a;
-  *hi = b > n - 1 ? n - 1 : b;
-}
-
-// Non-sink query range [lo, hi] live for key j (j >= sink), clipped to [0, n).
-__host__ __device__ __forceinline__ void mask_col_range(const MaskSpec& m, int j, int n,
-                                                        int* lo, int* hi) {
-  const int a = j - m.wr, b = j + m.wl;
-  *lo = a < 0 ? 0 : a;
-  *hi = b > n - 1 ? n - 1 : b;
-}
-
-// Tile classification over rows [m0, m1) x keys [n0, n1) for the same mask:
-// tile_any = at least one live entry, tile_full = every entry live.
-__host__ __device__ __forceinline__ bool tile_any(const MaskSpec& m, int m0, int m1, int n0,
-                                                  int n1) {
-  if (m0 >= m1 || n0 >= n1) return false;
-  if (n0 < m.sink) return true;
-  const int dmax = (n1 - 1) - m0;  // largest j - i in the tile
-  const int dmin = n0 - (m1 - 1);  // smallest j - i in the tile
-  return dmax >= -m.wl && dmin <= m.wr;
-}
-
-__host__ __device__ __forceinline__ bool tile_full(const MaskSpec& m, int m0, int m1, int n0,
-                                                   int n1) {
-  const int a = n0 > m.sink ? n0 : m.sink;  // first column not covered by the sinks
-  if (a >= n1) return true;
-  const int dmax = (n1 - 1) - m0;
-  const int dmin = a - (m1 - 1);
-  return dmin >= -m.wl && dmax <= m.wr;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -156,6 +98,7 @@ struct Problem {
   MaskSpec mask;
   bool sparse;
   bool deterministic;  // ATTN_FLAG_DETERMINISTIC
+  bool cuda_cores;     // ATTN_FLAG_CUDA_CORES
   // sparse fields (cmp_ratio > 0 only in the CFA case: no index list, every
   // compressed row whose block ends at or before the query is selected)
   int n_ori, n_cmp, topk, ori_wl, ori_wr, cmp_ratio;

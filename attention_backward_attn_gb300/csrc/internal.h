@@ -9,9 +9,15 @@
 
 namespace attn {
 
+// Rows of one head in the dense tensor-core path's fp16 copies: the length
+// rounded up to whole 128-row tiles. The rows past the length are zero, so a
+// tile that crosses the end of a sequence loads finite values; the kernel's
+// per-element mask keeps them out of every sum.
+inline int tc_rows(int s) { return (s + 127) / 128 * 128; }
+
 // Workspace layout: [DevStatus (256 B)] then, for the tensor-core path, fp16
-// copies of Q, dO [B, Hq, Sq, D] and K, V [B, Hk, Sk, D] (head-major rows),
-// each region aligned to 1 KiB.
+// copies of Q, dO [B, Hq, tc_rows(Sq), D] and K, V [B, Hk, tc_rows(Sk), D]
+// (head-major rows, zero past the length), each region aligned to 1 KiB.
 // The sparse tensor-core path stages one fp16 copy of the shared KV rows
 // [ori rows ; cmp rows] ([(n_ori + n_cmp) * Hk][D]) instead.
 struct WorkspaceLayout {
@@ -38,7 +44,8 @@ cudaError_t launch_bwd_simt(const Problem& p, const void* q, const void* k, cons
 // ---- preprocess.cu ----
 // One fused kernel: clears the status record, zeroes dbias / the sparse dKV
 // buffers, computes delta, and (if do16 != nullptr) writes fp16
-// head-major copies of q, k, v and dO, and (if kv16 != nullptr) the fp16
+// head-major copies of q, k, v and dO with tc_rows(S) rows per head (zero
+// past the length), and (if kv16 != nullptr) the fp16
 // copy of the sparse shared KV rows. dk_zero / dv_zero (may be nullptr) are
 // zeroed; dk / dv are recorded in the status record (reserved[2..5]) so the
 // backward can check it received the buffers this pass prepared. An fp16

@@ -34,6 +34,7 @@ constexpr int kPreBlocksPerSM = 4;
 
 struct PreParams {
   int B, Hq, Hk, Sq, Sk;
+  int Sqs, Sks;  // rows per head of the fp16 copies (tile-rounded; zero past Sq / Sk)
   int64_t o0, o1, o2, d0, d1, d2, q0, q1, q2, k0, k1, k2, v0, v1, v2;
   const bf16* o;
   const bf16* dO;
@@ -155,19 +156,25 @@ preprocess_kernel(const PreParams p) {
   constexpr int U = D >= 512 ? 1 : 2;  // D = 512 rows are 1 KiB: one slot keeps registers in budget
   static_assert(kIB % (RPW * U) == 0, "a warp step stays inside one row block");
   float amax_q = 0.f, amax_do = 0.f, amax_k = 0.f, amax_v = 0.f;
-  const int64_t nq = (int64_t)p.B * ((p.Sq + kIB - 1) / kIB) * kIB * p.Hq;
-  const int64_t nk = (int64_t)p.B * ((p.Sk + kIB - 1) / kIB) * kIB * p.Hk;
+  // query rows visited: the staged rows per head when staging (their tail past
+  // Sq is written as zeros), else the rows themselves
+  const int sq_it = p.do16 != nullptr ? p.Sqs : p.Sq;
+  const int64_t nq = (int64_t)p.B * ((sq_it + kIB - 1) / kIB) * kIB * p.Hq;
+  const int64_t nk = (int64_t)p.B * ((p.Sks + kIB - 1) / kIB) * kIB * p.Hk;
   const int64_t nq_steps = nq / (RPW * U);
   const int64_t n_steps = nq_steps + (p.do16 != nullptr ? 2 * nk / (RPW * U) : 0);
   for (int64_t step = warp0; step < n_steps; step += nwarps) {
     if (step < nq_steps) {
       const int64_t r0 = step * RPW * U;
       int h, i0, b;
-      decompose(r0, p.Hq, p.Sq, &b, &h, &i0);
+      decompose(r0, p.Hq, sq_it, &b, &h, &i0);
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
       uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * RPW + sub;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) of[u][c] = df[u][c] = qf[u][c] = z4;
         if (i < p.Sq) {
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
@@ -183,8 +190,8 @@ preprocess_kernel(const PreParams p) {
         const int i = i0 + u * RPW + sub;
         const bool valid = i < p.Sq;
         float s = 0.f;
-        if (valid) {
-          const int64_t hm = ((int64_t)b * p.Hq + h) * p.Sq + i;  // head-major row
+        if (i < sq_it) {  // a real row, or a zero row of the staged tail
+          const int64_t hm = ((int64_t)b * p.Hq + h) * sq_it + i;  // head-major row
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             const int e0 = (cl + c * LPR) * 8;
@@ -210,14 +217,16 @@ preprocess_kernel(const PreParams p) {
       const int64_t r0 = (step - nq_steps) * RPW * U;
       const bool is_v = r0 >= nk;
       int g, j0, b;
-      decompose(is_v ? r0 - nk : r0, p.Hk, p.Sk, &b, &g, &j0);
+      decompose(is_v ? r0 - nk : r0, p.Hk, p.Sks, &b, &g, &j0);
       const bf16* src0 = is_v ? p.v + b * p.v0 + g * p.v2 : p.k + b * p.k0 + g * p.k2;
       const int64_t s1 = is_v ? p.v1 : p.k1;
-      __half* dst0 = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sk) * D;
+      __half* dst0 = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sks) * D;
       uint4 f[U][CPL];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + u * RPW + sub;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) f[u][c] = make_uint4(0u, 0u, 0u, 0u);
         if (j < p.Sk) {
 #pragma unroll
           for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src0 + j * s1 + (cl + c * LPR) * 8);
@@ -226,7 +235,7 @@ preprocess_kernel(const PreParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + u * RPW + sub;
-        if (j >= p.Sk) continue;
+        if (j >= p.Sks) continue;  // rows in [Sk, Sks) are written as zeros
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float x[8];
@@ -335,6 +344,8 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.Hk = pr.Hk;
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
+  p.Sqs = do16 != nullptr ? tc_rows(pr.Sq) : pr.Sq;
+  p.Sks = do16 != nullptr ? tc_rows(pr.Sk) : pr.Sk;
   p.o0 = pr.os[0]; p.o1 = pr.os[1]; p.o2 = pr.os[2];
   p.d0 = pr.dos[0]; p.d1 = pr.dos[1]; p.d2 = pr.dos[2];
   p.q0 = pr.qs[0]; p.q1 = pr.qs[1]; p.q2 = pr.qs[2];

@@ -119,6 +119,8 @@ enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, 
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
+  int Sqs, Sks;    // rows per head of the fp16 copies: Sq, Sk rounded up to whole tiles
+  int ragged;      // Sq or Sk is not a whole number of tiles
   int cs;          // key-major CTAs per key tile (query-head split)
   int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
   float scale;
@@ -144,32 +146,45 @@ __device__ __forceinline__ uint32_t bits_between(int a, int b) {
 }
 
 
-// Live (query head, query tile) pairs of a key tile.
+__device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+
+// Whether some entry of the tile rows [m0, m0 + BM) x keys [n0, n0 + BN) is
+// dead (masked, or past the end of the queries or keys), so that the tile
+// needs the per-element mask.
+__device__ __forceinline__ bool tile_cut(const TcParams& p, int m0, int n0) {
+  return m0 + BM > p.Sq || n0 + BN > p.Sk || !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+}
+
+// Live (query head, query tile) pairs of a key tile, heads outer: the live
+// query tiles form one range (live_query_tiles), so the walk touches live
+// tiles only.
 struct QTileIter {
-  int hpc, nmt, n0, hl, mt;
-  MaskSpec mask;
-  __device__ QTileIter(int hpc_, int nmt_, int n0_, MaskSpec m)
-      : hpc(hpc_), nmt(nmt_), n0(n0_), hl(0), mt(-1), mask(m) {}
+  int hpc, lo, hi, hl, mt;
+  __device__ QTileIter(int hpc_, int n0, const TcParams& p) : hpc(hpc_), hl(0) {
+    live_query_tiles(p.mask, p.Sq, p.Sk, BM, BN, n0, &lo, &hi);
+    mt = lo - 1;
+  }
   __device__ bool next() {
-    for (;;) {
-      if (++mt >= nmt) {
-        mt = 0;
-        if (++hl >= hpc) return false;
-      }
-      if (tile_any(mask, mt * BM, mt * BM + BM, n0, n0 + BN)) return true;
+    if (lo > hi) return false;
+    if (++mt > hi) {
+      mt = lo;
+      if (++hl >= hpc) return false;
     }
+    return true;
   }
 };
 
-// Live key tiles of a query tile.
+// Live key tiles of a query tile, ascending: the sink tiles, then the window
+// tiles (live_key_tiles).
 struct KTileIter {
-  int nnt, m0, nt;
-  MaskSpec mask;
-  __device__ KTileIter(int nnt_, int m0_, MaskSpec m) : nnt(nnt_), m0(m0_), nt(-1), mask(m) {}
+  int s_end, w_lo, w_hi, nt;
+  __device__ KTileIter(int m0, const TcParams& p) : nt(-1) {
+    live_key_tiles(p.mask, p.Sq, p.Sk, BM, BN, m0, &s_end, &w_lo, &w_hi);
+  }
   __device__ bool next() {
-    while (++nt < nnt)
-      if (tile_any(mask, m0, m0 + BM, nt * BN, nt * BN + BN)) return true;
-    return false;
+    if (++nt < s_end) return true;
+    if (nt < w_lo) nt = w_lo;
+    return nt <= w_hi;
   }
 };
 
@@ -190,11 +205,17 @@ __device__ __forceinline__ void init_common(const Ctx& c, uint32_t tmem_slot_add
 }
 
 // ======================================================= key-major CTA ====
-template <int D, bool BIAS, bool DBIAS>
+// RB: bias / dbias accesses clamped or predicated for ragged lengths (a
+// separate instantiation, so that aligned problems keep unconditional,
+// freely scheduled loads and reductions)
+template <int D, bool BIAS, bool DBIAS, bool RB>
 __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, const CUtensorMap* tmdO,
                                        const TcParams& p, uint8_t* smem, uint32_t sbase) {
   using L = SmemKV<D>;
+  // The bias variants run ragged lengths only as RB instantiations; the others
+  // take both and test the lengths at run time.
+  constexpr bool kMayBeRagged = RB || (!BIAS && !DBIAS);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cs = p.cs;
@@ -208,13 +229,16 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   const int r = p.Hq / p.Hk;
   const int hpc = r / cs;
   const int h_first = g * r + rank * hpc;
-  const int nmt = p.Sq / BM;
 
   Ctx c;
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  const uint32_t counts[kKvBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1, 256, 1};
+  // a ragged problem's query-tile barriers take one more arrival: the
+  // producer warp's plain copy of LSE / delta (the TMA bulk copy needs whole
+  // 16-byte-aligned tiles)
+  const uint32_t qf = p.ragged ? 2u : 1u;
+  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 256, 1, 1, 1, 256, 1};
   init_common(c, sbase + L::MISC, kKvBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
@@ -227,35 +251,67 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
+    // lane 0 waits and issues the copies; with ragged lengths the whole warp
+    // also copies the tile's LSE / delta rows (zero past Sq)
     if (lane == 0) {
-      const int krow = (b * p.Hk + g) * p.Sk + n0;
+      const int krow = (b * p.Hk + g) * p.Sks + n0;
       ptx::mbar_arrive_expect_tx(c.bar(kKvFull), 2 * L::kTile);
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         ptx::tma_load_2d(sK + hf * kSlab, tmK, c.bar(kKvFull), hf * 64, krow);
         ptx::tma_load_2d(sV + hf * kSlab, tmV, c.bar(kKvFull), hf * 64, krow);
       }
-      QTileIter it(hpc, nmt, n0, p.mask);
+    }
+    int issued[2] = {0, 0};
+    if (lane == 0 || p.ragged) {  // warp-uniform when ragged
+      QTileIter it(hpc, n0, p);
       int t = 0;
-      int issued[2] = {0, 0};
       while (it.next()) {
         const int st = t & 1;
         const int use = t >> 1;
-        if (use > 0 && !wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1)) break;
-        const int h = h_first + it.hl;
-        const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + it.mt * BM;
-        const uint32_t full = c.bar(kQFull0 + st);
-        ptx::mbar_arrive_expect_tx(full, 2 * L::kTile + 2 * 512);
-#pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
-          ptx::tma_load_2d(sbase + L::Q + st * L::kTile + hf * kSlab, tmQ, full, hf * 64, (int)row);
-          ptx::tma_load_2d(sbase + L::dO + st * L::kTile + hf * kSlab, tmdO, full, hf * 64, (int)row);
+        if (p.ragged) {
+          bool go = true;
+          if (lane == 0 && use > 0) go = wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1);
+          __syncwarp();
+          if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        } else if (lane == 0 && use > 0 && !wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1)) {
+          break;
         }
-        ptx::bulk_load(sbase + L::LSE + st * 512, p.lse + row, 512, full);
-        ptx::bulk_load(sbase + L::DLT + st * 512, p.delta + row, 512, full);
+        const int h = h_first + it.hl;
+        const int m0 = it.mt * BM;
+        const int64_t row = ((int64_t)b * p.Hq + h) * p.Sqs + m0;   // staged fp16 rows
+        const int64_t lrow = ((int64_t)b * p.Hq + h) * p.Sq + m0;   // LSE / delta rows
+        const uint32_t full = c.bar(kQFull0 + st);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(full, 2 * L::kTile + (p.ragged ? 0 : 2 * 512));
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            ptx::tma_load_2d(sbase + L::Q + st * L::kTile + hf * kSlab, tmQ, full, hf * 64, (int)row);
+            ptx::tma_load_2d(sbase + L::dO + st * L::kTile + hf * kSlab, tmdO, full, hf * 64, (int)row);
+          }
+          if (!p.ragged) {
+            ptx::bulk_load(sbase + L::LSE + st * 512, p.lse + lrow, 512, full);
+            ptx::bulk_load(sbase + L::DLT + st * 512, p.delta + lrow, 512, full);
+          }
+        }
+        if (p.ragged) {
+          float* lse_s = reinterpret_cast<float*>(smem + L::LSE + st * 512);
+          float* dl_s = reinterpret_cast<float*>(smem + L::DLT + st * 512);
+#pragma unroll
+          for (int u = 0; u < BM / 32; ++u) {
+            const int q = u * 32 + lane;
+            const bool in = m0 + q < p.Sq;
+            lse_s[q] = in ? p.lse[lrow + q] : 0.f;
+            dl_s[q] = in ? p.delta[lrow + q] : 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(full);
+        }
         issued[st] = use + 1;
         ++t;
       }
+    }
+    if (lane == 0) {
       // no copy may still be landing in shared memory when the CTA ends
       drain_bar(c, kKvFull, 0);
       for (int st = 0; st < 2; ++st)
@@ -297,7 +353,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // TMEM, then dP(t+1) after dK(t) released those columns. The softmax of
       // tile t+1 overlaps dV(t), dK(t) and dP(t+1).
       bool ok = wait_bar(c, kKvFull, 0, 2);
-      QTileIter it(hpc, nmt, n0, p.mask);
+      QTileIter it(hpc, n0, p);
       bool have = ok && it.next();
       if (have) {
         have = wait_bar(c, kQFull0, 0, 3);
@@ -376,7 +432,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int jl = lg * 32 + lane;                   // key row within the tile
     const int j = n0 + jl;
-    QTileIter it(hpc, nmt, n0, p.mask);
+    QTileIter it(hpc, n0, p);
     int t = 0;
     bool ok = true;
     while (it.next()) {
@@ -390,15 +446,27 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       const int m0 = it.mt * BM;
       // Live queries of this key row within the tile, [qlo, qhi]. A row
       // without live keys has LSE = -inf; it can only sit in a partial tile,
-      // where this mask zeroes its probabilities.
-      const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      // where this mask zeroes its probabilities. So do the rows past Sq and
+      // a key row past Sk (zero operands in the staged copies).
+      const bool partial = kMayBeRagged ? tile_cut(p, m0, n0)
+                                        : !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      const int qcap = p.Sq - 1 - m0;        // last query of the tile
       int qlo = 0, qhi = BM - 1;
-      if (partial && j >= p.mask.sink) {
-        qlo = j - p.mask.wr - m0;  // bits_between clamps to the tile
-        qhi = j + p.mask.wl - m0;
+      if (partial) {
+        if (j >= p.mask.sink) {
+          qlo = j - p.mask.wr - m0;  // bits_between clamps to the tile
+          qhi = j + p.mask.wl - m0;
+        }
+        if constexpr (kMayBeRagged) {
+          qhi = imin(qhi, qcap);
+          if (j >= p.Sk) qhi = qlo - 1;
+        }
       }
+      // bias / dbias element (query m0 + q, key j); reads of rows and keys
+      // past the lengths are clamped into the tensor (their P is zero)
+      const int jc = kMayBeRagged ? imin(j, p.Sk - 1) : j;
       const float* brow = nullptr;
-      if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
+      if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + jc;
       float* dbrow = nullptr;
       if constexpr (DBIAS) dbrow = p.dbias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       const uint32_t ps_row = sDS + wg * kSlab + jl * 128;
@@ -421,7 +489,11 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + e4);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
             float bv[4];
-            if constexpr (BIAS) {
+            if constexpr (BIAS && RB) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                bv[u] = __ldg(brow + (int64_t)imin(q0 + e4 + u, qcap) * p.Sk);
+            } else if constexpr (BIAS) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
             }
@@ -466,6 +538,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int q0 = wg * 64 + cc * 32;
+        uint32_t live_d = 0xffffffffu;
+        if constexpr (DBIAS && RB) live_d = partial ? bits_between(qlo - q0, qhi - q0 + 1) : live_d;
         uint32_t dr[32];
         ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
         ptx::tmem_wait_ld();
@@ -482,7 +556,13 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
                       dv[u + 1]);
             ptx::mul2(de[u], de[u + 1], pv[cc * 32 + e4 + u], pv[cc * 32 + e4 + u + 1], t0, t1);
           }
-          if constexpr (DBIAS) {
+          if constexpr (DBIAS && RB) {
+            // live entries only: rows past Sq and a key past Sk have no dbias
+            // element (and a dead entry's dS is zero)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if ((live_d >> (e4 + u)) & 1u) atomicAdd(dbrow + (int64_t)(q0 + e4 + u) * p.Sk, de[u]);
+          } else if constexpr (DBIAS) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) atomicAdd(dbrow + (int64_t)(q0 + e4 + u) * p.Sk, de[u]);
           }
@@ -533,7 +613,10 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
         }
       }
-      if (cs == 1) {
+      if (n0 + ejl >= p.Sk) {
+        // a padding row past Sk: nothing to write (the TMEM loads above are
+        // warp-wide, so the row still took part in them)
+      } else if (cs == 1) {
         // the whole row goes out as one copy-engine store
         ptx::fence_async_shared();
         ptx::bulk_store(grow, srow, D * 4);
@@ -570,15 +653,15 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 }
 
 // ===================================================== query-major CTA ====
-template <int D, bool BIAS>
+template <int D, bool BIAS, bool RB>
 __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                       const CUtensorMap* tmV, const CUtensorMap* tmdO,
                                       const TcParams& p, uint8_t* smem, uint32_t sbase, int qi) {
   using L = SmemQ<D>;
+  constexpr bool kMayBeRagged = RB || !BIAS;  // as in the key-major CTA (dbias is not used here)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nmt = p.Sq / BM;
-  const int nnt = p.Sk / BN;
+  const int nmt = p.Sqs / BM;
   const int bh = qi % (p.B * p.Hq);
   const int mt = nmt - 1 - qi / (p.B * p.Hq);  // later query tiles first (heavier when causal)
   const int h = bh % p.Hq;
@@ -604,21 +687,21 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      const int qrow = (b * p.Hq + h) * p.Sq + m0;
+      const int qrow = (b * p.Hq + h) * p.Sqs + m0;
       ptx::mbar_arrive_expect_tx(c.bar(qQdoFull), 2 * L::kTile);
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf) {
         ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
         ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
       }
-      KTileIter it(nnt, m0, p.mask);
+      KTileIter it(m0, p);
       int t = 0;
       int issued[2] = {0, 0};
       while (it.next()) {
         const int st = t & 1;
         const int use = t >> 1;
         if (use > 0 && !wait_bar(c, qKvEmpty0 + st, (use - 1) & 1, 21)) break;
-        const int krow = (b * p.Hk + g) * p.Sk + it.nt * BN;
+        const int krow = (b * p.Hk + g) * p.Sks + it.nt * BN;
         const uint32_t full = c.bar(qKvFull0 + st);
         ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
 #pragma unroll
@@ -668,7 +751,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // one tile ahead, so the softmax computes P(t+1) while dQ(t) and
       // dP(t+1) are on the tensor pipe; only its dS half waits for dP.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
-      KTileIter it(nnt, m0, p.mask);
+      KTileIter it(m0, p);
       bool have = ok && it.next();
       bool have1 = false;
       if (have) {
@@ -732,25 +815,33 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int il = lg * 32 + lane;                   // query row within the tile
     const int i = m0 + il;
-    const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + i;
-    const float nl = p.lse[row] * -kLog2e;           // -inf rows: see the partial-tile mask
-    const float dl = p.delta[row];
+    const bool row_in = i < p.Sq;                    // rows past Sq are padding (not stored)
+    const int ic = row_in ? i : p.Sq - 1;
+    const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + ic;
+    const float nl = row_in ? p.lse[row] * -kLog2e : 0.f;  // -inf rows: see the partial-tile mask
+    const float dl = row_in ? p.delta[row] : 0.f;
     const float* brow = nullptr;
-    if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + i) * p.Sk;
-    KTileIter it(nnt, m0, p.mask);
+    if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
+    KTileIter it(m0, p);
     int t = 0;
     bool ok = true;
     while (it.next()) {
       if (!wait_bar(c, qSFull, t & 1, 27)) { ok = false; break; }
       ptx::tc_fence_after();
       const int n0 = it.nt * BN;
-      const bool partial = !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      const bool partial = kMayBeRagged ? tile_cut(p, m0, n0)
+                                        : !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+      const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
       // live keys of this query row within the tile: [klo, khi] plus the sinks
       int klo = 0, khi = BN - 1, ksink = 0;
       if (partial) {
         klo = i - p.mask.wl - n0;  // bits_between clamps to the tile
         khi = i + p.mask.wr - n0;
         ksink = p.mask.sink - n0;
+        if constexpr (kMayBeRagged) {
+          khi = imin(khi, kcap - 1);
+          ksink = imin(ksink, kcap);
+        }
       }
       const uint32_t t_S = t_S0 + (t & 1) * 128;
       // phase 1: P from S (registers)
@@ -768,7 +859,12 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
 #pragma unroll
           for (int e4 = 0; e4 < 32; e4 += 4) {
             float bv[4];
-            if constexpr (BIAS) {
+            if constexpr (BIAS && RB) {
+              // keys past Sk read the last one (their P is zero); a bias row
+              // of ragged length is not 16-byte aligned
+#pragma unroll
+              for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + n0 + imin(k0 + e4 + u, kcap - 1));
+            } else if constexpr (BIAS) {
               const float4 b4 = __ldg(reinterpret_cast<const float4*>(brow + n0 + k0 + e4));
               bv[0] = b4.x;
               bv[1] = b4.y;
@@ -830,8 +926,9 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     // thread = query row; warpgroup wg writes columns [wg D/2, wg D/2 + D/2)
     if (epi_ok) {
       ptx::tc_fence_after();
-      // staged in the (idle) K / V stages, then one copy-engine store per half row
-      float* grow = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D + wg * (D / 2);
+      // staged in the (idle) K / V stages, then one copy-engine store per half
+      // row (rows past Sq are not stored)
+      float* grow = p.dq + (((int64_t)b * p.Sq + ic) * p.Hq + h) * D + wg * (D / 2);
       const uint32_t srow = sbase + L::STAGE + il * L::kStageRow + wg * (D / 2) * 4;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -850,10 +947,12 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
                              __uint_as_float(v[e + 2]) * p.scale,
                              __uint_as_float(v[e + 3]) * p.scale);
       }
-      ptx::fence_async_shared();
-      ptx::bulk_store(grow, srow, D / 2 * 4);
-      ptx::bulk_commit();
-      ptx::bulk_wait_all();
+      if (row_in) {
+        ptx::fence_async_shared();
+        ptx::bulk_store(grow, srow, D / 2 * 4);
+        ptx::bulk_commit();
+        ptx::bulk_wait_all();
+      }
     }
   }
 
@@ -868,7 +967,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   }
 }
 
-template <int D, bool BIAS, bool DBIAS>
+template <int D, bool BIAS, bool DBIAS, bool RB>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -900,10 +999,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (bits && (threadIdx.x & 31) == 0) report(p.status, ATTN_ERR_RANGE, bits);
   }
   if ((int)blockIdx.x < p.kv_ctas) {
-    kv_cta<D, BIAS, DBIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
+    kv_cta<D, BIAS, DBIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
   } else {
     const int qi = (int)blockIdx.x - p.kv_ctas;
-    q_cta<D, BIAS>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
+    q_cta<D, BIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
   }
 }
 
@@ -922,11 +1021,11 @@ bool make_map(CUtensorMap* m, const __half* base, uint64_t rows, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool BIAS, bool DBIAS>
+template <int D, bool BIAS, bool DBIAS, bool RB>
 cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& dO, const TcParams& p, int grid,
                            cudaStream_t stream) {
-  auto kern = attn_bwd_tc_kernel<D, BIAS, DBIAS>;
+  auto kern = attn_bwd_tc_kernel<D, BIAS, DBIAS, RB>;
   static bool configured = false;  // attribute set once per process and variant
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -941,10 +1040,16 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
 template <int D>
 cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      const CUtensorMap& dO, const TcParams& p, int grid, cudaStream_t stream) {
-  if (p.bias && p.dbias) return launch_variant<D, true, true>(q, k, v, dO, p, grid, stream);
-  if (p.bias) return launch_variant<D, true, false>(q, k, v, dO, p, grid, stream);
-  if (p.dbias) return launch_variant<D, false, true>(q, k, v, dO, p, grid, stream);
-  return launch_variant<D, false, false>(q, k, v, dO, p, grid, stream);
+  // without bias and dbias, ragged lengths need no separate instantiation
+  if (p.ragged) {
+    if (p.bias && p.dbias) return launch_variant<D, true, true, true>(q, k, v, dO, p, grid, stream);
+    if (p.bias) return launch_variant<D, true, false, true>(q, k, v, dO, p, grid, stream);
+    if (p.dbias) return launch_variant<D, false, true, true>(q, k, v, dO, p, grid, stream);
+  }
+  if (p.bias && p.dbias) return launch_variant<D, true, true, false>(q, k, v, dO, p, grid, stream);
+  if (p.bias) return launch_variant<D, true, false, false>(q, k, v, dO, p, grid, stream);
+  if (p.dbias) return launch_variant<D, false, true, false>(q, k, v, dO, p, grid, stream);
+  return launch_variant<D, false, false, false>(q, k, v, dO, p, grid, stream);
 }
 
 // Query heads per KV head are split over cs key-major CTAs. Every CTA pays a
@@ -985,12 +1090,12 @@ int tc_head_split(const Problem& p) {
   // deterministic: one CTA per key tile writes dK / dV (no partial sums added
   // in arrival order)
   if (p.deterministic) return 1;
-  return head_split(p.Hq / p.Hk, p.B * p.Hk * (p.Sk / BN), sm_count());
+  return head_split(p.Hq / p.Hk, p.B * p.Hk * (tc_rows(p.Sk) / BN), sm_count());
 }
 
 bool tc_supported(const Problem& p) {
   return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0 &&
-         p.Sq % BM == 0 && p.Sk % BN == 0 && encode_fn() != nullptr;
+         encode_fn() != nullptr;
 }
 
 cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k16,
@@ -998,8 +1103,8 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
                           const float* delta, const float* bias, float* dq, float* dk,
                           float* dv, float* dbias, DevStatus* st, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo;
-  const uint64_t qrows = (uint64_t)pr.B * pr.Hq * pr.Sq;
-  const uint64_t krows = (uint64_t)pr.B * pr.Hk * pr.Sk;
+  const uint64_t qrows = (uint64_t)pr.B * pr.Hq * tc_rows(pr.Sq);
+  const uint64_t krows = (uint64_t)pr.B * pr.Hk * tc_rows(pr.Sk);
   if (!make_map(&mq, q16, qrows, pr.D) || !make_map(&mk, k16, krows, pr.D) ||
       !make_map(&mv, v16, krows, pr.D) || !make_map(&mdo, do16, qrows, pr.D))
     return cudaErrorInvalidValue;
@@ -1009,8 +1114,11 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Hk = pr.Hk;
   p.Sq = pr.Sq;
   p.Sk = pr.Sk;
+  p.Sqs = tc_rows(pr.Sq);
+  p.Sks = tc_rows(pr.Sk);
+  p.ragged = (p.Sqs != p.Sq || p.Sks != p.Sk) ? 1 : 0;
   p.cs = tc_head_split(pr);
-  p.kv_ctas = pr.B * pr.Hk * (pr.Sk / BN) * p.cs;
+  p.kv_ctas = pr.B * pr.Hk * (p.Sks / BN) * p.cs;
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.mask = pr.mask;
@@ -1022,7 +1130,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dv = dv;
   p.dbias = dbias;
   p.status = st;
-  const int q_ctas = pr.B * pr.Hq * (pr.Sq / BM);
+  const int q_ctas = pr.B * pr.Hq * (p.Sqs / BM);
   const int grid = p.kv_ctas + q_ctas;
   if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
   return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);

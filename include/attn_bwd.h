@@ -90,6 +90,12 @@ typedef struct attn_problem {
  * default.) */
 #define ATTN_FLAG_DETERMINISTIC 1
 
+/* Run the CUDA-core kernels (no tensor cores, bf16 operands read directly)
+ * even where the tensor-core path applies: a second, independent
+ * implementation of the same backward, for cross-checks. attn_bwd_path then
+ * returns 2. Slower. */
+#define ATTN_FLAG_CUDA_CORES 2
+
 /* Key mask, positions aligned top-left ("22_sink_tokens_fmha.py"):
  *   live(i, j) = (j < num_sink) || (i - window_left <= j && j <= i + window_right)
  * with a negative window bound meaning that side is unbounded. Causal is

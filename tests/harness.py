@@ -116,7 +116,7 @@ def to_dev_f32(x, dev):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
 
 
-def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False):
+def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False, cuda_cores=False):
     import attention_backward_attn_gb300 as ab
     q, k, v, o, do = (to_dev_bf16(x, dev) for x in (w.q, w.k, w.v, O_b, w.do))
     lse = to_dev_f32(L_f, dev)
@@ -124,10 +124,11 @@ def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False):
     mask = ab.mask_from(w.window_left, w.window_right, w.num_sink,
                         getattr(w, "bottom_right", False))
     return ab.BackwardPlan(q, k, v, o, do, lse, w.scale, mask=mask, bias=bias,
-                           want_dbias=w.want_dbias, deterministic=deterministic)
+                           want_dbias=w.want_dbias, deterministic=deterministic,
+                           cuda_cores=cuda_cores)
 
 
-def gpu_sparse_plan(w, O_b, L_f, dev="cuda"):
+def gpu_sparse_plan(w, O_b, L_f, dev="cuda", cuda_cores=False):
     import torch
     import attention_backward_attn_gb300 as ab
     q = to_dev_bf16(w.q[None], dev)
@@ -139,4 +140,5 @@ def gpu_sparse_plan(w, O_b, L_f, dev="cuda"):
     idx = None if w.cmp_idx is None else torch.from_numpy(w.cmp_idx).to(dev)
     return ab.BackwardPlan(q, None, None, o, do, lse, w.scale, ori_kv=okv, cmp_kv=ckv,
                            cmp_idx=idx, ori_win_left=w.ori_win_left,
-                           ori_win_right=w.ori_win_right, cmp_ratio=cfa_ratio(w) or 0)
+                           ori_win_right=w.ori_win_right, cmp_ratio=cfa_ratio(w) or 0,
+                           cuda_cores=cuda_cores)

@@ -172,7 +172,11 @@ def test_problem_flags(ab):
     assert ab.attn_bwd_path(p, None, None) in (1, 2)
     p.flags = ab.ATTN_FLAG_DETERMINISTIC
     assert ab.attn_bwd_path(p, None, None) in (1, 2)
-    p.flags = 2  # unknown bit
+    p.flags = ab.ATTN_FLAG_CUDA_CORES  # the SIMT kernels, whatever the shape
+    assert ab.attn_bwd_path(p, None, None) == 2
+    p.flags = ab.ATTN_FLAG_CUDA_CORES | ab.ATTN_FLAG_DETERMINISTIC
+    assert ab.attn_bwd_path(p, None, None) == 2
+    p.flags = 4  # unknown bit
     assert ab.attn_bwd_path(p, None, None) == 0
 
 

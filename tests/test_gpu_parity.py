@@ -81,7 +81,7 @@ SMALL_DENSE = {
     "br_causal_sq384_sk128_d64": lambda: make_dense("br2", 28, B=2, Hq=4, Hk=4, Sq=384,
                                                     Sk=128, D=64, window_left=-1,
                                                     window_right=0, bottom_right=True),
-    # bottom-right window + sinks, ragged lengths (SIMT kernels), bias
+    # bottom-right window + sinks, ragged lengths, bias
     "br_window_sink_sq150_sk230_d64": lambda: make_dense("br3", 29, B=1, Hq=4, Hk=2, Sq=150,
                                                          Sk=230, D=64, window_left=31,
                                                          window_right=0, num_sink=3,
@@ -92,15 +92,70 @@ SMALL_DENSE = {
 }
 
 
-# cases whose shapes the tcgen05 kernel takes (D in {64, 128}, lengths multiples of 128)
-TC_CASES = {"gqa4_causal_s384_d128", "alibi_dbias_s256_d64", "window128_sink4_s640_d128",
-            "br_causal_sq128_sk384_d128", "br_causal_sq384_sk128_d64"}
+def _dense_path(w):
+    """The tcgen05 kernel takes every dense problem with D in {64, 128}, of any
+    lengths (a ragged last tile is masked per element); the SIMT kernels the rest."""
+    return 1 if w.D in (64, 128) else 2
 
 
 @pytest.mark.parametrize("name", list(SMALL_DENSE))
 def test_dense_small(name):
     w = SMALL_DENSE[name]()
-    plan, O_b, L_f = _run_dense(w, expect_path=1 if name in TC_CASES else 2)
+    plan, O_b, L_f = _run_dense(w, expect_path=_dense_path(w))
+    _compare_dense(w, plan, O_b, L_f)
+
+
+@pytest.mark.parametrize("name", list(SMALL_DENSE))
+def test_dense_small_cuda_cores(name):
+    # the same cases through the SIMT kernels (ATTN_FLAG_CUDA_CORES)
+    torch = _torch()
+    w = SMALL_DENSE[name]()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    plan = H.gpu_dense_plan(w, O_b, L_f, cuda_cores=True)
+    assert plan.path == 2
+    plan.run()
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+    _compare_dense(w, plan, O_b, L_f)
+
+
+# Lengths that are not whole 128-row tiles on the tensor-core path: the staged
+# fp16 copies are zero past each length and the last query / key tile takes
+# the per-element mask.
+RAGGED_TC = {
+    # GQA 4:1 causal, both lengths ragged, D = 128
+    "gqa4_causal_sq200_sk200_d128": lambda: make_dense("rg1", 60, B=2, Hq=8, Hk=2, Sq=200,
+                                                       Sk=200, D=128, window_left=-1,
+                                                       window_right=0),
+    # bias + dbias with a key length that is not a multiple of 4 (scalar bias
+    # reads), Sq < Sk
+    "alibi_dbias_sq130_sk250_d64": lambda: make_dense("rg2", 61, B=2, Hq=2, Hk=2, Sq=130,
+                                                      Sk=250, D=64, alibi=True,
+                                                      want_dbias=True),
+    # bias with Sk a multiple of 4 (vector bias reads on whole key tiles), a
+    # two-sided window and sinks, Sq > Sk
+    "window_sinks_bias_sq300_sk260_d64": lambda: make_dense("rg3", 62, B=1, Hq=2, Hk=1,
+                                                            Sq=300, Sk=260, D=64,
+                                                            window_left=70, window_right=9,
+                                                            num_sink=2, alibi=True),
+    # one query against 5 keys (a single key would make dS = P (dP - D)
+    # vanish identically: exact zeros the fp16 operands do not reproduce)
+    "single_query_sk5_d128": lambda: make_dense("rg4", 63, B=1, Hq=2, Hk=1, Sq=1, Sk=5, D=128),
+    # 5 queries at the end of 700 keys: bottom-right causal with sinks
+    "br_sink_sq5_sk700_d64": lambda: make_dense("rg5", 64, B=1, Hq=4, Hk=2, Sq=5, Sk=700,
+                                                D=64, window_left=-1, window_right=0,
+                                                num_sink=4, bottom_right=True),
+    # GQA 8:1 on one ragged key tile: the query heads are split over CTAs whose
+    # partial dK / dV rows are added (rows past Sk are not)
+    "gqa8_split_sq96_sk100_d128": lambda: make_dense("rg6", 65, B=1, Hq=8, Hk=1, Sq=96,
+                                                     Sk=100, D=128, want_dbias=True),
+}
+
+
+@pytest.mark.parametrize("name", list(RAGGED_TC))
+def test_ragged_tensor_core(name):
+    w = RAGGED_TC[name]()
+    plan, O_b, L_f = _run_dense(w, expect_path=1)
     _compare_dense(w, plan, O_b, L_f)
 
 
@@ -141,10 +196,10 @@ DETERMINISTIC = {
     # own CTA and the 8 partial dK / dV sums are added in arrival order
     "gqa8_s256_d128": (lambda: make_dense("det", 25, B=1, Hq=8, Hk=1, Sq=256, Sk=256, D=128,
                                           window_left=-1, window_right=0), 1),
-    # SIMT kernels (ragged lengths), dbias over 3 batches
+    # ragged lengths (staged copies padded to whole tiles), dbias over 3 batches
     "ragged_alibi_dbias_s200_d64": (lambda: make_dense("detr", 26, B=3, Hq=2, Hk=2, Sq=200,
                                                        Sk=200, D=64, alibi=True,
-                                                       want_dbias=True), 2),
+                                                       want_dbias=True), 1),
 }
 
 
