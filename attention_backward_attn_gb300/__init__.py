@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "AttnError", "Problem", "Mask", "Sparse", "lib", "status_string",
-    "problem_from", "mask_from", "sparse_from", "ATTN_FLAG_DETERMINISTIC",
+    "problem_from", "varlen_problem", "mask_from", "sparse_from", "ATTN_FLAG_DETERMINISTIC",
     "ATTN_FLAG_CUDA_CORES",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
@@ -47,6 +47,8 @@ class Problem(ctypes.Structure):
         ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
         ("do_stride", ctypes.c_int64 * 3),
         ("flags", ctypes.c_int32),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("total_q", ctypes.c_int32), ("total_k", ctypes.c_int32),
     ]
 
 
@@ -163,6 +165,32 @@ def problem_from(q, k=None, v=None, o=None, do=None, scale: Optional[float] = No
     return p
 
 
+def varlen_problem(q, k, v, o, do, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                   max_seqlen_k: int, scale: Optional[float] = None,
+                   deterministic: bool = False) -> Problem:
+    """Problem descriptor of a variable-length batch: packed q / o / do
+    [total_q, Hq, D] and k / v [total_k, Hk, D]; cu_seqlens_* int32 device
+    tensors of B + 1 cumulative lengths; the max lengths bound every sequence."""
+    Tq, Hq, D = q.shape
+    Tk, Hk = k.shape[0], k.shape[1]
+
+    def st(t):  # (batch: unused, token, head) strides
+        return (ctypes.c_int64 * 3)(0, t.stride(0), t.stride(1))
+
+    p = Problem()
+    p.B = cu_seqlens_q.numel() - 1
+    p.Hq, p.Hk, p.D = Hq, Hk, D
+    p.Sq, p.Sk = int(max_seqlen_q), int(max_seqlen_k)
+    p.scale = float(scale if scale is not None else D ** -0.5)
+    p.q_stride, p.k_stride, p.v_stride = st(q), st(k), st(v)
+    p.o_stride, p.do_stride = st(o), st(do)
+    p.flags = ATTN_FLAG_DETERMINISTIC if deterministic else 0
+    p.cu_seqlens_q = cu_seqlens_q.data_ptr()
+    p.cu_seqlens_k = cu_seqlens_k.data_ptr()
+    p.total_q, p.total_k = Tq, Tk
+    return p
+
+
 def mask_from(window_left: int = -1, window_right: int = -1, num_sink: int = 0,
               bottom_right: bool = False) -> Optional[Mask]:
     """(window_left, window_right) around the diagonal j = i (top-left) or
@@ -269,19 +297,34 @@ class BackwardPlan:
 
     Dense: q, k, v, o, do bf16 BSHD; lse fp32 [B, Hq, Sq]; bias fp32 [Hq, Sq, Sk]
     or None. Sparse (pass ori_kv etc. and k = v = None): q, o, do [1, Sq, Hq, D].
+    Variable-length (pass cu_seqlens_q / cu_seqlens_k, int32 device tensors of
+    B + 1 cumulative lengths, and the max lengths): q, o, do packed
+    [total_q, Hq, D], k, v [total_k, Hk, D]; lse fp32 [B, Hq, max_seqlen_q].
     run() enqueues attn_bwd_preprocess then attn_bwd on the current stream.
     """
 
     def __init__(self, q, k, v, o, do, lse, scale, mask: Optional[Mask] = None, bias=None,
                  want_dbias=False, ori_kv=None, cmp_kv=None, cmp_idx=None,
                  ori_win_left=-1, ori_win_right=-1, cmp_ratio=0, deterministic=False,
-                 cuda_cores=False):
+                 cuda_cores=False, cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None,
+                 max_seqlen_k=None):
         import torch
         dev = q.device
         self.q, self.k, self.v, self.o, self.do, self.lse, self.bias = q, k, v, o, do, lse, bias
-        B, Sq, Hq, D = q.shape
         self.sparse = None
-        if ori_kv is not None:
+        if cu_seqlens_q is not None:
+            B, Sq, Hq = cu_seqlens_q.numel() - 1, int(max_seqlen_q), q.shape[1]
+            Sk = int(max_seqlen_k)
+        else:
+            B, Sq, Hq, _ = q.shape
+            Sk = k.shape[1] if k is not None else 0
+        if cu_seqlens_q is not None:
+            self._keep = (cu_seqlens_q, cu_seqlens_k)
+            self.prob = varlen_problem(q, k, v, o, do, cu_seqlens_q, cu_seqlens_k, Sq, Sk,
+                                       scale, deterministic=deterministic)
+            self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+            self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        elif ori_kv is not None:
             Hk = ori_kv.shape[1]
             self.d_ori = torch.empty(ori_kv.shape, dtype=torch.float32, device=dev)
             self.d_cmp = (torch.empty(cmp_kv.shape, dtype=torch.float32, device=dev)
@@ -302,7 +345,7 @@ class BackwardPlan:
         self.delta = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
         self.dbias = None
         if want_dbias:
-            self.dbias = torch.empty((Hq, Sq, k.shape[1]), dtype=torch.float32, device=dev)
+            self.dbias = torch.empty((Hq, Sq, Sk), dtype=torch.float32, device=dev)
         self.ws_bytes = attn_bwd_workspace_size(self.prob, mask, self.sparse)
         if self.ws_bytes == 0:
             raise AttnError(1, "attn_bwd_workspace_size")

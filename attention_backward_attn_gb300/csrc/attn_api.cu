@@ -26,10 +26,10 @@ attn_status_t mask_spec_of(const attn_mask_t* mask, int Sq, int Sk, MaskSpec* ou
       return ATTN_ERR_INVALID_ARG;
     const bool open_l = mask->window_left < 0 || mask->window_left >= kMaskMaxBound;
     const bool open_r = mask->window_right < 0 || mask->window_right >= kMaskMaxBound;
-    const int off = mask->bottom_right ? Sk - Sq : 0;
-    m.wl = open_l ? kMaskUnbounded : mask->window_left - off;
-    m.wr = open_r ? kMaskUnbounded : mask->window_right + off;
+    m.wl = open_l ? kMaskUnbounded : mask->window_left;
+    m.wr = open_r ? kMaskUnbounded : mask->window_right;
     m.sink = mask->num_sink;
+    m = mask_aligned(m, mask->bottom_right ? Sk - Sq : 0);
   }
   *out = m;
   return ATTN_OK;
@@ -70,7 +70,24 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
   p.deterministic = (a.flags & ATTN_FLAG_DETERMINISTIC) != 0;
   p.cuda_cores = (a.flags & ATTN_FLAG_CUDA_CORES) != 0;
   if (a.Sq > kMaxMaskedLen || a.Sk > kMaxMaskedLen) return ATTN_ERR_UNSUPPORTED;
-  const attn_status_t ms = mask_spec_of(mask, a.Sq, a.Sk, &p.mask);
+  p.varlen = a.cu_seqlens_q != nullptr || a.cu_seqlens_k != nullptr;
+  if (p.varlen) {
+    // per-sequence lengths live on the device: the mask stays top-left here
+    // and the kernels align it per sequence
+    if (a.cu_seqlens_q == nullptr || a.cu_seqlens_k == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (a.total_q < 0 || a.total_k < 0 || a.Sk < 0) return ATTN_ERR_INVALID_ARG;
+    if (sp != nullptr || p.cuda_cores || (a.D != 64 && a.D != 128)) return ATTN_ERR_UNSUPPORTED;
+    if ((int64_t)a.total_q * a.Hq >= (int64_t(1) << 31) ||
+        (int64_t)a.total_k * a.Hk >= (int64_t(1) << 31))
+      return ATTN_ERR_UNSUPPORTED;
+    p.cu_q = a.cu_seqlens_q;
+    p.cu_k = a.cu_seqlens_k;
+    p.total_q = a.total_q;
+    p.total_k = a.total_k;
+    p.br = mask != nullptr && mask->bottom_right == 1;
+  }
+  const attn_status_t ms =
+      p.varlen ? mask_spec_of(mask, 0, 0, &p.mask) : mask_spec_of(mask, a.Sq, a.Sk, &p.mask);
   if (ms != ATTN_OK) return ms;
   p.sparse = sp != nullptr;
   if (p.sparse && p.deterministic) return ATTN_ERR_UNSUPPORTED;  // dKV: reduction over tokens
@@ -97,6 +114,8 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
     if (a.Sk < 0) return ATTN_ERR_INVALID_ARG;
     if (!strides_ok(a.k_stride) || !strides_ok(a.v_stride)) return ATTN_ERR_INVALID_ARG;
   }
+  // variable-length batches run on the dense tensor-core kernel only
+  if (p.varlen && !tc_supported(p)) return ATTN_ERR_UNSUPPORTED;
   *out = p;
   return ATTN_OK;
 }
@@ -109,8 +128,8 @@ struct Sizes {
 
 Sizes sizes_of(const Problem& p) {
   Sizes n;
-  n.q = (int64_t)p.B * p.Sq * p.Hq * p.D;
-  n.k = (int64_t)p.B * p.Sk * p.Hk * p.D;
+  n.q = (int64_t)(p.varlen ? p.total_q : (int64_t)p.B * p.Sq) * p.Hq * p.D;
+  n.k = (int64_t)(p.varlen ? p.total_k : (int64_t)p.B * p.Sk) * p.Hk * p.D;
   n.rows = (int64_t)p.B * p.Hq * p.Sq;
   n.ori = (int64_t)p.n_ori * p.Hk * p.D;
   return n;
@@ -217,6 +236,7 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
   Problem p;
   attn_status_t s = make_problem(prob, mask, sparse, &p);
   if (s != ATTN_OK) return s;
+  if (p.varlen) return ATTN_ERR_UNSUPPORTED;  // the forward has no varlen variant
   const Sizes n = sizes_of(p);
   if (!need(q, n.q) || !need(o, n.q) || !need(lse, n.rows)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(bias))
@@ -334,6 +354,8 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
   // per-batch terms in batch order; within one batch each element has one
   // writer. bias and dbias are shared by the batches.
   const int n_launch = (p.deterministic && dbias != nullptr) ? p.B : 1;
+  // the per-batch launches offset pointers by whole sequences
+  if (p.varlen && n_launch > 1) return ATTN_ERR_UNSUPPORTED;
   Problem pb = p;
   if (n_launch > 1) pb.B = 1;
   const int64_t rows_q = (int64_t)p.Hq * p.Sq, rows_k = (int64_t)p.Hk * p.Sk;
@@ -375,6 +397,9 @@ attn_status_t attn_bwd_dsinks(const attn_problem_t* prob, const float* sinks,
       dsinks == nullptr)
     return ATTN_ERR_INVALID_ARG;
   if (prob->B <= 0 || prob->Hq <= 0 || prob->Sq <= 0) return ATTN_ERR_INVALID_ARG;
+  // lse / delta of a variable-length batch hold unused entries past each length
+  if (prob->cu_seqlens_q != nullptr || prob->cu_seqlens_k != nullptr)
+    return ATTN_ERR_UNSUPPORTED;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(sinks) | reinterpret_cast<uintptr_t>(lse) |
                         reinterpret_cast<uintptr_t>(delta) | reinterpret_cast<uintptr_t>(dsinks);
   if (mis & 3u) return ATTN_ERR_INVALID_ARG;

@@ -33,6 +33,22 @@ __device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t deta
   }
 }
 
+// Rows [*start, *start + *len) of sequence b of a variable-length batch
+// (cumulative lengths cu); false (and an empty span) when the bounds are out
+// of order, past `total` rows, or longer than max_len.
+__device__ __forceinline__ bool seq_span(const int32_t* cu, int b, int total, int max_len,
+                                         int* start, int* len) {
+  const int a = cu[b], e = cu[b + 1];
+  if (a < 0 || e < a || e > total || e - a > max_len) {
+    *start = 0;
+    *len = 0;
+    return false;
+  }
+  *start = a;
+  *len = e - a;
+  return true;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -99,6 +115,13 @@ struct Problem {
   bool sparse;
   bool deterministic;  // ATTN_FLAG_DETERMINISTIC
   bool cuda_cores;     // ATTN_FLAG_CUDA_CORES
+  // variable-length batch: per-sequence bounds on the device (Sq, Sk are
+  // upper bounds); the mask is then top-left and br asks for bottom-right
+  // alignment per sequence
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  bool varlen, br;
   // sparse fields (cmp_ratio > 0 only in the CFA case: no index list, every
   // compressed row whose block ends at or before the query is selected)
   int n_ori, n_cmp, topk, ori_wl, ori_wr, cmp_ratio;

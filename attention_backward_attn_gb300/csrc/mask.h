@@ -28,6 +28,14 @@ struct MaskSpec {
   int sink;
 };
 
+// The bounds of a mask whose diagonal is moved by off keys (bottom-right
+// alignment of a top-left mask: off = Sk - Sq); open sides stay open.
+ATTN_HD MaskSpec mask_aligned(MaskSpec m, int off) {
+  if (m.wl != kMaskUnbounded) m.wl -= off;
+  if (m.wr != kMaskUnbounded) m.wr += off;
+  return m;
+}
+
 ATTN_HD bool mask_live(const MaskSpec& m, int i, int j) {
   if (j < m.sink) return true;
   return j >= i - m.wl && j <= i + m.wr;

@@ -35,6 +35,10 @@ constexpr int kPreBlocksPerSM = 4;
 struct PreParams {
   int B, Hq, Hk, Sq, Sk;
   int Sqs, Sks;  // rows per head of the fp16 copies (tile-rounded; zero past Sq / Sk)
+  // variable-length batch: sequence bounds (nullptr: fixed lengths Sq, Sk)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
   int64_t o0, o1, o2, d0, d1, d2, q0, q1, q2, k0, k1, k2, v0, v1, v2;
   const bf16* o;
   const bf16* dO;
@@ -168,6 +172,13 @@ preprocess_kernel(const PreParams p) {
       const int64_t r0 = step * RPW * U;
       int h, i0, b;
       decompose(r0, p.Hq, sq_it, &b, &h, &i0);
+      // rows of this sequence: [0, len) at token offsets tok + i (varlen) or
+      // batch offsets b * stride[0]
+      int tok = 0, len = p.Sq;
+      if (p.cu_q != nullptr) seq_span(p.cu_q, b, p.total_q, p.Sq, &tok, &len);
+      const bf16* ob = p.o + (p.cu_q ? tok * p.o1 : b * p.o0) + h * p.o2;
+      const bf16* dob = p.dO + (p.cu_q ? tok * p.d1 : b * p.d0) + h * p.d2;
+      const bf16* qb = p.q + (p.cu_q ? tok * p.q1 : b * p.q0) + h * p.q2;
       const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
       uint4 of[U][CPL], df[U][CPL], qf[U][CPL];
 #pragma unroll
@@ -175,20 +186,20 @@ preprocess_kernel(const PreParams p) {
         const int i = i0 + u * RPW + sub;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) of[u][c] = df[u][c] = qf[u][c] = z4;
-        if (i < p.Sq) {
+        if (i < len) {
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             const int e0 = (cl + c * LPR) * 8;
-            of[u][c] = load_raw(p.o + b * p.o0 + i * p.o1 + h * p.o2 + e0);
-            df[u][c] = load_raw(p.dO + b * p.d0 + i * p.d1 + h * p.d2 + e0);
-            if (p.do16 != nullptr) qf[u][c] = load_raw(p.q + b * p.q0 + i * p.q1 + h * p.q2 + e0);
+            of[u][c] = load_raw(ob + i * p.o1 + e0);
+            df[u][c] = load_raw(dob + i * p.d1 + e0);
+            if (p.do16 != nullptr) qf[u][c] = load_raw(qb + i * p.q1 + e0);
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int i = i0 + u * RPW + sub;
-        const bool valid = i < p.Sq;
+        const bool valid = i < len;
         float s = 0.f;
         if (i < sq_it) {  // a real row, or a zero row of the staged tail
           const int64_t hm = ((int64_t)b * p.Hq + h) * sq_it + i;  // head-major row
@@ -218,8 +229,11 @@ preprocess_kernel(const PreParams p) {
       const bool is_v = r0 >= nk;
       int g, j0, b;
       decompose(is_v ? r0 - nk : r0, p.Hk, p.Sks, &b, &g, &j0);
-      const bf16* src0 = is_v ? p.v + b * p.v0 + g * p.v2 : p.k + b * p.k0 + g * p.k2;
+      int tok = 0, len = p.Sk;
+      if (p.cu_k != nullptr) seq_span(p.cu_k, b, p.total_k, p.Sk, &tok, &len);
       const int64_t s1 = is_v ? p.v1 : p.k1;
+      const int64_t bo = p.cu_k ? tok * s1 : b * (is_v ? p.v0 : p.k0);
+      const bf16* src0 = (is_v ? p.v + p.v2 * g : p.k + p.k2 * g) + bo;
       __half* dst0 = (is_v ? p.v16 : p.k16) + (((int64_t)b * p.Hk + g) * p.Sks) * D;
       uint4 f[U][CPL];
 #pragma unroll
@@ -227,7 +241,7 @@ preprocess_kernel(const PreParams p) {
         const int j = j0 + u * RPW + sub;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) f[u][c] = make_uint4(0u, 0u, 0u, 0u);
-        if (j < p.Sk) {
+        if (j < len) {
 #pragma unroll
           for (int c = 0; c < CPL; ++c) f[u][c] = load_raw(src0 + j * s1 + (cl + c * LPR) * 8);
         }
@@ -235,7 +249,7 @@ preprocess_kernel(const PreParams p) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + u * RPW + sub;
-        if (j >= p.Sks) continue;  // rows in [Sk, Sks) are written as zeros
+        if (j >= p.Sks) continue;  // rows in [len, Sks) are written as zeros
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
           float x[8];
@@ -346,6 +360,10 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.Sk = pr.Sk;
   p.Sqs = do16 != nullptr ? tc_rows(pr.Sq) : pr.Sq;
   p.Sks = do16 != nullptr ? tc_rows(pr.Sk) : pr.Sk;
+  p.cu_q = pr.varlen ? pr.cu_q : nullptr;
+  p.cu_k = pr.varlen ? pr.cu_k : nullptr;
+  p.total_q = pr.total_q;
+  p.total_k = pr.total_k;
   p.o0 = pr.os[0]; p.o1 = pr.os[1]; p.o2 = pr.os[2];
   p.d0 = pr.dos[0]; p.d1 = pr.dos[1]; p.d2 = pr.dos[2];
   p.q0 = pr.qs[0]; p.q1 = pr.qs[1]; p.q2 = pr.qs[2];
@@ -372,7 +390,7 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.zero_nb = d_ori ? (int64_t)pr.n_ori * pr.Hk * pr.D : 0;
   p.zero_c = d_cmp;
   p.zero_nc = d_cmp ? (int64_t)pr.n_cmp * pr.Hk * pr.D : 0;
-  const int64_t nkd = (int64_t)pr.B * pr.Sk * pr.Hk * pr.D;
+  const int64_t nkd = (pr.varlen ? (int64_t)pr.total_k : (int64_t)pr.B * pr.Sk) * pr.Hk * pr.D;
   p.zero_d = dk_zero;
   p.zero_nd = dk_zero ? nkd : 0;
   p.zero_e = dv_zero;

@@ -120,7 +120,13 @@ enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
   int Sqs, Sks;    // rows per head of the fp16 copies: Sq, Sk rounded up to whole tiles
-  int ragged;      // Sq or Sk is not a whole number of tiles
+  int ragged;      // Sq or Sk is not a whole number of tiles, or a variable-length batch
+  // variable-length batch (cu_q == nullptr: fixed lengths Sq, Sk): sequence
+  // bounds, and bottom-right alignment per sequence (br) of the top-left mask
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
+  int br;
   int cs;          // key-major CTAs per key tile (query-head split)
   int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
   float scale;
@@ -151,8 +157,40 @@ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 // Whether some entry of the tile rows [m0, m0 + BM) x keys [n0, n0 + BN) is
 // dead (masked, or past the end of the queries or keys), so that the tile
 // needs the per-element mask.
-__device__ __forceinline__ bool tile_cut(const TcParams& p, int m0, int n0) {
-  return m0 + BM > p.Sq || n0 + BN > p.Sk || !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
+// One sequence of the batch as a CTA sees it: its lengths, the first rows of
+// its dq and dk / dv in the outputs, and the mask aligned to it.
+struct Seq {
+  int lq, lk;
+  int64_t oq, ok;
+  MaskSpec mask;
+};
+
+// False (nothing to do; bad bounds are recorded) when the varlen bounds of
+// sequence b are out of order or out of range.
+__device__ __forceinline__ bool seq_of(const TcParams& p, int b, Seq* s) {
+  if (p.cu_q == nullptr) {
+    s->lq = p.Sq;
+    s->lk = p.Sk;
+    s->oq = (int64_t)b * p.Sq;
+    s->ok = (int64_t)b * p.Sk;
+    s->mask = p.mask;
+    return true;
+  }
+  int tq, tk;
+  const bool okq = seq_span(p.cu_q, b, p.total_q, p.Sq, &tq, &s->lq);
+  const bool okk = seq_span(p.cu_k, b, p.total_k, p.Sk, &tk, &s->lk);
+  if (!okq || !okk) {
+    if (threadIdx.x == 0) report(p.status, ATTN_ERR_INVALID_ARG, b);
+    return false;
+  }
+  s->oq = tq;
+  s->ok = tk;
+  s->mask = p.br ? mask_aligned(p.mask, s->lk - s->lq) : p.mask;
+  return true;
+}
+
+__device__ __forceinline__ bool tile_cut(const Seq& s, int m0, int n0) {
+  return m0 + BM > s.lq || n0 + BN > s.lk || !tile_full(s.mask, m0, m0 + BM, n0, n0 + BN);
 }
 
 // Live (query head, query tile) pairs of a key tile, heads outer: the live
@@ -160,8 +198,8 @@ __device__ __forceinline__ bool tile_cut(const TcParams& p, int m0, int n0) {
 // tiles only.
 struct QTileIter {
   int hpc, lo, hi, hl, mt;
-  __device__ QTileIter(int hpc_, int n0, const TcParams& p) : hpc(hpc_), hl(0) {
-    live_query_tiles(p.mask, p.Sq, p.Sk, BM, BN, n0, &lo, &hi);
+  __device__ QTileIter(int hpc_, int n0, const Seq& s) : hpc(hpc_), hl(0) {
+    live_query_tiles(s.mask, s.lq, s.lk, BM, BN, n0, &lo, &hi);
     mt = lo - 1;
   }
   __device__ bool next() {
@@ -178,8 +216,8 @@ struct QTileIter {
 // tiles (live_key_tiles).
 struct KTileIter {
   int s_end, w_lo, w_hi, nt;
-  __device__ KTileIter(int m0, const TcParams& p) : nt(-1) {
-    live_key_tiles(p.mask, p.Sq, p.Sk, BM, BN, m0, &s_end, &w_lo, &w_hi);
+  __device__ KTileIter(int m0, const Seq& s) : nt(-1) {
+    live_key_tiles(s.mask, s.lq, s.lk, BM, BN, m0, &s_end, &w_lo, &w_hi);
   }
   __device__ bool next() {
     if (++nt < s_end) return true;
@@ -229,6 +267,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   const int r = p.Hq / p.Hk;
   const int hpc = r / cs;
   const int h_first = g * r + rank * hpc;
+  Seq sq;
+  if (!seq_of(p, b, &sq) || n0 >= sq.lk) return;  // a key tile past this sequence's keys
 
   Ctx c;
   c.bars = sbase + L::BAR;
@@ -264,7 +304,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     }
     int issued[2] = {0, 0};
     if (lane == 0 || p.ragged) {  // warp-uniform when ragged
-      QTileIter it(hpc, n0, p);
+      QTileIter it(hpc, n0, sq);
       int t = 0;
       while (it.next()) {
         const int st = t & 1;
@@ -300,7 +340,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 #pragma unroll
           for (int u = 0; u < BM / 32; ++u) {
             const int q = u * 32 + lane;
-            const bool in = m0 + q < p.Sq;
+            const bool in = m0 + q < sq.lq;
             lse_s[q] = in ? p.lse[lrow + q] : 0.f;
             dl_s[q] = in ? p.delta[lrow + q] : 0.f;
           }
@@ -353,7 +393,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // TMEM, then dP(t+1) after dK(t) released those columns. The softmax of
       // tile t+1 overlaps dV(t), dK(t) and dP(t+1).
       bool ok = wait_bar(c, kKvFull, 0, 2);
-      QTileIter it(hpc, n0, p);
+      QTileIter it(hpc, n0, sq);
       bool have = ok && it.next();
       if (have) {
         have = wait_bar(c, kQFull0, 0, 3);
@@ -432,7 +472,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int jl = lg * 32 + lane;                   // key row within the tile
     const int j = n0 + jl;
-    QTileIter it(hpc, n0, p);
+    QTileIter it(hpc, n0, sq);
     int t = 0;
     bool ok = true;
     while (it.next()) {
@@ -448,23 +488,23 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // without live keys has LSE = -inf; it can only sit in a partial tile,
       // where this mask zeroes its probabilities. So do the rows past Sq and
       // a key row past Sk (zero operands in the staged copies).
-      const bool partial = kMayBeRagged ? tile_cut(p, m0, n0)
-                                        : !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
-      const int qcap = p.Sq - 1 - m0;        // last query of the tile
+      const bool partial = kMayBeRagged ? tile_cut(sq, m0, n0)
+                                        : !tile_full(sq.mask, m0, m0 + BM, n0, n0 + BN);
+      const int qcap = sq.lq - 1 - m0;       // last query of the tile
       int qlo = 0, qhi = BM - 1;
       if (partial) {
-        if (j >= p.mask.sink) {
-          qlo = j - p.mask.wr - m0;  // bits_between clamps to the tile
-          qhi = j + p.mask.wl - m0;
+        if (j >= sq.mask.sink) {
+          qlo = j - sq.mask.wr - m0;  // bits_between clamps to the tile
+          qhi = j + sq.mask.wl - m0;
         }
         if constexpr (kMayBeRagged) {
           qhi = imin(qhi, qcap);
-          if (j >= p.Sk) qhi = qlo - 1;
+          if (j >= sq.lk) qhi = qlo - 1;
         }
       }
       // bias / dbias element (query m0 + q, key j); reads of rows and keys
       // past the lengths are clamped into the tensor (their P is zero)
-      const int jc = kMayBeRagged ? imin(j, p.Sk - 1) : j;
+      const int jc = kMayBeRagged ? imin(j, sq.lk - 1) : j;
       const float* brow = nullptr;
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + jc;
       float* dbrow = nullptr;
@@ -593,7 +633,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     const uint32_t t_acc = ewg == 0 ? t_dK : t_dV;
     const float mul = ewg == 0 ? p.scale : 1.f;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float* grow = (ewg == 0 ? p.dk : p.dv) + (((int64_t)b * p.Sk + n0 + ejl) * p.Hk + g) * D;
+    float* grow = (ewg == 0 ? p.dk : p.dv) + ((sq.ok + n0 + ejl) * p.Hk + g) * D;
     const uint32_t srow = sbase + L::STAGE + (ewg * 128 + ejl) * L::kStageRow;
     if (epi_ok) {
 #pragma unroll 1
@@ -613,7 +653,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, a0, a1, a2, a3);
         }
       }
-      if (n0 + ejl >= p.Sk) {
+      if (n0 + ejl >= sq.lk) {
         // a padding row past Sk: nothing to write (the TMEM loads above are
         // warp-wide, so the row still took part in them)
       } else if (cs == 1) {
@@ -668,6 +708,8 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   const int b = bh / p.Hq;
   const int g = h / (p.Hq / p.Hk);
   const int m0 = mt * BM;
+  Seq sq;
+  if (!seq_of(p, b, &sq) || m0 >= sq.lq) return;  // a query tile past this sequence's queries
 
   Ctx c;
   c.bars = sbase + L::BAR;
@@ -694,7 +736,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
         ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
       }
-      KTileIter it(m0, p);
+      KTileIter it(m0, sq);
       int t = 0;
       int issued[2] = {0, 0};
       while (it.next()) {
@@ -751,7 +793,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // one tile ahead, so the softmax computes P(t+1) while dQ(t) and
       // dP(t+1) are on the tensor pipe; only its dS half waits for dP.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
-      KTileIter it(m0, p);
+      KTileIter it(m0, sq);
       bool have = ok && it.next();
       bool have1 = false;
       if (have) {
@@ -815,29 +857,29 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int il = lg * 32 + lane;                   // query row within the tile
     const int i = m0 + il;
-    const bool row_in = i < p.Sq;                    // rows past Sq are padding (not stored)
-    const int ic = row_in ? i : p.Sq - 1;
+    const bool row_in = i < sq.lq;                   // rows past the length: padding (not stored)
+    const int ic = row_in ? i : sq.lq - 1;
     const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + ic;
     const float nl = row_in ? p.lse[row] * -kLog2e : 0.f;  // -inf rows: see the partial-tile mask
     const float dl = row_in ? p.delta[row] : 0.f;
     const float* brow = nullptr;
     if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
-    KTileIter it(m0, p);
+    KTileIter it(m0, sq);
     int t = 0;
     bool ok = true;
     while (it.next()) {
       if (!wait_bar(c, qSFull, t & 1, 27)) { ok = false; break; }
       ptx::tc_fence_after();
       const int n0 = it.nt * BN;
-      const bool partial = kMayBeRagged ? tile_cut(p, m0, n0)
-                                        : !tile_full(p.mask, m0, m0 + BM, n0, n0 + BN);
-      const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
+      const bool partial = kMayBeRagged ? tile_cut(sq, m0, n0)
+                                        : !tile_full(sq.mask, m0, m0 + BM, n0, n0 + BN);
+      const int kcap = sq.lk - n0;  // keys [0, kcap) of the tile exist
       // live keys of this query row within the tile: [klo, khi] plus the sinks
       int klo = 0, khi = BN - 1, ksink = 0;
       if (partial) {
-        klo = i - p.mask.wl - n0;  // bits_between clamps to the tile
-        khi = i + p.mask.wr - n0;
-        ksink = p.mask.sink - n0;
+        klo = i - sq.mask.wl - n0;  // bits_between clamps to the tile
+        khi = i + sq.mask.wr - n0;
+        ksink = sq.mask.sink - n0;
         if constexpr (kMayBeRagged) {
           khi = imin(khi, kcap - 1);
           ksink = imin(ksink, kcap);
@@ -928,7 +970,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       ptx::tc_fence_after();
       // staged in the (idle) K / V stages, then one copy-engine store per half
       // row (rows past Sq are not stored)
-      float* grow = p.dq + (((int64_t)b * p.Sq + ic) * p.Hq + h) * D + wg * (D / 2);
+      float* grow = p.dq + ((sq.oq + ic) * p.Hq + h) * D + wg * (D / 2);
       const uint32_t srow = sbase + L::STAGE + il * L::kStageRow + wg * (D / 2) * 4;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -1116,7 +1158,12 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.Sk = pr.Sk;
   p.Sqs = tc_rows(pr.Sq);
   p.Sks = tc_rows(pr.Sk);
-  p.ragged = (p.Sqs != p.Sq || p.Sks != p.Sk) ? 1 : 0;
+  p.cu_q = pr.varlen ? pr.cu_q : nullptr;
+  p.cu_k = pr.varlen ? pr.cu_k : nullptr;
+  p.total_q = pr.total_q;
+  p.total_k = pr.total_k;
+  p.br = pr.br ? 1 : 0;
+  p.ragged = (p.Sqs != p.Sq || p.Sks != p.Sk || pr.varlen) ? 1 : 0;
   p.cs = tc_head_split(pr);
   p.kv_ctas = pr.B * pr.Hk * (p.Sks / BN) * p.cs;
   p.scale = pr.scale;

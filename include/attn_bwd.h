@@ -75,6 +75,31 @@ typedef struct attn_problem {
   int64_t do_stride[3];
   int32_t flags;          /* ATTN_FLAG_* bits; 0 = defaults. Pass the same value to
                              attn_bwd_preprocess and attn_bwd. */
+  /* Variable-length batch, packed token-major ("TND") rows. With
+   * cu_seqlens_q == NULL (zero-initialised struct) the fixed-length layout
+   * above applies. Otherwise sequence b holds the query rows
+   * [cu_seqlens_q[b], cu_seqlens_q[b + 1]) and the key rows
+   * [cu_seqlens_k[b], cu_seqlens_k[b + 1]) (device arrays of B + 1 int32:
+   * first entry 0, nondecreasing, last at most total_q / total_k), and Sq, Sk
+   * are upper bounds of the per-sequence lengths. Then:
+   *  - q, o, dO, dq are [total_q, Hq, D] (stride[1] between tokens,
+   *    stride[2] between heads, stride[0] unused; dq contiguous), k, v, dk,
+   *    dv are [total_k, Hk, D];
+   *  - lse and delta keep the padded [B, Hq, Sq] layout (entries past a
+   *    sequence's length are neither read nor written);
+   *  - bias / dbias [Hq, Sq, Sk] are indexed by positions within the sequence;
+   *  - a mask aligns per sequence (bottom-right uses that sequence's lengths).
+   * The dense tensor-core path only: the sparse variant, D = 512,
+   * ATTN_FLAG_CUDA_CORES, attn_fwd_lse, attn_bwd_dsinks and deterministic
+   * dbias over several sequences return ATTN_ERR_UNSUPPORTED. cu_seqlens are
+   * checked on the device: a sequence whose bounds are out of order or out
+   * of range is skipped and ATTN_ERR_INVALID_ARG recorded in the status
+   * record with detail = its index. (Ascend "sparse_flash_mla_grad" takes
+   * the TND layout with per-sequence lengths; the CK sink-token page names
+   * both causal alignments.) */
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int32_t total_q, total_k;
 } attn_problem_t;
 
 /* Deterministic dense backward: dq, dk, dv and dbias are bitwise the same on

@@ -32,6 +32,8 @@ from .dense import (
     preprocess,
     dsinks,
     backward,
+    varlen_forward,
+    varlen_backward,
 )
 from .sparse import (
     selected_rows,
@@ -48,6 +50,8 @@ __all__ = [
     "preprocess",
     "dsinks",
     "backward",
+    "varlen_forward",
+    "varlen_backward",
     "selected_rows",
     "sparse_forward",
     "sparse_backward",

@@ -230,3 +230,74 @@ def _scatter_cols(block: np.ndarray, cols: np.ndarray) -> np.ndarray:
     out = np.zeros((block.shape[0], int(cols[-1] - cols[0] + 1)))
     out[:, cols - cols[0]] = block
     return out
+
+
+# --------------------------------------------------------------------------
+# Variable-length batches: packed sequences in token-major rows [T, H, D]
+# (the TND layout of the Ascend "sparse_flash_mla_grad" page), each sequence
+# its own attention problem.
+# --------------------------------------------------------------------------
+
+def _sequence(X: np.ndarray, a: int, e: int) -> np.ndarray:
+    """Rows [a, e) of a packed [T, H, D] tensor as a [1, H, e - a, D] batch."""
+    return np.asarray(X[a:e], np.float64).transpose(1, 0, 2)[None]
+
+
+def varlen_forward(Q, K, V, cu_q, cu_k, scale: float, max_q: int, window_left: int = -1,
+                   window_right: int = -1, num_sink: int = 0, bottom_right: bool = False,
+                   bias: Optional[np.ndarray] = None):
+    """forward() on every sequence of a packed batch.
+
+    Sequence b holds query rows cu_q[b] .. cu_q[b+1]-1 and key rows
+    cu_k[b] .. cu_k[b+1]-1; its mask is live_mask over its own lengths (so a
+    bottom-right alignment uses its own Sk - Sq) and its bias is the
+    top-left [Sq_b, Sk_b] corner of bias [Hq, max_q, max_k].
+    Returns O [Tq, Hq, Dv] and LSE [B, Hq, max_q] (-inf past each length).
+    """
+    B = len(cu_q) - 1
+    Hq, Dv = Q.shape[1], V.shape[2]
+    O = np.zeros((Q.shape[0], Hq, Dv))
+    LSE = np.full((B, Hq, max_q), -np.inf)
+    for b in range(B):
+        qa, qe, ka, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if qe == qa:
+            continue
+        m = live_mask(qe - qa, ke - ka, window_left, window_right, num_sink, bottom_right)
+        bb = None if bias is None else bias[:, :qe - qa, :ke - ka]
+        Ob, Lb = forward(_sequence(Q, qa, qe), _sequence(K, ka, ke), _sequence(V, ka, ke), scale,
+                         m, bb)
+        O[qa:qe] = Ob[0].transpose(1, 0, 2)
+        LSE[b, :, :qe - qa] = Lb[0]
+    return O, LSE
+
+
+def varlen_backward(Q, K, V, O, dO, LSE, cu_q, cu_k, scale: float, max_q: int, max_k: int,
+                    window_left: int = -1, window_right: int = -1, num_sink: int = 0,
+                    bottom_right: bool = False, bias: Optional[np.ndarray] = None):
+    """backward() on every sequence of a packed batch (layouts as in
+    varlen_forward; LSE [B, Hq, max_q]).
+
+    Returns dQ [Tq, Hq, D], dK [Tk, Hk, D], dV [Tk, Hk, Dv], and dbias
+    [Hq, max_q, max_k]: the sum over sequences of each sequence's dS placed
+    at its positions.
+    """
+    B = len(cu_q) - 1
+    Hq = Q.shape[1]
+    dQ = np.zeros(Q.shape)
+    dK = np.zeros(K.shape)
+    dV = np.zeros(V.shape)
+    dbias = np.zeros((Hq, max_q, max_k))
+    for b in range(B):
+        qa, qe, ka, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if qe == qa or ke == ka:
+            continue
+        m = live_mask(qe - qa, ke - ka, window_left, window_right, num_sink, bottom_right)
+        bb = None if bias is None else bias[:, :qe - qa, :ke - ka]
+        gq, gk, gv, gb = backward(_sequence(Q, qa, qe), _sequence(K, ka, ke), _sequence(V, ka, ke),
+                                  _sequence(O, qa, qe), _sequence(dO, qa, qe),
+                                  np.asarray(LSE, np.float64)[b:b + 1, :, :qe - qa], scale, m, bb)
+        dQ[qa:qe] = gq[0].transpose(1, 0, 2)
+        dK[ka:ke] = gk[0].transpose(1, 0, 2)
+        dV[ka:ke] = gv[0].transpose(1, 0, 2)
+        dbias[:, :qe - qa, :ke - ka] += gb
+    return dQ, dK, dV, dbias

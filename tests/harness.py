@@ -142,3 +142,35 @@ def gpu_sparse_plan(w, O_b, L_f, dev="cuda", cuda_cores=False):
                            cmp_idx=idx, ori_win_left=w.ori_win_left,
                            ori_win_right=w.ori_win_right, cmp_ratio=cfa_ratio(w) or 0,
                            cuda_cores=cuda_cores)
+
+
+def varlen_forward_inputs(w):
+    """Oracle forward of a packed batch -> (O bf16-exact float32 [Tq, Hq, D],
+    LSE float32 [B, Hq, max_q])."""
+    bias = None if w.bias is None else w.bias.astype(np.float64)
+    O, L = oracle.varlen_forward(w.q, w.k, w.v, w.cu_q, w.cu_k, w.scale, w.max_q,
+                                 w.window_left, w.window_right, w.num_sink, w.bottom_right, bias)
+    return np.ascontiguousarray(bf16_round(O.astype(np.float32))), L.astype(np.float32)
+
+
+def varlen_reference(w, O_b, L_f):
+    bias = None if w.bias is None else w.bias.astype(np.float64)
+    dq, dk, dv, db = oracle.varlen_backward(w.q, w.k, w.v, O_b, w.do, L_f, w.cu_q, w.cu_k,
+                                            w.scale, w.max_q, w.max_k, w.window_left,
+                                            w.window_right, w.num_sink, w.bottom_right, bias)
+    return dict(dq=dq, dk=dk, dv=dv, dbias=db)
+
+
+def gpu_varlen_plan(w, O_b, L_f, dev="cuda", deterministic=False):
+    import torch
+    import attention_backward_attn_gb300 as ab
+    q, k, v, o, do = (to_dev_bf16(x, dev) for x in (w.q, w.k, w.v, O_b, w.do))
+    lse = to_dev_f32(L_f, dev)
+    bias = None if w.bias is None else to_dev_f32(w.bias, dev)
+    mask = ab.mask_from(w.window_left, w.window_right, w.num_sink, w.bottom_right)
+    cu_q = torch.from_numpy(np.asarray(w.cu_q, np.int32)).to(dev)
+    cu_k = torch.from_numpy(np.asarray(w.cu_k, np.int32)).to(dev)
+    return ab.BackwardPlan(q, k, v, o, do, lse, w.scale, mask=mask, bias=bias,
+                           want_dbias=w.want_dbias, deterministic=deterministic,
+                           cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=w.max_q,
+                           max_seqlen_k=w.max_k)

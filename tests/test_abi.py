@@ -180,6 +180,37 @@ def test_problem_flags(ab):
     assert ab.attn_bwd_path(p, None, None) == 0
 
 
+def test_varlen_descriptor_validation(ab):
+    fake = 1 << 20  # never dereferenced: host validation only
+    p = _prob(ab, B=3, Sq=300, Sk=300)
+    p.cu_seqlens_q = fake  # without cu_seqlens_k
+    p.total_q, p.total_k = 500, 500
+    assert ab.attn_bwd_path(p, None, None) == 0
+    assert _call_bwd(ab, p) == 1
+    p.cu_seqlens_k = fake
+    p.total_q = -1
+    assert _call_bwd(ab, p) == 1
+    p.total_q = 500
+    # the variable-length layout runs on the dense tensor-core kernel only
+    p.flags = ab.ATTN_FLAG_CUDA_CORES
+    assert ab.attn_bwd_path(p, None, None) == 0
+    p.flags = 0
+    assert ab.attn_bwd_path(_varlen(ab, D=512), None, None) == 0
+    sp = _varlen(ab, B=1, Hq=16, Hk=1, Sk=0, D=512)
+    s = ab.Sparse()
+    s.ori_kv, s.n_ori, s.ori_win_left, s.ori_win_right, s.d_ori_kv = fake, 128, 31, 0, fake
+    assert ab.attn_bwd_path(sp, None, s) == 0
+    # lse / delta of a packed batch hold unused entries: no dsinks
+    assert ab.lib.attn_bwd_dsinks(ctypes.byref(p), fake, fake, fake, fake, None) == 2
+
+
+def _varlen(ab, **kw):
+    p = _prob(ab, **kw)
+    p.cu_seqlens_q = p.cu_seqlens_k = 1 << 20
+    p.total_q = p.total_k = 64
+    return p
+
+
 def test_read_status_rejects_null(ab):
     code = ab.lib.attn_read_device_status(None, None, None)
     assert code == 1

@@ -10,7 +10,7 @@ import pytest
 
 import harness as H
 import oracle
-from workloads import make_workload, make_dense, make_sparse
+from workloads import make_workload, make_dense, make_sparse, make_varlen
 
 pytestmark = pytest.mark.gpu
 
@@ -185,6 +185,87 @@ def test_tensor_core_cases(name):
     w = TC_EXTRA[name]()
     plan, O_b, L_f = _run_dense(w, expect_path=1)
     _compare_dense(w, plan, O_b, L_f)
+
+
+# Variable-length batches (packed token-major rows, cu_seqlens): every
+# sequence is its own problem, masks align per sequence.
+VARLEN = {
+    # GQA 4:1 causal, D = 128: an empty query sequence, ragged and aligned lengths
+    "gqa4_causal_mixed_d128": lambda: make_varlen("vl1", 70, [100, 0, 300, 257],
+                                                  [100, 64, 300, 257], Hq=8, Hk=2, D=128,
+                                                  window_left=-1, window_right=0),
+    # bottom-right causal per sequence with ALiBi bias and dbias, D = 64; Sq < Sk,
+    # Sq = Sk, a single query against 129 keys
+    "br_alibi_dbias_d64": lambda: make_varlen("vl2", 71, [130, 64, 1], [200, 64, 129], Hq=2,
+                                              Hk=2, D=64, window_left=-1, window_right=0,
+                                              bottom_right=True, alibi=True, want_dbias=True),
+    # GQA 8:1 window + sinks, a sequence without keys, max lengths above every length
+    "window_sinks_gqa8_d128": lambda: make_varlen("vl3", 72, [384, 5, 200, 30], [384, 700, 90, 0],
+                                                  Hq=8, Hk=1, D=128, window_left=60,
+                                                  window_right=3, num_sink=2, max_q=400,
+                                                  max_k=720),
+}
+
+
+@pytest.mark.parametrize("name", list(VARLEN))
+def test_varlen(name):
+    torch = _torch()
+    w = VARLEN[name]()
+    O_b, L_f = H.varlen_forward_inputs(w)
+    plan = H.gpu_varlen_plan(w, O_b, L_f)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+    ref = H.varlen_reference(w, O_b, L_f)
+    H.check_close("dq", plan.dq.cpu().numpy(), ref["dq"])
+    H.check_close("dk", plan.dk.cpu().numpy(), ref["dk"])
+    H.check_close("dv", plan.dv.cpu().numpy(), ref["dv"])
+    if w.want_dbias:
+        H.check_close("dbias", plan.dbias.cpu().numpy(), ref["dbias"])
+    delta = plan.delta.cpu().numpy()
+    for b in range(w.B):
+        n = int(w.cu_q[b + 1] - w.cu_q[b])
+        rows = slice(int(w.cu_q[b]), int(w.cu_q[b + 1]))
+        want = (O_b[rows].astype(np.float64) * w.do[rows].astype(np.float64)).sum(-1).T
+        np.testing.assert_allclose(delta[b, :, :n], want, rtol=1e-5,
+                                   atol=1e-5 * max(1.0, np.abs(want).max(initial=0.0)))
+
+
+def test_varlen_equal_lengths_match_the_fixed_length_run():
+    # the same three sequences as a padded batch and as a packed one: the
+    # same tiles in the same order, so bitwise-equal gradients (deterministic
+    # mode, so that no partial sums are added in arrival order)
+    torch = _torch()
+    w = make_dense("ve", 73, B=3, Hq=4, Hk=1, Sq=200, Sk=200, D=128, window_left=-1,
+                   window_right=0)
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    dense = H.gpu_dense_plan(w, O_b, L_f, deterministic=True)
+    dense.run()
+    pack = lambda x: np.ascontiguousarray(x.reshape(-1, *x.shape[2:]))
+    v = make_varlen("ve", 73, [200] * 3, [200] * 3, Hq=4, Hk=1, D=128, window_left=-1,
+                    window_right=0)
+    v.q, v.k, v.v, v.do = pack(w.q), pack(w.k), pack(w.v), pack(w.do)
+    var = H.gpu_varlen_plan(v, pack(O_b), L_f, deterministic=True)
+    var.run()
+    torch.cuda.synchronize()
+    assert dense.device_status()[0] == 0 and var.device_status()[0] == 0
+    for a, b in ((dense.dq, var.dq), (dense.dk, var.dk), (dense.dv, var.dv)):
+        assert torch.equal(a.reshape(b.shape), b)
+
+
+def test_varlen_bad_bounds_are_reported():
+    # decreasing bounds for sequence 1 (the others stay valid): it is skipped
+    # and recorded (detail 1)
+    torch = _torch()
+    w = VARLEN["gqa4_causal_mixed_d128"]()
+    O_b, L_f = H.varlen_forward_inputs(w)
+    plan = H.gpu_varlen_plan(w, O_b, L_f)
+    plan._keep[0].copy_(torch.tensor([0, 100, 90, 390, 647], dtype=torch.int32))
+    plan.run()
+    torch.cuda.synchronize()
+    code, detail = plan.device_status()
+    assert code == 1 and detail == 1
 
 
 # Deterministic mode (ATTN_FLAG_DETERMINISTIC): bitwise-identical outputs over

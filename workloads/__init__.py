@@ -207,6 +207,76 @@ def make_dense(
     )
 
 
+@dataclasses.dataclass
+class VarlenWorkload:
+    """Variable-length batch in packed token-major ("TND") layout:
+    q, do [Tq, Hq, D]; k, v [Tk, Hk, D]; sequence b holds query rows
+    cu_q[b] .. cu_q[b + 1] - 1 and key rows cu_k[b] .. cu_k[b + 1] - 1.
+    max_q / max_k bound the lengths; bias is float32 [Hq, max_q, max_k]
+    indexed by positions within a sequence."""
+    name: str
+    Hq: int
+    Hk: int
+    D: int
+    cu_q: np.ndarray
+    cu_k: np.ndarray
+    max_q: int
+    max_k: int
+    scale: float
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    do: np.ndarray
+    bias: Optional[np.ndarray] = None
+    window_left: int = -1
+    window_right: int = -1
+    num_sink: int = 0
+    want_dbias: bool = False
+    bottom_right: bool = False
+
+    @property
+    def B(self) -> int:
+        return len(self.cu_q) - 1
+
+
+def make_varlen(
+    name: str,
+    seed: int,
+    lens_q,
+    lens_k,
+    Hq: int,
+    Hk: int,
+    D: int,
+    window_left: int = -1,
+    window_right: int = -1,
+    num_sink: int = 0,
+    alibi: bool = False,
+    want_dbias: bool = False,
+    bottom_right: bool = False,
+    max_q: Optional[int] = None,
+    max_k: Optional[int] = None,
+) -> VarlenWorkload:
+    """Draw packed q, k, v, dO (in that order) from default_rng(seed), N(0,1), bf16."""
+    lens_q = np.asarray(lens_q, np.int64)
+    lens_k = np.asarray(lens_k, np.int64)
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    max_q = int(lens_q.max()) if max_q is None else int(max_q)
+    max_k = int(lens_k.max()) if max_k is None else int(max_k)
+    rng = np.random.default_rng(seed)
+    q = _normal_bf16(rng, (int(cu_q[-1]), Hq, D))
+    k = _normal_bf16(rng, (int(cu_k[-1]), Hk, D))
+    v = _normal_bf16(rng, (int(cu_k[-1]), Hk, D))
+    do = _normal_bf16(rng, (int(cu_q[-1]), Hq, D))
+    bias = alibi_bias(Hq, max_q, max_k) if alibi else None
+    return VarlenWorkload(
+        name=name, Hq=Hq, Hk=Hk, D=D, cu_q=cu_q, cu_k=cu_k, max_q=max_q, max_k=max_k,
+        scale=float(1.0 / np.sqrt(D)), q=q, k=k, v=v, do=do, bias=bias,
+        window_left=window_left, window_right=window_right, num_sink=num_sink,
+        want_dbias=want_dbias, bottom_right=bottom_right,
+    )
+
+
 def make_sparse(
     name: str,
     seed: int,
