@@ -90,7 +90,6 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
       p.varlen ? mask_spec_of(mask, 0, 0, &p.mask) : mask_spec_of(mask, a.Sq, a.Sk, &p.mask);
   if (ms != ATTN_OK) return ms;
   p.sparse = sp != nullptr;
-  if (p.sparse && p.deterministic) return ATTN_ERR_UNSUPPORTED;  // dKV: reduction over tokens
   if (p.sparse) {
     if (mask != nullptr) return ATTN_ERR_INVALID_ARG;  // the sparse window replaces it
     if (a.B != 1) return ATTN_ERR_INVALID_ARG;
@@ -116,6 +115,9 @@ attn_status_t make_problem(const attn_problem_t* prob, const attn_mask_t* mask,
   }
   // variable-length batches run on the dense tensor-core kernel only
   if (p.varlen && !tc_supported(p)) return ATTN_ERR_UNSUPPORTED;
+  // the ordered sparse dKV reduction follows the tensor-core kernel's slots
+  if (p.sparse && p.deterministic && (p.cuda_cores || !tc_sparse_supported(p)))
+    return ATTN_ERR_UNSUPPORTED;
   *out = p;
   return ATTN_OK;
 }
@@ -157,6 +159,23 @@ WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
     w.kv16 = off;
     off = align_up(off + kvbytes, 1024);
     w.staged = true;
+    if (p.deterministic) {
+      // per item (token, KV head): dKV rows at their slots, the row list,
+      // {count, window rows, first window row}; per item and compressed row:
+      // first slot and multiplicity
+      const size_t items = (size_t)p.Sq * p.Hk;
+      const size_t slots = items * (size_t)sparse_det_stride(p);
+      w.det_part = off;
+      off = align_up(off + slots * p.D * sizeof(float), 1024);
+      w.det_rows = off;
+      off = align_up(off + slots * sizeof(int32_t), 1024);
+      w.det_meta = off;
+      off = align_up(off + items * 3 * sizeof(int32_t), 1024);
+      w.det_slot = off;
+      off = align_up(off + items * p.n_cmp * sizeof(int32_t), 1024);
+      w.det_mult = off;
+      off = align_up(off + items * p.n_cmp * sizeof(int32_t), 1024);
+    }
   } else if (tensor_core_path) {
     const size_t qbytes = (size_t)p.B * p.Hq * tc_rows(p.Sq) * p.D * sizeof(__half);
     const size_t kbytes = (size_t)p.B * p.Hk * tc_rows(p.Sk) * p.D * sizeof(__half);
@@ -341,8 +360,20 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
   DevStatus* st = reinterpret_cast<DevStatus*>(ws + w.status);
   if (tc && p.sparse) {
     const __half* kv16 = reinterpret_cast<const __half*>(ws + w.kv16);
-    return cuda_status(launch_bwd_sparse_tc(p, q, dO, kv16, sparse->cmp_idx, lse, delta, dq,
-                                            sparse->d_ori_kv, sparse->d_cmp_kv, st, stream));
+    SparseDet det;
+    if (p.deterministic) {
+      det.part = reinterpret_cast<float*>(ws + w.det_part);
+      det.rows = reinterpret_cast<int32_t*>(ws + w.det_rows);
+      det.meta = reinterpret_cast<int32_t*>(ws + w.det_meta);
+      det.slot = reinterpret_cast<int32_t*>(ws + w.det_slot);
+      det.mult = reinterpret_cast<int32_t*>(ws + w.det_mult);
+      det.stride = (int)sparse_det_stride(p);
+    }
+    cudaError_t e = launch_bwd_sparse_tc(p, q, dO, kv16, sparse->cmp_idx, lse, delta, dq,
+                                         sparse->d_ori_kv, sparse->d_cmp_kv, det, st, stream);
+    if (e == cudaSuccess && p.deterministic)
+      e = launch_sparse_det_reduce(p, det, sparse->d_ori_kv, sparse->d_cmp_kv, stream);
+    return cuda_status(e);
   }
   if (p.sparse) {
     return cuda_status(launch_bwd_simt(p, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias,

@@ -23,6 +23,8 @@ inline int tc_rows(int s) { return (s + 127) / 128 * 128; }
 struct WorkspaceLayout {
   size_t status = 0;
   size_t q16 = 0, k16 = 0, v16 = 0, do16 = 0, kv16 = 0;
+  // deterministic sparse dKV (SparseDet below)
+  size_t det_part = 0, det_rows = 0, det_meta = 0, det_slot = 0, det_mult = 0;
   size_t total = 0;
   bool staged = false;
 };
@@ -75,10 +77,33 @@ cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16
                           float* dv, float* dbias, DevStatus* st, cudaStream_t stream);
 
 // ---- tc_sparse.cu ----
+// Deterministic sparse dKV: the tensor-core kernel stores every item's
+// (item = token Hk + KV head) dKV rows at their slots in `part`
+// ([items * stride][512] fp32) with the item's row list in `rows` and
+// {row count, window rows, first window row} in `meta`; sparse_det.cu then
+// finds, per item and compressed row, the first slot holding it (`slot`,
+// [items * n_cmp]) and how many slots do (`mult`), and adds each dKV row's
+// contributions in token order.
+struct SparseDet {
+  float* part = nullptr;
+  int32_t* rows = nullptr;
+  int32_t* meta = nullptr;
+  int32_t* slot = nullptr;
+  int32_t* mult = nullptr;
+  int stride = 0;
+};
+int64_t sparse_det_stride(const Problem& p);  // slots per item: the row bound rounded to 128
+
 bool tc_sparse_supported(const Problem& p);
 cudaError_t launch_bwd_sparse_tc(const Problem& p, const void* q, const void* dO,
                                  const __half* kv16, const int32_t* idx, const float* lse,
                                  const float* delta, float* dq, float* d_ori, float* d_cmp,
-                                 DevStatus* st, cudaStream_t stream);
+                                 const SparseDet& det, DevStatus* st, cudaStream_t stream);
+
+// ---- sparse_det.cu ----
+// After launch_bwd_sparse_tc in deterministic mode: writes d_ori / d_cmp
+// (every row, zero where no token selected it) from det.part.
+cudaError_t launch_sparse_det_reduce(const Problem& p, const SparseDet& det, float* d_ori,
+                                     float* d_cmp, cudaStream_t stream);
 
 }  // namespace attn

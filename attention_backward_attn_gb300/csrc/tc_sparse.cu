@@ -118,6 +118,15 @@ struct SpParams {
   float* d_ori;        // [n_ori][Hk][512]
   float* d_cmp;        // [n_cmp][Hk][512]
   DevStatus* status;
+  // Deterministic mode (det_part != nullptr): each item's dKV rows are stored
+  // to det_part[(item det_stride + slot)][512] instead of being added into
+  // d_ori / d_cmp; det_rows holds the item's row list (same slots) and
+  // det_meta[3 item .. +2] = {row count, window rows, first window row}.
+  // item = token Hk + KV head. attn_bwd then adds them per row in token order.
+  float* det_part;
+  int32_t* det_rows;
+  int32_t* det_meta;
+  int det_stride;
 };
 
 // Selected rows of (token i, KV head g) as row ids of the fp16 copy
@@ -126,13 +135,16 @@ struct SpParams {
 // row whose block ends at or before the query (CFA). Returns the count; the
 // list is padded to a multiple of 128 with its first entry (masked later).
 // Run by one full warp.
-__device__ int build_rows(const SpParams& p, int i, int g, int32_t* rows, int lane) {
+__device__ int build_rows(const SpParams& p, int i, int g, int32_t* rows, int lane,
+                          int* nwin_out, int* lo_out) {
   const int pos = (p.n_ori - p.Sq) + i;
   int lo = p.wl >= 0 ? pos - p.wl : 0;
   int hi = p.wr >= 0 ? pos + p.wr : p.n_ori - 1;
   lo = max(lo, 0);
   hi = min(hi, p.n_ori - 1);
   const int nwin = hi >= lo ? hi - lo + 1 : 0;
+  *nwin_out = nwin;
+  *lo_out = lo;
   for (int j = lane; j < nwin; j += 32) rows[j] = (lo + j) * p.Hk + g;
   int n = nwin;
   if (p.ratio > 0) {  // CFA
@@ -256,7 +268,17 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int k = 0; k < n_tok; ++k) {
       const int b = k & 1, i = item_i(k), g = item_g(k);
       if (k >= 2 && !wait_bar(c, sRowsFree0 + b, (uint32_t)((k - 2) >> 1) & 1u, 30)) break;
-      const int n = build_rows(p, i, g, rows_of(b), lane);
+      int nwin, wlo;
+      const int n = build_rows(p, i, g, rows_of(b), lane, &nwin, &wlo);
+      if (p.det_part != nullptr) {  // the row list of the item's stored dKV rows
+        const int64_t item = (int64_t)i * p.Hk + g;
+        for (int j = lane; j < n; j += 32) p.det_rows[item * p.det_stride + j] = rows_of(b)[j];
+        if (lane == 0) {
+          p.det_meta[3 * item] = n;
+          p.det_meta[3 * item + 1] = nwin;
+          p.det_meta[3 * item + 2] = wlo;
+        }
+      }
       for (int h = lane; h < kSpR; h += 32) {
         const int64_t r = (int64_t)(g * kSpR + h) * p.Sq + i;
         const float lv = p.lse[r];
@@ -609,6 +631,16 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           ptx::mbar_arrive(c.bar(sDkvEmpty));
           float* const ori_base = p.d_ori + 128 * cc + dl;
           float* const cmp_base = p.d_cmp - (int64_t)ori_rows * kSpD + 128 * cc + dl;
+          if (p.det_part != nullptr) {
+            // deterministic mode: store the rows at their slots (no reduction)
+            float* const part = p.det_part +
+                                (((int64_t)i * p.Hk + g) * p.det_stride + 128 * t + 64 * bb) * kSpD +
+                                128 * cc + dl;
+#pragma unroll
+            for (int u = 0; u < 64; ++u)
+              if (u < nt) part[(int64_t)u * kSpD] = __uint_as_float(v[u]);
+            continue;
+          }
 #pragma unroll
           for (int n0 = 0; n0 < 64; n0 += 8) {
             if (n0 < nt) {
@@ -694,6 +726,8 @@ int64_t max_selected_rows(const Problem& p) {
 
 }  // namespace
 
+int64_t sparse_det_stride(const Problem& p) { return (max_selected_rows(p) + 127) / 128 * 128; }
+
 bool tc_sparse_supported(const Problem& p) {
   return p.sparse && p.D == kSpD && p.B == 1 && p.Hq == kSpR * p.Hk && p.Sq > 0 && p.n_ori > 0 &&
          max_selected_rows(p) <= kSpMaxRows &&
@@ -704,7 +738,7 @@ bool tc_sparse_supported(const Problem& p) {
 cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* dO,
                                  const __half* kv16, const int32_t* idx, const float* lse,
                                  const float* delta, float* dq, float* d_ori, float* d_cmp,
-                                 DevStatus* st, cudaStream_t stream) {
+                                 const SparseDet& det, DevStatus* st, cudaStream_t stream) {
   CUtensorMap mq, mdo;
   if (!make_qmap(&mq, q, pr.Sq, pr.Hq, pr.qs[1], pr.qs[2]) ||
       !make_qmap(&mdo, dO, pr.Sq, pr.Hq, pr.dos[1], pr.dos[2]))
@@ -729,6 +763,10 @@ cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* d
   p.d_ori = d_ori;
   p.d_cmp = d_cmp;
   p.status = st;
+  p.det_part = det.part;
+  p.det_rows = det.rows;
+  p.det_meta = det.meta;
+  p.det_stride = det.stride;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_sparse_tc_kernel,

@@ -191,7 +191,7 @@ def run_ours(args):
         ab.attn_fwd_lse(prob, None, sp, q, None, None, None, o, lse)
         plan = ab.BackwardPlan(q, None, None, o, do, lse, w.scale, ori_kv=okv, cmp_kv=ckv,
                                cmp_idx=idx, ori_win_left=w.ori_win_left,
-                               ori_win_right=w.ori_win_right)
+                               ori_win_right=w.ori_win_right, deterministic=args.deterministic)
         bias = None
     else:
         q, k, v, do = (up_bf16(x) for x in (w.q, w.k, w.v, w.do))
@@ -202,7 +202,7 @@ def run_ours(args):
         prob = ab.problem_from(q, k, v, o, do, w.scale)
         ab.attn_fwd_lse(prob, mask, None, q, k, v, bias, o, lse)
         plan = ab.BackwardPlan(q, k, v, o, do, lse, w.scale, mask=mask, bias=bias,
-                               want_dbias=w.want_dbias)
+                               want_dbias=w.want_dbias, deterministic=args.deterministic)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
@@ -312,12 +312,17 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": flops / (mean_bwd_ms * 1e-3) / 1e12,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
         launches_per_step = 2
+        if args.deterministic and sparse:
+            launches_per_step = 4  # + compressed-row slot table + ordered row sums
+        elif args.deterministic and w.want_dbias:
+            launches_per_step = 1 + w.B  # one backward launch per batch
     else:
         roof = {"bound": "alu", "achieved": flops / (mean_bwd_ms * 1e-3) / 1e12,
                 "peak": SIMT_FP32_PEAK_TFLOPS, "unit": "TFLOP/s"}
         launches_per_step = 3
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = NCU_TRAFFIC.get(args.workload) if not overrides_of(args) else None
+    roof["traffic"] = (NCU_TRAFFIC.get(args.workload)
+                       if not overrides_of(args) and not args.deterministic else None)
     roof["peak_source"] = peaks_src
     roof["kernel"] = "attn_bwd (" + path + ")"
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e12
@@ -337,7 +342,7 @@ def run_ours(args):
         "config": {"workload": args.workload, "overrides": overrides_of(args) or None,
                    "flops_per_step": flops,
                    "algorithmic_bytes_per_step": algorithmic_bytes(w),
-                   "path": path, "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
+                   "path": path, "deterministic": bool(args.deterministic), "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                    "launch": "attn_bwd_preprocess + attn_bwd captured once into one CUDA graph (the backward a programmatic dependent of the pre-pass), replayed per step",
                    "parallelism": f"replicas x{ws}"},
         "pct_of_peak": round(100.0 * value / ws / peaks["bf16_tflops"], 2),
@@ -513,6 +518,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the bitwise-reproducible mode (ATTN_FLAG_DETERMINISTIC)")
     ap.add_argument("--override", nargs="*", default=[], metavar="KEY=INT",
                     help="shrink the workload (e.g. Sq=1024 n_ori=1024 n_cmp=256) for a "
                          "profiler capture; the JSON line then records the overrides")

@@ -107,8 +107,12 @@ typedef struct attn_problem {
  * key tile's query heads over CTAs, whose partial sums would be added in
  * arrival order), and with dbias and B > 1 attn_bwd runs one launch per batch
  * so that each dbias element receives its per-batch terms in batch order.
- * Slower than the default. The sparse path's dKV is a reduction over tokens
- * in arrival order: a sparse problem with this flag returns
+ * Slower than the default. Sparse variant: the tensor-core kernel stores
+ * every (token, KV head)'s dKV rows in the workspace instead of adding them
+ * into d_ori_kv / d_cmp_kv, and a second pass adds each row's terms in token
+ * order and writes the rows (the workspace then holds Sq * Hk * (selected-row
+ * bound rounded up to 128) * D fp32 values, 5.4 GB at 4096 tokens x 640
+ * rows); sparse shapes outside the tensor-core kernel return
  * ATTN_ERR_UNSUPPORTED. (Composable_kernel "34_bwd_gqa_fmha.py" names
  * atomics vs a deterministic reduction for dK / dV; the Ascend
  * "sparse_flash_mla_grad" page notes its operator is not deterministic by

@@ -128,7 +128,7 @@ def gpu_dense_plan(w, O_b, L_f, dev="cuda", deterministic=False, cuda_cores=Fals
                            cuda_cores=cuda_cores)
 
 
-def gpu_sparse_plan(w, O_b, L_f, dev="cuda", cuda_cores=False):
+def gpu_sparse_plan(w, O_b, L_f, dev="cuda", cuda_cores=False, deterministic=False):
     import torch
     import attention_backward_attn_gb300 as ab
     q = to_dev_bf16(w.q[None], dev)
@@ -141,7 +141,7 @@ def gpu_sparse_plan(w, O_b, L_f, dev="cuda", cuda_cores=False):
     return ab.BackwardPlan(q, None, None, o, do, lse, w.scale, ori_kv=okv, cmp_kv=ckv,
                            cmp_idx=idx, ori_win_left=w.ori_win_left,
                            ori_win_right=w.ori_win_right, cmp_ratio=cfa_ratio(w) or 0,
-                           cuda_cores=cuda_cores)
+                           cuda_cores=cuda_cores, deterministic=deterministic)
 
 
 def varlen_forward_inputs(w):

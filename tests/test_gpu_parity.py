@@ -463,6 +463,50 @@ def test_sparse_tensor_core(name):
         assert np.all(plan.dq.cpu().numpy()[0, :36] == 0)
 
 
+def _with_repeats(w):
+    """Top-k lists in which some indices repeat (each repeat counts once more)."""
+    idx = w.cmp_idx.copy()
+    idx[1::3, :, 1] = idx[1::3, :, 0]
+    idx[2::5, :, 2:4] = idx[2::5, :, 0:1]
+    w.cmp_idx = idx
+    return w
+
+
+# Deterministic sparse dKV: per-slot rows added in token order afterwards.
+DET_SPARSE = {
+    "tc_scfa_s200_h64": lambda: TC_SPARSE["tc_scfa_s200_h64"](),
+    "tc_scfa_hk2_delta": lambda: TC_SPARSE["tc_scfa_hk2_delta"](),
+    "tc_swa_s160_h64": lambda: TC_SPARSE["tc_swa_s160_h64"](),
+    "tc_cfa_hk2_delta": lambda: TC_SPARSE["tc_cfa_hk2_delta"](),
+    "tc_scfa_rows500": lambda: TC_SPARSE["tc_scfa_rows500"](),
+    "tc_scfa_repeats": lambda: _with_repeats(TC_SPARSE["tc_scfa_persistent_mix"]()),
+}
+
+
+@pytest.mark.parametrize("name", list(DET_SPARSE))
+def test_sparse_deterministic_mode(name):
+    torch = _torch()
+    w = DET_SPARSE[name]()
+    O_b, L_f, _, _ = H.sparse_forward_inputs(w)
+    plan = H.gpu_sparse_plan(w, O_b, L_f, deterministic=True)
+    assert plan.path == 1
+    runs = []
+    for _ in range(3):
+        plan.d_ori.fill_(float("nan"))  # every row is written, not added
+        if plan.d_cmp is not None:
+            plan.d_cmp.fill_(float("nan"))
+        plan.run()
+        torch.cuda.synchronize()
+        code, detail = plan.device_status()
+        assert code == 0, (code, detail)
+        outs = [plan.dq, plan.d_ori] + ([plan.d_cmp] if plan.d_cmp is not None else [])
+        runs.append([t.cpu().numpy().copy() for t in outs])
+    for later in runs[1:]:
+        for a, b in zip(runs[0], later):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    _compare_sparse(w, plan, O_b, L_f)
+
+
 def test_sparse_tensor_core_bad_index_is_reported():
     torch = _torch()
     w = TC_SPARSE["tc_scfa_s200_h64"]()
@@ -560,15 +604,27 @@ def test_full_gqa4_window1024_sink4_s8192_d128():
 
 
 def test_full_sparse_scfa_s4096_h64_d512():
+    torch = _torch()
     w = make_workload("sparse_scfa_s4096_h64_d512")
     plan, O_b, L_f = _run_sparse(w, expect_path=1)
     _compare_sparse(w, plan, O_b, L_f)
+    # the deterministic mode at full size: twice bitwise the same, and parity
+    del plan
+    det = H.gpu_sparse_plan(w, O_b, L_f, deterministic=True)
+    outs = []
+    for _ in range(2):
+        det.run()
+        torch.cuda.synchronize()
+        assert det.device_status()[0] == 0
+        outs.append((det.d_ori.clone(), det.d_cmp.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    _compare_sparse(w, det, O_b, L_f)
 
 
 SINK_CASES = {
     # dense, tensor-core path, GQA 4:1 causal
     "dense_tc": lambda: make_workload("gqa4_causal_s1024_d128", Hq=8, Hk=2, Sq=256, Sk=256),
-    # dense, SIMT path (ragged), window + sinks tokens
+    # dense, ragged lengths, window + sinks tokens
     "dense_simt": lambda: SMALL_DENSE["ragged_causal_sink_s200_d64"](),
     # sparse, tensor-core path
     "sparse_tc": lambda: TC_SPARSE["tc_scfa_hk2_delta"](),
