@@ -139,6 +139,12 @@ Sizes sizes_of(const Problem& p) {
 
 bool need(const void* ptr, int64_t count) { return count == 0 || ptr != nullptr; }
 
+// Deterministic dense mode with dbias over several batches: per-batch slices
+// of dbias in the workspace, summed in batch order afterwards.
+bool dbias_split(const Problem& p, const float* dbias) {
+  return !p.sparse && p.deterministic && p.B > 1 && dbias != nullptr;
+}
+
 bool use_tensor_cores(const Problem& p) {
   if (p.cuda_cores) return false;
   return p.sparse ? tc_sparse_supported(p) : tc_supported(p);
@@ -189,6 +195,12 @@ WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
     w.v16 = off;
     off = align_up(off + kbytes, 1024);
     w.staged = true;
+  }
+  if (!p.sparse && p.deterministic && p.B > 1) {
+    // per-batch dbias slices (used when dbias is requested)
+    off = align_up(off, 1024);
+    w.det_dbias = off;
+    off = align_up(off + (size_t)p.B * p.Hq * p.Sq * p.Sk * sizeof(float), 1024);
   }
   w.total = off;
   return w;
@@ -314,8 +326,13 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
     return w.staged ? reinterpret_cast<__half*>(ws + off) : nullptr;
   };
   const bool dense_staged = w.staged && !p.sparse;
+  // deterministic dbias over several batches: zero the per-batch slices
+  const bool split = dbias_split(p, dbias);
+  Problem pk = p;
+  pk.dbias_bstride = split ? (int64_t)p.Hq * p.Sq * p.Sk : 0;
+  float* dbias_zero = split ? reinterpret_cast<float*>(ws + w.det_dbias) : dbias;
   return cuda_status(launch_preprocess(
-      p, q, k, v, o, dO, delta, dbias, d_ori, d_cmp, dense_staged ? staged(w.q16) : nullptr,
+      pk, q, k, v, o, dO, delta, dbias_zero, d_ori, d_cmp, dense_staged ? staged(w.q16) : nullptr,
       dense_staged ? staged(w.k16) : nullptr, dense_staged ? staged(w.v16) : nullptr,
       dense_staged ? staged(w.do16) : nullptr, p.sparse ? sparse->ori_kv : nullptr,
       p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr,
@@ -380,44 +397,28 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
                                        sparse->ori_kv, sparse->cmp_kv, sparse->cmp_idx,
                                        sparse->d_ori_kv, sparse->d_cmp_kv, st, stream));
   }
-  // Deterministic dbias over several batches: one launch per batch (B = 1
-  // sub-problems on offset pointers), so that every dbias element receives its
-  // per-batch terms in batch order; within one batch each element has one
-  // writer. bias and dbias are shared by the batches.
-  const int n_launch = (p.deterministic && dbias != nullptr) ? p.B : 1;
-  // the per-batch launches offset pointers by whole sequences
-  if (p.varlen && n_launch > 1) return ATTN_ERR_UNSUPPORTED;
-  Problem pb = p;
-  if (n_launch > 1) pb.B = 1;
-  const int64_t rows_q = (int64_t)p.Hq * p.Sq, rows_k = (int64_t)p.Hk * p.Sk;
-  for (int b = 0; b < n_launch; ++b) {
-    const int64_t bq = b;  // 0 when there is a single launch
-    const float* lse_b = lse + bq * rows_q;
-    const float* delta_b = delta + bq * rows_q;
-    float* dq_b = dq + bq * rows_q * p.D;
-    float* dk_b = dk + bq * rows_k * p.D;
-    float* dv_b = dv + bq * rows_k * p.D;
-    cudaError_t e;
-    if (tc) {
-      // staged fp16 copies are head-major [B, H, tc_rows(S), D]
-      const int64_t sq16 = bq * p.Hq * tc_rows(p.Sq) * p.D, sk16 = bq * p.Hk * tc_rows(p.Sk) * p.D;
-      const __half* q16 = reinterpret_cast<const __half*>(ws + w.q16) + sq16;
-      const __half* k16 = reinterpret_cast<const __half*>(ws + w.k16) + sk16;
-      const __half* v16 = reinterpret_cast<const __half*>(ws + w.v16) + sk16;
-      const __half* do16 = reinterpret_cast<const __half*>(ws + w.do16) + sq16;
-      e = launch_bwd_tc(pb, q16, k16, v16, do16, lse_b, delta_b, bias, dq_b, dk_b, dv_b, dbias,
-                        st, stream);
-    } else {
-      // bf16 inputs: batch stride in elements, 2 bytes each
-      const char* qb = static_cast<const char*>(q) + bq * p.qs[0] * 2;
-      const char* kb = static_cast<const char*>(k) + bq * p.ks[0] * 2;
-      const char* vb = static_cast<const char*>(v) + bq * p.vs[0] * 2;
-      const char* dob = static_cast<const char*>(dO) + bq * p.dos[0] * 2;
-      e = launch_bwd_simt(pb, qb, kb, vb, dob, lse_b, delta_b, bias, dq_b, dk_b, dv_b, dbias,
-                          nullptr, nullptr, nullptr, nullptr, nullptr, st, stream);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
+  // Deterministic dbias over several batches: every batch adds its terms
+  // into its own zeroed slice of the workspace (one writer per element, so
+  // each slice holds exact values), and a second pass sums the slices in
+  // batch order into dbias.
+  const bool split = dbias_split(p, dbias);
+  float* dbias_acc = split ? reinterpret_cast<float*>(ws + w.det_dbias) : dbias;
+  Problem pk = p;
+  pk.dbias_bstride = split ? (int64_t)p.Hq * p.Sq * p.Sk : 0;
+  cudaError_t e;
+  if (tc) {
+    e = launch_bwd_tc(pk, reinterpret_cast<const __half*>(ws + w.q16),
+                      reinterpret_cast<const __half*>(ws + w.k16),
+                      reinterpret_cast<const __half*>(ws + w.v16),
+                      reinterpret_cast<const __half*>(ws + w.do16), lse, delta, bias, dq, dk, dv,
+                      dbias_acc, st, stream);
+  } else {
+    e = launch_bwd_simt(pk, q, k, v, dO, lse, delta, bias, dq, dk, dv, dbias_acc, nullptr,
+                        nullptr, nullptr, nullptr, nullptr, st, stream);
   }
+  if (e == cudaSuccess && split)
+    e = launch_sum_slices(dbias_acc, p.B, pk.dbias_bstride, dbias, stream);
+  if (e != cudaSuccess) return cuda_status(e);
   return ATTN_OK;
 }
 

@@ -122,6 +122,9 @@ struct Problem {
   const int32_t* cu_k;
   int total_q, total_k;
   bool varlen, br;
+  // > 0: dbias is accumulated into per-batch slices this many floats apart
+  // (deterministic mode, B > 1), summed in batch order afterwards
+  int64_t dbias_bstride;
   // sparse fields (cmp_ratio > 0 only in the CFA case: no index list, every
   // compressed row whose block ends at or before the query is selected)
   int n_ori, n_cmp, topk, ori_wl, ori_wr, cmp_ratio;

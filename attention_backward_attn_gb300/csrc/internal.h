@@ -25,6 +25,8 @@ struct WorkspaceLayout {
   size_t q16 = 0, k16 = 0, v16 = 0, do16 = 0, kv16 = 0;
   // deterministic sparse dKV (SparseDet below)
   size_t det_part = 0, det_rows = 0, det_meta = 0, det_slot = 0, det_mult = 0;
+  // deterministic dense dbias over several batches: B per-batch slices
+  size_t det_dbias = 0;
   size_t total = 0;
   bool staged = false;
 };
@@ -60,6 +62,11 @@ cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, co
                               __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
                               __half* kv16, float* dk_zero, float* dv_zero, float* dk,
                               float* dv, DevStatus* st, cudaStream_t stream);
+
+// out[e] = slices[0][e] + slices[1][e] + ... + slices[n - 1][e] (in that
+// order), slices `stride` floats apart, e < stride.
+cudaError_t launch_sum_slices(const float* slices, int n, int64_t stride, float* out,
+                              cudaStream_t stream);
 
 // dsinks[h] = -sum_{b, i} exp(sinks[h] - lse[b, h, i]) delta[b, h, i], one
 // CTA per head, fixed-order reduction.

@@ -338,7 +338,44 @@ dsinks_kernel(int B, int Hq, int Sq, const float* __restrict__ sinks,
   if (threadIdx.x == 0) dsinks[h] = (float)part[0];
 }
 
+// Deterministic sum of per-batch slices: each thread adds its elements over
+// the slices in slice order (4 at a time when the slices are 16-byte apart).
+__global__ void __launch_bounds__(256)
+sum_slices_kernel(const float* __restrict__ slices, int n, int64_t stride,
+                  float* __restrict__ out) {
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((stride & 3) == 0) {
+    for (int64_t e = t0; e < stride / 4; e += step) {
+      float4 acc = reinterpret_cast<const float4*>(slices)[e];
+      for (int b = 1; b < n; ++b) {
+        const float4 v = reinterpret_cast<const float4*>(slices + b * stride)[e];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      reinterpret_cast<float4*>(out)[e] = acc;
+    }
+  } else {
+    for (int64_t e = t0; e < stride; e += step) {
+      float acc = slices[e];
+      for (int b = 1; b < n; ++b) acc += slices[b * stride + e];
+      out[e] = acc;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sum_slices(const float* slices, int n, int64_t stride, float* out,
+                              cudaStream_t stream) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sum_slices_kernel<<<sms * 8, 256, 0, stream>>>(slices, n, stride, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dsinks(int B, int Hq, int Sq, const float* sinks, const float* lse,
                           const float* delta, float* dsinks, cudaStream_t stream) {
@@ -385,7 +422,9 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.kv_cmp_rows = kv16 && cmp_kv ? (int64_t)pr.n_cmp * pr.Hk : 0;
   p.kv16 = kv16;
   p.zero_a = dbias;
-  p.zero_na = dbias ? (int64_t)pr.Hq * pr.Sq * pr.Sk : 0;
+  p.zero_na = dbias ? (pr.dbias_bstride > 0 ? pr.B * pr.dbias_bstride
+                                             : (int64_t)pr.Hq * pr.Sq * pr.Sk)
+                    : 0;
   p.zero_b = d_ori;
   p.zero_nb = d_ori ? (int64_t)pr.n_ori * pr.Hk * pr.D : 0;
   p.zero_c = d_cmp;

@@ -176,7 +176,7 @@ bwd_dq_kernel(int B, int Hq, int Hk, int Sq, int Sk, float scale, MaskSpec mask,
               const bf16* __restrict__ v, const bf16* __restrict__ dO,
               const float* __restrict__ lse, const float* __restrict__ delta,
               const float* __restrict__ bias, float* __restrict__ dq,
-              float* __restrict__ dbias) {
+              float* __restrict__ dbias, int64_t dbias_bstride) {
   constexpr int EPL = D / 32;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -213,7 +213,7 @@ bwd_dq_kernel(int B, int Hq, int Hk, int Sq, int Sk, float scale, MaskSpec mask,
       const float ds = p * (dp - Dl);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ds, kv[e], acc[e]);
-      if (dbias && lane == 0) atomicAdd(dbias + brow + j, ds);
+      if (dbias && lane == 0) atomicAdd(dbias + b * dbias_bstride + brow + j, ds);
     };
     const int ns = min(mask.sink, Sk);
     for (int j = 0; j < ns; ++j) visit(j);
@@ -469,7 +469,7 @@ cudaError_t bwd_impl(const Problem& p, const void* q, const void* k, const void*
   if (qwarps > 0) {
     bwd_dq_kernel<D><<<blocks_for_warps(qwarps), block, 0, stream>>>(
         p.B, p.Hq, p.Hk, p.Sq, p.Sk, p.scale, p.mask, st, qb, kb, vb, dob, lse, delta, bias,
-        dq, dbias);
+        dq, dbias, p.dbias_bstride);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -139,6 +139,7 @@ struct TcParams {
   float* dk;
   float* dv;
   float* dbias;
+  int64_t dbias_bstride;  // > 0: batch b adds into its own dbias slice, b dbias_bstride floats on
   DevStatus* status;
 };
 
@@ -393,6 +394,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // TMEM, then dP(t+1) after dK(t) released those columns. The softmax of
       // tile t+1 overlaps dV(t), dK(t) and dP(t+1).
       bool ok = wait_bar(c, kKvFull, 0, 2);
+      int n_tiles = 0;  // tiles whose dK MMAs were issued
       QTileIter it(hpc, n0, sq);
       bool have = ok && it.next();
       if (have) {
@@ -448,6 +450,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         }
         ptx::mma_commit(c.bar(kQEmpty0 + st));
         ptx::mma_commit(c.bar(kMma4));
+        ++n_tiles;
         if (have && !s_done) {
           if (!wait_bar(c, kQFull0 + st1, qpar, 5)) break;
           ptx::tc_fence_after();
@@ -463,6 +466,16 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         ++t;
       }
       ptx::mma_commit(c.bar(kAccFull));
+      // The last dV / dK / Q-stage commits are waited by nobody else: wait
+      // for them here, so that no commit arrival is still in flight when the
+      // CTA exits (a late one would land on the barriers of the next CTA on
+      // this SM).
+      if (n_tiles > 0) {
+        drain_bar(c, kMma3, (n_tiles - 1) & 1);
+        drain_bar(c, kMma4, (n_tiles - 1) & 1);
+        drain_bar(c, kQEmpty0, (((n_tiles + 1) >> 1) - 1) & 1);
+        if (n_tiles > 1) drain_bar(c, kQEmpty0 + 1, ((n_tiles >> 1) - 1) & 1);
+      }
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -508,7 +521,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       const float* brow = nullptr;
       if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + jc;
       float* dbrow = nullptr;
-      if constexpr (DBIAS) dbrow = p.dbias + ((int64_t)h * p.Sq + m0) * p.Sk + j;
+      if constexpr (DBIAS)
+        dbrow = p.dbias + b * p.dbias_bstride + ((int64_t)h * p.Sq + m0) * p.Sk + j;
       const uint32_t ps_row = sDS + wg * kSlab + jl * 128;
       // phase 1: P^T from S^T as fp16 into shared memory, 128B-swizzled K-major
       // rows (one key row per thread; A operand of dV)
@@ -793,6 +807,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // one tile ahead, so the softmax computes P(t+1) while dQ(t) and
       // dP(t+1) are on the tensor pipe; only its dS half waits for dP.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
+      int n_tiles = 0;  // tiles whose dQ MMAs were issued
       KTileIter it(m0, sq);
       bool have = ok && it.next();
       bool have1 = false;
@@ -831,6 +846,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         }
         ptx::mma_commit(c.bar(qMma3));
         ptx::mma_commit(c.bar(qKvEmpty0 + st));
+        ++n_tiles;
         if (!have1) break;  // tile t was the last one
         ptx::tc_fence_after();
         issue_dP(t + 1);  // the softmax already read dP(t)
@@ -848,6 +864,12 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ++t;
       }
       ptx::mma_commit(c.bar(qAccFull));
+      // the last dQ / K-V-stage commits: waited here (see the key-major CTA)
+      if (n_tiles > 0) {
+        drain_bar(c, qMma3, (n_tiles - 1) & 1);
+        drain_bar(c, qKvEmpty0, (((n_tiles + 1) >> 1) - 1) & 1);
+        if (n_tiles > 1) drain_bar(c, qKvEmpty0 + 1, ((n_tiles >> 1) - 1) & 1);
+      }
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -1176,6 +1198,7 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dk = dk;
   p.dv = dv;
   p.dbias = dbias;
+  p.dbias_bstride = pr.dbias_bstride;
   p.status = st;
   const int q_ctas = pr.B * pr.Hq * (p.Sqs / BM);
   const int grid = p.kv_ctas + q_ctas;

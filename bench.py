@@ -314,8 +314,8 @@ def run_ours(args):
         launches_per_step = 2
         if args.deterministic and sparse:
             launches_per_step = 4  # + compressed-row slot table + ordered row sums
-        elif args.deterministic and w.want_dbias:
-            launches_per_step = 1 + w.B  # one backward launch per batch
+        elif args.deterministic and w.want_dbias and w.B > 1:
+            launches_per_step = 3  # + the batch-ordered sum of the per-batch dbias slices
     else:
         roof = {"bound": "alu", "achieved": flops / (mean_bwd_ms * 1e-3) / 1e12,
                 "peak": SIMT_FP32_PEAK_TFLOPS, "unit": "TFLOP/s"}

@@ -90,8 +90,8 @@ typedef struct attn_problem {
    *  - bias / dbias [Hq, Sq, Sk] are indexed by positions within the sequence;
    *  - a mask aligns per sequence (bottom-right uses that sequence's lengths).
    * The dense tensor-core path only: the sparse variant, D = 512,
-   * ATTN_FLAG_CUDA_CORES, attn_fwd_lse, attn_bwd_dsinks and deterministic
-   * dbias over several sequences return ATTN_ERR_UNSUPPORTED. cu_seqlens are
+   * ATTN_FLAG_CUDA_CORES, attn_fwd_lse and attn_bwd_dsinks return
+   * ATTN_ERR_UNSUPPORTED. cu_seqlens are
    * checked on the device: a sequence whose bounds are out of order or out
    * of range is skipped and ATTN_ERR_INVALID_ARG recorded in the status
    * record with detail = its index. (Ascend "sparse_flash_mla_grad" takes

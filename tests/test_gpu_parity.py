@@ -232,6 +232,24 @@ def test_varlen(name):
                                    atol=1e-5 * max(1.0, np.abs(want).max(initial=0.0)))
 
 
+def test_varlen_deterministic_dbias():
+    # per-sequence dbias slices summed in sequence order: bitwise repeatable
+    torch = _torch()
+    w = VARLEN["br_alibi_dbias_d64"]()
+    O_b, L_f = H.varlen_forward_inputs(w)
+    plan = H.gpu_varlen_plan(w, O_b, L_f, deterministic=True)
+    outs = []
+    for _ in range(2):
+        plan.run()
+        torch.cuda.synchronize()
+        assert plan.device_status()[0] == 0
+        outs.append(plan.dbias.clone())
+    assert torch.equal(outs[0], outs[1])
+    ref = H.varlen_reference(w, O_b, L_f)
+    H.check_close("dbias", plan.dbias.cpu().numpy(), ref["dbias"])
+    H.check_close("dq", plan.dq.cpu().numpy(), ref["dq"])
+
+
 def test_varlen_equal_lengths_match_the_fixed_length_run():
     # the same three sequences as a padded batch and as a packed one: the
     # same tiles in the same order, so bitwise-equal gradients (deterministic
@@ -271,7 +289,7 @@ def test_varlen_bad_bounds_are_reported():
 # Deterministic mode (ATTN_FLAG_DETERMINISTIC): bitwise-identical outputs over
 # repeated runs, and the usual oracle parity.
 DETERMINISTIC = {
-    # dbias over 3 batches on the tensor-core path: one launch per batch
+    # dbias over 3 batches on the tensor-core path: per-batch slices summed in order
     "alibi_dbias_s256_d64": (lambda: SMALL_DENSE["alibi_dbias_s256_d64"](), 1),
     # GQA 8:1 on two key tiles: by default each query head of a key tile gets its
     # own CTA and the 8 partial dK / dV sums are added in arrival order
@@ -304,6 +322,36 @@ def test_deterministic_mode(name):
         for a, b in zip(runs[0], later):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     _compare_dense(w, plan, O_b, L_f)
+
+
+def test_deterministic_dbias_graph_replay_full_size():
+    # per-batch dbias slices summed in batch order, captured in a CUDA graph
+    # and replayed as the benchmark does: every replay gives the same bits
+    torch = _torch()
+    w = make_workload("mha_alibi_dbias_s2048_d64")
+    up = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda().to(torch.bfloat16)
+    import attention_backward_attn_gb300 as ab
+    q, k, v, do = (up(x) for x in (w.q, w.k, w.v, w.do))
+    bias = torch.from_numpy(w.bias).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+    ab.attn_fwd_lse(ab.problem_from(q, k, v, o, do, w.scale), None, None, q, k, v, bias, o, lse)
+    plan = ab.BackwardPlan(q, k, v, o, do, lse, w.scale, bias=bias, want_dbias=True,
+                           deterministic=True)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+    ref = [t.clone() for t in (plan.dq, plan.dk, plan.dbias)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.run()
+    for _ in range(5):
+        g.replay()
+        torch.cuda.synchronize()
+        assert plan.device_status()[0] == 0
+        for a, b in zip(ref, (plan.dq, plan.dk, plan.dbias)):
+            assert torch.equal(a, b)
 
 
 def test_head_split_needs_the_prepared_dk_dv():
