@@ -365,8 +365,8 @@ def run_ours(args):
 # scaled by the token count: its DRAM bytes are Q, dO and dQ, all linear in Sq). An entry
 # goes back to None when its kernel changes.
 NCU_TRAFFIC = {
-    "gqa4_causal_s1024_d128": None,
-    "sparse_scfa_s4096_h64_d512": None,
+    "gqa4_causal_s1024_d128": 29.718e6,
+    "sparse_scfa_s4096_h64_d512": 4 * 224.48e6,
 }
 
 # CUDA-core fp32 FMA rate for the SIMT fallback's roofline: 152 SMs x 128
