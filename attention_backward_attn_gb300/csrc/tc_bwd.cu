@@ -112,10 +112,13 @@ constexpr int smem_total() {
 enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kP1Full = 6, kAccFull = 7,
              kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kKvBars = 12 };
 // barrier indices, query-major CTA
-// qSFull / qdPFull: S / dP of the tile in TMEM; qDsFull: dS written over S
-// (256 arrivals; dP read); qMma3: dQ of the tile done (its S buffer free).
-enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull = 5, qDsFull = 6, qAccFull = 7,
-            qMma3 = 8, qdPFull = 9, kQBars = 10 };
+// qSFull0 / qSFull1: S of the tile in TMEM buffer 0 / 1 (one barrier per
+// buffer: S(t+2) may complete before the softmax has polled for S(t+1), and
+// on a shared barrier that second phase would hide the first); qdPFull: dP of
+// the tile in TMEM; qDsFull: dS written over S (256 arrivals; dP read);
+// qMma3: dQ of the tile done (its S buffer free).
+enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull0 = 5, qDsFull = 6, qAccFull = 7,
+            qMma3 = 8, qdPFull = 9, qSFull1 = 10, kQBars = 11 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
@@ -729,7 +732,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1};
+  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1, 1};
   init_common(c, sbase + L::MISC, kQBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   // TMEM: [0, D) dQ, then S buffers 0 / 1 and dP (128 columns each)
@@ -816,7 +819,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         if (have) {
           ptx::tc_fence_after();
           issue_S(0);
-          ptx::mma_commit(c.bar(qSFull));
+          ptx::mma_commit(c.bar(qSFull0));
           issue_dP(0);
           ptx::mma_commit(c.bar(qdPFull));
           have1 = it.next();
@@ -825,7 +828,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
             if (have1) {
               ptx::tc_fence_after();
               issue_S(1);
-              ptx::mma_commit(c.bar(qSFull));
+              ptx::mma_commit(c.bar(qSFull1));
             }
           }
         }
@@ -858,7 +861,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
           if (!wait_bar(c, qMma3, t & 1, 25)) break;
           ptx::tc_fence_after();
           issue_S(t + 2);
-          ptx::mma_commit(c.bar(qSFull));
+          ptx::mma_commit(c.bar(st == 0 ? qSFull0 : qSFull1));
         }
         have1 = have2;
         ++t;
@@ -890,7 +893,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     int t = 0;
     bool ok = true;
     while (it.next()) {
-      if (!wait_bar(c, qSFull, t & 1, 27)) { ok = false; break; }
+      if (!wait_bar(c, (t & 1) ? qSFull1 : qSFull0, (t >> 1) & 1, 27)) { ok = false; break; }
       ptx::tc_fence_after();
       const int n0 = it.nt * BN;
       const bool partial = kMayBeRagged ? tile_cut(sq, m0, n0)
