@@ -279,6 +279,7 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
     if (!need(k, n.k) || !need(v, n.k) || !aligned16(k) || !aligned16(v))
       return ATTN_ERR_INVALID_ARG;
   }
+  if (fwd_tc_supported(p)) return cuda_status(launch_fwd_tc(p, q, k, v, bias, o, lse, stream));
   // Device conditions of the forward (bad sparse indices) are skipped but not
   // recorded: the forward has no workspace.
   return cuda_status(launch_fwd_simt(p, q, k, v, bias, sparse ? sparse->ori_kv : nullptr,

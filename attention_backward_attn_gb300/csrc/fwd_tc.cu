@@ -1,0 +1,449 @@
+// Tensor-core forward with log-sum-exp (the inputs O, LSE of the backward).
+//
+// O = softmax(scale Q K^T + bias, masked) V and LSE = natural log-sum-exp of
+// the masked logits (CK "34_bwd_gqa_fmha.py" cpu_fwd_with_intermediates, CK
+// "28_backward_dbias_fmha.py" cpu_attention_fwd_bias, CK
+// "22_sink_tokens_fmha.py" masked CPU forward), for dense problems with
+// D in {64, 128} whose q / k / v rows are packed over (batch, position).
+//
+// One CTA per (batch, query head, 128-row query tile), two passes over the
+// live key tiles of the mask:
+//   pass 1  S = Q K^T into TMEM; the softmax warps keep each row's running
+//           maximum and sum of exponentials and end with the row's LSE;
+//   pass 2  S again; P = exp(S - LSE) is exact (no rescaling of O), written
+//           as bf16 over S in TMEM, and O += P V accumulates in TMEM.
+// The second S costs one extra MMA per tile (3 instead of 2) and saves the
+// running rescale of the O accumulator. Operands are the caller's bf16 rows,
+// loaded by TMA through 3-D tensor maps (d, head, batch * position); P is
+// rounded to bf16 for its MMA (O is stored as bf16).
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 4-7 / 8-11 two softmax warpgroups (key columns 0-63 / 64-127
+// of a tile; thread = query row), which also write O. Every mbarrier wait is
+// bounded (the CTA gives up after ~2 s and exits; the forward has no status
+// record to report into).
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+#include "tc_util.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // key rows per tile
+constexpr int kFwdThreads = 384;
+constexpr int kFSlab = 128 * 128;  // [128 rows][64 bf16] 128B-swizzled slab, bytes
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTile = (D / 64) * kFSlab;
+  static constexpr int Q = 0;
+  static constexpr int K = Q + kTile;       // 2 stages
+  static constexpr int V = K + 2 * kTile;   // 2 stages
+  static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] (max, sum)
+  static constexpr int BAR = STAT + 2 * 128 * 8;
+  static constexpr int MISC = BAR + 128;      // TMEM base, abort flag
+  static constexpr int TOTAL = MISC + 16;
+};
+
+// fQFull: Q landed. fKvFull / fKvEmpty: key-tile stage (K, plus V in pass 2).
+// fSFull: S of a step in TMEM buffer 0 / 1. fSRead: pass-1 S read (256
+// arrivals). fPFull: pass-2 P written over S (256 arrivals). fPvDone: the
+// P V MMAs of a step completed. fOFull: every MMA completed.
+enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fSRead0 = 7, fPFull0 = 9,
+              fPvDone0 = 11, fOFull = 13, kFwdBars = 14 };
+
+struct FwdParams {
+  int B, Hq, Hk, Sq, Sk;
+  float scale_log2;
+  MaskSpec mask;
+  const float* bias;  // [Hq, Sq, Sk] or nullptr
+  __nv_bfloat16* o;
+  int64_t os0, os1, os2;
+  float* lse;  // [B, Hq, Sq]
+};
+
+constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  // kind::f16 with A and B of type bf16 (format 1 in the A / B type fields)
+  return ptx::idesc_f16_f32(M, N, a_mn, b_mn) | (1u << 7) | (1u << 10);
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ int imin2(int a, int b) { return a < b ? a : b; }
+
+// The k-th live key tile of a query tile (sink tiles, then the window range).
+struct KeyTiles {
+  int s_end, w_first, count;
+  __device__ KeyTiles(const FwdParams& p, int m0) {
+    int w_lo, w_hi;
+    live_key_tiles(p.mask, p.Sq, p.Sk, kBM, kBN, m0, &s_end, &w_lo, &w_hi);
+    w_first = w_lo > s_end ? w_lo : s_end;
+    count = s_end + (w_hi >= w_first ? w_hi - w_first + 1 : 0);
+  }
+  __device__ int tile(int k) const { return k < s_end ? k : w_first + (k - s_end); }
+};
+
+// Phase index of the use of S buffer bf by pass-2 step u (steps T.. 2T-1;
+// buffer bf = step parity): the count of earlier pass-2 steps of that parity.
+__device__ __forceinline__ int pass2_use(int u, int T) {
+  const int first = (T & 1) == (u & 1) ? T : T + 1;
+  return (u - first) >> 1;
+}
+
+template <int D, bool BIAS>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_u32(smem);
+  if (sbase & 1023u) return;  // 128B-swizzle atoms need 1 KiB alignment (uniform over the grid)
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nmt = (p.Sq + kBM - 1) / kBM;
+  const int bh = (int)blockIdx.x % (p.B * p.Hq);
+  const int mt = nmt - 1 - (int)blockIdx.x / (p.B * p.Hq);  // later query tiles first
+  const int h = bh % p.Hq;
+  const int b = bh / p.Hq;
+  const int g = h / (p.Hq / p.Hk);
+  const int m0 = mt * kBM;
+  const KeyTiles tiles(p, m0);
+  const int T = tiles.count;
+
+  Ctx c;
+  c.bars = sbase + L::BAR;
+  c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+  c.status = nullptr;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kFwdBars; ++i) {
+      const bool many = (i >= fSRead0 && i < fPvDone0);  // SRead / PFull: 256 arrivals
+      ptx::mbar_init(c.bar(i), many ? 256u : 1u);
+    }
+    *c.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + L::MISC, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
+  const uint32_t t_O = tmem;          // [0, D): O accumulator
+  const uint32_t t_S0 = tmem + 128;   // S buffers 0 / 1 (128 columns each)
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      const int qrow = b * p.Sq + m0;
+      ptx::mbar_arrive_expect_tx(c.bar(fQFull), L::kTile);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf)
+        ptx::tma_load_3d(sbase + L::Q + hf * kFSlab, &tmQ, c.bar(fQFull), hf * 64, h, qrow);
+      int issued[2] = {0, 0};
+      for (int u = 0; u < 2 * T; ++u) {
+        const int st = u & 1, use = u >> 1;
+        if (use > 0 && !wait_bar(c, fKvEmpty0 + st, (use - 1) & 1, 1)) break;
+        const bool pass2 = u >= T;
+        const int krow = b * p.Sk + tiles.tile(pass2 ? u - T : u) * kBN;
+        const uint32_t full = c.bar(fKvFull0 + st);
+        ptx::mbar_arrive_expect_tx(full, (pass2 ? 2 : 1) * L::kTile);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          ptx::tma_load_3d(sbase + L::K + st * L::kTile + hf * kFSlab, &tmK, full, hf * 64, g,
+                           krow);
+          if (pass2)
+            ptx::tma_load_3d(sbase + L::V + st * L::kTile + hf * kFSlab, &tmV, full, hf * 64, g,
+                             krow);
+        }
+        issued[st] = use + 1;
+      }
+      // no copy may still be landing in shared memory when the CTA ends
+      drain_bar(c, fQFull, 0);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] > 0) drain_bar(c, fKvFull0 + st, (issued[st] - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t id_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_O = idesc_bf16(128, D, false, true);
+      const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t dK = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
+      const uint64_t dVmn = ptx::smem_desc_sw128(sbase + L::V, kFSlab, 1024);
+      int n_kv[2] = {0, 0}, n_pv[2] = {0, 0};
+      // O += P V of pass-2 step v once P replaced S(v) in TMEM
+      auto issue_pv = [&](int v) -> bool {
+        const int sv = v & 1;
+        if (!wait_bar(c, fPFull0 + sv, pass2_use(v, T) & 1, 6)) return false;
+        ptx::tc_fence_after();
+        const uint32_t t_S = t_S0 + sv * 128;
+        const uint64_t dv = ptx::desc_add(dVmn, sv * L::kTile);
+#pragma unroll
+        for (int s = 0; s < kBN / 16; ++s) {
+          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_O, a_col, ptx::desc_add(dv, s * 2048), id_O, (v > T || s > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(c.bar(fKvEmpty0 + sv));  // K and V of the step read
+        ptx::mma_commit(c.bar(fPvDone0 + sv));   // its S buffer free again
+        ++n_kv[sv];
+        ++n_pv[sv];
+        return true;
+      };
+      // S(u) goes first, then the P V of the previous pass-2 step (its P is
+      // being written while S(u) runs)
+      bool ok = T == 0 || wait_bar(c, fQFull, 0, 2);
+      int pending = -1;
+      for (int u = 0; ok && u < 2 * T; ++u) {
+        const int st = u & 1, use = u >> 1;
+        if (!wait_bar(c, fKvFull0 + st, use & 1, 3)) break;
+        // the S buffer of step u - 2 must be free: read (pass 1) or consumed
+        // by its P V MMAs (pass 2, issued in the previous iteration)
+        if (u >= 2) {
+          const bool was_pass2 = u - 2 >= T;
+          const bool freed = was_pass2
+                                 ? wait_bar(c, fPvDone0 + st, pass2_use(u - 2, T) & 1, 4)
+                                 : wait_bar(c, fSRead0 + st, ((u - 2) >> 1) & 1, 5);
+          if (!freed) break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t t_S = t_S0 + st * 128;
+        const uint64_t dk = ptx::desc_add(dK, st * L::kTile);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kFSlab + (s & 3) * 32;
+          ptx::mma_ss(t_S, ptx::desc_add(dQ, off), ptx::desc_add(dk, off), id_S, s > 0);
+        }
+        ptx::mma_commit(c.bar(fSFull0 + st));
+        if (u < T) {
+          ptx::mma_commit(c.bar(fKvEmpty0 + st));  // K read: the stage is free again
+          ++n_kv[st];
+        }
+        if (pending >= 0 && !issue_pv(pending)) break;
+        pending = u >= T ? u : -1;
+      }
+      if (pending >= 0) issue_pv(pending);
+      ptx::mma_commit(c.bar(fOFull));
+      // commit arrivals no other role waits for: waited here before the CTA exits
+      for (int st = 0; st < 2; ++st) {
+        if (n_kv[st] > 0) drain_bar(c, fKvEmpty0 + st, (n_kv[st] - 1) & 1);
+        if (n_pv[st] > 0) drain_bar(c, fPvDone0 + st, (n_pv[st] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ----------------------------------------------- softmax warpgroups --
+    const int wg = (warp - 4) >> 2;  // key columns [64 wg, 64 wg + 64) of a tile
+    const int lg = warp & 3;
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int il = lg * 32 + lane;  // query row within the tile
+    const int i = m0 + il;
+    const bool row_in = i < p.Sq;
+    const int ic = row_in ? i : p.Sq - 1;
+    const float* brow = nullptr;
+    if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
+    // log2-domain logits of this thread's 64 keys of step u's tile (dead: -inf)
+    auto logits = [&](int u, float* x) -> bool {
+      const int st = u & 1;
+      if (!wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10)) return false;
+      ptx::tc_fence_after();
+      uint32_t sr[64];
+      const uint32_t t_S = t_S0 + st * 128 + lane_off + wg * 64;
+      ptx::tmem_ld32(t_S, sr);
+      ptx::tmem_ld32(t_S + 32, sr + 32);
+      ptx::tmem_wait_ld();
+      const int n0 = tiles.tile(u < T ? u : u - T) * kBN;
+      const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
+      const bool partial = m0 + kBM > p.Sq || n0 + kBN > p.Sk ||
+                           !tile_full(p.mask, m0, m0 + kBM, n0, n0 + kBN);
+      int klo = 0, khi = kBN - 1, ksink = 0;
+      if (partial) {
+        klo = i - p.mask.wl - n0;
+        khi = imin2(i + p.mask.wr - n0, kcap - 1);
+        ksink = imin2(p.mask.sink - n0, kcap);
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const int kk = wg * 64 + e;  // key within the tile
+        float xv = __uint_as_float(sr[e]) * p.scale_log2;
+        if constexpr (BIAS) xv = fmaf(__ldg(brow + n0 + imin2(kk, kcap - 1)), kLog2e, xv);
+        const bool live = !partial || (kk >= klo && kk <= khi) || kk < ksink;
+        x[e] = live ? xv : -INFINITY;
+      }
+      return true;
+    };
+    bool ok = true;
+    // pass 1: running maximum and sum of 2^x per row half
+    float m = -INFINITY, l = 0.f;
+    for (int u = 0; u < T; ++u) {
+      float x[64];
+      if (!logits(u, x)) { ok = false; break; }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(fSRead0 + (u & 1)));
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
+      const float mn = fmaxf(m, mx);
+      if (mn != -INFINITY) {
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sum += ptx::ex2(x[e] - mn);
+        l = (m == -INFINITY ? 0.f : l * ptx::ex2(m - mn)) + sum;
+        m = mn;
+      }
+    }
+    // the two halves of a row meet in shared memory
+    float* stat = reinterpret_cast<float*>(smem + L::STAT);
+    stat[(wg * 128 + il) * 2] = m;
+    stat[(wg * 128 + il) * 2 + 1] = l;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float m_o = stat[((1 - wg) * 128 + il) * 2];
+    const float l_o = stat[((1 - wg) * 128 + il) * 2 + 1];
+    const float mm = fmaxf(m, m_o);
+    float lsum = 0.f;
+    if (m != -INFINITY) lsum += l * ptx::ex2(m - mm);
+    if (m_o != -INFINITY) lsum += l_o * ptx::ex2(m_o - mm);
+    const float lse2 = lsum > 0.f ? mm + log2f(lsum) : -INFINITY;  // log2 domain
+    if (wg == 0 && row_in)
+      p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = lse2 == -INFINITY ? -INFINITY : lse2 / kLog2e;
+    // pass 2: P = 2^(x - LSE2) as bf16 over S
+    for (int u = T; ok && u < 2 * T; ++u) {
+      float x[64];
+      if (!logits(u, x)) { ok = false; break; }
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        const float p0 = lse2 == -INFINITY ? 0.f : ptx::ex2(x[e] - lse2);
+        const float p1 = lse2 == -INFINITY ? 0.f : ptx::ex2(x[e + 1] - lse2);
+        pk[e / 2] = pack_bf162(p0, p1);
+      }
+      const uint32_t t_S = t_S0 + (u & 1) * 128 + lane_off + wg * 64;
+      ptx::tmem_st16(t_S, pk);
+      ptx::tmem_st16(t_S + 16, pk + 16);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(fPFull0 + (u & 1)));
+    }
+    // O: this warpgroup writes columns [wg D/2, wg D/2 + D/2) of its row
+    if (ok && (T == 0 || wait_bar(c, fOFull, 0, 11))) {
+      ptx::tc_fence_after();
+      __nv_bfloat16* orow = p.o + b * p.os0 + (int64_t)ic * p.os1 + h * p.os2 + wg * (D / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t v[32];
+        if (T > 0) {
+          ptx::tmem_ld32(t_O + lane_off + wg * (D / 2) + cc * 32, v);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (row_in) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack_bf162(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            w.y = pack_bf162(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            w.z = pack_bf162(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+            w.w = pack_bf162(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+            *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
+          }
+        }
+      }
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (lane == 0) drain_bar(c, fOFull, 0);
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// [rows][H][D] bf16 with element strides (row, head): 3-D map (d, head, row),
+// boxes of 64 d x 1 head x 128 rows, 128B swizzle.
+bool make_map3(CUtensorMap* m, const void* base, int64_t rows, int H, int D, int64_t s_row,
+               int64_t s_head) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)s_head * 2, (cuuint64_t)s_row * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool BIAS>
+cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const FwdParams& p, int grid, cudaStream_t stream) {
+  auto kern = attn_fwd_tc_kernel<D, BIAS>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FwdSmem<D>::TOTAL);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<grid, kFwdThreads, FwdSmem<D>::TOTAL, stream>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fwd_tc_supported(const Problem& p) {
+  // rows of one head must be evenly spaced over (batch, position): the tensor
+  // maps view q / k / v as [batch * position][head][d]
+  const bool packed_q = p.B == 1 || p.qs[0] == (int64_t)p.Sq * p.qs[1];
+  const bool packed_k = p.B == 1 || (p.ks[0] == (int64_t)p.Sk * p.ks[1] &&
+                                     p.vs[0] == (int64_t)p.Sk * p.vs[1]);
+  return !p.sparse && !p.varlen && !p.cuda_cores && (p.D == 64 || p.D == 128) && p.B > 0 &&
+         p.Sq > 0 && p.Sk > 0 && packed_q && packed_k && p.qs[1] > 0 && p.ks[1] > 0 &&
+         p.vs[1] > 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_fwd_tc(const Problem& pr, const void* q, const void* k, const void* v,
+                          const float* bias, void* o, float* lse, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map3(&mq, q, (int64_t)pr.B * pr.Sq, pr.Hq, pr.D, pr.qs[1], pr.qs[2]) ||
+      !make_map3(&mk, k, (int64_t)pr.B * pr.Sk, pr.Hk, pr.D, pr.ks[1], pr.ks[2]) ||
+      !make_map3(&mv, v, (int64_t)pr.B * pr.Sk, pr.Hk, pr.D, pr.vs[1], pr.vs[2]))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.B = pr.B;
+  p.Hq = pr.Hq;
+  p.Hk = pr.Hk;
+  p.Sq = pr.Sq;
+  p.Sk = pr.Sk;
+  p.scale_log2 = pr.scale * kLog2e;
+  p.mask = pr.mask;
+  p.bias = bias;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.os0 = pr.os[0];
+  p.os1 = pr.os[1];
+  p.os2 = pr.os[2];
+  p.lse = lse;
+  const int grid = pr.B * pr.Hq * ((pr.Sq + kBM - 1) / kBM);
+  if (pr.D == 64)
+    return bias ? launch_fwd_variant<64, true>(mq, mk, mv, p, grid, stream)
+                : launch_fwd_variant<64, false>(mq, mk, mv, p, grid, stream);
+  return bias ? launch_fwd_variant<128, true>(mq, mk, mv, p, grid, stream)
+              : launch_fwd_variant<128, false>(mq, mk, mv, p, grid, stream);
+}
+
+}  // namespace attn

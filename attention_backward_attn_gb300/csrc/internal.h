@@ -83,6 +83,14 @@ cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16
                           const float* delta, const float* bias, float* dq, float* dk,
                           float* dv, float* dbias, DevStatus* st, cudaStream_t stream);
 
+// ---- fwd_tc.cu ----
+// Dense forward on the tensor cores (D in {64, 128}, q / k / v rows evenly
+// spaced over batch and position); attn_fwd_lse falls back to the SIMT
+// forward otherwise.
+bool fwd_tc_supported(const Problem& p);
+cudaError_t launch_fwd_tc(const Problem& p, const void* q, const void* k, const void* v,
+                          const float* bias, void* o, float* lse, cudaStream_t stream);
+
 // ---- tc_sparse.cu ----
 // Deterministic sparse dKV: the tensor-core kernel stores every item's
 // (item = token Hk + KV head) dKV rows at their slots in `part`

@@ -178,7 +178,14 @@ typedef struct attn_sparse {
  * ("34_bwd_gqa_fmha.py" cpu_fwd_with_intermediates, "28_backward_dbias_fmha.py"
  * cpu_attention_fwd_bias, "22_sink_tokens_fmha.py" cpu_attention_fwd_masked).
  * Writes o (bf16, o_stride layout) and lse (fp32 [B, Hq, Sq], natural log).
- * sparse != NULL selects the sparse variant (k, v, bias must then be NULL). */
+ * sparse != NULL selects the sparse variant (k, v, bias must then be NULL).
+ * Dense problems with D in {64, 128} whose q / k / v rows are evenly spaced
+ * over (batch, position) (stride[0] == S * stride[1], or B == 1) run on the
+ * tensor cores: bf16 operands, two passes over the live key tiles (row
+ * statistics, then O with the exact probabilities), P rounded to bf16 for
+ * its MMA; LSE is computed in fp32 from the exact logits. Other shapes, and
+ * ATTN_FLAG_CUDA_CORES, run the fp32 CUDA-core forward. A variable-length
+ * batch returns ATTN_ERR_UNSUPPORTED. */
 attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
                            const attn_sparse_t* sparse,
                            const void* q, const void* k, const void* v,
