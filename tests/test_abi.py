@@ -180,6 +180,21 @@ def test_problem_flags(ab):
     assert ab.attn_bwd_path(p, None, None) == 0
 
 
+def test_deterministic_workspace_holds_the_dbias_slices(ab):
+    # deterministic mode with B > 1 reserves one dbias slice per batch
+    # (B * Hq * Sq * Sk floats) on top of the default workspace
+    p = _prob(ab, B=3, Hq=4, Hk=2, Sq=200, Sk=136, D=64)
+    base = ab.attn_bwd_workspace_size(p)
+    p.flags = ab.ATTN_FLAG_DETERMINISTIC
+    det = ab.attn_bwd_workspace_size(p)
+    assert det >= base + 3 * 4 * 200 * 136 * 4
+    # a single batch needs no slices
+    p1 = _prob(ab, B=1, Hq=4, Hk=2, Sq=200, Sk=136, D=64)
+    base1 = ab.attn_bwd_workspace_size(p1)
+    p1.flags = ab.ATTN_FLAG_DETERMINISTIC
+    assert ab.attn_bwd_workspace_size(p1) == base1
+
+
 def test_varlen_descriptor_validation(ab):
     fake = 1 << 20  # never dereferenced: host validation only
     p = _prob(ab, B=3, Sq=300, Sk=300)
