@@ -299,6 +299,10 @@ DETERMINISTIC = {
     "ragged_alibi_dbias_s200_d64": (lambda: make_dense("detr", 26, B=3, Hq=2, Hk=2, Sq=200,
                                                        Sk=200, D=64, alibi=True,
                                                        want_dbias=True), 1),
+    # the same on the SIMT kernels (ATTN_FLAG_CUDA_CORES): per-batch dbias slices too
+    "simt_alibi_dbias_s200_d64": (lambda: make_dense("dets", 27, B=3, Hq=2, Hk=2, Sq=200,
+                                                     Sk=200, D=64, alibi=True,
+                                                     want_dbias=True), 2),
 }
 
 
@@ -308,7 +312,7 @@ def test_deterministic_mode(name):
     make, path = DETERMINISTIC[name]
     w = make()
     O_b, L_f, _, _ = H.dense_forward_inputs(w)
-    plan = H.gpu_dense_plan(w, O_b, L_f, deterministic=True)
+    plan = H.gpu_dense_plan(w, O_b, L_f, deterministic=True, cuda_cores=(path == 2))
     assert plan.path == path
     runs = []
     for _ in range(3):
