@@ -193,21 +193,26 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
                            cudaStream_t stream);
 
 /* Bytes of device workspace that attn_bwd_preprocess and attn_bwd need for
- * this problem (a status record plus fp16 staging of the operands of the
- * tensor-core path). Returns 0 if the arguments are invalid. */
+ * this problem: a status record, the fp16 staging of the operands of the
+ * tensor-core path (lengths rounded up to whole 128-row tiles), and with
+ * ATTN_FLAG_DETERMINISTIC the per-batch dbias slices (dense, B > 1) or the
+ * per-slot dKV rows (sparse). Returns 0 if the arguments are invalid. */
 size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
                                const attn_sparse_t* sparse);
 
 /* Backward pre-pass ("34_bwd_gqa_fmha.py" cpu_bwd_gqa: D = rowsum(dO * O);
  * Ascend formula phase 2: SoftmaxGrad(dO, O)):
  *  - delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d] in fp32;
- *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL), for
- *    the sparse variant sparse->d_ori_kv / d_cmp_kv, and dk / dv when the
- *    tensor-core path splits a KV head's query-head group over several CTAs
- *    that add their partial sums (small problems);
+ *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL; in
+ *    the deterministic mode with B > 1, the per-batch dbias slices of the
+ *    workspace instead, which attn_bwd then sums into dbias), for the sparse
+ *    variant sparse->d_ori_kv / d_cmp_kv, and dk / dv when the tensor-core
+ *    path splits a KV head's query-head group over several CTAs that add
+ *    their partial sums (small problems);
  *  - clears the workspace status record;
  *  - when attn_bwd will take the tensor-core path, writes fp16 copies of q,
- *    k, v and dO into the workspace (head-major [B, H, S, D] rows) for it.
+ *    k, v and dO into the workspace (head-major rows, each head's length
+ *    rounded up to whole 128-row tiles with zero rows) for it.
  *    Every bf16 value of magnitude in [2^-14, 65504] converts exactly; a
  *    larger one is recorded as ATTN_ERR_RANGE.
  * q, k, v, dbias, dk and dv are the same tensors later passed to attn_bwd
