@@ -25,8 +25,9 @@
 //         phase 2: dS^T = P^T (dP^T - D), fp16 into TMEM over dP^T (A of MMA4)
 //   MMA3  dV += P^T dO       (A = P^T K-major, B = dO MN-major)
 //   MMA4  dK += dS^T Q       (A = dS^T in TMEM, B = Q MN-major)
-// Issue order dV(t), S(t+1), dK(t), dP(t+1): phase 1 of the next tile runs
-// while dK(t) and dP(t+1) are on the tensor pipe.
+// Issue order S(t+1) (as soon as the softmax has read S^T(t) and the next
+// Q / dO stage has landed), dV(t), dK(t), dP(t+1): phase 1 of the next tile
+// runs while dV(t), dK(t) and dP(t+1) are on the tensor pipe.
 //
 // Query-major CTAs (dQ): one CTA per (batch, query head, 128-row query tile)
 // loops over the live key tiles of its KV head, recomputing S and dP:
@@ -37,6 +38,13 @@
 // dQ accumulates in TMEM over all key tiles and is written once: no atomics
 // and no zero-filled accumulation buffer. S is double-buffered so that the
 // next tile's MMA1' runs during this tile's softmax.
+//
+// Lengths need not be whole tiles: the pre-pass stages every head's rows
+// rounded up to 128 with zero rows past the length, a tile that crosses a
+// length takes the per-element mask, and rows past the lengths are not
+// stored. A variable-length batch gives every CTA its sequence's bounds,
+// output rows and mask alignment (Seq). Live tiles come from closed-form
+// ranges (mask.h), so the walk never visits a dead tile.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 4-7 and 8-11 two softmax warpgroups (columns 0-63 / 64-127 of
