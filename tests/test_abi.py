@@ -260,3 +260,28 @@ def test_tile_classes_match_oracle_mask(ab, spec):
             tile = m[mt * tq:(mt + 1) * tq, nt * tk:(nt + 1) * tk]
             expect = 0 if not tile.any() else (2 if tile.all() else 1)
             assert cls == expect, (mt, nt, cls, expect)
+
+
+def test_tile_classes_random_masks(ab):
+    # 300 random (lengths, window, sinks, alignment, tile) draws against the
+    # oracle's element mask, vectorised per draw
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(123)
+    for _ in range(300):
+        Sq, Sk = (int(x) for x in rng.integers(1, 300, size=2))
+        wl = int(rng.choice([-1, int(rng.integers(0, 200))]))
+        wr = int(rng.choice([-1, int(rng.integers(0, 200))]))
+        ns = int(rng.choice([0, int(rng.integers(0, 40))]))
+        br = int(rng.integers(0, 2))
+        tq, tk = (int(rng.choice([8, 16, 32, 64, 128])) for _ in range(2))
+        m = oracle.live_mask(Sq, Sk, wl, wr, ns, bottom_right=bool(br))
+        got = np.asarray(ab.attn_mask_tile_classes(ab.Mask(wl, wr, ns, br), Sq, Sk, tq, tk))
+        nmt, nnt = -(-Sq // tq), -(-Sk // tk)
+        pad = np.zeros((nmt * tq, nnt * tk), dtype=np.int8)
+        pad[:Sq, :Sk] = m
+        cnt = pad.reshape(nmt, tq, nnt, tk).sum(axis=(1, 3))
+        rows = np.minimum(tq, Sq - np.arange(nmt) * tq)[:, None]
+        cols = np.minimum(tk, Sk - np.arange(nnt) * tk)[None, :]
+        expect = np.where(cnt == 0, 0, np.where(cnt == rows * cols, 2, 1))
+        assert np.array_equal(got, expect), (Sq, Sk, wl, wr, ns, br, tq, tk)
