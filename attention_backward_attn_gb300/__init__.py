@@ -21,7 +21,8 @@ __all__ = [
     "ATTN_FLAG_CUDA_CORES",
     "attn_fwd_lse", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_workspace_size",
     "attn_read_device_status", "attn_bwd_path", "attn_bwd_noalloc", "BackwardPlan",
-    "attn_bwd_dsinks",
+    "attn_bwd_dsinks", "attn_mask_tile_classes", "attn_debug_mask_live",
+    "attn_debug_sparse_rows",
 ]
 
 ATTN_OK = 0
@@ -100,6 +101,11 @@ def _load():
     L.attn_mask_tile_classes.argtypes = [P(Mask), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, vp]
     L.attn_mask_tile_classes.restype = st
+    L.attn_debug_mask_live.argtypes = [P(Mask), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       vp, vp, vp, vp]
+    L.attn_debug_mask_live.restype = st
+    L.attn_debug_sparse_rows.argtypes = [P(Problem), P(Sparse), vp, vp, ctypes.c_int32, vp]
+    L.attn_debug_sparse_rows.restype = st
     return L
 
 
@@ -284,6 +290,25 @@ def attn_mask_tile_classes(mask: Optional[Mask], Sq: int, Sk: int, tile_q: int =
     _check(lib.attn_mask_tile_classes(_ref(mask), Sq, Sk, tile_q, tile_k, buf),
            "attn_mask_tile_classes")
     return [[buf[m * nnt + n] for n in range(nnt)] for m in range(nmt)]
+
+
+def attn_debug_mask_live(mask: Optional[Mask], Sq: int, Sk: int, aligned_variant: int,
+                         kv_live, q_live, outside, stream=None):
+    """Per-element live sets of the dense tensor-core backward's two kinds of
+    CTA (see include/attn_bwd.h): kv_live / q_live uint8 [Sq, Sk] and outside
+    int32 [1], zeroed device tensors."""
+    _check(lib.attn_debug_mask_live(_ref(mask), Sq, Sk, aligned_variant, _ptr(kv_live),
+                                    _ptr(q_live), _ptr(outside), _stream(stream)),
+           "attn_debug_mask_live")
+
+
+def attn_debug_sparse_rows(prob: Problem, sparse: Sparse, rows, counts, max_rows: int,
+                           stream=None):
+    """Selected-row lists of the sparse tensor-core backward: rows int32
+    [Sq * Hk, max_rows] and counts int32 [Sq * Hk] device tensors."""
+    _check(lib.attn_debug_sparse_rows(ctypes.byref(prob), ctypes.byref(sparse), _ptr(rows),
+                                      _ptr(counts), max_rows, _stream(stream)),
+           "attn_debug_sparse_rows")
 
 
 def attn_read_device_status(workspace, stream=None):

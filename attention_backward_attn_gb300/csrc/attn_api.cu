@@ -246,6 +246,35 @@ attn_status_t attn_mask_tile_classes(const attn_mask_t* mask, int32_t Sq, int32_
   return ATTN_OK;
 }
 
+attn_status_t attn_debug_mask_live(const attn_mask_t* mask, int32_t Sq, int32_t Sk,
+                                   int32_t aligned_variant, uint8_t* kv_live, uint8_t* q_live,
+                                   int32_t* outside, cudaStream_t stream) {
+  if (Sq <= 0 || Sk <= 0 || kv_live == nullptr || q_live == nullptr || outside == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (aligned_variant != 0 && aligned_variant != 1) return ATTN_ERR_INVALID_ARG;
+  if (aligned_variant == 1 && (Sq % 128 != 0 || Sk % 128 != 0)) return ATTN_ERR_INVALID_ARG;
+  if (Sq > kMaxMaskedLen || Sk > kMaxMaskedLen) return ATTN_ERR_UNSUPPORTED;
+  MaskSpec m;
+  const attn_status_t ms = mask_spec_of(mask, Sq, Sk, &m);
+  if (ms != ATTN_OK) return ms;
+  return cuda_status(
+      launch_mask_probe(m, Sq, Sk, aligned_variant == 1, kv_live, q_live, outside, stream));
+}
+
+attn_status_t attn_debug_sparse_rows(const attn_problem_t* prob, const attn_sparse_t* sparse,
+                                     int32_t* rows, int32_t* counts, int32_t max_rows,
+                                     cudaStream_t stream) {
+  if (sparse == nullptr || rows == nullptr || counts == nullptr) return ATTN_ERR_INVALID_ARG;
+  Problem p;
+  attn_status_t s = make_problem(prob, nullptr, sparse, &p);
+  if (s != ATTN_OK) return s;
+  const int64_t bound = sparse_row_bound(p);
+  if (bound > 1024) return ATTN_ERR_UNSUPPORTED;
+  if (max_rows < bound) return ATTN_ERR_INVALID_ARG;
+  if (p.topk > 0 && sparse->cmp_idx == nullptr) return ATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_rows_probe(p, sparse->cmp_idx, rows, counts, max_rows, stream));
+}
+
 int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
                       const attn_sparse_t* sparse) {
   Problem p;

@@ -78,6 +78,13 @@ bool tc_supported(const Problem& p);
 // Key-major CTAs per (key tile, KV head) of the dense tensor-core kernel; when
 // above 1 they add partial dK / dV sums into buffers the pre-pass zeroed.
 int tc_head_split(const Problem& p);
+// Diagnostic: the per-element live sets of the dense tensor-core kernel's
+// key-major and query-major CTAs for one sequence of lengths Sq x Sk
+// (mask_probe_kernel in tc_bwd.cu). aligned_variant selects the
+// instantiation that assumes whole tiles (Sq, Sk multiples of 128).
+cudaError_t launch_mask_probe(const MaskSpec& m, int Sq, int Sk, bool aligned_variant,
+                              uint8_t* kv_live, uint8_t* q_live, int32_t* outside,
+                              cudaStream_t stream);
 cudaError_t launch_bwd_tc(const Problem& p, const __half* q16, const __half* k16,
                           const __half* v16, const __half* do16, const float* lse,
                           const float* delta, const float* bias, float* dq, float* dk,
@@ -114,6 +121,16 @@ cudaError_t launch_bwd_sparse_tc(const Problem& p, const void* q, const void* dO
                                  const __half* kv16, const int32_t* idx, const float* lse,
                                  const float* delta, float* dq, float* d_ori, float* d_cmp,
                                  const SparseDet& det, DevStatus* st, cudaStream_t stream);
+
+// Selected rows per (token, KV head) of a sparse problem: the window plus the
+// compressed rows (before padding to whole tiles).
+int64_t sparse_row_bound(const Problem& p);
+// Diagnostic: the selected-row lists of the sparse tensor-core kernel
+// (build_rows), one per item = token Hk + KV head, into rows[item][stride]
+// with their lengths in counts[item]; stride >= sparse_row_bound(p) and the
+// bound must be at most 1024.
+cudaError_t launch_rows_probe(const Problem& p, const int32_t* idx, int32_t* rows,
+                              int32_t* counts, int stride, cudaStream_t stream);
 
 // ---- sparse_det.cu ----
 // After launch_bwd_sparse_tc in deterministic mode: writes d_ori / d_cmp

@@ -117,8 +117,10 @@ constexpr int smem_total() {
 // memory, S^T read (256 arrivals); kP2Full: dS^T written over dP^T in TMEM
 // (256 arrivals); kMma3: dV of the tile done (the P^T buffer is free again);
 // kMma4: dK of the tile done (the dP^T columns are free again).
+// kSFree: the softmax has copied S^T into registers (256 arrivals), so the
+// next tile's MMA1 may overwrite it.
 enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kP1Full = 6, kAccFull = 7,
-             kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kKvBars = 12 };
+             kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kSFree = 12, kKvBars = 13 };
 // barrier indices, query-major CTA
 // qSFull0 / qSFull1: S of the tile in TMEM buffer 0 / 1 (one barrier per
 // buffer: S(t+2) may complete before the softmax has polled for S(t+1), and
@@ -163,12 +165,8 @@ __device__ __forceinline__ uint32_t bits_between(int a, int b) {
   return below_b & ~((1u << a) - 1u);
 }
 
-
 __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 
-// Whether some entry of the tile rows [m0, m0 + BM) x keys [n0, n0 + BN) is
-// dead (masked, or past the end of the queries or keys), so that the tile
-// needs the per-element mask.
 // One sequence of the batch as a CTA sees it: its lengths, the first rows of
 // its dq and dk / dv in the outputs, and the mask aligned to it.
 struct Seq {
@@ -201,8 +199,77 @@ __device__ __forceinline__ bool seq_of(const TcParams& p, int b, Seq* s) {
   return true;
 }
 
+// Whether some entry of the tile rows [m0, m0 + BM) x keys [n0, n0 + BN) is
+// dead (masked, or past the end of the queries or keys), so that the tile
+// needs the per-element mask.
 __device__ __forceinline__ bool tile_cut(const Seq& s, int m0, int n0) {
   return m0 + BM > s.lq || n0 + BN > s.lk || !tile_full(s.mask, m0, m0 + BM, n0, n0 + BN);
+}
+
+// Per-element mask of one row of a tile, as both kinds of CTA apply it. The
+// tile at (m0, n0) needs it when the mask cuts the tile (or, kMayBeRagged,
+// the tile crosses a length); the return value says so. Otherwise every
+// entry of the tile is live and the ranges are the whole tile.
+//
+// Key-major view, key row j: the live queries of the tile are [*qlo, *qhi]
+// (tile-relative, may reach outside [0, BM): the chunk bits clip them). A
+// sink key is live for every query; queries past the length and a key past
+// its length are dead.
+template <bool kMayBeRagged>
+__device__ __forceinline__ bool kv_row_live(const Seq& s, int m0, int n0, int j, int* qlo,
+                                            int* qhi) {
+  const bool partial = kMayBeRagged ? tile_cut(s, m0, n0)
+                                    : !tile_full(s.mask, m0, m0 + BM, n0, n0 + BN);
+  int lo = 0, hi = BM - 1;
+  if (partial) {
+    if (j >= s.mask.sink) {
+      lo = j - s.mask.wr - m0;
+      hi = j + s.mask.wl - m0;
+    }
+    if constexpr (kMayBeRagged) {
+      hi = imin(hi, s.lq - 1 - m0);
+      if (j >= s.lk) hi = lo - 1;
+    }
+  }
+  *qlo = lo;
+  *qhi = hi;
+  return partial;
+}
+
+// Live queries [q0, q0 + 32) of a key row: bit u for query q0 + u.
+__device__ __forceinline__ uint32_t kv_chunk_bits(int qlo, int qhi, int q0) {
+  return bits_between(qlo - q0, qhi - q0 + 1);
+}
+
+// Query-major view, query row i: the live keys of the tile are the window
+// [*klo, *khi] plus the sink keys [0, *ksink) (tile-relative); keys past the
+// length are dead. (Rows past the query length are padding: their staged
+// Q / dO rows are zero, so dS is zero there whatever the mask says, and they
+// are not stored.)
+template <bool kMayBeRagged>
+__device__ __forceinline__ bool q_row_live(const Seq& s, int m0, int n0, int i, int* klo,
+                                           int* khi, int* ksink) {
+  const bool partial = kMayBeRagged ? tile_cut(s, m0, n0)
+                                    : !tile_full(s.mask, m0, m0 + BM, n0, n0 + BN);
+  int lo = 0, hi = BN - 1, sk = 0;
+  if (partial) {
+    lo = i - s.mask.wl - n0;
+    hi = i + s.mask.wr - n0;
+    sk = s.mask.sink - n0;
+    if constexpr (kMayBeRagged) {
+      hi = imin(hi, s.lk - n0 - 1);
+      sk = imin(sk, s.lk - n0);
+    }
+  }
+  *klo = lo;
+  *khi = hi;
+  *ksink = sk;
+  return partial;
+}
+
+// Live keys [k0, k0 + 32) of a query row: bit u for key k0 + u.
+__device__ __forceinline__ uint32_t q_chunk_bits(int klo, int khi, int ksink, int k0) {
+  return bits_between(klo - k0, khi - k0 + 1) | bits_between(-k0, ksink - k0);
 }
 
 // Live (query head, query tile) pairs of a key tile, heads outer: the live
@@ -290,7 +357,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   // producer warp's plain copy of LSE / delta (the TMA bulk copy needs whole
   // 16-byte-aligned tiles)
   const uint32_t qf = p.ragged ? 2u : 1u;
-  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 256, 1, 1, 1, 256, 1};
+  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 256, 1, 1, 1, 256, 1, 256};
   init_common(c, sbase + L::MISC, kKvBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
@@ -400,10 +467,12 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           ptx::mma_ss(t_dP, ptx::desc_add(dV, off), ptx::desc_add(ddo, off), id_S, s > 0);
         }
       };
-      // Per tile t: dV(t) as soon as P^T(t) is in shared memory, then S(t+1)
-      // (the softmax has read S^T(t)); dK(t) once dS^T(t) replaced dP^T(t) in
-      // TMEM, then dP(t+1) after dK(t) released those columns. The softmax of
-      // tile t+1 overlaps dV(t), dK(t) and dP(t+1).
+      // Per tile t: S(t+1) as soon as the softmax has copied S^T(t) into its
+      // registers (kSFree, before its exponentials), dV(t) once P^T(t) is in
+      // shared memory, dK(t) once dS^T(t) replaced dP^T(t) in TMEM, then
+      // dP(t+1) after dK(t) released those columns. S(t+1) is ready by the
+      // time the softmax finishes tile t, and the softmax of tile t+1
+      // overlaps dV(t), dK(t) and dP(t+1).
       bool ok = wait_bar(c, kKvFull, 0, 2);
       int n_tiles = 0;  // tiles whose dK MMAs were issued
       QTileIter it(hpc, n0, sq);
@@ -423,11 +492,9 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         const int st = t & 1;
         const uint64_t dq_mn = ptx::desc_add(dQmn, st * L::kTile);
         const uint64_t ddo_mn = ptx::desc_add(ddOmn, st * L::kTile);
-        if (!wait_bar(c, kP1Full, t & 1, 4)) break;
-        ptx::tc_fence_after();
-        // The softmax has read S^T(t): S(t+1) goes first (the softmax's next
-        // step waits on it), then dV(t). S(t+1) needs its Q stage, which dK(t-1)
-        // released; if that load has not landed yet, dV(t) goes first.
+        // S(t+1) goes first (the softmax's next step waits on it), once the
+        // softmax has copied S^T(t) out of TMEM. It needs its Q stage, which
+        // dK(t-1) released; if that load has not landed yet, dV(t) goes first.
         have = it.next();
         const int st1 = (t + 1) & 1;
         const uint32_t qpar = ((t + 1) >> 1) & 1;
@@ -440,7 +507,10 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             s_done = true;
           }
         };
+        if (have && !wait_bar(c, kSFree, t & 1, 13)) break;
         try_S();
+        if (!wait_bar(c, kP1Full, t & 1, 4)) break;
+        ptx::tc_fence_after();
         // MMA3 dV += P^T dO : A = P^T K-major over queries, B = dO MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
@@ -512,20 +582,9 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // without live keys has LSE = -inf; it can only sit in a partial tile,
       // where this mask zeroes its probabilities. So do the rows past Sq and
       // a key row past Sk (zero operands in the staged copies).
-      const bool partial = kMayBeRagged ? tile_cut(sq, m0, n0)
-                                        : !tile_full(sq.mask, m0, m0 + BM, n0, n0 + BN);
+      int qlo, qhi;
+      const bool partial = kv_row_live<kMayBeRagged>(sq, m0, n0, j, &qlo, &qhi);
       const int qcap = sq.lq - 1 - m0;       // last query of the tile
-      int qlo = 0, qhi = BM - 1;
-      if (partial) {
-        if (j >= sq.mask.sink) {
-          qlo = j - sq.mask.wr - m0;  // bits_between clamps to the tile
-          qhi = j + sq.mask.wl - m0;
-        }
-        if constexpr (kMayBeRagged) {
-          qhi = imin(qhi, qcap);
-          if (j >= sq.lk) qhi = qlo - 1;
-        }
-      }
       // bias / dbias element (query m0 + q, key j); reads of rows and keys
       // past the lengths are clamped into the tensor (their P is zero)
       const int jc = kMayBeRagged ? imin(j, sq.lk - 1) : j;
@@ -544,11 +603,12 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar(kSFree));  // S^T(t) is in registers: MMA1 may overwrite it
         uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
-          const uint32_t live = bits_between(qlo - q0, qhi - q0 + 1);
+          const uint32_t live = kv_chunk_bits(qlo, qhi, q0);
 #pragma unroll
           for (int e4 = 0; e4 < 32; e4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse_s + q0 + e4);
@@ -604,7 +664,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       for (int cc = 0; cc < 2; ++cc) {
         const int q0 = wg * 64 + cc * 32;
         uint32_t live_d = 0xffffffffu;
-        if constexpr (DBIAS && RB) live_d = partial ? bits_between(qlo - q0, qhi - q0 + 1) : live_d;
+        if constexpr (DBIAS && RB) live_d = partial ? kv_chunk_bits(qlo, qhi, q0) : live_d;
         uint32_t dr[32];
         ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
         ptx::tmem_wait_ld();
@@ -904,20 +964,9 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       if (!wait_bar(c, (t & 1) ? qSFull1 : qSFull0, (t >> 1) & 1, 27)) { ok = false; break; }
       ptx::tc_fence_after();
       const int n0 = it.nt * BN;
-      const bool partial = kMayBeRagged ? tile_cut(sq, m0, n0)
-                                        : !tile_full(sq.mask, m0, m0 + BM, n0, n0 + BN);
       const int kcap = sq.lk - n0;  // keys [0, kcap) of the tile exist
-      // live keys of this query row within the tile: [klo, khi] plus the sinks
-      int klo = 0, khi = BN - 1, ksink = 0;
-      if (partial) {
-        klo = i - sq.mask.wl - n0;  // bits_between clamps to the tile
-        khi = i + sq.mask.wr - n0;
-        ksink = sq.mask.sink - n0;
-        if constexpr (kMayBeRagged) {
-          khi = imin(khi, kcap - 1);
-          ksink = imin(ksink, kcap);
-        }
-      }
+      int klo, khi, ksink;
+      const bool partial = q_row_live<kMayBeRagged>(sq, m0, n0, i, &klo, &khi, &ksink);
       const uint32_t t_S = t_S0 + (t & 1) * 128;
       // phase 1: P from S (registers)
       float pv[64];
@@ -929,8 +978,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int k0 = wg * 64 + cc * 32;  // first key of this chunk within the tile
-          const uint32_t live =
-              bits_between(klo - k0, khi - k0 + 1) | bits_between(-k0, ksink - k0);
+          const uint32_t live = q_chunk_bits(klo, khi, ksink, k0);
 #pragma unroll
           for (int e4 = 0; e4 < 32; e4 += 4) {
             float bv[4];
@@ -1081,6 +1129,60 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
+// ------------------------------------------------------------ mask probe --
+// The per-element live sets the two kinds of CTA compute for one sequence,
+// through the same tile walks (QTileIter / KTileIter) and row predicates
+// (kv_row_live / q_row_live and their chunk bits) as the backward kernel.
+// Blocks [0, nkt) take the key-major view (thread = key row of a key tile)
+// and add 1 to kv_live[i][j] for every entry they treat as live; blocks
+// [nkt, nkt + nqt) take the query-major view (thread = query row) and add 1
+// to q_live[i][j]. A live entry outside [0, lq) x [0, lk) (key-major), or at
+// a key past lk (query-major), is counted in *outside instead. A tile the
+// walk visited twice shows up as 2.
+template <bool kMayBeRagged>
+__global__ void __launch_bounds__(128)
+mask_probe_kernel(const Seq s, int nkt, uint8_t* kv_live, uint8_t* q_live, int* outside) {
+  const int t = (int)threadIdx.x;
+  if ((int)blockIdx.x < nkt) {
+    const int n0 = (int)blockIdx.x * BN;
+    const int j = n0 + t;
+    QTileIter it(1, n0, s);
+    while (it.next()) {
+      const int m0 = it.mt * BM;
+      int qlo, qhi;
+      const bool partial = kv_row_live<kMayBeRagged>(s, m0, n0, j, &qlo, &qhi);
+      for (int q0 = 0; q0 < BM; q0 += 32) {
+        const uint32_t live = partial ? kv_chunk_bits(qlo, qhi, q0) : 0xffffffffu;
+        for (int u = 0; u < 32; ++u) {
+          if (!((live >> u) & 1u)) continue;
+          const int i = m0 + q0 + u;
+          if (i >= s.lq || j >= s.lk) atomicAdd(outside, 1);
+          else kv_live[(int64_t)i * s.lk + j] += 1;
+        }
+      }
+    }
+  } else {
+    const int m0 = ((int)blockIdx.x - nkt) * BM;
+    const int i = m0 + t;
+    if (i >= s.lq) return;  // padding rows: not stored, dS zero (see q_row_live)
+    KTileIter it(m0, s);
+    while (it.next()) {
+      const int n0 = it.nt * BN;
+      int klo, khi, ksink;
+      const bool partial = q_row_live<kMayBeRagged>(s, m0, n0, i, &klo, &khi, &ksink);
+      for (int k0 = 0; k0 < BN; k0 += 32) {
+        const uint32_t live = partial ? q_chunk_bits(klo, khi, ksink, k0) : 0xffffffffu;
+        for (int u = 0; u < 32; ++u) {
+          if (!((live >> u) & 1u)) continue;
+          const int j = n0 + k0 + u;
+          if (j >= s.lk) atomicAdd(outside, 1);
+          else q_live[(int64_t)i * s.lk + j] += 1;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ host --
 
 // Row-major [rows][D] fp16 matrix, boxes of 128 rows x 64 columns, 128B swizzle.
@@ -1171,6 +1273,23 @@ int tc_head_split(const Problem& p) {
 bool tc_supported(const Problem& p) {
   return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0 &&
          encode_fn() != nullptr;
+}
+
+cudaError_t launch_mask_probe(const MaskSpec& m, int Sq, int Sk, bool aligned_variant,
+                              uint8_t* kv_live, uint8_t* q_live, int32_t* outside,
+                              cudaStream_t stream) {
+  Seq s;
+  s.lq = Sq;
+  s.lk = Sk;
+  s.oq = 0;
+  s.ok = 0;
+  s.mask = m;
+  const int nkt = tc_rows(Sk) / BN, nqt = tc_rows(Sq) / BM;
+  if (aligned_variant)
+    mask_probe_kernel<false><<<nkt + nqt, 128, 0, stream>>>(s, nkt, kv_live, q_live, outside);
+  else
+    mask_probe_kernel<true><<<nkt + nqt, 128, 0, stream>>>(s, nkt, kv_live, q_live, outside);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k16,

@@ -83,19 +83,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Four rows r0..r3 (any order, any values in range) of a 2-D tensor map whose
-// box is one row high, columns [x, x + box width), written to 4 consecutive
-// box rows at dst (the map's swizzle applied as for a 4-row box).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t x, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
-
 // 16-byte global -> shared copy through L2 only (cp.async, completion tracked
 // per thread with commit / wait groups).
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
@@ -271,47 +258,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// ---------------------------------------------------------------- cluster ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of every CTA of the cluster (release / acquire on shared memory).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
                "f"(d)
                : "memory");
 }
 
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
-// Same reduction without a compiler memory barrier: for streams of
-// reductions into buffers this thread never reads back, so that the loads
+// fp32 reduction into global memory without a compiler memory barrier: for
+// streams of reductions into buffers this thread never reads back, so that the loads
 // feeding later reductions may be scheduled ahead of earlier ones.
 __device__ __forceinline__ void red_add_f32_stream(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v));

@@ -257,6 +257,12 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t sX = sbase + L::X, sKV = sbase + L::KV, sG = sbase + L::G;
+  // tcgen05.commit arrivals the MMA thread sent to each barrier (counted so
+  // that the teardown can wait for the last phase of every one of them: an
+  // arrival still in flight at exit would land on the barriers of the next
+  // CTA this SM runs, which belongs to another launch since the CTAs are
+  // persistent)
+  int n_ring = 0, n_st = 0, n_gfree = 0, n_dkv = 0, n_xfree = 0, n_dq = 0;
   auto rows_of = [&](int b) { return reinterpret_cast<int32_t*>(smem + L::ROWS + b * 4 * kSpMaxRows); };
   auto rows_addr = [&](int b) { return sbase + L::ROWS + b * 4 * kSpMaxRows; };
   auto lse_of = [&](int b) { return reinterpret_cast<float*>(smem + L::LSE + b * 4 * kSpR); };
@@ -332,6 +338,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 4; ++k)
           ptx::mma_ss(tS, ptx::desc_add(a0, 32 * k), ptx::desc_add(b0, 32 * k), idA, (s | k) != 0);
         ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+        ++n_ring;
         if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
         return true;
       };
@@ -363,6 +370,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           ptx::mma_ss(tmem + 128, ptx::desc_add(a0, 2048 * kk),
                       ptx::desc_add(dG, (kk >> 2) * kSpSlot + (kk & 3) * 32), idC, kk != 0);
         ptx::mma_commit(c.bar(sDkvFull));
+        ++n_dkv;
         ++issued;
       };
       // After sGFull of tile t: two independent streams. The MMA-C blocks go
@@ -383,6 +391,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             if (!next || (r & 1) == 0) b_slot(t, next ? r >> 1 : r);
             else a_next(r >> 1);
             ptx::mma_commit(c.bar(sKvEmpty0 + slot));
+            ++n_ring;
             if (++slot == kSpSlots) { slot = 0; ph ^= 1u; }
             ++r;
             did = true;
@@ -423,6 +432,7 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           for (int s = 0; s < 8 && ok; ++s) ok = a_slab(s);
           if (!ok) break;
           ptx::mma_commit(c.bar(sStFull));
+          ++n_st;
         }
         for (int t = 0; t < T && ok; ++t, ++gt) {
           if (!wait_bar(c, sGFull, (uint32_t)gt & 1u, 43)) { ok = false; break; }
@@ -437,14 +447,20 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           const bool next = t + 1 < T;
           if (!(ok = tile_streams(t, next))) break;
           ptx::mma_commit(c.bar(sGFree));
-          if (next) ptx::mma_commit(c.bar(sStFull));
+          ++n_gfree;
+          if (next) {
+            ptx::mma_commit(c.bar(sStFull));
+            ++n_st;
+          }
         }
         if (!ok) break;
         // with no tiles, dQ^T was not touched, but sDqFull of this token must not
         // complete before the drain consumed the previous one
         if (T == 0 && k > 0 && !wait_bar(c, sDqFree, (uint32_t)(k - 1) & 1u, 47)) break;
-        ptx::mma_commit(c.bar(sXFree));   // completes when every MMA reading X did
+        ptx::mma_commit(c.bar(sXFree));  // completes when every MMA reading X did
+        ++n_xfree;
         ptx::mma_commit(c.bar(sDqFull));  // dQ^T of the token (T = 0: nothing to wait for)
+        ++n_dq;
       }
       ptx::mma_commit(c.bar(sDone));  // completes once every MMA above has
     }
@@ -695,10 +711,48 @@ attn_bwd_sparse_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    if (lane == 0) drain_bar(c, sDone, 0);
+    if (lane == 0) {
+      drain_bar(c, sDone, 0);  // every MMA of this CTA has completed
+      // and every commit arrival has landed, including those no role waits
+      // for (the last ring-slot releases, sGFree, sXFree) and those whose
+      // waiter left early on an abort
+      auto last = [&](int which, int n) {
+        if (n > 0) drain_bar(c, which, (uint32_t)(n - 1) & 1u);
+      };
+      // ring slot u % kSpSlots took the u-th release
+      for (int sl = 0; sl < kSpSlots; ++sl)
+        last(sKvEmpty0 + sl, n_ring / kSpSlots + (sl < n_ring % kSpSlots ? 1 : 0));
+      last(sStFull, n_st);
+      last(sGFree, n_gfree);
+      last(sDkvFull, n_dkv);
+      last(sXFree, n_xfree);
+      last(sDqFull, n_dq);
+    }
     __syncwarp();
     ptx::tmem_dealloc(tmem, 512);
   }
+}
+
+// ------------------------------------------------------------ rows probe --
+// The selected-row lists the backward kernel works on: one warp per item
+// (token i, KV head g) runs build_rows, as warp 0 of the kernel does, and
+// writes the item's list (rows of the fp16 copy [ori ; cmp] viewed as
+// [(n_ori + n_cmp) Hk][512], so original row r of KV head g is r Hk + g and
+// compressed row c is (n_ori + c) Hk + g) to rows[item][0, n) and n to
+// counts[item], item = i Hk + g.
+constexpr int kProbeWarps = 4;
+
+__global__ void __launch_bounds__(32 * kProbeWarps)
+rows_probe_kernel(const SpParams p, int32_t* rows, int32_t* counts, int stride) {
+  __shared__ int32_t buf[kProbeWarps][kSpMaxRows];
+  const int w = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  const int item = (int)blockIdx.x * kProbeWarps + w;
+  if (item >= p.Sq * p.Hk) return;
+  const int i = item / p.Hk, g = item % p.Hk;
+  int nwin, lo;
+  const int n = build_rows(p, i, g, buf[w], lane, &nwin, &lo);
+  for (int j = lane; j < n; j += 32) rows[(int64_t)item * stride + j] = buf[w][j];
+  if (lane == 0) counts[item] = n;
 }
 
 // ------------------------------------------------------------------ host --
@@ -727,6 +781,29 @@ int64_t max_selected_rows(const Problem& p) {
 }  // namespace
 
 int64_t sparse_det_stride(const Problem& p) { return (max_selected_rows(p) + 127) / 128 * 128; }
+
+int64_t sparse_row_bound(const Problem& p) { return max_selected_rows(p); }
+
+cudaError_t launch_rows_probe(const Problem& pr, const int32_t* idx, int32_t* rows,
+                              int32_t* counts, int stride, cudaStream_t stream) {
+  SpParams p{};
+  p.Sq = pr.Sq;
+  p.Hq = pr.Hq;
+  p.Hk = pr.Hk;
+  p.n_ori = pr.n_ori;
+  p.n_cmp = pr.n_cmp;
+  p.topk = pr.topk;
+  p.ratio = pr.cmp_ratio;
+  p.wl = pr.ori_wl;
+  p.wr = pr.ori_wr;
+  p.idx = pr.n_cmp > 0 && pr.cmp_ratio == 0 ? idx : nullptr;
+  p.status = nullptr;  // out-of-range indices are skipped, not reported
+  const int64_t items = (int64_t)pr.Sq * pr.Hk;
+  if (items == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((items + kProbeWarps - 1) / kProbeWarps);
+  rows_probe_kernel<<<grid, 32 * kProbeWarps, 0, stream>>>(p, rows, counts, stride);
+  return cudaGetLastError();
+}
 
 bool tc_sparse_supported(const Problem& p) {
   return p.sparse && p.D == kSpD && p.B == 1 && p.Hq == kSpR * p.Hk && p.Sq > 0 && p.n_ori > 0 &&

@@ -105,9 +105,11 @@ typedef struct attn_problem {
 /* Deterministic dense backward: dq, dk, dv and dbias are bitwise the same on
  * every run. dk / dv are then written by one CTA per key tile (no split of a
  * key tile's query heads over CTAs, whose partial sums would be added in
- * arrival order), and with dbias and B > 1 attn_bwd runs one launch per batch
- * so that each dbias element receives its per-batch terms in batch order.
- * Slower than the default. Sparse variant: the tensor-core kernel stores
+ * arrival order). With dbias and B > 1, the backward kernel (still one
+ * launch) adds each batch's terms into that batch's own slice of the
+ * workspace (one writer per element, so every slice holds exact values), and
+ * a second kernel sums the slices into dbias in batch order; the workspace
+ * then holds B * Hq * Sq * Sk more fp32 values. Slower than the default. Sparse variant: the tensor-core kernel stores
  * every (token, KV head)'s dKV rows in the workspace instead of adding them
  * into d_ori_kv / d_cmp_kv, and a second pass adds each row's terms in token
  * order and writes the rows (the workspace then holds Sq * Hk * (selected-row
@@ -288,13 +290,17 @@ const char* attn_status_string(attn_status_t status);
  *   needs more than 32 MiB of workspace (attn_bwd_workspace_size).
  * - The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
- *   stream capture.
+ *   stream capture. The address belongs to the device's context: if that
+ *   context is replaced (cudaDeviceReset), the next call looks it up again,
+ *   and that call too should come before any stream capture.
  * - All calls share the array and it keeps the last call's contents (the
  *   pre-pass rewrites everything the backward reads). Calls whose work
  *   overlaps on the GPU race on it: order them on one stream or synchronise.
  * - device_status may be NULL. Otherwise the call synchronises `stream` and
  *   stores the device-side status code in device_status[0] and its detail in
- *   device_status[1] (as attn_read_device_status would). */
+ *   device_status[1] (as attn_read_device_status would). If the status
+ *   record cannot be read back (the synchronisation or the copy fails), the
+ *   call returns ATTN_ERR_CUDA and leaves device_status unwritten. */
 attn_status_t attn_bwd_noalloc(const attn_problem_t* prob, const attn_mask_t* mask,
                                const attn_sparse_t* sparse,
                                const void* q, const void* k, const void* v,
@@ -312,6 +318,45 @@ attn_status_t attn_bwd_noalloc(const attn_problem_t* prob, const attn_mask_t* ma
  * ATTN_ERR_INVALID_ARG for non-positive sizes or a NULL out. */
 attn_status_t attn_mask_tile_classes(const attn_mask_t* mask, int32_t Sq, int32_t Sk,
                                      int32_t tile_q, int32_t tile_k, int8_t* out);
+
+/* Diagnostic (tests): the per-element live sets of the dense tensor-core
+ * backward, read back from the device. For one sequence of Sq queries and Sk
+ * keys under `mask` (NULL = every entry live; bottom_right honoured), a kernel
+ * walks the live tiles and applies the per-element predicate exactly as the
+ * backward's two kinds of CTA do: the key-major CTAs (dK, dV; a thread per key
+ * row) and the query-major CTAs (dQ; a thread per query row). For every entry
+ * it treats as live it adds 1 to kv_live[i * Sk + j] (key-major view) or
+ * q_live[i * Sk + j] (query-major view); a live entry outside the lengths
+ * adds 1 to *outside instead. With a correct mask both arrays equal the mask
+ * ("22_sink_tokens_fmha.py" mask builders) as 0 / 1 bytes and *outside stays
+ * 0; a 2 would mean a tile visited twice.
+ * kv_live, q_live: device uint8 [Sq, Sk]; outside: device int32 [1]; all
+ * zeroed by the caller, written on `stream`. aligned_variant = 1 probes the
+ * kernel instantiation that assumes whole 128-row tiles (Sq and Sk must then
+ * be multiples of 128), 0 the one that handles any lengths. Returns
+ * ATTN_ERR_INVALID_ARG for non-positive sizes, NULL outputs or a bad variant. */
+attn_status_t attn_debug_mask_live(const attn_mask_t* mask, int32_t Sq, int32_t Sk,
+                                   int32_t aligned_variant, uint8_t* kv_live, uint8_t* q_live,
+                                   int32_t* outside, cudaStream_t stream);
+
+/* Diagnostic (tests): the selected-row lists of the sparse tensor-core
+ * backward (Ascend "sparse_flash_mla_grad" formula, phase 1), built on the
+ * device by the same routine the backward kernel runs. For every item =
+ * i * Hk + g (query token i, KV head g) it writes the item's rows, in the
+ * order the kernel processes them (the original-KV window ascending, then
+ * the valid top-k entries in slot order, or every eligible compressed row
+ * for CFA), to rows[item * max_rows + 0 .. n - 1] and n to counts[item]. A
+ * row is an index into [ori rows ; cmp rows] x Hk: original row r of KV
+ * head g is r * Hk + g, compressed row c is (n_ori + c) * Hk + g. Indices
+ * that are -1 or out of range are skipped. rows: device int32
+ * [Sq * Hk, max_rows]; counts: device int32 [Sq * Hk]. prob / sparse as for
+ * attn_bwd (gradient pointers unused). Returns ATTN_ERR_INVALID_ARG when
+ * max_rows is below the per-item bound (window + topk, or window + n_cmp
+ * for CFA) and ATTN_ERR_UNSUPPORTED when that bound exceeds 1024 (the
+ * tensor-core kernel's limit). */
+attn_status_t attn_debug_sparse_rows(const attn_problem_t* prob, const attn_sparse_t* sparse,
+                                     int32_t* rows, int32_t* counts, int32_t max_rows,
+                                     cudaStream_t stream);
 
 /* Which backward kernel attn_bwd would launch for these arguments:
  * 0 = none (invalid / unsupported), 1 = tcgen05 tensor-core kernel,

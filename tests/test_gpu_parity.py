@@ -356,6 +356,19 @@ def test_deterministic_dbias_graph_replay_full_size():
         assert plan.device_status()[0] == 0
         for a, b in zip(ref, (plan.dq, plan.dk, plan.dbias)):
             assert torch.equal(a, b)
+    # and the replayed result is the oracle's, on heads 0 and 15 (all batches)
+    O_b = o.float().cpu().numpy()
+    L_f = lse.cpu().numpy()
+    heads = [0, w.Hq - 1]
+    bh = lambda x: H.bhsd(x[:, :, heads])
+    dQ, dK, dV, dB = oracle.backward(bh(w.q), bh(w.k), bh(w.v), bh(O_b), bh(w.do),
+                                     L_f[:, heads].astype(np.float64), w.scale, None,
+                                     w.bias[heads].astype(np.float64))
+    t = lambda x: x.transpose(0, 2, 1, 3)
+    H.check_close("dq", plan.dq.cpu().numpy()[:, :, heads], t(dQ))
+    H.check_close("dk", plan.dk.cpu().numpy()[:, :, heads], t(dK))
+    H.check_close("dv", plan.dv.cpu().numpy()[:, :, heads], t(dV))
+    H.check_close("dbias", plan.dbias.cpu().numpy()[heads], dB)
 
 
 def test_head_split_needs_the_prepared_dk_dv():

@@ -6,8 +6,9 @@ fixed at start-up, or paths that must not stall other streams. For them the
 library keeps its workspace in a fixed device array. This test calls that
 entry point through the C ABI twice in a row (the second call runs on the
 array's stale contents from the first) and checks each result against the
-regular attn_bwd_preprocess + attn_bwd path with the parity tolerance of the
-other tests. It lives in its own file, collected last.
+regular attn_bwd_preprocess + attn_bwd path, and against the float64 oracle,
+with the parity tolerance of the other tests. It lives in its own file,
+collected last.
 """
 
 import numpy as np
@@ -55,9 +56,13 @@ def test_noalloc_matches_regular_path_twice(first, second):
         got = _noalloc_run(ab, torch, plan)
         torch.cuda.synchronize()
         assert plan.device_status()[0] == 0
-        for name in ("dq", "dk", "dv", "delta") + (("dbias",) if w.want_dbias else ()):
+        names = ("dq", "dk", "dv", "delta") + (("dbias",) if w.want_dbias else ())
+        for name in names:
             ref = getattr(plan, name).cpu().numpy()
             H.check_close(name, got[name].cpu().numpy(), ref)
+        oracle_ref = H.dense_reference(w, O_b, L_f)
+        for name in names:
+            H.check_close(name, got[name].cpu().numpy(), oracle_ref[name])
 
 
 def test_noalloc_rejects_problems_beyond_its_workspace():
