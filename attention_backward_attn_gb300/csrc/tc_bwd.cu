@@ -19,25 +19,29 @@
 // cs > 1), so no post-pass over per-head gradients exists. Per
 // tile, so that one thread owns one key row of the softmax:
 //   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
-//   MMA2  dP^T = V  dO^T
+//   MMA2  dP^T = V  dO^T     (into the same TMEM columns, once S^T was read)
 //   SFU   phase 1: P^T = exp2(S^T scale log2e + bias log2e - LSE log2e),
 //                  fp16 into SMEM (A operand of MMA3)
 //         phase 2: dS^T = P^T (dP^T - D), fp16 into TMEM over dP^T (A of MMA4)
 //   MMA3  dV += P^T dO       (A = P^T K-major, B = dO MN-major)
 //   MMA4  dK += dS^T Q       (A = dS^T in TMEM, B = Q MN-major)
-// Issue order S(t+1) (as soon as the softmax has read S^T(t) and the next
-// Q / dO stage has landed), dV(t), dK(t), dP(t+1): phase 1 of the next tile
-// runs while dV(t), dK(t) and dP(t+1) are on the tensor pipe.
+// TMEM holds dK, dV and two 128-column buffers; tile t uses buffer t & 1
+// for S^T, then dP^T, then dS^T. Issue order per tile: dP(t) (as soon as
+// the softmax has copied S^T(t) into registers), S(t+1) into the other
+// buffer (free once dK(t-1) has read it), dV(t), dK(t). No MMA has to wait
+// for an earlier one to complete, so the tensor pipe runs while the softmax
+// works on the same tile.
 //
 // Query-major CTAs (dQ): one CTA per (batch, query head, 128-row query tile)
 // loops over the live key tiles of its KV head, recomputing S and dP:
 //   MMA1' S  = Q  K^T        (M = queries, N = keys)
-//   MMA2' dP = dO V^T
-//   SFU   dS = exp2(...) (dP - D), fp16 into TMEM over S
+//   MMA2' dP = dO V^T        (into the same TMEM columns, once S was read)
+//   SFU   dS = exp2(...) (dP - D), fp16 into TMEM over dP
 //   MMA3' dQ += dS K         (A = dS in TMEM, B = K MN-major)
 // dQ accumulates in TMEM over all key tiles and is written once: no atomics
-// and no zero-filled accumulation buffer. S is double-buffered so that the
-// next tile's MMA1' runs during this tile's softmax.
+// and no zero-filled accumulation buffer. Tile t uses TMEM buffer t % 3 of
+// three, so S(t+1) goes out right after dP(t) and the softmax never waits for
+// the next S.
 //
 // Lengths need not be whole tiles: the pre-pass stages every head's rows
 // rounded up to 128 with zero rows past the length, a tile that crosses a
@@ -81,9 +85,12 @@ struct SmemKV {
   static constexpr int dS = dO + 2 * kTile;  // P^T: [128 keys][128 queries] fp16, 2 slabs
   static constexpr int LSE = dS + 2 * kSlab; // 2 stages x 128 fp32
   static constexpr int DLT = LSE + 1024;     // 2 stages x 128 fp32
-  static constexpr int BAR = DLT + 1024;     // mbarriers
-  static constexpr int MISC = BAR + 128;     // TMEM base, abort flag
-  static constexpr int TOTAL = MISC + 16;
+  static constexpr int BAR = DLT + 1024;     // mbarriers (up to 32)
+  static constexpr int MISC = BAR + 256;     // TMEM base, abort flag
+  // D = 64 with a bias: the tile's bias [128 queries][128 keys] fp32 as four
+  // TMA boxes of 32 keys (128B-swizzled 128-byte rows), one stage
+  static constexpr int BIAS = (MISC + 16 + 1023) / 1024 * 1024;
+  static constexpr int TOTAL = D == 64 ? BIAS + 4 * kSlab : MISC + 16;
   // end-of-kernel staging of dK / dV rows for the bulk reductions (reuses Q..dS)
   static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
   static constexpr int STAGE = Q;
@@ -98,14 +105,38 @@ struct SmemQ {
   static constexpr int dO = Q + kTile;
   static constexpr int K = dO + kTile;      // 2 stages
   static constexpr int V = K + 2 * kTile;   // 2 stages
-  static constexpr int BAR = V + 2 * kTile;
-  static constexpr int MISC = BAR + 128;
-  static constexpr int TOTAL = MISC + 16;
+  static constexpr int BAR = V + 2 * kTile;  // mbarriers (up to 32)
+  static constexpr int MISC = BAR + 256;
+  // D = 64 with a bias: two stages of the tile's bias [128 queries][128 keys]
+  // fp32 (four 128B-swizzled TMA boxes of 32 keys each)
+  static constexpr int BIAS = (MISC + 16 + 1023) / 1024 * 1024;
+  static constexpr int TOTAL = D == 64 ? BIAS + 2 * 4 * kSlab : MISC + 16;
   // end-of-kernel staging of dQ rows for the copy-engine stores (reuses K, V)
   static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
   static constexpr int STAGE = K;
   static_assert(128 * kStageRow <= 4 * kTile, "staging fits");
 };
+
+static_assert(SmemKV<64>::TOTAL <= 232448 && SmemQ<64>::TOTAL <= 232448 &&
+                  SmemKV<128>::TOTAL <= 232448 && SmemQ<128>::TOTAL <= 232448,
+              "shared memory per CTA");
+
+// Bias tiles through TMA (D = 64, whole tiles): a box is [128 rows][32 fp32]
+// with the 128-byte swizzle, so the 16-byte chunk c of row r sits at chunk
+// c ^ (r & 7). Byte offset of element (row r, column k) of a [128][128] tile
+// stored as four such boxes.
+__device__ __forceinline__ uint32_t bias_off(int r, int k) {
+  return (uint32_t)((k >> 5) * kSlab + r * 128 + ((((k & 31) >> 2) ^ (r & 7)) << 4) +
+                    (k & 3) * 4);
+}
+
+// Whether a kernel instantiation reads its bias tiles through TMA into
+// shared memory (room for them at D = 64; whole tiles only, so that every
+// box is inside the bias tensor and its rows are 16-byte aligned).
+template <int D, bool BIAS, bool RB>
+constexpr bool tma_bias() {
+  return BIAS && !RB && D == 64;
+}
 
 template <int D>
 constexpr int smem_total() {
@@ -113,22 +144,28 @@ constexpr int smem_total() {
 }
 
 // barrier indices, key-major CTA
-// kSFull / kdPFull: S^T / dP^T of the tile in TMEM; kP1Full: P^T in shared
-// memory, S^T read (256 arrivals); kP2Full: dS^T written over dP^T in TMEM
-// (256 arrivals); kMma3: dV of the tile done (the P^T buffer is free again);
-// kMma4: dK of the tile done (the dP^T columns are free again).
-// kSFree: the softmax has copied S^T into registers (256 arrivals), so the
-// next tile's MMA1 may overwrite it.
-enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull = 5, kP1Full = 6, kAccFull = 7,
-             kMma3 = 8, kdPFull = 9, kP2Full = 10, kMma4 = 11, kSFree = 12, kKvBars = 13 };
+// Tile t works in TMEM buffer t & 1: MMA1 writes S^T there (kSFull0 + (t & 1)),
+// the softmax copies it out (kSFree), MMA2 writes dP^T over it (kdPFull), the
+// softmax turns dP^T into dS^T written back into the same columns
+// (kP2Full, 256 arrivals) and MMA4 reads it (kMma40 + (t & 1): that buffer
+// is free again). P^T goes to shared memory (kP1Full, 256 arrivals) for MMA3
+// (kMma3: dV of the tile done, the P^T buffer is free again).
+// kBiasFull / kBiasEmpty: the tile's bias landed in shared memory / was read
+// by the softmax (256 arrivals), on the TMA bias path.
+enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull0 = 5, kSFree = 7, kP1Full = 8,
+             kP2Full = 9, kdPFull = 10, kMma3 = 11, kMma40 = 12, kAccFull = 14, kBiasFull = 15,
+             kBiasEmpty = 16, kKvBars = 17 };
 // barrier indices, query-major CTA
-// qSFull0 / qSFull1: S of the tile in TMEM buffer 0 / 1 (one barrier per
-// buffer: S(t+2) may complete before the softmax has polled for S(t+1), and
-// on a shared barrier that second phase would hide the first); qdPFull: dP of
-// the tile in TMEM; qDsFull: dS written over S (256 arrivals; dP read);
-// qMma3: dQ of the tile done (its S buffer free).
-enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull0 = 5, qDsFull = 6, qAccFull = 7,
-            qMma3 = 8, qdPFull = 9, qSFull1 = 10, kQBars = 11 };
+// Tile t works in TMEM buffer t % 3: MMA1' writes S there (qSFull0 + t % 3),
+// the softmax copies it out (qSFree), MMA2' writes dP over it (qdPFull), the
+// softmax writes dS back into the same columns (qDsFull, 256 arrivals) and
+// MMA3' reads it (qMma30 + t % 3: that buffer is free again). One S-ready and
+// one MMA3'-done barrier per buffer, so that no barrier can complete two
+// phases before its waiter polls the first.
+// qBiasFull0/1 / qBiasEmpty0/1: the two bias stages (TMA bias path).
+enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull0 = 5, qSFree = 8, qdPFull = 9,
+            qDsFull = 10, qMma30 = 11, qAccFull = 14, qBiasFull0 = 15, qBiasEmpty0 = 17,
+            kQBars = 19 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
@@ -328,11 +365,13 @@ __device__ __forceinline__ void init_common(const Ctx& c, uint32_t tmem_slot_add
 template <int D, bool BIAS, bool DBIAS, bool RB>
 __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, const CUtensorMap* tmdO,
-                                       const TcParams& p, uint8_t* smem, uint32_t sbase) {
+                                       const CUtensorMap* tmB, const TcParams& p, uint8_t* smem,
+                                       uint32_t sbase) {
   using L = SmemKV<D>;
   // The bias variants run ragged lengths only as RB instantiations; the others
   // take both and test the lengths at run time.
   constexpr bool kMayBeRagged = RB || (!BIAS && !DBIAS);
+  constexpr bool kTB = tma_bias<D, BIAS, RB>();  // bias tiles through TMA (whole tiles)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cs = p.cs;
@@ -357,13 +396,14 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   // producer warp's plain copy of LSE / delta (the TMA bulk copy needs whole
   // 16-byte-aligned tiles)
   const uint32_t qf = p.ragged ? 2u : 1u;
-  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 256, 1, 1, 1, 256, 1, 256};
+  // kKvFull, kQFull0/1, kQEmpty0/1, kSFull0/1, kSFree, kP1Full, kP2Full, kdPFull, kMma3,
+  // kMma40/1, kAccFull, kBiasFull, kBiasEmpty
+  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 1, 256, 256, 256, 1, 1, 1, 1, 1, 1, 256};
   init_common(c, sbase + L::MISC, kKvBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
-  const uint32_t t_S = tmem + 2 * D;
-  const uint32_t t_dP = tmem + 2 * D + 128;
+  const uint32_t t_buf0 = tmem + 2 * D;  // tile t: S^T / dP^T / dS^T at t_buf0 + (t & 1) 128
   const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::dS;
   bool epi_ok = false;
   int n_iters = 0;
@@ -382,6 +422,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       }
     }
     int issued[2] = {0, 0};
+    int bias_issued = 0;
     if (lane == 0 || p.ragged) {  // warp-uniform when ragged
       QTileIter it(hpc, n0, sq);
       int t = 0;
@@ -412,6 +453,17 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             ptx::bulk_load(sbase + L::LSE + st * 512, p.lse + lrow, 512, full);
             ptx::bulk_load(sbase + L::DLT + st * 512, p.delta + lrow, 512, full);
           }
+          if constexpr (kTB) {
+            // the tile's bias rows (one stage: once the softmax read tile t - 1's)
+            if (t > 0 && !wait_bar(c, kBiasEmpty, (t - 1) & 1, 14)) break;
+            const uint32_t bfull = c.bar(kBiasFull);
+            ptx::mbar_arrive_expect_tx(bfull, 4 * kSlab);
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+              ptx::tma_load_2d(sbase + L::BIAS + bx * kSlab, tmB, bfull, n0 + 32 * bx,
+                               h * p.Sq + m0);
+            ++bias_issued;
+          }
         }
         if (p.ragged) {
           float* lse_s = reinterpret_cast<float*>(smem + L::LSE + st * 512);
@@ -435,6 +487,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       drain_bar(c, kKvFull, 0);
       for (int st = 0; st < 2; ++st)
         if (issued[st] > 0) drain_bar(c, kQFull0 + st, (issued[st] - 1) & 1);
+      if (bias_issued > 0) drain_bar(c, kBiasFull, (bias_issued - 1) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -451,63 +504,69 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       const uint64_t ddOk = ptx::smem_desc_sw128(sbase + L::dO, 16, 1024);
       const uint64_t dQmn = ptx::smem_desc_sw128(sbase + L::Q, kSlab, 1024);
       const uint64_t ddOmn = ptx::smem_desc_sw128(sbase + L::dO, kSlab, 1024);
-      auto issue_S = [&](int st) {  // MMA1 S^T = K Q^T (both K-major over d)
+      auto issue_S = [&](int st, uint32_t dst) {  // MMA1 S^T = K Q^T (both K-major over d)
         const uint64_t dq = ptx::desc_add(dQk, st * L::kTile);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_S, ptx::desc_add(dK, off), ptx::desc_add(dq, off), id_S, s > 0);
+          ptx::mma_ss(dst, ptx::desc_add(dK, off), ptx::desc_add(dq, off), id_S, s > 0);
         }
       };
-      auto issue_dP = [&](int st) {  // MMA2 dP^T = V dO^T
+      auto issue_dP = [&](int st, uint32_t dst) {  // MMA2 dP^T = V dO^T
         const uint64_t ddo = ptx::desc_add(ddOk, st * L::kTile);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dP, ptx::desc_add(dV, off), ptx::desc_add(ddo, off), id_S, s > 0);
+          ptx::mma_ss(dst, ptx::desc_add(dV, off), ptx::desc_add(ddo, off), id_S, s > 0);
         }
       };
-      // Per tile t: S(t+1) as soon as the softmax has copied S^T(t) into its
-      // registers (kSFree, before its exponentials), dV(t) once P^T(t) is in
-      // shared memory, dK(t) once dS^T(t) replaced dP^T(t) in TMEM, then
-      // dP(t+1) after dK(t) released those columns. S(t+1) is ready by the
-      // time the softmax finishes tile t, and the softmax of tile t+1
-      // overlaps dV(t), dK(t) and dP(t+1).
+      // Per tile t (TMEM buffer t & 1): dP(t) over S^T(t) as soon as the
+      // softmax has copied S^T(t) into its registers (kSFree), then S(t+1)
+      // into the other buffer (once dK(t-1) has read dS^T(t-1) there and the
+      // next Q stage has landed), dV(t) once P^T(t) is in shared memory,
+      // dK(t) once dS^T(t) is in TMEM. No MMA waits for the one before it to
+      // complete, so the softmax of tile t (its exponentials) overlaps dP(t),
+      // S(t+1), and dV / dK of tile t - 1.
       bool ok = wait_bar(c, kKvFull, 0, 2);
       int n_tiles = 0;  // tiles whose dK MMAs were issued
+      int n_dv = 0;     // tiles whose dV MMAs were issued
       QTileIter it(hpc, n0, sq);
       bool have = ok && it.next();
       if (have) {
         have = wait_bar(c, kQFull0, 0, 3);
         if (have) {
           ptx::tc_fence_after();
-          issue_S(0);
-          ptx::mma_commit(c.bar(kSFull));
-          issue_dP(0);
-          ptx::mma_commit(c.bar(kdPFull));
+          issue_S(0, t_buf0);
+          ptx::mma_commit(c.bar(kSFull0));
         }
       }
       int t = 0;
       while (have) {
         const int st = t & 1;
+        const uint32_t buf = t_buf0 + st * 128;
         const uint64_t dq_mn = ptx::desc_add(dQmn, st * L::kTile);
         const uint64_t ddo_mn = ptx::desc_add(ddOmn, st * L::kTile);
-        // S(t+1) goes first (the softmax's next step waits on it), once the
-        // softmax has copied S^T(t) out of TMEM. It needs its Q stage, which
-        // dK(t-1) released; if that load has not landed yet, dV(t) goes first.
-        have = it.next();
-        const int st1 = (t + 1) & 1;
+        if (!wait_bar(c, kSFree, t & 1, 13)) break;
+        ptx::tc_fence_after();
+        issue_dP(st, buf);
+        ptx::mma_commit(c.bar(kdPFull));
+        // S(t+1) into buffer st ^ 1: Q(t+1) must have landed (its stage was
+        // released by dK(t-1)) and dK(t-1) must have read dS^T(t-1) from that
+        // buffer (its completion is phase (t - 1) >> 1 of kMma40 + (st ^ 1)).
+        const bool have1 = it.next();
+        const int st1 = st ^ 1;
         const uint32_t qpar = ((t + 1) >> 1) & 1;
-        bool s_done = false;
+        const uint32_t mpar = t > 0 ? ((t - 1) >> 1) & 1 : 0;
+        bool s_done = !have1;
         auto try_S = [&]() {
-          if (have && !s_done && ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
+          if (!s_done && (t == 0 || ptx::mbar_try_wait(c.bar(kMma40 + st1), mpar)) &&
+              ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
             ptx::tc_fence_after();
-            issue_S(st1);
-            ptx::mma_commit(c.bar(kSFull));
+            issue_S(st1, t_buf0 + st1 * 128);
+            ptx::mma_commit(c.bar(kSFull0 + st1));
             s_done = true;
           }
         };
-        if (have && !wait_bar(c, kSFree, t & 1, 13)) break;
         try_S();
         if (!wait_bar(c, kP1Full, t & 1, 4)) break;
         ptx::tc_fence_after();
@@ -519,43 +578,43 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(kMma3));
+        ++n_dv;
         try_S();
         if (!wait_bar(c, kP2Full, t & 1, 7)) break;
         ptx::tc_fence_after();
-        // MMA4 dK += dS^T Q : A = dS^T (TMEM fp16 pairs), B = Q MN-major over d
+        // MMA4 dK += dS^T Q : A = dS^T (TMEM fp16 pairs in this tile's buffer),
+        // B = Q MN-major over d
 #pragma unroll
         for (int s = 0; s < BM / 16; ++s) {
-          const uint32_t a_col = t_dP + (s >> 2) * 64 + (s & 3) * 8;
+          const uint32_t a_col = buf + (s >> 2) * 64 + (s & 3) * 8;
           ptx::mma_ts(t_dK, a_col, ptx::desc_add(dq_mn, s * 2048), id_KV,
                       (t > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(kQEmpty0 + st));
-        ptx::mma_commit(c.bar(kMma4));
+        ptx::mma_commit(c.bar(kMma40 + st));
         ++n_tiles;
-        if (have && !s_done) {
+        if (!s_done) {
+          if (t > 0 && !wait_bar(c, kMma40 + st1, mpar, 6)) break;
           if (!wait_bar(c, kQFull0 + st1, qpar, 5)) break;
           ptx::tc_fence_after();
-          issue_S(st1);
-          ptx::mma_commit(c.bar(kSFull));
+          issue_S(st1, t_buf0 + st1 * 128);
+          ptx::mma_commit(c.bar(kSFull0 + st1));
         }
-        if (have) {
-          if (!wait_bar(c, kMma4, t & 1, 6)) break;
-          ptx::tc_fence_after();
-          issue_dP(st1);
-          ptx::mma_commit(c.bar(kdPFull));
-        }
+        have = have1;
         ++t;
       }
       ptx::mma_commit(c.bar(kAccFull));
       // The last dV / dK / Q-stage commits are waited by nobody else: wait
       // for them here, so that no commit arrival is still in flight when the
       // CTA exits (a late one would land on the barriers of the next CTA on
-      // this SM).
-      if (n_tiles > 0) {
-        drain_bar(c, kMma3, (n_tiles - 1) & 1);
-        drain_bar(c, kMma4, (n_tiles - 1) & 1);
-        drain_bar(c, kQEmpty0, (((n_tiles + 1) >> 1) - 1) & 1);
-        if (n_tiles > 1) drain_bar(c, kQEmpty0 + 1, ((n_tiles >> 1) - 1) & 1);
+      // this SM). Buffer / stage b took the commits of tiles b, b + 2, ...
+      if (n_dv > 0) drain_bar(c, kMma3, (n_dv - 1) & 1);
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const int n_b = (n_tiles + 1 - b2) >> 1;
+        if (n_b > 0) {
+          drain_bar(c, kMma40 + b2, (n_b - 1) & 1);
+          drain_bar(c, kQEmpty0 + b2, (n_b - 1) & 1);
+        }
       }
     }
     __syncwarp();
@@ -574,8 +633,9 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       if (!wait_bar(c, kQFull0 + st, (t >> 1) & 1, 8)) { ok = false; break; }
       const float* lse_s = reinterpret_cast<const float*>(smem + L::LSE + st * 512);
       const float* dl_s = reinterpret_cast<const float*>(smem + L::DLT + st * 512);
-      if (!wait_bar(c, kSFull, t & 1, 9)) { ok = false; break; }
+      if (!wait_bar(c, kSFull0 + st, (t >> 1) & 1, 9)) { ok = false; break; }
       ptx::tc_fence_after();
+      const uint32_t buf = t_buf0 + st * 128;  // this tile's TMEM buffer
       const int h = h_first + it.hl;
       const int m0 = it.mt * BM;
       // Live queries of this key row within the tile, [qlo, qhi]. A row
@@ -589,7 +649,10 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // past the lengths are clamped into the tensor (their P is zero)
       const int jc = kMayBeRagged ? imin(j, sq.lk - 1) : j;
       const float* brow = nullptr;
-      if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + jc;
+      if constexpr (BIAS && !kTB) brow = p.bias + ((int64_t)h * p.Sq + m0) * p.Sk + jc;
+      if constexpr (kTB) {
+        if (!wait_bar(c, kBiasFull, t & 1, 15)) { ok = false; break; }
+      }
       float* dbrow = nullptr;
       if constexpr (DBIAS)
         dbrow = p.dbias + b * p.dbias_bstride + ((int64_t)h * p.Sq + m0) * p.Sk + j;
@@ -599,11 +662,11 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       float pv[64];
       {
         uint32_t sr[64];
-        ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
-        ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
+        ptx::tmem_ld32(buf + lane_off + wg * 64, sr);
+        ptx::tmem_ld32(buf + lane_off + wg * 64 + 32, sr + 32);
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(c.bar(kSFree));  // S^T(t) is in registers: MMA1 may overwrite it
+        ptx::mbar_arrive(c.bar(kSFree));  // S^T(t) is in registers: MMA2 may overwrite it
         uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -618,6 +681,12 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 #pragma unroll
               for (int u = 0; u < 4; ++u)
                 bv[u] = __ldg(brow + (int64_t)imin(q0 + e4 + u, qcap) * p.Sk);
+            } else if constexpr (kTB) {
+              // bias (query q0 + e4 + u, key jl) of the tile in shared memory
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                bv[u] = *reinterpret_cast<const float*>(smem + L::BIAS +
+                                                        bias_off(q0 + e4 + u, jl));
             } else if constexpr (BIAS) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + (int64_t)(q0 + e4 + u) * p.Sk);
@@ -645,6 +714,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             pk[cc * 16 + e4 / 2 + 1] = pack_half2(pv[cc * 32 + e4 + 2], pv[cc * 32 + e4 + 3]);
           }
         }
+        if constexpr (kTB) ptx::mbar_arrive(c.bar(kBiasEmpty));  // bias tile read
         // the previous tile's dV has finished reading the P^T buffer
         if (t > 0 && !wait_bar(c, kMma3, (t - 1) & 1, 12)) { ok = false; break; }
 #pragma unroll
@@ -657,7 +727,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         ptx::mbar_arrive(c.bar(kP1Full));
       }
       // phase 2: dS^T = P^T (dP^T - D), fp16 pairs over the front half of this
-      // group's dP^T columns (A operand of dK)
+      // group's dP^T columns in the tile's buffer (A operand of dK)
       if (!wait_bar(c, kdPFull, t & 1, 10)) { ok = false; break; }
       ptx::tc_fence_after();
 #pragma unroll
@@ -666,7 +736,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         uint32_t live_d = 0xffffffffu;
         if constexpr (DBIAS && RB) live_d = partial ? kv_chunk_bits(qlo, qhi, q0) : live_d;
         uint32_t dr[32];
-        ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
+        ptx::tmem_ld32(buf + lane_off + wg * 64 + cc * 32, dr);
         ptx::tmem_wait_ld();
         uint32_t dk[16];
 #pragma unroll
@@ -695,7 +765,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
         }
         // columns [cc 16, cc 16 + 16) were read above (chunk 0 covers 0-31)
-        ptx::tmem_st16(t_dP + lane_off + wg * 64 + cc * 16, dk);
+        ptx::tmem_st16(buf + lane_off + wg * 64 + cc * 16, dk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -781,9 +851,11 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
 template <int D, bool BIAS, bool RB>
 __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                       const CUtensorMap* tmV, const CUtensorMap* tmdO,
-                                      const TcParams& p, uint8_t* smem, uint32_t sbase, int qi) {
+                                      const CUtensorMap* tmB, const TcParams& p, uint8_t* smem,
+                                      uint32_t sbase, int qi) {
   using L = SmemQ<D>;
   constexpr bool kMayBeRagged = RB || !BIAS;  // as in the key-major CTA (dbias is not used here)
+  constexpr bool kTB = tma_bias<D, BIAS, RB>();  // bias tiles through TMA (whole tiles)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nmt = p.Sqs / BM;
@@ -800,13 +872,17 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 256, 1, 1, 1, 1};
+  // qQdoFull, qKvFull0/1, qKvEmpty0/1, qSFull0/1/2, qSFree, qdPFull, qDsFull, qMma30/1/2,
+  // qAccFull, qBiasFull0/1, qBiasEmpty0/1
+  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 1, 256, 1, 1, 1, 1,
+                                   1, 1, 256, 256};
   init_common(c, sbase + L::MISC, kQBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
-  // TMEM: [0, D) dQ, then S buffers 0 / 1 and dP (128 columns each)
+  // TMEM: [0, D) dQ, then three 128-column buffers; tile t works in buffer
+  // t % 3 (S, then dP over it, then dS over the front half of each
+  // warpgroup's columns)
   const uint32_t t_dQ = tmem;
-  const uint32_t t_S0 = tmem + 128;
-  const uint32_t t_dP = tmem + 384;
+  const uint32_t t_buf0 = tmem + 128;
   const uint32_t sQ = sbase + L::Q, sdO = sbase + L::dO;
   bool epi_ok = false;
   int n_iters = 0;
@@ -827,7 +903,20 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       while (it.next()) {
         const int st = t & 1;
         const int use = t >> 1;
-        if (use > 0 && !wait_bar(c, qKvEmpty0 + st, (use - 1) & 1, 21)) break;
+        if constexpr (kTB) {
+          // the tile's bias into stage st once the softmax read tile t - 2's
+          if (use > 0 && !wait_bar(c, qBiasEmpty0 + st, (use - 1) & 1, 20)) break;
+          const uint32_t bfull = c.bar(qBiasFull0 + st);
+          ptx::mbar_arrive_expect_tx(bfull, 4 * kSlab);
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx)
+            ptx::tma_load_2d(sbase + L::BIAS + st * 4 * kSlab + bx * kSlab, tmB, bfull,
+                             it.nt * BN + 32 * bx, h * p.Sq + m0);
+        }
+        if (use > 0 && !wait_bar(c, qKvEmpty0 + st, (use - 1) & 1, 21)) {
+          if constexpr (kTB) issued[st] = -(use + 1);  // the bias copy of this use is in flight
+          break;
+        }
         const int krow = (b * p.Hk + g) * p.Sks + it.nt * BN;
         const uint32_t full = c.bar(qKvFull0 + st);
         ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
@@ -840,8 +929,14 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ++t;
       }
       drain_bar(c, qQdoFull, 0);
-      for (int st = 0; st < 2; ++st)
-        if (issued[st] > 0) drain_bar(c, qKvFull0 + st, (issued[st] - 1) & 1);
+      for (int st = 0; st < 2; ++st) {
+        // issued[st] = uses of stage st whose K / V (and bias) copies went
+        // out; negative: the last use's bias copy went out without its K / V
+        const int n_kv = issued[st] >= 0 ? issued[st] : -issued[st] - 1;
+        const int n_b = issued[st] >= 0 ? issued[st] : -issued[st];
+        if (n_kv > 0) drain_bar(c, qKvFull0 + st, (n_kv - 1) & 1);
+        if (kTB && n_b > 0) drain_bar(c, qBiasFull0 + st, (n_b - 1) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -856,90 +951,116 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       const uint64_t dKk = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dVk = ptx::smem_desc_sw128(sbase + L::V, 16, 1024);
       const uint64_t dKmn = ptx::smem_desc_sw128(sbase + L::K, kSlab, 1024);
-      auto issue_S = [&](int t) {  // MMA1' S = Q K^T into S buffer t & 1
+      auto issue_S = [&](int t) {  // MMA1' S = Q K^T into buffer t % 3 (K / V stage t & 1)
         const uint64_t dk = ptx::desc_add(dKk, (t & 1) * L::kTile);
-        const uint32_t dst = t_S0 + (t & 1) * 128;
+        const uint32_t dst = t_buf0 + (t % 3) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(dst, ptx::desc_add(dQ, off), ptx::desc_add(dk, off), id_S, s > 0);
         }
       };
-      auto issue_dP = [&](int t) {  // MMA2' dP = dO V^T
+      auto issue_dP = [&](int t) {  // MMA2' dP = dO V^T over S(t) in buffer t % 3
         const uint64_t dv = ptx::desc_add(dVk, (t & 1) * L::kTile);
+        const uint32_t dst = t_buf0 + (t % 3) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dP, ptx::desc_add(ddO, off), ptx::desc_add(dv, off), id_S, s > 0);
+          ptx::mma_ss(dst, ptx::desc_add(ddO, off), ptx::desc_add(dv, off), id_S, s > 0);
         }
       };
-      // Per tile t: dQ(t) once dS(t) replaced S(t) in TMEM, dP(t+1) (the
-      // softmax read dP(t)), then S(t+2) into the buffer dQ(t) released. S is
-      // one tile ahead, so the softmax computes P(t+1) while dQ(t) and
-      // dP(t+1) are on the tensor pipe; only its dS half waits for dP.
+      auto issue_dQ = [&](int t) {  // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major
+        const uint64_t dk = ptx::desc_add(dKmn, (t & 1) * L::kTile);
+        const uint32_t src = t_buf0 + (t % 3) * 128;
+#pragma unroll
+        for (int s = 0; s < BN / 16; ++s) {
+          const uint32_t a_col = src + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_dQ, a_col, ptx::desc_add(dk, s * 2048), id_dQ,
+                      (t > 0 || s > 0) ? 1u : 0u);
+        }
+      };
+      // Per tile t (TMEM buffer t % 3): dP(t) over S(t) as soon as the softmax
+      // has copied S(t) into its registers (qSFree); then S(t+1) and dQ(t),
+      // whichever can go first. S(t+1) needs the next K / V stage (released
+      // by dQ(t-1)) and buffer (t+1) % 3, last read by dQ(t-2); dQ(t) needs
+      // dS(t). The softmax's exponentials of tile t overlap dP(t), S(t+1)
+      // and dQ(t-1); S(t+1) is ready before the softmax finishes tile t.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
       int n_tiles = 0;  // tiles whose dQ MMAs were issued
       KTileIter it(m0, sq);
       bool have = ok && it.next();
-      bool have1 = false;
       if (have) {
         have = wait_bar(c, qKvFull0, 0, 23);
         if (have) {
           ptx::tc_fence_after();
           issue_S(0);
           ptx::mma_commit(c.bar(qSFull0));
-          issue_dP(0);
-          ptx::mma_commit(c.bar(qdPFull));
-          have1 = it.next();
-          if (have1) {
-            if (!wait_bar(c, qKvFull0 + 1, 0, 24)) { have = have1 = false; }
-            if (have1) {
-              ptx::tc_fence_after();
-              issue_S(1);
-              ptx::mma_commit(c.bar(qSFull1));
-            }
-          }
         }
       }
       int t = 0;
       while (have) {
-        const int st = t & 1;
-        if (!wait_bar(c, qDsFull, t & 1, 26)) break;
+        const int st = t & 1, bt = t % 3;
+        if (!wait_bar(c, qSFree, t & 1, 24)) break;
         ptx::tc_fence_after();
-        // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major over d
-        const uint64_t dk = ptx::desc_add(dKmn, st * L::kTile);
-        const uint32_t t_S = t_S0 + st * 128;
-#pragma unroll
-        for (int s = 0; s < BN / 16; ++s) {
-          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_dQ, a_col, ptx::desc_add(dk, s * 2048), id_dQ,
-                      (t > 0 || s > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(c.bar(qMma3));
-        ptx::mma_commit(c.bar(qKvEmpty0 + st));
-        ++n_tiles;
-        if (!have1) break;  // tile t was the last one
-        ptx::tc_fence_after();
-        issue_dP(t + 1);  // the softmax already read dP(t)
+        issue_dP(t);
         ptx::mma_commit(c.bar(qdPFull));
-        const bool have2 = it.next();
-        if (have2) {
-          // S(t+2) into buffer t & 1 once dQ(t) has read dS(t) from it
-          if (!wait_bar(c, qKvFull0 + st, ((t + 2) >> 1) & 1, 24)) break;
-          if (!wait_bar(c, qMma3, t & 1, 25)) break;
-          ptx::tc_fence_after();
-          issue_S(t + 2);
-          ptx::mma_commit(c.bar(st == 0 ? qSFull0 : qSFull1));
+        const bool have1 = it.next();
+        const int b1 = (t + 1) % 3;
+        const uint32_t kvpar = ((t + 1) >> 1) & 1;              // fill of K / V stage st ^ 1
+        const uint32_t mpar = t >= 2 ? ((t - 2) / 3) & 1 : 0u;  // dQ(t-2) on qMma30 + b1
+        bool s_done = !have1, q_done = false;
+        uint32_t idle = 0;
+        uint64_t t0 = 0;
+        while (!s_done || !q_done) {
+          bool did = false;
+          if (!s_done && (t < 2 || ptx::mbar_test_wait(c.bar(qMma30 + b1), mpar)) &&
+              ptx::mbar_test_wait(c.bar(qKvFull0 + (st ^ 1)), kvpar)) {
+            ptx::tc_fence_after();
+            issue_S(t + 1);
+            ptx::mma_commit(c.bar(qSFull0 + b1));
+            s_done = true;
+            did = true;
+          }
+          if (!q_done && ptx::mbar_test_wait(c.bar(qDsFull), t & 1)) {
+            ptx::tc_fence_after();
+            issue_dQ(t);
+            ptx::mma_commit(c.bar(qMma30 + bt));
+            ptx::mma_commit(c.bar(qKvEmpty0 + st));
+            ++n_tiles;
+            q_done = true;
+            did = true;
+          }
+          if (did) {
+            idle = 0;
+            t0 = 0;
+          } else if ((++idle & 63u) == 0) {  // bounded, as every other wait
+            if (*c.abort) { ok = false; break; }
+            const uint64_t now = ptx::globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kTimeoutNs) {
+              *c.abort = 1;
+              report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 25);
+              ok = false;
+              break;
+            }
+          }
         }
-        have1 = have2;
+        if (!ok) break;
+        have = have1;
         ++t;
       }
       ptx::mma_commit(c.bar(qAccFull));
-      // the last dQ / K-V-stage commits: waited here (see the key-major CTA)
-      if (n_tiles > 0) {
-        drain_bar(c, qMma3, (n_tiles - 1) & 1);
-        drain_bar(c, qKvEmpty0, (((n_tiles + 1) >> 1) - 1) & 1);
-        if (n_tiles > 1) drain_bar(c, qKvEmpty0 + 1, ((n_tiles >> 1) - 1) & 1);
+      // the last dQ / K-V-stage commits: waited here (see the key-major CTA);
+      // buffer b took the dQ commits of tiles b, b + 3, ..., stage s those of
+      // tiles s, s + 2, ...
+      for (int b3 = 0; b3 < 3; ++b3) {
+        const int n_b = (n_tiles - b3 + 2) / 3;
+        if (n_b > 0) drain_bar(c, qMma30 + b3, (n_b - 1) & 1);
+      }
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int n_s = (n_tiles + 1 - s2) >> 1;
+        if (n_s > 0) drain_bar(c, qKvEmpty0 + s2, (n_s - 1) & 1);
       }
     }
     __syncwarp();
@@ -956,18 +1077,24 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
     const float nl = row_in ? p.lse[row] * -kLog2e : 0.f;  // -inf rows: see the partial-tile mask
     const float dl = row_in ? p.delta[row] : 0.f;
     const float* brow = nullptr;
-    if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
+    if constexpr (BIAS && !kTB) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
+    // TMA bias: this row's 128-byte rows of the four boxes (chunk c of the
+    // row sits at chunk c ^ (il & 7))
+    const uint32_t brow_s = L::BIAS + il * 128;
     KTileIter it(m0, sq);
     int t = 0;
     bool ok = true;
     while (it.next()) {
-      if (!wait_bar(c, (t & 1) ? qSFull1 : qSFull0, (t >> 1) & 1, 27)) { ok = false; break; }
+      if (!wait_bar(c, qSFull0 + t % 3, (t / 3) & 1, 27)) { ok = false; break; }
       ptx::tc_fence_after();
       const int n0 = it.nt * BN;
       const int kcap = sq.lk - n0;  // keys [0, kcap) of the tile exist
       int klo, khi, ksink;
       const bool partial = q_row_live<kMayBeRagged>(sq, m0, n0, i, &klo, &khi, &ksink);
-      const uint32_t t_S = t_S0 + (t & 1) * 128;
+      const uint32_t t_S = t_buf0 + (t % 3) * 128;  // this tile's TMEM buffer
+      if constexpr (kTB) {
+        if (!wait_bar(c, qBiasFull0 + (t & 1), (t >> 1) & 1, 30)) { ok = false; break; }
+      }
       // phase 1: P from S (registers)
       float pv[64];
       {
@@ -975,6 +1102,8 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ptx::tmem_ld32(t_S + lane_off + wg * 64, sr);
         ptx::tmem_ld32(t_S + lane_off + wg * 64 + 32, sr + 32);
         ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar(qSFree));  // S(t) is in registers: MMA2' may overwrite it
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int k0 = wg * 64 + cc * 32;  // first key of this chunk within the tile
@@ -987,6 +1116,15 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
               // of ragged length is not 16-byte aligned
 #pragma unroll
               for (int u = 0; u < 4; ++u) bv[u] = __ldg(brow + n0 + imin(k0 + e4 + u, kcap - 1));
+            } else if constexpr (kTB) {
+              // keys k0 + e4 .. + 3: box k0 / 32, 16-byte chunk e4 / 4 of the row
+              const float4 b4 = *reinterpret_cast<const float4*>(
+                  smem + brow_s + (t & 1) * 4 * kSlab + (k0 >> 5) * kSlab +
+                  ((((uint32_t)e4 >> 2) ^ ((uint32_t)il & 7u)) << 4));
+              bv[0] = b4.x;
+              bv[1] = b4.y;
+              bv[2] = b4.z;
+              bv[3] = b4.w;
             } else if constexpr (BIAS) {
               const float4 b4 = __ldg(reinterpret_cast<const float4*>(brow + n0 + k0 + e4));
               bv[0] = b4.x;
@@ -1013,14 +1151,15 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
           }
         }
       }
+      if constexpr (kTB) ptx::mbar_arrive(c.bar(qBiasEmpty0 + (t & 1)));  // bias stage read
       // phase 2: dS = P (dP - D), fp16 pairs over the (already read) front
-      // half of this group's S columns (A operand of dQ)
+      // half of this group's dP columns in the tile's buffer (A operand of dQ)
       if (!wait_bar(c, qdPFull, t & 1, 29)) { ok = false; break; }
       ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t dr[32];
-        ptx::tmem_ld32(t_dP + lane_off + wg * 64 + cc * 32, dr);
+        ptx::tmem_ld32(t_S + lane_off + wg * 64 + cc * 32, dr);
         ptx::tmem_wait_ld();
         uint32_t dk[16];
 #pragma unroll
@@ -1094,7 +1233,7 @@ template <int D, bool BIAS, bool DBIAS, bool RB>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   // 1 KiB alignment of the 128B-swizzle atoms (uniform over the grid)
@@ -1107,6 +1246,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
     ptx::prefetch_tmap(&tmdO);
+    if constexpr (tma_bias<D, BIAS, RB>()) ptx::prefetch_tmap(&tmB);
   }
   // everything below reads what the pre-pass wrote (launched as its
   // programmatic dependent, this grid may start before the pre-pass ends)
@@ -1122,10 +1262,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     if (bits && (threadIdx.x & 31) == 0) report(p.status, ATTN_ERR_RANGE, bits);
   }
   if ((int)blockIdx.x < p.kv_ctas) {
-    kv_cta<D, BIAS, DBIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase);
+    kv_cta<D, BIAS, DBIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase);
   } else {
     const int qi = (int)blockIdx.x - p.kv_ctas;
-    q_cta<D, BIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, p, smem, sbase, qi);
+    q_cta<D, BIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase, qi);
   }
 }
 
@@ -1198,10 +1338,29 @@ bool make_map(CUtensorMap* m, const __half* base, uint64_t rows, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The kernel's tensor maps: fp16 staged q, k, v, dO, and the fp32 bias (TMA
+// bias path only; a copy of q otherwise, never read).
+struct TcMaps {
+  CUtensorMap q, k, v, dO, bias;
+};
+
+// Row-major [rows][cols] fp32 bias (rows = heads x queries), boxes of 128
+// rows x 32 columns (128 bytes), 128B swizzle: the tiles the TMA bias path
+// loads (cols a multiple of 4, so that rows are 16-byte aligned).
+bool make_bias_map(CUtensorMap* m, const float* base, uint64_t rows, int cols) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, bool BIAS, bool DBIAS, bool RB>
-cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                           const CUtensorMap& dO, const TcParams& p, int grid,
-                           cudaStream_t stream) {
+cudaError_t launch_variant(const TcMaps& m, const TcParams& p, int grid, cudaStream_t stream) {
   auto kern = attn_bwd_tc_kernel<D, BIAS, DBIAS, RB>;
   static bool configured = false;  // attribute set once per process and variant
   if (!configured) {
@@ -1210,23 +1369,22 @@ cudaError_t launch_variant(const CUtensorMap& q, const CUtensorMap& k, const CUt
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(kern, dim3(grid), dim3(kThreads), (size_t)smem_total<D>(), stream, q,
-                          k, v, dO, p);
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), (size_t)smem_total<D>(), stream, m.q,
+                          m.k, m.v, m.dO, m.bias, p);
 }
 
 template <int D>
-cudaError_t launch_d(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                     const CUtensorMap& dO, const TcParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_d(const TcMaps& m, const TcParams& p, int grid, cudaStream_t stream) {
   // without bias and dbias, ragged lengths need no separate instantiation
   if (p.ragged) {
-    if (p.bias && p.dbias) return launch_variant<D, true, true, true>(q, k, v, dO, p, grid, stream);
-    if (p.bias) return launch_variant<D, true, false, true>(q, k, v, dO, p, grid, stream);
-    if (p.dbias) return launch_variant<D, false, true, true>(q, k, v, dO, p, grid, stream);
+    if (p.bias && p.dbias) return launch_variant<D, true, true, true>(m, p, grid, stream);
+    if (p.bias) return launch_variant<D, true, false, true>(m, p, grid, stream);
+    if (p.dbias) return launch_variant<D, false, true, true>(m, p, grid, stream);
   }
-  if (p.bias && p.dbias) return launch_variant<D, true, true, false>(q, k, v, dO, p, grid, stream);
-  if (p.bias) return launch_variant<D, true, false, false>(q, k, v, dO, p, grid, stream);
-  if (p.dbias) return launch_variant<D, false, true, false>(q, k, v, dO, p, grid, stream);
-  return launch_variant<D, false, false, false>(q, k, v, dO, p, grid, stream);
+  if (p.bias && p.dbias) return launch_variant<D, true, true, false>(m, p, grid, stream);
+  if (p.bias) return launch_variant<D, true, false, false>(m, p, grid, stream);
+  if (p.dbias) return launch_variant<D, false, true, false>(m, p, grid, stream);
+  return launch_variant<D, false, false, false>(m, p, grid, stream);
 }
 
 // Query heads per KV head are split over cs key-major CTAs. Every CTA pays a
@@ -1332,8 +1490,17 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.status = st;
   const int q_ctas = pr.B * pr.Hq * (p.Sqs / BM);
   const int grid = p.kv_ctas + q_ctas;
-  if (pr.D == 64) return launch_d<64>(mq, mk, mv, mdo, p, grid, stream);
-  return launch_d<128>(mq, mk, mv, mdo, p, grid, stream);
+  TcMaps maps;
+  maps.q = mq;
+  maps.k = mk;
+  maps.v = mv;
+  maps.dO = mdo;
+  maps.bias = mq;
+  if (pr.D == 64 && bias != nullptr && !p.ragged &&
+      !make_bias_map(&maps.bias, bias, (uint64_t)pr.Hq * pr.Sq, pr.Sk))
+    return cudaErrorInvalidValue;
+  if (pr.D == 64) return launch_d<64>(maps, p, grid, stream);
+  return launch_d<128>(maps, p, grid, stream);
 }
 
 }  // namespace attn

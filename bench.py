@@ -365,7 +365,6 @@ def run_ours(args):
 # scaled by the token count: its DRAM bytes are Q, dO and dQ, all linear in Sq). An entry
 # goes back to None when its kernel changes.
 NCU_TRAFFIC = {
-    "gqa4_causal_s1024_d128": 29.720e6,
     "sparse_scfa_s4096_h64_d512": 4 * 224.48e6,
 }
 
