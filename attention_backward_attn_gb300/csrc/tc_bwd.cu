@@ -80,10 +80,9 @@ struct SmemKV {
   static constexpr int kTile = (D / 64) * kSlab;  // a [128][D] fp16 operand tile
   static constexpr int K = 0;
   static constexpr int V = K + kTile;
-  static constexpr int Q = V + kTile;        // 2 stages
-  static constexpr int dO = Q + 2 * kTile;   // 2 stages
-  static constexpr int dS = dO + 2 * kTile;  // P^T: [128 keys][128 queries] fp16, 2 slabs
-  static constexpr int LSE = dS + 2 * kSlab; // 2 stages x 128 fp32
+  static constexpr int Q = V + kTile;        // 3 stages
+  static constexpr int dO = Q + 3 * kTile;   // 2 stages
+  static constexpr int LSE = dO + 2 * kTile; // 2 stages x 128 fp32 (with the dO stage)
   static constexpr int DLT = LSE + 1024;     // 2 stages x 128 fp32
   static constexpr int BAR = DLT + 1024;     // mbarriers (up to 32)
   static constexpr int MISC = BAR + 256;     // TMEM base, abort flag
@@ -91,21 +90,22 @@ struct SmemKV {
   // TMA boxes of 32 keys (128B-swizzled 128-byte rows), one stage
   static constexpr int BIAS = (MISC + 16 + 1023) / 1024 * 1024;
   static constexpr int TOTAL = D == 64 ? BIAS + 4 * kSlab : MISC + 16;
-  // end-of-kernel staging of dK / dV rows for the bulk reductions (reuses Q..dS)
+  // end-of-kernel staging of dK / dV rows for the bulk reductions (reuses Q, dO)
   static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
   static constexpr int STAGE = Q;
-  static_assert(2 * 128 * kStageRow <= 4 * kTile + 2 * kSlab, "staging fits");
+  static_assert(2 * 128 * kStageRow <= 5 * kTile, "staging fits");
 };
 
 // Shared memory of a query-major CTA.
 template <int D>
 struct SmemQ {
   static constexpr int kTile = (D / 64) * kSlab;
+  static constexpr int kKS = D == 128 ? 3 : 2;  // K stages (the bias stages take the room at D = 64)
   static constexpr int Q = 0;
   static constexpr int dO = Q + kTile;
-  static constexpr int K = dO + kTile;      // 2 stages
-  static constexpr int V = K + 2 * kTile;   // 2 stages
-  static constexpr int BAR = V + 2 * kTile;  // mbarriers (up to 32)
+  static constexpr int K = dO + kTile;          // kKS stages
+  static constexpr int V = K + kKS * kTile;     // 2 stages
+  static constexpr int BAR = V + 2 * kTile;     // mbarriers (up to 32)
   static constexpr int MISC = BAR + 256;
   // D = 64 with a bias: two stages of the tile's bias [128 queries][128 keys]
   // fp32 (four 128B-swizzled TMA boxes of 32 keys each)
@@ -114,7 +114,7 @@ struct SmemQ {
   // end-of-kernel staging of dQ rows for the copy-engine stores (reuses K, V)
   static constexpr int kStageRow = D * 4 + 16;  // padded fp32 row: conflict-free v4 stores
   static constexpr int STAGE = K;
-  static_assert(128 * kStageRow <= 4 * kTile, "staging fits");
+  static_assert(128 * kStageRow <= (kKS + 2) * kTile, "staging fits");
 };
 
 static_assert(SmemKV<64>::TOTAL <= 232448 && SmemQ<64>::TOTAL <= 232448 &&
@@ -146,26 +146,28 @@ constexpr int smem_total() {
 // barrier indices, key-major CTA
 // Tile t works in TMEM buffer t & 1: MMA1 writes S^T there (kSFull0 + (t & 1)),
 // the softmax copies it out (kSFree), MMA2 writes dP^T over it (kdPFull), the
-// softmax turns dP^T into dS^T written back into the same columns
-// (kP2Full, 256 arrivals) and MMA4 reads it (kMma40 + (t & 1): that buffer
-// is free again). P^T goes to shared memory (kP1Full, 256 arrivals) for MMA3
-// (kMma3: dV of the tile done, the P^T buffer is free again).
-// kBiasFull / kBiasEmpty: the tile's bias landed in shared memory / was read
-// by the softmax (256 arrivals), on the TMA bias path.
-enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 3, kSFull0 = 5, kSFree = 7, kP1Full = 8,
-             kP2Full = 9, kdPFull = 10, kMma3 = 11, kMma40 = 12, kAccFull = 14, kBiasFull = 15,
-             kBiasEmpty = 16, kKvBars = 17 };
+// softmax writes dS^T and P^T back into the same columns (kP2Full, 256
+// arrivals) and MMA3 / MMA4 read them (kMma40 + (t & 1): that buffer is free
+// again). Q(t) uses stage t % 3 (kQFull0.., kQEmpty0.. once dK(t) read it),
+// dO(t) with LSE / delta stage t & 1 (kOFull0.., kOEmpty0.. once dV(t) read
+// it). kBiasFull / kBiasEmpty: the tile's bias landed in shared memory / was
+// read by the softmax (256 arrivals), on the TMA bias path.
+enum BarKV { kKvFull = 0, kQFull0 = 1, kQEmpty0 = 4, kOFull0 = 7, kOEmpty0 = 9, kSFull0 = 11,
+             kSFree = 13, kdPFull = 14, kP2Full = 15, kMma40 = 16, kAccFull = 18,
+             kBiasFull = 19, kBiasEmpty = 20, kKvBars = 21 };
 // barrier indices, query-major CTA
 // Tile t works in TMEM buffer t % 3: MMA1' writes S there (qSFull0 + t % 3),
 // the softmax copies it out (qSFree), MMA2' writes dP over it (qdPFull), the
 // softmax writes dS back into the same columns (qDsFull, 256 arrivals) and
 // MMA3' reads it (qMma30 + t % 3: that buffer is free again). One S-ready and
 // one MMA3'-done barrier per buffer, so that no barrier can complete two
-// phases before its waiter polls the first.
-// qBiasFull0/1 / qBiasEmpty0/1: the two bias stages (TMA bias path).
-enum BarQ { qQdoFull = 0, qKvFull0 = 1, qKvEmpty0 = 3, qSFull0 = 5, qSFree = 8, qdPFull = 9,
-            qDsFull = 10, qMma30 = 11, qAccFull = 14, qBiasFull0 = 15, qBiasEmpty0 = 17,
-            kQBars = 19 };
+// phases before its waiter polls the first. K(t) uses stage t % kKS
+// (qKFull0.., qKEmpty0.. once dQ(t) read it), V(t) stage t & 1 (qVFull0..,
+// qVEmpty0.. once dP(t) read it); qBiasFull0/1 / qBiasEmpty0/1: the two bias
+// stages (TMA bias path).
+enum BarQ { qQdoFull = 0, qKFull0 = 1, qKEmpty0 = 4, qVFull0 = 7, qVEmpty0 = 9, qSFull0 = 11,
+            qSFree = 14, qdPFull = 15, qDsFull = 16, qMma30 = 17, qAccFull = 20,
+            qBiasFull0 = 21, qBiasEmpty0 = 23, kQBars = 25 };
 
 struct TcParams {
   int B, Hq, Hk, Sq, Sk;
@@ -392,26 +394,28 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  // a ragged problem's query-tile barriers take one more arrival: the
-  // producer warp's plain copy of LSE / delta (the TMA bulk copy needs whole
-  // 16-byte-aligned tiles)
-  const uint32_t qf = p.ragged ? 2u : 1u;
-  // kKvFull, kQFull0/1, kQEmpty0/1, kSFull0/1, kSFree, kP1Full, kP2Full, kdPFull, kMma3,
-  // kMma40/1, kAccFull, kBiasFull, kBiasEmpty
-  const uint32_t counts[kKvBars] = {1, qf, qf, 1, 1, 1, 1, 256, 256, 256, 1, 1, 1, 1, 1, 1, 256};
+  // a ragged problem's dO barriers take one more arrival: the producer warp's
+  // plain copy of LSE / delta (the TMA bulk copy needs whole 16-byte-aligned
+  // tiles)
+  const uint32_t of = p.ragged ? 2u : 1u;
+  // kKvFull, kQFull0-2, kQEmpty0-2, kOFull0/1, kOEmpty0/1, kSFull0/1, kSFree, kdPFull,
+  // kP2Full, kMma40/1, kAccFull, kBiasFull, kBiasEmpty
+  const uint32_t counts[kKvBars] = {1, 1, 1, 1, 1, 1, 1, of, of, 1, 1, 1, 1,
+                                    256, 1, 256, 1, 1, 1, 1, 256};
   init_common(c, sbase + L::MISC, kKvBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
-  const uint32_t t_buf0 = tmem + 2 * D;  // tile t: S^T / dP^T / dS^T at t_buf0 + (t & 1) 128
-  const uint32_t sK = sbase + L::K, sV = sbase + L::V, sDS = sbase + L::dS;
+  const uint32_t t_buf0 = tmem + 2 * D;  // tile t: S^T / dP^T / (dS^T, P^T) at t_buf0 + (t & 1) 128
+  const uint32_t sK = sbase + L::K, sV = sbase + L::V;
   bool epi_ok = false;
   int n_iters = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     // lane 0 waits and issues the copies; with ragged lengths the whole warp
-    // also copies the tile's LSE / delta rows (zero past Sq)
+    // also copies the tile's LSE / delta rows (zero past Sq). Q stages rotate
+    // over three buffers, dO (with LSE / delta) over two.
     if (lane == 0) {
       const int krow = (b * p.Hk + g) * p.Sks + n0;
       ptx::mbar_arrive_expect_tx(c.bar(kKvFull), 2 * L::kTile);
@@ -421,53 +425,66 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         ptx::tma_load_2d(sV + hf * kSlab, tmV, c.bar(kKvFull), hf * 64, krow);
       }
     }
-    int issued[2] = {0, 0};
+    int q_issued[3] = {0, 0, 0};
+    int o_issued[2] = {0, 0};
     int bias_issued = 0;
     if (lane == 0 || p.ragged) {  // warp-uniform when ragged
       QTileIter it(hpc, n0, sq);
       int t = 0;
       while (it.next()) {
-        const int st = t & 1;
-        const int use = t >> 1;
-        if (p.ragged) {
-          bool go = true;
-          if (lane == 0 && use > 0) go = wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1);
-          __syncwarp();
-          if (!__shfl_sync(0xffffffffu, go, 0)) break;
-        } else if (lane == 0 && use > 0 && !wait_bar(c, kQEmpty0 + st, (use - 1) & 1, 1)) {
-          break;
-        }
+        const int qs = t % 3, qu = t / 3;  // Q stage and its use count
+        const int os = t & 1, ou = t >> 1; // dO stage and its use count
         const int h = h_first + it.hl;
         const int m0 = it.mt * BM;
         const int64_t row = ((int64_t)b * p.Hq + h) * p.Sqs + m0;   // staged fp16 rows
         const int64_t lrow = ((int64_t)b * p.Hq + h) * p.Sq + m0;   // LSE / delta rows
-        const uint32_t full = c.bar(kQFull0 + st);
+        bool go = true;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(full, 2 * L::kTile + (p.ragged ? 0 : 2 * 512));
+          // Q(t) once dK(t-3) released its stage
+          if (qu > 0) go = wait_bar(c, kQEmpty0 + qs, (qu - 1) & 1, 1);
+          if (go) {
+            const uint32_t qfull = c.bar(kQFull0 + qs);
+            ptx::mbar_arrive_expect_tx(qfull, L::kTile);
 #pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-            ptx::tma_load_2d(sbase + L::Q + st * L::kTile + hf * kSlab, tmQ, full, hf * 64, (int)row);
-            ptx::tma_load_2d(sbase + L::dO + st * L::kTile + hf * kSlab, tmdO, full, hf * 64, (int)row);
+            for (int hf = 0; hf < D / 64; ++hf)
+              ptx::tma_load_2d(sbase + L::Q + qs * L::kTile + hf * kSlab, tmQ, qfull, hf * 64,
+                               (int)row);
+            q_issued[qs] = qu + 1;
           }
-          if (!p.ragged) {
-            ptx::bulk_load(sbase + L::LSE + st * 512, p.lse + lrow, 512, full);
-            ptx::bulk_load(sbase + L::DLT + st * 512, p.delta + lrow, 512, full);
+          // dO(t), LSE(t), delta(t) once dV(t-2) released the stage
+          if (go && ou > 0) go = wait_bar(c, kOEmpty0 + os, (ou - 1) & 1, 16);
+          if (go) {
+            const uint32_t ofull = c.bar(kOFull0 + os);
+            ptx::mbar_arrive_expect_tx(ofull, L::kTile + (p.ragged ? 0 : 2 * 512));
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf)
+              ptx::tma_load_2d(sbase + L::dO + os * L::kTile + hf * kSlab, tmdO, ofull, hf * 64,
+                               (int)row);
+            if (!p.ragged) {
+              ptx::bulk_load(sbase + L::LSE + os * 512, p.lse + lrow, 512, ofull);
+              ptx::bulk_load(sbase + L::DLT + os * 512, p.delta + lrow, 512, ofull);
+            }
+            o_issued[os] = ou + 1;
           }
           if constexpr (kTB) {
             // the tile's bias rows (one stage: once the softmax read tile t - 1's)
-            if (t > 0 && !wait_bar(c, kBiasEmpty, (t - 1) & 1, 14)) break;
-            const uint32_t bfull = c.bar(kBiasFull);
-            ptx::mbar_arrive_expect_tx(bfull, 4 * kSlab);
+            if (go && t > 0) go = wait_bar(c, kBiasEmpty, (t - 1) & 1, 14);
+            if (go) {
+              const uint32_t bfull = c.bar(kBiasFull);
+              ptx::mbar_arrive_expect_tx(bfull, 4 * kSlab);
 #pragma unroll
-            for (int bx = 0; bx < 4; ++bx)
-              ptx::tma_load_2d(sbase + L::BIAS + bx * kSlab, tmB, bfull, n0 + 32 * bx,
-                               h * p.Sq + m0);
-            ++bias_issued;
+              for (int bx = 0; bx < 4; ++bx)
+                ptx::tma_load_2d(sbase + L::BIAS + bx * kSlab, tmB, bfull, n0 + 32 * bx,
+                                 h * p.Sq + m0);
+              ++bias_issued;
+            }
           }
         }
         if (p.ragged) {
-          float* lse_s = reinterpret_cast<float*>(smem + L::LSE + st * 512);
-          float* dl_s = reinterpret_cast<float*>(smem + L::DLT + st * 512);
+          __syncwarp();
+          if (!__shfl_sync(0xffffffffu, go, 0)) break;
+          float* lse_s = reinterpret_cast<float*>(smem + L::LSE + os * 512);
+          float* dl_s = reinterpret_cast<float*>(smem + L::DLT + os * 512);
 #pragma unroll
           for (int u = 0; u < BM / 32; ++u) {
             const int q = u * 32 + lane;
@@ -476,17 +493,20 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
             dl_s[q] = in ? p.delta[lrow + q] : 0.f;
           }
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(full);
+          if (lane == 0) ptx::mbar_arrive(c.bar(kOFull0 + os));
+        } else if (!go) {
+          break;
         }
-        issued[st] = use + 1;
         ++t;
       }
     }
     if (lane == 0) {
       // no copy may still be landing in shared memory when the CTA ends
       drain_bar(c, kKvFull, 0);
-      for (int st = 0; st < 2; ++st)
-        if (issued[st] > 0) drain_bar(c, kQFull0 + st, (issued[st] - 1) & 1);
+      for (int s = 0; s < 3; ++s)
+        if (q_issued[s] > 0) drain_bar(c, kQFull0 + s, (q_issued[s] - 1) & 1);
+      for (int s = 0; s < 2; ++s)
+        if (o_issued[s] > 0) drain_bar(c, kOFull0 + s, (o_issued[s] - 1) & 1);
       if (bias_issued > 0) drain_bar(c, kBiasFull, (bias_issued - 1) & 1);
     }
     __syncwarp();
@@ -498,123 +518,139 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // operand descriptors, built once (K steps add their offsets)
       const uint64_t dK = ptx::smem_desc_sw128(sK, 16, 1024);
       const uint64_t dV = ptx::smem_desc_sw128(sV, 16, 1024);
-      const uint64_t dDS = ptx::smem_desc_sw128(sDS, 16, 1024);
-      // stage 0 of Q / dO in K-major and MN-major views (stage st: + st kTile)
+      // stage 0 of Q / dO in K-major and MN-major views (stage s: + s kTile)
       const uint64_t dQk = ptx::smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t ddOk = ptx::smem_desc_sw128(sbase + L::dO, 16, 1024);
       const uint64_t dQmn = ptx::smem_desc_sw128(sbase + L::Q, kSlab, 1024);
       const uint64_t ddOmn = ptx::smem_desc_sw128(sbase + L::dO, kSlab, 1024);
-      auto issue_S = [&](int st, uint32_t dst) {  // MMA1 S^T = K Q^T (both K-major over d)
-        const uint64_t dq = ptx::desc_add(dQk, st * L::kTile);
+      auto issue_S = [&](int t) {  // MMA1 S^T = K Q^T (both K-major over d) into buffer t & 1
+        const uint64_t dq = ptx::desc_add(dQk, (t % 3) * L::kTile);
+        const uint32_t dst = t_buf0 + (t & 1) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(dst, ptx::desc_add(dK, off), ptx::desc_add(dq, off), id_S, s > 0);
         }
       };
-      auto issue_dP = [&](int st, uint32_t dst) {  // MMA2 dP^T = V dO^T
-        const uint64_t ddo = ptx::desc_add(ddOk, st * L::kTile);
+      auto issue_dP = [&](int t) {  // MMA2 dP^T = V dO^T over S^T(t)
+        const uint64_t ddo = ptx::desc_add(ddOk, (t & 1) * L::kTile);
+        const uint32_t dst = t_buf0 + (t & 1) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
           ptx::mma_ss(dst, ptx::desc_add(dV, off), ptx::desc_add(ddo, off), id_S, s > 0);
         }
       };
+      // MMA3 dV += P^T dO and MMA4 dK += dS^T Q, A operands from the tile's
+      // TMEM buffer: the 16 queries of K step s sit in chunk ((s & 3) >> 1) of
+      // warpgroup (s >> 2)'s 64 columns, dS^T in its first 16 columns and P^T
+      // in the next 16, 8 columns (fp16 pairs) per step. B = dO / Q MN-major.
+      auto issue_dVdK = [&](int t) {
+        const uint32_t buf = t_buf0 + (t & 1) * 128;
+        const uint64_t ddo_mn = ptx::desc_add(ddOmn, (t & 1) * L::kTile);
+        const uint64_t dq_mn = ptx::desc_add(dQmn, (t % 3) * L::kTile);
+#pragma unroll
+        for (int s = 0; s < BM / 16; ++s) {
+          const uint32_t col = buf + (s >> 2) * 64 + ((s >> 1) & 1) * 32 + (s & 1) * 8;
+          ptx::mma_ts(t_dV, col + 16, ptx::desc_add(ddo_mn, s * 2048), id_KV,
+                      (t > 0 || s > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int s = 0; s < BM / 16; ++s) {
+          const uint32_t col = buf + (s >> 2) * 64 + ((s >> 1) & 1) * 32 + (s & 1) * 8;
+          ptx::mma_ts(t_dK, col, ptx::desc_add(dq_mn, s * 2048), id_KV,
+                      (t > 0 || s > 0) ? 1u : 0u);
+        }
+      };
       // Per tile t (TMEM buffer t & 1): dP(t) over S^T(t) as soon as the
-      // softmax has copied S^T(t) into its registers (kSFree), then S(t+1)
-      // into the other buffer (once dK(t-1) has read dS^T(t-1) there and the
-      // next Q stage has landed), dV(t) once P^T(t) is in shared memory,
-      // dK(t) once dS^T(t) is in TMEM. No MMA waits for the one before it to
-      // complete, so the softmax of tile t (its exponentials) overlaps dP(t),
-      // S(t+1), and dV / dK of tile t - 1.
+      // softmax has copied S^T(t) into its registers (kSFree); then S(t+1)
+      // into the other buffer (once dV / dK of tile t - 1 have read it and
+      // Q(t+1) has landed) and dV(t), dK(t) (once P^T(t) and dS^T(t) are in
+      // TMEM), whichever can go first. The softmax computes the exponentials
+      // of tile t while dP(t), S(t+1) and dV / dK(t-1) run.
       bool ok = wait_bar(c, kKvFull, 0, 2);
-      int n_tiles = 0;  // tiles whose dK MMAs were issued
-      int n_dv = 0;     // tiles whose dV MMAs were issued
+      int n_tiles = 0;  // tiles whose dV / dK MMAs were issued
       QTileIter it(hpc, n0, sq);
       bool have = ok && it.next();
       if (have) {
         have = wait_bar(c, kQFull0, 0, 3);
         if (have) {
           ptx::tc_fence_after();
-          issue_S(0, t_buf0);
+          issue_S(0);
           ptx::mma_commit(c.bar(kSFull0));
         }
       }
       int t = 0;
       while (have) {
-        const int st = t & 1;
-        const uint32_t buf = t_buf0 + st * 128;
-        const uint64_t dq_mn = ptx::desc_add(dQmn, st * L::kTile);
-        const uint64_t ddo_mn = ptx::desc_add(ddOmn, st * L::kTile);
+        const int b2 = t & 1;
         if (!wait_bar(c, kSFree, t & 1, 13)) break;
+        if (!wait_bar(c, kOFull0 + b2, (t >> 1) & 1, 5)) break;
         ptx::tc_fence_after();
-        issue_dP(st, buf);
+        issue_dP(t);
         ptx::mma_commit(c.bar(kdPFull));
-        // S(t+1) into buffer st ^ 1: Q(t+1) must have landed (its stage was
-        // released by dK(t-1)) and dK(t-1) must have read dS^T(t-1) from that
-        // buffer (its completion is phase (t - 1) >> 1 of kMma40 + (st ^ 1)).
         const bool have1 = it.next();
-        const int st1 = st ^ 1;
-        const uint32_t qpar = ((t + 1) >> 1) & 1;
-        const uint32_t mpar = t > 0 ? ((t - 1) >> 1) & 1 : 0;
-        bool s_done = !have1;
-        auto try_S = [&]() {
-          if (!s_done && (t == 0 || ptx::mbar_try_wait(c.bar(kMma40 + st1), mpar)) &&
-              ptx::mbar_try_wait(c.bar(kQFull0 + st1), qpar)) {
+        const int n1 = b2 ^ 1;                                   // buffer of tile t + 1
+        const uint32_t qpar = ((t + 1) / 3) & 1;                 // fill of Q stage (t+1) % 3
+        const uint32_t mpar = t > 0 ? ((t - 1) >> 1) & 1 : 0u;  // dV / dK(t-1) done
+        bool s_done = !have1, k_done = false;
+        uint32_t idle = 0;
+        uint64_t t0 = 0;
+        while (!s_done || !k_done) {
+          bool did = false;
+          if (!s_done && (t == 0 || ptx::mbar_test_wait(c.bar(kMma40 + n1), mpar)) &&
+              ptx::mbar_test_wait(c.bar(kQFull0 + (t + 1) % 3), qpar)) {
             ptx::tc_fence_after();
-            issue_S(st1, t_buf0 + st1 * 128);
-            ptx::mma_commit(c.bar(kSFull0 + st1));
+            issue_S(t + 1);
+            ptx::mma_commit(c.bar(kSFull0 + n1));
             s_done = true;
+            did = true;
           }
-        };
-        try_S();
-        if (!wait_bar(c, kP1Full, t & 1, 4)) break;
-        ptx::tc_fence_after();
-        // MMA3 dV += P^T dO : A = P^T K-major over queries, B = dO MN-major over d
-#pragma unroll
-        for (int s = 0; s < BM / 16; ++s) {
-          const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
-          ptx::mma_ss(t_dV, ptx::desc_add(dDS, off), ptx::desc_add(ddo_mn, s * 2048), id_KV,
-                      (t > 0 || s > 0) ? 1u : 0u);
+          if (!k_done && ptx::mbar_test_wait(c.bar(kP2Full), t & 1)) {
+            ptx::tc_fence_after();
+            issue_dVdK(t);
+            ptx::mma_commit(c.bar(kOEmpty0 + b2));     // dO(t) read by dP(t) and dV(t)
+            ptx::mma_commit(c.bar(kQEmpty0 + t % 3));  // Q(t) read by S(t) and dK(t)
+            ptx::mma_commit(c.bar(kMma40 + b2));       // buffer t & 1 free again
+            ++n_tiles;
+            k_done = true;
+            did = true;
+          }
+          if (did) {
+            idle = 0;
+            t0 = 0;
+          } else if ((++idle & 63u) == 0) {  // bounded, as every other wait
+            if (*c.abort) { ok = false; break; }
+            const uint64_t now = ptx::globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kTimeoutNs) {
+              *c.abort = 1;
+              report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 6);
+              ok = false;
+              break;
+            }
+          }
         }
-        ptx::mma_commit(c.bar(kMma3));
-        ++n_dv;
-        try_S();
-        if (!wait_bar(c, kP2Full, t & 1, 7)) break;
-        ptx::tc_fence_after();
-        // MMA4 dK += dS^T Q : A = dS^T (TMEM fp16 pairs in this tile's buffer),
-        // B = Q MN-major over d
-#pragma unroll
-        for (int s = 0; s < BM / 16; ++s) {
-          const uint32_t a_col = buf + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_dK, a_col, ptx::desc_add(dq_mn, s * 2048), id_KV,
-                      (t > 0 || s > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(c.bar(kQEmpty0 + st));
-        ptx::mma_commit(c.bar(kMma40 + st));
-        ++n_tiles;
-        if (!s_done) {
-          if (t > 0 && !wait_bar(c, kMma40 + st1, mpar, 6)) break;
-          if (!wait_bar(c, kQFull0 + st1, qpar, 5)) break;
-          ptx::tc_fence_after();
-          issue_S(st1, t_buf0 + st1 * 128);
-          ptx::mma_commit(c.bar(kSFull0 + st1));
-        }
+        if (!ok) break;
         have = have1;
         ++t;
       }
       ptx::mma_commit(c.bar(kAccFull));
-      // The last dV / dK / Q-stage commits are waited by nobody else: wait
-      // for them here, so that no commit arrival is still in flight when the
-      // CTA exits (a late one would land on the barriers of the next CTA on
-      // this SM). Buffer / stage b took the commits of tiles b, b + 2, ...
-      if (n_dv > 0) drain_bar(c, kMma3, (n_dv - 1) & 1);
-      for (int b2 = 0; b2 < 2; ++b2) {
-        const int n_b = (n_tiles + 1 - b2) >> 1;
+      // The last commits of the stage and buffer barriers are waited by nobody
+      // else: wait for them here, so that no commit arrival is still in flight
+      // when the CTA exits (a late one would land on the barriers of the next
+      // CTA on this SM). Buffer / dO stage b took the commits of tiles b,
+      // b + 2, ...; Q stage s those of tiles s, s + 3, ...
+      for (int bb = 0; bb < 2; ++bb) {
+        const int n_b = (n_tiles + 1 - bb) >> 1;
         if (n_b > 0) {
-          drain_bar(c, kMma40 + b2, (n_b - 1) & 1);
-          drain_bar(c, kQEmpty0 + b2, (n_b - 1) & 1);
+          drain_bar(c, kMma40 + bb, (n_b - 1) & 1);
+          drain_bar(c, kOEmpty0 + bb, (n_b - 1) & 1);
         }
+      }
+      for (int s = 0; s < 3; ++s) {
+        const int n_s = (n_tiles + 2 - s) / 3;
+        if (n_s > 0) drain_bar(c, kQEmpty0 + s, (n_s - 1) & 1);
       }
     }
     __syncwarp();
@@ -629,13 +665,13 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     int t = 0;
     bool ok = true;
     while (it.next()) {
-      const int st = t & 1;
-      if (!wait_bar(c, kQFull0 + st, (t >> 1) & 1, 8)) { ok = false; break; }
-      const float* lse_s = reinterpret_cast<const float*>(smem + L::LSE + st * 512);
-      const float* dl_s = reinterpret_cast<const float*>(smem + L::DLT + st * 512);
-      if (!wait_bar(c, kSFull0 + st, (t >> 1) & 1, 9)) { ok = false; break; }
+      const int b2 = t & 1;
+      if (!wait_bar(c, kOFull0 + b2, (t >> 1) & 1, 8)) { ok = false; break; }  // LSE / delta
+      const float* lse_s = reinterpret_cast<const float*>(smem + L::LSE + b2 * 512);
+      const float* dl_s = reinterpret_cast<const float*>(smem + L::DLT + b2 * 512);
+      if (!wait_bar(c, kSFull0 + b2, (t >> 1) & 1, 9)) { ok = false; break; }
       ptx::tc_fence_after();
-      const uint32_t buf = t_buf0 + st * 128;  // this tile's TMEM buffer
+      const uint32_t buf = t_buf0 + b2 * 128;  // this tile's TMEM buffer
       const int h = h_first + it.hl;
       const int m0 = it.mt * BM;
       // Live queries of this key row within the tile, [qlo, qhi]. A row
@@ -656,9 +692,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       float* dbrow = nullptr;
       if constexpr (DBIAS)
         dbrow = p.dbias + b * p.dbias_bstride + ((int64_t)h * p.Sq + m0) * p.Sk + j;
-      const uint32_t ps_row = sDS + wg * kSlab + jl * 128;
-      // phase 1: P^T from S^T as fp16 into shared memory, 128B-swizzled K-major
-      // rows (one key row per thread; A operand of dV)
+      // phase 1: P^T from S^T, fp32 in registers (one key row per thread)
       float pv[64];
       {
         uint32_t sr[64];
@@ -667,7 +701,6 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c.bar(kSFree));  // S^T(t) is in registers: MMA2 may overwrite it
-        uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int q0 = wg * 64 + cc * 32;  // first query of this chunk within the tile
@@ -710,24 +743,13 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
               for (int u = 0; u < 4; ++u)
                 if (!((live >> (e4 + u)) & 1u)) pv[cc * 32 + e4 + u] = 0.f;
             }
-            pk[cc * 16 + e4 / 2] = pack_half2(pv[cc * 32 + e4], pv[cc * 32 + e4 + 1]);
-            pk[cc * 16 + e4 / 2 + 1] = pack_half2(pv[cc * 32 + e4 + 2], pv[cc * 32 + e4 + 3]);
           }
         }
         if constexpr (kTB) ptx::mbar_arrive(c.bar(kBiasEmpty));  // bias tile read
-        // the previous tile's dV has finished reading the P^T buffer
-        if (t > 0 && !wait_bar(c, kMma3, (t - 1) & 1, 12)) { ok = false; break; }
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const uint32_t chunk = (uint32_t)q4 ^ (uint32_t)(jl & 7);
-          ptx::st_shared_v4(ps_row + chunk * 16, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2],
-                            pk[4 * q4 + 3]);
-        }
-        ptx::fence_async_shared();
-        ptx::mbar_arrive(c.bar(kP1Full));
       }
-      // phase 2: dS^T = P^T (dP^T - D), fp16 pairs over the front half of this
-      // group's dP^T columns in the tile's buffer (A operand of dK)
+      // phase 2: dS^T = P^T (dP^T - D). Each 32-query chunk of dP^T, once
+      // read, takes dS^T (16 columns of fp16 pairs, A operand of dK) and P^T
+      // (the next 16 columns, A operand of dV) in its place.
       if (!wait_bar(c, kdPFull, t & 1, 10)) { ok = false; break; }
       ptx::tc_fence_after();
 #pragma unroll
@@ -738,7 +760,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         uint32_t dr[32];
         ptx::tmem_ld32(buf + lane_off + wg * 64 + cc * 32, dr);
         ptx::tmem_wait_ld();
-        uint32_t dk[16];
+        uint32_t dk[16], pk[16];
 #pragma unroll
         for (int e4 = 0; e4 < 32; e4 += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(dl_s + q0 + e4);
@@ -763,9 +785,12 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
           }
           dk[e4 / 2] = pack_half2(de[0], de[1]);
           dk[e4 / 2 + 1] = pack_half2(de[2], de[3]);
+          pk[e4 / 2] = pack_half2(pv[cc * 32 + e4], pv[cc * 32 + e4 + 1]);
+          pk[e4 / 2 + 1] = pack_half2(pv[cc * 32 + e4 + 2], pv[cc * 32 + e4 + 3]);
         }
-        // columns [cc 16, cc 16 + 16) were read above (chunk 0 covers 0-31)
-        ptx::tmem_st16(buf + lane_off + wg * 64 + cc * 16, dk);
+        // this chunk's 32 columns were read above
+        ptx::tmem_st16(buf + lane_off + wg * 64 + cc * 32, dk);
+        ptx::tmem_st16(buf + lane_off + wg * 64 + cc * 32 + 16, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -872,10 +897,10 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   c.bars = sbase + L::BAR;
   c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
   c.status = p.status;
-  // qQdoFull, qKvFull0/1, qKvEmpty0/1, qSFull0/1/2, qSFree, qdPFull, qDsFull, qMma30/1/2,
-  // qAccFull, qBiasFull0/1, qBiasEmpty0/1
-  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 1, 1, 256, 1, 256, 1, 1, 1, 1,
-                                   1, 1, 256, 256};
+  // qQdoFull, qKFull0-2, qKEmpty0-2, qVFull0/1, qVEmpty0/1, qSFull0-2, qSFree, qdPFull,
+  // qDsFull, qMma30-2, qAccFull, qBiasFull0/1, qBiasEmpty0/1
+  const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,
+                                   256, 1, 256, 1, 1, 1, 1, 1, 1, 256, 256};
   init_common(c, sbase + L::MISC, kQBars, counts, warp);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   // TMEM: [0, D) dQ, then three 128-column buffers; tile t works in buffer
@@ -897,45 +922,49 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
         ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
       }
+      // K(t) rotates over kKS stages (released by dQ(t)), V(t) over two
+      // (released by dP(t)), the bias (TMA bias path) over two (released by
+      // the softmax's phase 1)
       KTileIter it(m0, sq);
       int t = 0;
-      int issued[2] = {0, 0};
+      int k_issued[3] = {0, 0, 0}, v_issued[2] = {0, 0}, b_issued[2] = {0, 0};
       while (it.next()) {
-        const int st = t & 1;
-        const int use = t >> 1;
+        const int ks = t % L::kKS, ku = t / L::kKS;
+        const int vs = t & 1, vu = t >> 1;
+        const int krow = (b * p.Hk + g) * p.Sks + it.nt * BN;
+        if (ku > 0 && !wait_bar(c, qKEmpty0 + ks, (ku - 1) & 1, 21)) break;
+        const uint32_t kfull = c.bar(qKFull0 + ks);
+        ptx::mbar_arrive_expect_tx(kfull, L::kTile);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          ptx::tma_load_2d(sbase + L::K + ks * L::kTile + hf * kSlab, tmK, kfull, hf * 64, krow);
+        k_issued[ks] = ku + 1;
+        if (vu > 0 && !wait_bar(c, qVEmpty0 + vs, (vu - 1) & 1, 20)) break;
+        const uint32_t vfull = c.bar(qVFull0 + vs);
+        ptx::mbar_arrive_expect_tx(vfull, L::kTile);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          ptx::tma_load_2d(sbase + L::V + vs * L::kTile + hf * kSlab, tmV, vfull, hf * 64, krow);
+        v_issued[vs] = vu + 1;
         if constexpr (kTB) {
-          // the tile's bias into stage st once the softmax read tile t - 2's
-          if (use > 0 && !wait_bar(c, qBiasEmpty0 + st, (use - 1) & 1, 20)) break;
-          const uint32_t bfull = c.bar(qBiasFull0 + st);
+          if (vu > 0 && !wait_bar(c, qBiasEmpty0 + vs, (vu - 1) & 1, 19)) break;
+          const uint32_t bfull = c.bar(qBiasFull0 + vs);
           ptx::mbar_arrive_expect_tx(bfull, 4 * kSlab);
 #pragma unroll
           for (int bx = 0; bx < 4; ++bx)
-            ptx::tma_load_2d(sbase + L::BIAS + st * 4 * kSlab + bx * kSlab, tmB, bfull,
+            ptx::tma_load_2d(sbase + L::BIAS + vs * 4 * kSlab + bx * kSlab, tmB, bfull,
                              it.nt * BN + 32 * bx, h * p.Sq + m0);
+          b_issued[vs] = vu + 1;
         }
-        if (use > 0 && !wait_bar(c, qKvEmpty0 + st, (use - 1) & 1, 21)) {
-          if constexpr (kTB) issued[st] = -(use + 1);  // the bias copy of this use is in flight
-          break;
-        }
-        const int krow = (b * p.Hk + g) * p.Sks + it.nt * BN;
-        const uint32_t full = c.bar(qKvFull0 + st);
-        ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
-#pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
-          ptx::tma_load_2d(sbase + L::K + st * L::kTile + hf * kSlab, tmK, full, hf * 64, krow);
-          ptx::tma_load_2d(sbase + L::V + st * L::kTile + hf * kSlab, tmV, full, hf * 64, krow);
-        }
-        issued[st] = use + 1;
         ++t;
       }
+      // no copy may still be landing in shared memory when the CTA ends
       drain_bar(c, qQdoFull, 0);
-      for (int st = 0; st < 2; ++st) {
-        // issued[st] = uses of stage st whose K / V (and bias) copies went
-        // out; negative: the last use's bias copy went out without its K / V
-        const int n_kv = issued[st] >= 0 ? issued[st] : -issued[st] - 1;
-        const int n_b = issued[st] >= 0 ? issued[st] : -issued[st];
-        if (n_kv > 0) drain_bar(c, qKvFull0 + st, (n_kv - 1) & 1);
-        if (kTB && n_b > 0) drain_bar(c, qBiasFull0 + st, (n_b - 1) & 1);
+      for (int s = 0; s < L::kKS; ++s)
+        if (k_issued[s] > 0) drain_bar(c, qKFull0 + s, (k_issued[s] - 1) & 1);
+      for (int s = 0; s < 2; ++s) {
+        if (v_issued[s] > 0) drain_bar(c, qVFull0 + s, (v_issued[s] - 1) & 1);
+        if (b_issued[s] > 0) drain_bar(c, qBiasFull0 + s, (b_issued[s] - 1) & 1);
       }
     }
     __syncwarp();
@@ -951,8 +980,8 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       const uint64_t dKk = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dVk = ptx::smem_desc_sw128(sbase + L::V, 16, 1024);
       const uint64_t dKmn = ptx::smem_desc_sw128(sbase + L::K, kSlab, 1024);
-      auto issue_S = [&](int t) {  // MMA1' S = Q K^T into buffer t % 3 (K / V stage t & 1)
-        const uint64_t dk = ptx::desc_add(dKk, (t & 1) * L::kTile);
+      auto issue_S = [&](int t) {  // MMA1' S = Q K^T into buffer t % 3 (K stage t % kKS)
+        const uint64_t dk = ptx::desc_add(dKk, (t % L::kKS) * L::kTile);
         const uint32_t dst = t_buf0 + (t % 3) * 128;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
@@ -970,7 +999,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         }
       };
       auto issue_dQ = [&](int t) {  // MMA3' dQ += dS K : A = dS (TMEM fp16 pairs), B = K MN-major
-        const uint64_t dk = ptx::desc_add(dKmn, (t & 1) * L::kTile);
+        const uint64_t dk = ptx::desc_add(dKmn, (t % L::kKS) * L::kTile);
         const uint32_t src = t_buf0 + (t % 3) * 128;
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
@@ -987,10 +1016,11 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // and dQ(t-1); S(t+1) is ready before the softmax finishes tile t.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
       int n_tiles = 0;  // tiles whose dQ MMAs were issued
+      int n_dp = 0;     // tiles whose dP MMAs were issued
       KTileIter it(m0, sq);
       bool have = ok && it.next();
       if (have) {
-        have = wait_bar(c, qKvFull0, 0, 23);
+        have = wait_bar(c, qKFull0, 0, 23);
         if (have) {
           ptx::tc_fence_after();
           issue_S(0);
@@ -1001,12 +1031,16 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       while (have) {
         const int st = t & 1, bt = t % 3;
         if (!wait_bar(c, qSFree, t & 1, 24)) break;
+        if (!wait_bar(c, qVFull0 + st, (t >> 1) & 1, 29)) break;
         ptx::tc_fence_after();
         issue_dP(t);
         ptx::mma_commit(c.bar(qdPFull));
+        ptx::mma_commit(c.bar(qVEmpty0 + st));  // V(t) read by dP(t) only
+        ++n_dp;
         const bool have1 = it.next();
         const int b1 = (t + 1) % 3;
-        const uint32_t kvpar = ((t + 1) >> 1) & 1;              // fill of K / V stage st ^ 1
+        const int k1 = (t + 1) % L::kKS;                        // K stage of tile t + 1
+        const uint32_t kpar = ((t + 1) / L::kKS) & 1;           // its fill for tile t + 1
         const uint32_t mpar = t >= 2 ? ((t - 2) / 3) & 1 : 0u;  // dQ(t-2) on qMma30 + b1
         bool s_done = !have1, q_done = false;
         uint32_t idle = 0;
@@ -1014,7 +1048,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         while (!s_done || !q_done) {
           bool did = false;
           if (!s_done && (t < 2 || ptx::mbar_test_wait(c.bar(qMma30 + b1), mpar)) &&
-              ptx::mbar_test_wait(c.bar(qKvFull0 + (st ^ 1)), kvpar)) {
+              ptx::mbar_test_wait(c.bar(qKFull0 + k1), kpar)) {
             ptx::tc_fence_after();
             issue_S(t + 1);
             ptx::mma_commit(c.bar(qSFull0 + b1));
@@ -1025,7 +1059,7 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
             ptx::tc_fence_after();
             issue_dQ(t);
             ptx::mma_commit(c.bar(qMma30 + bt));
-            ptx::mma_commit(c.bar(qKvEmpty0 + st));
+            ptx::mma_commit(c.bar(qKEmpty0 + t % L::kKS));  // K(t) read by S(t) and dQ(t)
             ++n_tiles;
             q_done = true;
             did = true;
@@ -1058,9 +1092,13 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         const int n_b = (n_tiles - b3 + 2) / 3;
         if (n_b > 0) drain_bar(c, qMma30 + b3, (n_b - 1) & 1);
       }
-      for (int s2 = 0; s2 < 2; ++s2) {
-        const int n_s = (n_tiles + 1 - s2) >> 1;
-        if (n_s > 0) drain_bar(c, qKvEmpty0 + s2, (n_s - 1) & 1);
+      for (int s2 = 0; s2 < L::kKS; ++s2) {
+        const int n_s = (n_tiles + L::kKS - 1 - s2) / L::kKS;
+        if (n_s > 0) drain_bar(c, qKEmpty0 + s2, (n_s - 1) & 1);
+      }
+      for (int s2 = 0; s2 < 2; ++s2) {  // dP commits: one per tile whose dP went out
+        const int n_s = (n_dp + 1 - s2) >> 1;
+        if (n_s > 0) drain_bar(c, qVEmpty0 + s2, (n_s - 1) & 1);
       }
     }
     __syncwarp();
