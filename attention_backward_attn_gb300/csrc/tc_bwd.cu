@@ -565,9 +565,11 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
       // Per tile t (TMEM buffer t & 1): dP(t) over S^T(t) as soon as the
       // softmax has copied S^T(t) into its registers (kSFree); then S(t+1)
       // into the other buffer (once dV / dK of tile t - 1 have read it and
-      // Q(t+1) has landed) and dV(t), dK(t) (once P^T(t) and dS^T(t) are in
-      // TMEM), whichever can go first. The softmax computes the exponentials
-      // of tile t while dP(t), S(t+1) and dV / dK(t-1) run.
+      // Q(t+1) has landed), then dV(t), dK(t) (once P^T(t) and dS^T(t) are in
+      // TMEM). The softmax computes the exponentials of tile t while dP(t),
+      // S(t+1) and dV / dK(t-1) run. Waits suspend the thread (mbarrier
+      // try_wait), so the MMA warp takes no issue slots from the softmax
+      // warps that share its SM sub-partition.
       bool ok = wait_bar(c, kKvFull, 0, 2);
       int n_tiles = 0;  // tiles whose dV / dK MMAs were issued
       QTileIter it(hpc, n0, sq);
@@ -592,45 +594,20 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         const int n1 = b2 ^ 1;                                   // buffer of tile t + 1
         const uint32_t qpar = ((t + 1) / 3) & 1;                 // fill of Q stage (t+1) % 3
         const uint32_t mpar = t > 0 ? ((t - 1) >> 1) & 1 : 0u;  // dV / dK(t-1) done
-        bool s_done = !have1, k_done = false;
-        uint32_t idle = 0;
-        uint64_t t0 = 0;
-        while (!s_done || !k_done) {
-          bool did = false;
-          if (!s_done && (t == 0 || ptx::mbar_test_wait(c.bar(kMma40 + n1), mpar)) &&
-              ptx::mbar_test_wait(c.bar(kQFull0 + (t + 1) % 3), qpar)) {
-            ptx::tc_fence_after();
-            issue_S(t + 1);
-            ptx::mma_commit(c.bar(kSFull0 + n1));
-            s_done = true;
-            did = true;
-          }
-          if (!k_done && ptx::mbar_test_wait(c.bar(kP2Full), t & 1)) {
-            ptx::tc_fence_after();
-            issue_dVdK(t);
-            ptx::mma_commit(c.bar(kOEmpty0 + b2));     // dO(t) read by dP(t) and dV(t)
-            ptx::mma_commit(c.bar(kQEmpty0 + t % 3));  // Q(t) read by S(t) and dK(t)
-            ptx::mma_commit(c.bar(kMma40 + b2));       // buffer t & 1 free again
-            ++n_tiles;
-            k_done = true;
-            did = true;
-          }
-          if (did) {
-            idle = 0;
-            t0 = 0;
-          } else if ((++idle & 63u) == 0) {  // bounded, as every other wait
-            if (*c.abort) { ok = false; break; }
-            const uint64_t now = ptx::globaltimer_ns();
-            if (t0 == 0) {
-              t0 = now;
-            } else if (now - t0 > kTimeoutNs) {
-              *c.abort = 1;
-              report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 6);
-              ok = false;
-              break;
-            }
-          }
+        if (have1) {
+          if (t > 0 && !wait_bar(c, kMma40 + n1, mpar, 6)) break;
+          if (!wait_bar(c, kQFull0 + (t + 1) % 3, qpar, 5)) break;
+          ptx::tc_fence_after();
+          issue_S(t + 1);
+          ptx::mma_commit(c.bar(kSFull0 + n1));
         }
+        if (!wait_bar(c, kP2Full, t & 1, 7)) break;
+        ptx::tc_fence_after();
+        issue_dVdK(t);
+        ptx::mma_commit(c.bar(kOEmpty0 + b2));     // dO(t) read by dP(t) and dV(t)
+        ptx::mma_commit(c.bar(kQEmpty0 + t % 3));  // Q(t) read by S(t) and dK(t)
+        ptx::mma_commit(c.bar(kMma40 + b2));       // buffer t & 1 free again
+        ++n_tiles;
         if (!ok) break;
         have = have1;
         ++t;
@@ -1009,11 +986,11 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         }
       };
       // Per tile t (TMEM buffer t % 3): dP(t) over S(t) as soon as the softmax
-      // has copied S(t) into its registers (qSFree); then S(t+1) and dQ(t),
-      // whichever can go first. S(t+1) needs the next K / V stage (released
-      // by dQ(t-1)) and buffer (t+1) % 3, last read by dQ(t-2); dQ(t) needs
-      // dS(t). The softmax's exponentials of tile t overlap dP(t), S(t+1)
-      // and dQ(t-1); S(t+1) is ready before the softmax finishes tile t.
+      // has copied S(t) into its registers (qSFree); then S(t+1), which needs
+      // its K stage and buffer (t+1) % 3, last read by dQ(t-2); then dQ(t)
+      // once dS(t) is in TMEM. The softmax's exponentials of tile t overlap
+      // dP(t), S(t+1) and dQ(t-1); S(t+1) is ready before the softmax
+      // finishes tile t.
       bool ok = wait_bar(c, qQdoFull, 0, 22);
       int n_tiles = 0;  // tiles whose dQ MMAs were issued
       int n_dp = 0;     // tiles whose dP MMAs were issued
@@ -1042,44 +1019,19 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         const int k1 = (t + 1) % L::kKS;                        // K stage of tile t + 1
         const uint32_t kpar = ((t + 1) / L::kKS) & 1;           // its fill for tile t + 1
         const uint32_t mpar = t >= 2 ? ((t - 2) / 3) & 1 : 0u;  // dQ(t-2) on qMma30 + b1
-        bool s_done = !have1, q_done = false;
-        uint32_t idle = 0;
-        uint64_t t0 = 0;
-        while (!s_done || !q_done) {
-          bool did = false;
-          if (!s_done && (t < 2 || ptx::mbar_test_wait(c.bar(qMma30 + b1), mpar)) &&
-              ptx::mbar_test_wait(c.bar(qKFull0 + k1), kpar)) {
-            ptx::tc_fence_after();
-            issue_S(t + 1);
-            ptx::mma_commit(c.bar(qSFull0 + b1));
-            s_done = true;
-            did = true;
-          }
-          if (!q_done && ptx::mbar_test_wait(c.bar(qDsFull), t & 1)) {
-            ptx::tc_fence_after();
-            issue_dQ(t);
-            ptx::mma_commit(c.bar(qMma30 + bt));
-            ptx::mma_commit(c.bar(qKEmpty0 + t % L::kKS));  // K(t) read by S(t) and dQ(t)
-            ++n_tiles;
-            q_done = true;
-            did = true;
-          }
-          if (did) {
-            idle = 0;
-            t0 = 0;
-          } else if ((++idle & 63u) == 0) {  // bounded, as every other wait
-            if (*c.abort) { ok = false; break; }
-            const uint64_t now = ptx::globaltimer_ns();
-            if (t0 == 0) {
-              t0 = now;
-            } else if (now - t0 > kTimeoutNs) {
-              *c.abort = 1;
-              report(c.status, ATTN_ERR_DEVICE_TIMEOUT, 25);
-              ok = false;
-              break;
-            }
-          }
+        if (have1) {
+          if (t >= 2 && !wait_bar(c, qMma30 + b1, mpar, 25)) break;
+          if (!wait_bar(c, qKFull0 + k1, kpar, 23)) break;
+          ptx::tc_fence_after();
+          issue_S(t + 1);
+          ptx::mma_commit(c.bar(qSFull0 + b1));
         }
+        if (!wait_bar(c, qDsFull, t & 1, 26)) break;
+        ptx::tc_fence_after();
+        issue_dQ(t);
+        ptx::mma_commit(c.bar(qMma30 + bt));
+        ptx::mma_commit(c.bar(qKEmpty0 + t % L::kKS));  // K(t) read by S(t) and dQ(t)
+        ++n_tiles;
         if (!ok) break;
         have = have1;
         ++t;
