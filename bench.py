@@ -361,11 +361,16 @@ def run_ours(args):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, per launch, from
-# the ncu captures summarised in profiles/ (the sparse figure is a 1024-token capture
-# scaled by the token count: its DRAM bytes are Q, dO and dQ, all linear in Sq). An entry
-# goes back to None when its kernel changes.
+# the ncu captures summarised in profiles/. Three are smaller captures scaled to the full
+# launch by the units processed, since their DRAM bytes grow in proportion: the sparse
+# one has 1024 of the 4096 tokens (Q, dO, dQ are linear in Sq), the ALiBi one 8 of the 16
+# heads (every tensor is per head), the windowed one S = 4096 of 8192 (fixed window: live
+# entries, CTAs and bytes linear in S). An entry goes back to None when its kernel changes.
 NCU_TRAFFIC = {
-    "sparse_scfa_s4096_h64_d512": 4 * 224.48e6,
+    "gqa4_causal_s1024_d128": 29.708032e6 + 3.072e3,
+    "mha_alibi_dbias_s2048_d64": 2 * (560.923136e6 + 212.339968e6),
+    "gqa4_window1024_sink4_s8192_d128": 2 * (156.406528e6 + 66.854144e6),
+    "sparse_scfa_s4096_h64_d512": 4 * (140.928e6 + 82.918912e6),
 }
 
 # CUDA-core fp32 FMA rate for the SIMT fallback's roofline: 152 SMs x 128
