@@ -344,12 +344,18 @@ struct KTileIter {
   }
 };
 
+// Barrier set-up by thread 0 (the producer), which then issues the CTA's
+// first copies at once (`early`: they complete on the barriers it has just
+// initialised), so that their latency overlaps the TMEM allocation and the
+// CTA-wide barrier.
+template <typename Early>
 __device__ __forceinline__ void init_common(const Ctx& c, uint32_t tmem_slot_addr, int nbars,
-                                            const uint32_t* counts, int warp) {
+                                            const uint32_t* counts, int warp, Early&& early) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < nbars; ++i) ptx::mbar_init(c.bar(i), counts[i]);
     *c.abort = 0;
     ptx::fence_mbar_init();
+    early();
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot_addr, 512);
@@ -402,12 +408,29 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   // kP2Full, kMma40/1, kAccFull, kBiasFull, kBiasEmpty
   const uint32_t counts[kKvBars] = {1, 1, 1, 1, 1, 1, 1, of, of, 1, 1, 1, 1,
                                     256, 1, 256, 1, 1, 1, 1, 256};
-  init_common(c, sbase + L::MISC, kKvBars, counts, warp);
+  const uint32_t sK = sbase + L::K, sV = sbase + L::V;
+  init_common(c, sbase + L::MISC, kKvBars, counts, warp, [&] {
+    // K / V of the key tile, and Q of its first live tile (stage 0)
+    const int krow = (b * p.Hk + g) * p.Sks + n0;
+    ptx::mbar_arrive_expect_tx(c.bar(kKvFull), 2 * L::kTile);
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) {
+      ptx::tma_load_2d(sK + hf * kSlab, tmK, c.bar(kKvFull), hf * 64, krow);
+      ptx::tma_load_2d(sV + hf * kSlab, tmV, c.bar(kKvFull), hf * 64, krow);
+    }
+    QTileIter it0(hpc, n0, sq);
+    if (it0.next()) {
+      const int row = (b * p.Hq + h_first + it0.hl) * p.Sqs + it0.mt * BM;
+      ptx::mbar_arrive_expect_tx(c.bar(kQFull0), L::kTile);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf)
+        ptx::tma_load_2d(sbase + L::Q + hf * kSlab, tmQ, c.bar(kQFull0), hf * 64, row);
+    }
+  });
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   const uint32_t t_dK = tmem;
   const uint32_t t_dV = tmem + D;
   const uint32_t t_buf0 = tmem + 2 * D;  // tile t: S^T / dP^T / (dS^T, P^T) at t_buf0 + (t & 1) 128
-  const uint32_t sK = sbase + L::K, sV = sbase + L::V;
   bool epi_ok = false;
   int n_iters = 0;
 
@@ -416,15 +439,7 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
     // lane 0 waits and issues the copies; with ragged lengths the whole warp
     // also copies the tile's LSE / delta rows (zero past Sq). Q stages rotate
     // over three buffers, dO (with LSE / delta) over two.
-    if (lane == 0) {
-      const int krow = (b * p.Hk + g) * p.Sks + n0;
-      ptx::mbar_arrive_expect_tx(c.bar(kKvFull), 2 * L::kTile);
-#pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-        ptx::tma_load_2d(sK + hf * kSlab, tmK, c.bar(kKvFull), hf * 64, krow);
-        ptx::tma_load_2d(sV + hf * kSlab, tmV, c.bar(kKvFull), hf * 64, krow);
-      }
-    }
+    // (K / V and the first Q went out with the barrier set-up)
     int q_issued[3] = {0, 0, 0};
     int o_issued[2] = {0, 0};
     int bias_issued = 0;
@@ -440,9 +455,11 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
         const int64_t lrow = ((int64_t)b * p.Hq + h) * p.Sq + m0;   // LSE / delta rows
         bool go = true;
         if (lane == 0) {
-          // Q(t) once dK(t-3) released its stage
+          // Q(t) once dK(t-3) released its stage (Q(0): already issued)
           if (qu > 0) go = wait_bar(c, kQEmpty0 + qs, (qu - 1) & 1, 1);
-          if (go) {
+          if (go && t == 0) {
+            q_issued[0] = 1;
+          } else if (go) {
             const uint32_t qfull = c.bar(kQFull0 + qs);
             ptx::mbar_arrive_expect_tx(qfull, L::kTile);
 #pragma unroll
@@ -878,27 +895,41 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   // qDsFull, qMma30-2, qAccFull, qBiasFull0/1, qBiasEmpty0/1
   const uint32_t counts[kQBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1,
                                    256, 1, 256, 1, 1, 1, 1, 1, 1, 256, 256};
-  init_common(c, sbase + L::MISC, kQBars, counts, warp);
+  const uint32_t sQ = sbase + L::Q, sdO = sbase + L::dO;
+  init_common(c, sbase + L::MISC, kQBars, counts, warp, [&] {
+    // Q / dO of the query tile, and K / V of its first live key tile (stage 0)
+    const int qrow = (b * p.Hq + h) * p.Sqs + m0;
+    ptx::mbar_arrive_expect_tx(c.bar(qQdoFull), 2 * L::kTile);
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) {
+      ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
+      ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
+    }
+    KTileIter it0(m0, sq);
+    if (it0.next()) {
+      const int krow = (b * p.Hk + g) * p.Sks + it0.nt * BN;
+      ptx::mbar_arrive_expect_tx(c.bar(qKFull0), L::kTile);
+      ptx::mbar_arrive_expect_tx(c.bar(qVFull0), L::kTile);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) {
+        ptx::tma_load_2d(sbase + L::K + hf * kSlab, tmK, c.bar(qKFull0), hf * 64, krow);
+        ptx::tma_load_2d(sbase + L::V + hf * kSlab, tmV, c.bar(qVFull0), hf * 64, krow);
+      }
+    }
+  });
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
   // TMEM: [0, D) dQ, then three 128-column buffers; tile t works in buffer
   // t % 3 (S, then dP over it, then dS over the front half of each
   // warpgroup's columns)
   const uint32_t t_dQ = tmem;
   const uint32_t t_buf0 = tmem + 128;
-  const uint32_t sQ = sbase + L::Q, sdO = sbase + L::dO;
   bool epi_ok = false;
   int n_iters = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      const int qrow = (b * p.Hq + h) * p.Sqs + m0;
-      ptx::mbar_arrive_expect_tx(c.bar(qQdoFull), 2 * L::kTile);
-#pragma unroll
-      for (int hf = 0; hf < D / 64; ++hf) {
-        ptx::tma_load_2d(sQ + hf * kSlab, tmQ, c.bar(qQdoFull), hf * 64, qrow);
-        ptx::tma_load_2d(sdO + hf * kSlab, tmdO, c.bar(qQdoFull), hf * 64, qrow);
-      }
+      // (Q / dO and the first K / V went out with the barrier set-up)
       // K(t) rotates over kKS stages (released by dQ(t)), V(t) over two
       // (released by dP(t)), the bias (TMA bias path) over two (released by
       // the softmax's phase 1)
@@ -909,19 +940,21 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
         const int ks = t % L::kKS, ku = t / L::kKS;
         const int vs = t & 1, vu = t >> 1;
         const int krow = (b * p.Hk + g) * p.Sks + it.nt * BN;
-        if (ku > 0 && !wait_bar(c, qKEmpty0 + ks, (ku - 1) & 1, 21)) break;
-        const uint32_t kfull = c.bar(qKFull0 + ks);
-        ptx::mbar_arrive_expect_tx(kfull, L::kTile);
+        if (t > 0) {
+          if (ku > 0 && !wait_bar(c, qKEmpty0 + ks, (ku - 1) & 1, 21)) break;
+          const uint32_t kfull = c.bar(qKFull0 + ks);
+          ptx::mbar_arrive_expect_tx(kfull, L::kTile);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          ptx::tma_load_2d(sbase + L::K + ks * L::kTile + hf * kSlab, tmK, kfull, hf * 64, krow);
+          for (int hf = 0; hf < D / 64; ++hf)
+            ptx::tma_load_2d(sbase + L::K + ks * L::kTile + hf * kSlab, tmK, kfull, hf * 64, krow);
+          if (vu > 0 && !wait_bar(c, qVEmpty0 + vs, (vu - 1) & 1, 20)) break;
+          const uint32_t vfull = c.bar(qVFull0 + vs);
+          ptx::mbar_arrive_expect_tx(vfull, L::kTile);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf)
+            ptx::tma_load_2d(sbase + L::V + vs * L::kTile + hf * kSlab, tmV, vfull, hf * 64, krow);
+        }
         k_issued[ks] = ku + 1;
-        if (vu > 0 && !wait_bar(c, qVEmpty0 + vs, (vu - 1) & 1, 20)) break;
-        const uint32_t vfull = c.bar(qVFull0 + vs);
-        ptx::mbar_arrive_expect_tx(vfull, L::kTile);
-#pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          ptx::tma_load_2d(sbase + L::V + vs * L::kTile + hf * kSlab, tmV, vfull, hf * 64, krow);
         v_issued[vs] = vu + 1;
         if constexpr (kTB) {
           if (vu > 0 && !wait_bar(c, qBiasEmpty0 + vs, (vu - 1) & 1, 19)) break;
@@ -1182,23 +1215,21 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
       // row (rows past Sq are not stored)
       float* grow = p.dq + ((sq.oq + ic) * p.Hq + h) * D + wg * (D / 2);
       const uint32_t srow = sbase + L::STAGE + il * L::kStageRow + wg * (D / 2) * 4;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        uint32_t v[32];
-        if (n_iters > 0) {
-          ptx::tmem_ld32(t_dQ + lane_off + wg * (D / 2) + cc * 32, v);
-          ptx::tmem_wait_ld();
-        } else {
+      uint32_t v[D / 2];
+      if (n_iters > 0) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
-        }
+        for (int cc = 0; cc < D / 64; ++cc)
+          ptx::tmem_ld32(t_dQ + lane_off + wg * (D / 2) + cc * 32, v + cc * 32);
+        ptx::tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          ptx::st_shared_v4f(srow + (cc * 32 + e) * 4, __uint_as_float(v[e]) * p.scale,
-                             __uint_as_float(v[e + 1]) * p.scale,
-                             __uint_as_float(v[e + 2]) * p.scale,
-                             __uint_as_float(v[e + 3]) * p.scale);
+        for (int e = 0; e < D / 2; ++e) v[e] = 0u;
       }
+#pragma unroll
+      for (int e = 0; e < D / 2; e += 4)
+        ptx::st_shared_v4f(srow + e * 4, __uint_as_float(v[e]) * p.scale,
+                           __uint_as_float(v[e + 1]) * p.scale, __uint_as_float(v[e + 2]) * p.scale,
+                           __uint_as_float(v[e + 3]) * p.scale);
       if (row_in) {
         ptx::fence_async_shared();
         ptx::bulk_store(grow, srow, D / 2 * 4);
