@@ -139,15 +139,22 @@ Sizes sizes_of(const Problem& p) {
 
 bool need(const void* ptr, int64_t count) { return count == 0 || ptr != nullptr; }
 
-// Deterministic dense mode with dbias over several batches: per-batch slices
-// of dbias in the workspace, summed in batch order afterwards.
-bool dbias_split(const Problem& p, const float* dbias) {
-  return !p.sparse && p.deterministic && p.B > 1 && dbias != nullptr;
-}
-
 bool use_tensor_cores(const Problem& p) {
   if (p.cuda_cores) return false;
   return p.sparse ? tc_sparse_supported(p) : tc_supported(p);
+}
+
+// dbias computed by the tensor-core kernel's batch-inner query-major CTAs:
+// stored once per element, neither zeroed first nor split by batch.
+bool dbias_in_q(const Problem& p, const float* dbias) {
+  return dbias != nullptr && !p.sparse && use_tensor_cores(p) && tc_dbias_in_q(p);
+}
+
+// Deterministic dense mode with dbias over several batches (other than the
+// batch-inner case): per-batch slices of dbias in the workspace, summed in
+// batch order afterwards.
+bool dbias_split(const Problem& p, const float* dbias) {
+  return !p.sparse && p.deterministic && p.B > 1 && dbias != nullptr && !dbias_in_q(p, dbias);
 }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
@@ -196,8 +203,9 @@ WorkspaceLayout workspace_layout(const Problem& p, bool tensor_core_path) {
     off = align_up(off + kbytes, 1024);
     w.staged = true;
   }
-  if (!p.sparse && p.deterministic && p.B > 1) {
-    // per-batch dbias slices (used when dbias is requested)
+  if (!p.sparse && p.deterministic && p.B > 1 && !(tensor_core_path && tc_dbias_in_q(p))) {
+    // per-batch dbias slices (used when dbias is requested and the
+    // batch-inner kernel does not apply)
     off = align_up(off, 1024);
     w.det_dbias = off;
     off = align_up(off + (size_t)p.B * p.Hq * p.Sq * p.Sk * sizeof(float), 1024);
@@ -360,7 +368,9 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
   const bool split = dbias_split(p, dbias);
   Problem pk = p;
   pk.dbias_bstride = split ? (int64_t)p.Hq * p.Sq * p.Sk : 0;
-  float* dbias_zero = split ? reinterpret_cast<float*>(ws + w.det_dbias) : dbias;
+  // (the batch-inner kernel stores every dbias entry itself)
+  float* dbias_zero = split ? reinterpret_cast<float*>(ws + w.det_dbias)
+                            : (dbias_in_q(p, dbias) ? nullptr : dbias);
   return cuda_status(launch_preprocess(
       pk, q, k, v, o, dO, delta, dbias_zero, d_ori, d_cmp, dense_staged ? staged(w.q16) : nullptr,
       dense_staged ? staged(w.k16) : nullptr, dense_staged ? staged(w.v16) : nullptr,

@@ -75,6 +75,12 @@ cudaError_t launch_dsinks(int B, int Hq, int Sq, const float* sinks, const float
 
 // ---- tc_bwd.cu ----
 bool tc_supported(const Problem& p);
+// Whether the dense tensor-core kernel computes a requested dbias in its
+// batch-inner query-major CTAs (D = 64, B <= 4, whole tiles, fixed lengths):
+// every element of a live tile is stored once (no atomics, no zero-filled
+// buffer, fixed summation order), so the pre-pass does not zero dbias and
+// deterministic mode needs no per-batch slices.
+bool tc_dbias_in_q(const Problem& p);
 // Key-major CTAs per (key tile, KV head) of the dense tensor-core kernel; when
 // above 1 they add partial dK / dV sums into buffers the pre-pass zeroed.
 int tc_head_split(const Problem& p);

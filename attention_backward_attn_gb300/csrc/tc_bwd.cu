@@ -181,6 +181,8 @@ struct TcParams {
   int br;
   int cs;          // key-major CTAs per key tile (query-head split)
   int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
+  int qb_ctas;     // batch-inner dbias mode: blocks [0, qb_ctas) are batch-inner
+                   // query-major, the rest key-major (without dbias)
   float scale;
   float scale_log2;
   MaskSpec mask;
@@ -344,6 +346,25 @@ struct KTileIter {
   }
 };
 
+// Four fp32 values into global memory: a plain 16-byte store, or (add) an
+// fp32 addition of each (red.global.add.v4.f32).
+__device__ __forceinline__ void put4(float* dst, float a, float b, float c, float d, bool add) {
+  if (add)
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+  else
+    *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+
+// Eight fp32 values as one 32-byte store (one full sector: half the store
+// instructions of 16-byte stores when each thread writes its own row).
+__device__ __forceinline__ void put8(float* dst, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 // Barrier set-up by thread 0 (the producer), which then issues the CTA's
 // first copies at once (`early`: they complete on the barriers it has just
 // initialised), so that their latency overlaps the TMEM allocation and the
@@ -374,7 +395,7 @@ template <int D, bool BIAS, bool DBIAS, bool RB>
 __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                        const CUtensorMap* tmV, const CUtensorMap* tmdO,
                                        const CUtensorMap* tmB, const TcParams& p, uint8_t* smem,
-                                       uint32_t sbase) {
+                                       uint32_t sbase, int kvi) {
   using L = SmemKV<D>;
   // The bias variants run ragged lengths only as RB instantiations; the others
   // take both and test the lengths at run time.
@@ -383,8 +404,8 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cs = p.cs;
-  const int rank = (int)(blockIdx.x % cs);
-  const int ci = (int)(blockIdx.x / cs);
+  const int rank = kvi % cs;
+  const int ci = kvi / cs;
   const int bg = ci % (p.B * p.Hk);  // (batch, KV head); key tile slowest = heaviest first
   const int nt = ci / (p.B * p.Hk);
   const int g = bg % p.Hk;
@@ -1250,7 +1271,356 @@ __device__ __forceinline__ void q_cta(const CUtensorMap* tmQ, const CUtensorMap*
   }
 }
 
-template <int D, bool BIAS, bool DBIAS, bool RB>
+// ============================================ batch-inner query-major CTA ====
+// Dense problems with a dbias output at D = 64 (whole tiles, fixed lengths,
+// B <= 4): the query-major CTA of (query head h, query tile) takes every
+// batch of that tile, batch innermost. For each live key tile it computes
+// S, dP and dS of every batch (dQ of batch b accumulating in its own TMEM
+// columns), sums dS over the batches in registers and stores that sum, the
+// tile of dbias = sum over b of dS, once: no atomics, no zero-filled dbias,
+// and a fixed summation order. The key-major CTAs then run without dbias.
+//
+// Shared memory: two sub-tile stages (Q, dO, K, V of one (key tile, batch))
+// and one bias tile (shared by the batches of a key tile). TMEM: dQ of
+// batch b in columns [b D, b D + D), two 128-column S / dP / dS buffers from
+// column 256. Sub-tile number T = key tile index x B + batch.
+template <int D>
+struct SmemQB {
+  static constexpr int kTile = (D / 64) * kSlab;
+  static constexpr int kStage = 4 * kTile;       // Q, dO, K, V of one sub-tile
+  static constexpr int ST = 0;                   // two stages
+  static constexpr int BIAS = ST + 2 * kStage;   // [128 queries][128 keys] fp32, four boxes of 32 keys
+  static constexpr int BAR = BIAS + 4 * kSlab;   // mbarriers (up to 32)
+  static constexpr int MISC = BAR + 256;         // TMEM base, abort flag
+  static constexpr int TOTAL = MISC + 16;
+};
+static_assert(SmemQB<64>::TOTAL <= 232448, "shared memory per CTA");
+
+// barrier indices, batch-inner query-major CTA: stage s full / released (by
+// dQ of its sub-tile), bias tile full / read (phase 1 of the key tile's last
+// batch, 256 arrivals), S of sub-tile T in buffer T & 1, S read, dP ready,
+// dS written (256), dQ of sub-tile T done (buffer T & 1 free), all dQ done.
+enum BarQB { bStFull0 = 0, bStEmpty0 = 2, bBiasFull = 4, bBiasEmpty = 5, bSFull0 = 6, bSFree = 8,
+             bdPFull = 9, bDsFull = 10, bMma0 = 11, bAccFull = 13, kQBBars = 14 };
+
+template <int D, bool BIAS>
+__device__ __forceinline__ void qb_cta(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                       const CUtensorMap* tmV, const CUtensorMap* tmdO,
+                                       const CUtensorMap* tmB, const TcParams& p, uint8_t* smem,
+                                       uint32_t sbase, int qi) {
+  using L = SmemQB<D>;
+  static_assert(D == 64, "batch-inner CTA: dQ of four batches and two buffers fill TMEM at D = 64");
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nmt = p.Sqs / BM;
+  const int h = qi % p.Hq;
+  const int m0 = (nmt - 1 - qi / p.Hq) * BM;
+  const int g = h / (p.Hq / p.Hk);
+  const int B = p.B;
+  Seq sq;
+  if (!seq_of(p, 0, &sq)) return;  // fixed lengths: every batch has the same sequence view
+
+  Ctx c;
+  c.bars = sbase + L::BAR;
+  c.abort = reinterpret_cast<volatile int*>(smem + L::MISC + 4);
+  c.status = p.status;
+  // bStFull0/1, bStEmpty0/1, bBiasFull, bBiasEmpty, bSFull0/1, bSFree, bdPFull, bDsFull,
+  // bMma0/1, bAccFull
+  const uint32_t counts[kQBBars] = {1, 1, 1, 1, 1, 256, 1, 1, 256, 1, 256, 1, 1, 1};
+  init_common(c, sbase + L::MISC, kQBBars, counts, warp, [] {});
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
+  const uint32_t t_dQ = tmem;          // batch b: [b D, b D + D)
+  const uint32_t t_buf0 = tmem + 256;  // sub-tile T: t_buf0 + (T & 1) 128
+  int n_live = 0;                      // live key tiles of this query tile
+  {
+    KTileIter it(m0, sq);
+    while (it.next()) ++n_live;
+  }
+  const int n_sub = n_live * B;
+  bool epi_ok = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      KTileIter it(m0, sq);
+      int t = 0;
+      int st_issued[2] = {0, 0};
+      bool go = true;
+      while (go && it.next()) {
+        const int n0 = it.nt * BN;
+        // the key tile's bias, once the previous key tile's batches read theirs
+        if (t > 0 && !(go = wait_bar(c, bBiasEmpty, (t - 1) & 1, 50))) break;
+        ptx::mbar_arrive_expect_tx(c.bar(bBiasFull), 4 * kSlab);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+          ptx::tma_load_2d(sbase + L::BIAS + bx * kSlab, tmB, c.bar(bBiasFull), n0 + 32 * bx,
+                           h * p.Sq + m0);
+        for (int b = 0; b < B; ++b) {
+          const int T = t * B + b;
+          const int s = T & 1, u = T >> 1;
+          if (u > 0 && !(go = wait_bar(c, bStEmpty0 + s, (u - 1) & 1, 51))) break;
+          const uint32_t full = c.bar(bStFull0 + s);
+          const uint32_t st = sbase + L::ST + s * L::kStage;
+          const int qrow = (b * p.Hq + h) * p.Sqs + m0;
+          const int krow = (b * p.Hk + g) * p.Sks + n0;
+          ptx::mbar_arrive_expect_tx(full, L::kStage);
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            ptx::tma_load_2d(st + hf * kSlab, tmQ, full, hf * 64, qrow);
+            ptx::tma_load_2d(st + L::kTile + hf * kSlab, tmdO, full, hf * 64, qrow);
+            ptx::tma_load_2d(st + 2 * L::kTile + hf * kSlab, tmK, full, hf * 64, krow);
+            ptx::tma_load_2d(st + 3 * L::kTile + hf * kSlab, tmV, full, hf * 64, krow);
+          }
+          st_issued[s] = u + 1;
+        }
+        ++t;
+      }
+      // no copy may still be landing in shared memory when the CTA ends
+      if (t > 0) drain_bar(c, bBiasFull, (t - 1) & 1);
+      for (int s = 0; s < 2; ++s)
+        if (st_issued[s] > 0) drain_bar(c, bStFull0 + s, (st_issued[s] - 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t id_S = ptx::idesc_f16_f32(128, 128, false, false);
+      constexpr uint32_t id_dQ = ptx::idesc_f16_f32(128, D, false, true);
+      // stage 0 views (stage s: + s kStage): Q, dO, K K-major; K MN-major
+      const uint64_t dQs = ptx::smem_desc_sw128(sbase + L::ST, 16, 1024);
+      const uint64_t ddOs = ptx::smem_desc_sw128(sbase + L::ST + L::kTile, 16, 1024);
+      const uint64_t dKs = ptx::smem_desc_sw128(sbase + L::ST + 2 * L::kTile, 16, 1024);
+      const uint64_t dVs = ptx::smem_desc_sw128(sbase + L::ST + 3 * L::kTile, 16, 1024);
+      const uint64_t dKmn = ptx::smem_desc_sw128(sbase + L::ST + 2 * L::kTile, kSlab, 1024);
+      auto issue_S = [&](int T) {  // S = Q K^T of sub-tile T into buffer T & 1
+        const uint32_t so = (T & 1) * L::kStage;
+        const uint32_t dst = t_buf0 + (T & 1) * 128;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
+          ptx::mma_ss(dst, ptx::desc_add(dQs, so + off), ptx::desc_add(dKs, so + off), id_S, s > 0);
+        }
+      };
+      auto issue_dP = [&](int T) {  // dP = dO V^T over S(T)
+        const uint32_t so = (T & 1) * L::kStage;
+        const uint32_t dst = t_buf0 + (T & 1) * 128;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint32_t off = (s >> 2) * kSlab + (s & 3) * 32;
+          ptx::mma_ss(dst, ptx::desc_add(ddOs, so + off), ptx::desc_add(dVs, so + off), id_S, s > 0);
+        }
+      };
+      // dQ_b += dS K (A = dS, fp16 pairs over the front half of each
+      // warpgroup's columns; B = K MN-major); the batch's first key tile
+      // (first) overwrites its accumulator
+      auto issue_dQ = [&](int T, int b, bool first) {
+        const uint64_t dk = ptx::desc_add(dKmn, (T & 1) * L::kStage);
+        const uint32_t src = t_buf0 + (T & 1) * 128;
+#pragma unroll
+        for (int s = 0; s < BN / 16; ++s) {
+          const uint32_t a_col = src + (s >> 2) * 64 + (s & 3) * 8;
+          ptx::mma_ts(t_dQ + b * D, a_col, ptx::desc_add(dk, s * 2048), id_dQ,
+                      (!first || s > 0) ? 1u : 0u);
+        }
+      };
+      // Per sub-tile T (buffer T & 1): dP(T) once the softmax has copied S(T)
+      // out; S(T+1) once dQ(T-1) has read its buffer and its stage landed;
+      // dQ(T) once dS(T) is in TMEM.
+      int n_done = 0;  // sub-tiles whose dQ went out
+      bool ok = n_sub == 0 || wait_bar(c, bStFull0, 0, 52);
+      if (ok && n_sub > 0) {
+        ptx::tc_fence_after();
+        issue_S(0);
+        ptx::mma_commit(c.bar(bSFull0));
+      }
+      for (int T = 0; ok && T < n_sub; ++T) {
+        ok = wait_bar(c, bSFree, T & 1, 53);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_dP(T);
+        ptx::mma_commit(c.bar(bdPFull));
+        if (T + 1 < n_sub) {
+          const int n1 = (T + 1) & 1;
+          ok = (T < 1 || wait_bar(c, bMma0 + n1, ((T - 1) >> 1) & 1, 54)) &&
+               wait_bar(c, bStFull0 + n1, ((T + 1) >> 1) & 1, 52);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_S(T + 1);
+          ptx::mma_commit(c.bar(bSFull0 + n1));
+        }
+        ok = wait_bar(c, bDsFull, T & 1, 55);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        issue_dQ(T, T % B, T < B);
+        ptx::mma_commit(c.bar(bMma0 + (T & 1)));
+        ptx::mma_commit(c.bar(bStEmpty0 + (T & 1)));  // Q / K read by S and dQ, dO / V by dP
+        ++n_done;
+      }
+      ptx::mma_commit(c.bar(bAccFull));
+      // the last buffer / stage releases, waited here (see the key-major CTA)
+      for (int bb = 0; bb < 2; ++bb) {
+        const int n_b = (n_done + 1 - bb) >> 1;
+        if (n_b > 0) {
+          drain_bar(c, bMma0 + bb, (n_b - 1) & 1);
+          drain_bar(c, bStEmpty0 + bb, (n_b - 1) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------ softmax / dS groups --
+    const int wg = (warp - 4) >> 2;  // 0: keys 0-63, 1: keys 64-127
+    const int lg = warp & 3;
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int il = lg * 32 + lane;   // query row within the tile
+    const int i = m0 + il;
+    // -LSE log2e and delta of this row in each batch (fixed lengths: every
+    // row exists)
+    float nl[4], dl[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t row = ((int64_t)(b < B ? b : 0) * p.Hq + h) * p.Sq + i;
+      nl[b] = p.lse[row] * -kLog2e;
+      dl[b] = p.delta[row];
+    }
+    // the bias tile's row il: chunk c of a box row sits at chunk c ^ (il & 7)
+    const uint32_t brow_s = L::BIAS + il * 128;
+    float* dbrow = p.dbias + ((int64_t)h * p.Sq + i) * p.Sk + wg * 64;
+    KTileIter it(m0, sq);
+    int t = 0;
+    bool ok = true;
+    while (ok && it.next()) {
+      const int n0 = it.nt * BN;
+      int klo, khi, ksink;
+      const bool partial = q_row_live<false>(sq, m0, n0, i, &klo, &khi, &ksink);
+      if (!wait_bar(c, bBiasFull, t & 1, 56)) { ok = false; break; }
+      float acc[64];  // sum over the batches of dS for keys n0 + wg 64 + [0, 64)
+#pragma unroll
+      for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+      for (int b = 0; b < B; ++b) {
+        const int T = t * B + b;
+        const uint32_t t_S = t_buf0 + (T & 1) * 128;
+        if (!wait_bar(c, bSFull0 + (T & 1), (T >> 1) & 1, 57)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const float nlb = b == 0 ? nl[0] : b == 1 ? nl[1] : b == 2 ? nl[2] : nl[3];
+        const float dlb = b == 0 ? dl[0] : b == 1 ? dl[1] : b == 2 ? dl[2] : dl[3];
+        // phase 1: P as fp16 pairs (the A operand precision of dQ)
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t sr[32];
+          ptx::tmem_ld32(t_S + lane_off + wg * 64 + cc * 32, sr);
+          ptx::tmem_wait_ld();
+          if (cc == 1) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(c.bar(bSFree));  // S(T) is in registers: dP may overwrite it
+          }
+          const int k0 = wg * 64 + cc * 32;
+          const uint32_t live = q_chunk_bits(klo, khi, ksink, k0);
+#pragma unroll
+          for (int e4 = 0; e4 < 32; e4 += 4) {
+            float bv[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (BIAS) {
+              const float4 b4 = *reinterpret_cast<const float4*>(
+                  smem + brow_s + (k0 >> 5) * kSlab +
+                  ((((uint32_t)e4 >> 2) ^ ((uint32_t)il & 7u)) << 4));
+              bv[0] = b4.x;
+              bv[1] = b4.y;
+              bv[2] = b4.z;
+              bv[3] = b4.w;
+            }
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              ptx::fma2(x[u], x[u + 1], __uint_as_float(sr[e4 + u]), __uint_as_float(sr[e4 + u + 1]),
+                        p.scale_log2, p.scale_log2, nlb, nlb);
+              if constexpr (BIAS)
+                ptx::fma2(x[u], x[u + 1], bv[u], bv[u + 1], kLog2e, kLog2e, x[u], x[u + 1]);
+            }
+            float pv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv[u] = ptx::ex2(x[u]);
+            if (partial) {  // warp-uniform: only tiles the mask cuts need the per-key test
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (!((live >> (e4 + u)) & 1u)) pv[u] = 0.f;
+            }
+            pk[cc * 16 + e4 / 2] = pack_half2(pv[0], pv[1]);
+            pk[cc * 16 + e4 / 2 + 1] = pack_half2(pv[2], pv[3]);
+          }
+        }
+        if (b == B - 1) ptx::mbar_arrive(c.bar(bBiasEmpty));  // the key tile's bias is read
+        // phase 2: dS = P (dP - D) as fp16 pairs over the front half of this
+        // group's dP columns (A operand of dQ), and into the batch sum
+        if (!wait_bar(c, bdPFull, T & 1, 58)) { ok = false; break; }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t dr[32];
+          ptx::tmem_ld32(t_S + lane_off + wg * 64 + cc * 32, dr);
+          ptx::tmem_wait_ld();
+          uint32_t dk[16];
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pk[cc * 16 + e2]));
+            float t0, t1, d0, d1;
+            ptx::sub2(t0, t1, __uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]), dlb,
+                      dlb);
+            ptx::mul2(d0, d1, pf.x, pf.y, t0, t1);
+            acc[cc * 32 + 2 * e2] += d0;
+            acc[cc * 32 + 2 * e2 + 1] += d1;
+            dk[e2] = pack_half2(d0, d1);
+          }
+          ptx::tmem_st16(t_S + lane_off + wg * 64 + cc * 16, dk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar(bDsFull));
+      }
+      if (!ok) break;
+      // this key tile's dbias: row i, keys n0 + wg 64 + [0, 64), the batch
+      // sum in batch order (dead entries have dS = 0)
+#pragma unroll
+      for (int e = 0; e < 64; e += 8) put8(dbrow + n0 + e, acc + e);
+      ++t;
+    }
+    epi_ok = ok && wait_bar(c, bAccFull, 0, 59);
+    // ---------------------------------------------------- dQ epilogue --
+    // batch b: row i, columns [wg D/2, wg D/2 + D/2) of dQ_b
+    if (epi_ok) {
+      ptx::tc_fence_after();
+      for (int b = 0; b < B; ++b) {
+        uint32_t v[D / 2];
+        if (n_sub > 0) {
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+            ptx::tmem_ld32(t_dQ + b * D + lane_off + wg * (D / 2) + cc * 32, v + cc * 32);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < D / 2; ++e) v[e] = 0u;
+        }
+        float* grow = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D + wg * (D / 2);
+#pragma unroll
+        for (int e = 0; e < D / 2; e += 4)
+          put4(grow + e, __uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
+               __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale, false);
+      }
+    }
+  }
+
+  // ----------------------------------------------------------- teardown --
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (lane == 0) drain_bar(c, bAccFull, 0);
+    __syncwarp();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BIAS, bool DBIAS, bool RB, bool QB>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -1282,8 +1652,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     bits = __reduce_or_sync(0xffffffffu, bits);
     if (bits && (threadIdx.x & 31) == 0) report(p.status, ATTN_ERR_RANGE, bits);
   }
-  if ((int)blockIdx.x < p.kv_ctas) {
-    kv_cta<D, BIAS, DBIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase);
+  if constexpr (QB) {
+    // batch-inner query-major CTAs first (the longest), then key-major ones
+    // without dbias
+    if ((int)blockIdx.x < p.qb_ctas)
+      qb_cta<D, BIAS>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase, (int)blockIdx.x);
+    else
+      kv_cta<D, BIAS, false, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase,
+                                 (int)blockIdx.x - p.qb_ctas);
+  } else if ((int)blockIdx.x < p.kv_ctas) {
+    kv_cta<D, BIAS, DBIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase, (int)blockIdx.x);
   } else {
     const int qi = (int)blockIdx.x - p.kv_ctas;
     q_cta<D, BIAS, RB>(&tmQ, &tmK, &tmV, &tmdO, &tmB, p, smem, sbase, qi);
@@ -1359,6 +1737,15 @@ bool make_map(CUtensorMap* m, const __half* base, uint64_t rows, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// dbias entries of tiles the mask leaves dead (batch-inner dbias mode, which
+// stores only the tiles it visits); n a multiple of 4, p 16-byte aligned.
+__global__ void zero_fill_kernel(float* p, int64_t n) {
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4;
+       i += (int64_t)gridDim.x * blockDim.x)
+    reinterpret_cast<float4*>(p)[i] = z;
+}
+
 // The kernel's tensor maps: fp16 staged q, k, v, dO, and the fp32 bias (TMA
 // bias path only; a copy of q otherwise, never read).
 struct TcMaps {
@@ -1380,22 +1767,30 @@ bool make_bias_map(CUtensorMap* m, const float* base, uint64_t rows, int cols) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool BIAS, bool DBIAS, bool RB>
+template <int D, bool BIAS, bool DBIAS, bool RB, bool QB = false>
 cudaError_t launch_variant(const TcMaps& m, const TcParams& p, int grid, cudaStream_t stream) {
-  auto kern = attn_bwd_tc_kernel<D, BIAS, DBIAS, RB>;
+  auto kern = attn_bwd_tc_kernel<D, BIAS, DBIAS, RB, QB>;
+  int smem = smem_total<D>();
+  if constexpr (QB) smem = smem > SmemQB<D>::TOTAL ? smem : SmemQB<D>::TOTAL;
   static bool configured = false;  // attribute set once per process and variant
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_total<D>());
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  return launch_dependent(kern, dim3(grid), dim3(kThreads), (size_t)smem_total<D>(), stream, m.q,
-                          m.k, m.v, m.dO, m.bias, p);
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), (size_t)smem, stream, m.q, m.k, m.v,
+                          m.dO, m.bias, p);
 }
 
 template <int D>
 cudaError_t launch_d(const TcMaps& m, const TcParams& p, int grid, cudaStream_t stream) {
+  if constexpr (D == 64) {
+    if (p.qb_ctas > 0) {
+      if (p.bias) return launch_variant<D, true, true, false, true>(m, p, grid, stream);
+      return launch_variant<D, false, true, false, true>(m, p, grid, stream);
+    }
+  }
   // without bias and dbias, ragged lengths need no separate instantiation
   if (p.ragged) {
     if (p.bias && p.dbias) return launch_variant<D, true, true, true>(m, p, grid, stream);
@@ -1447,6 +1842,13 @@ int tc_head_split(const Problem& p) {
   // in arrival order)
   if (p.deterministic) return 1;
   return head_split(p.Hq / p.Hk, p.B * p.Hk * (tc_rows(p.Sk) / BN), sm_count());
+}
+
+bool tc_dbias_in_q(const Problem& p) {
+  // dQ of B batches (B D columns) and two S / dP buffers fit TMEM at D = 64;
+  // whole tiles and fixed lengths (the CTA's sub-tiles share one sequence view)
+  return tc_supported(p) && !p.cuda_cores && p.D == 64 && p.B <= 4 && !p.varlen &&
+         p.Sq % BM == 0 && p.Sk % BN == 0;
 }
 
 bool tc_supported(const Problem& p) {
@@ -1509,8 +1911,27 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.dbias = dbias;
   p.dbias_bstride = pr.dbias_bstride;
   p.status = st;
-  const int q_ctas = pr.B * pr.Hq * (p.Sqs / BM);
+  // dbias in batch-inner query-major CTAs (one per query head and query
+  // tile) when it applies; then the tiles the mask leaves dead are never
+  // visited, and their dbias entries are zeroed first
+  const bool qb = dbias != nullptr && tc_dbias_in_q(pr);
+  p.qb_ctas = qb ? pr.Hq * (p.Sqs / BM) : 0;
+  const int q_ctas = qb ? p.qb_ctas : pr.B * pr.Hq * (p.Sqs / BM);
   const int grid = p.kv_ctas + q_ctas;
+  if (qb) {
+    bool any_dead = false;
+    for (int n0 = 0; n0 < p.Sks && !any_dead; n0 += BN) {
+      int lo, hi;
+      live_query_tiles(pr.mask, pr.Sq, pr.Sk, BM, BN, n0, &lo, &hi);
+      any_dead = lo != 0 || hi != p.Sqs / BM - 1;
+    }
+    if (any_dead) {
+      const int64_t n = (int64_t)pr.Hq * pr.Sq * pr.Sk;
+      zero_fill_kernel<<<std::min<int64_t>((n / 4 + 255) / 256, 4096), 256, 0, stream>>>(dbias, n);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
   TcMaps maps;
   maps.q = mq;
   maps.k = mk;
