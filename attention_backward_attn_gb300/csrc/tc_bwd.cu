@@ -21,16 +21,17 @@
 //   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
 //   MMA2  dP^T = V  dO^T     (into the same TMEM columns, once S^T was read)
 //   SFU   phase 1: P^T = exp2(S^T scale log2e + bias log2e - LSE log2e),
-//                  fp16 into SMEM (A operand of MMA3)
-//         phase 2: dS^T = P^T (dP^T - D), fp16 into TMEM over dP^T (A of MMA4)
-//   MMA3  dV += P^T dO       (A = P^T K-major, B = dO MN-major)
+//                  kept in fp32 registers
+//         phase 2: dS^T = P^T (dP^T - D); dS^T and P^T go as fp16 pairs into
+//                  the columns of dP^T just read (A operands of MMA3 / MMA4)
+//   MMA3  dV += P^T dO       (A = P^T in TMEM, B = dO MN-major)
 //   MMA4  dK += dS^T Q       (A = dS^T in TMEM, B = Q MN-major)
 // TMEM holds dK, dV and two 128-column buffers; tile t uses buffer t & 1
-// for S^T, then dP^T, then dS^T. Issue order per tile: dP(t) (as soon as
-// the softmax has copied S^T(t) into registers), S(t+1) into the other
-// buffer (free once dK(t-1) has read it), dV(t), dK(t). No MMA has to wait
-// for an earlier one to complete, so the tensor pipe runs while the softmax
-// works on the same tile.
+// for S^T, then dP^T, then dS^T / P^T. Issue order per tile: dP(t) (as soon
+// as the softmax has copied S^T(t) into registers), S(t+1) into the other
+// buffer (free once dV / dK(t-1) have read it), dV(t), dK(t). No MMA has to
+// wait for an earlier one to complete, so the tensor pipe runs while the
+// softmax works on the same tile.
 //
 // Query-major CTAs (dQ): one CTA per (batch, query head, 128-row query tile)
 // loops over the live key tiles of its KV head, recomputing S and dP:
@@ -42,6 +43,13 @@
 // and no zero-filled accumulation buffer. Tile t uses TMEM buffer t % 3 of
 // three, so S(t+1) goes out right after dP(t) and the softmax never waits for
 // the next S.
+//
+// dbias at D = 64 (B <= 4, whole tiles, fixed lengths): batch-inner
+// query-major CTAs instead, one per (query head, query tile) over all
+// batches, batch innermost; each sums dS over the batches in registers and
+// stores every dbias element of a live tile once, and the key-major CTAs run
+// without dbias (details at qb_cta). Otherwise the key-major softmax adds dS
+// into dbias with fp32 reductions.
 //
 // Lengths need not be whole tiles: the pre-pass stages every head's rows
 // rounded up to 128 with zero rows past the length, a tile that crosses a

@@ -105,11 +105,15 @@ typedef struct attn_problem {
 /* Deterministic dense backward: dq, dk, dv and dbias are bitwise the same on
  * every run. dk / dv are then written by one CTA per key tile (no split of a
  * key tile's query heads over CTAs, whose partial sums would be added in
- * arrival order). With dbias and B > 1, the backward kernel (still one
+ * arrival order). dbias on the tensor-core path at D = 64 with B <= 4 and
+ * fixed lengths in whole 128-row tiles is deterministic in either mode (one
+ * CTA sums dS over the batches in a fixed order and stores each element
+ * once). Other dbias problems with B > 1: the backward kernel (still one
  * launch) adds each batch's terms into that batch's own slice of the
  * workspace (one writer per element, so every slice holds exact values), and
  * a second kernel sums the slices into dbias in batch order; the workspace
- * then holds B * Hq * Sq * Sk more fp32 values. Slower than the default. Sparse variant: the tensor-core kernel stores
+ * then holds B * Hq * Sq * Sk more fp32 values. Slower than the default.
+ * Sparse variant: the tensor-core kernel stores
  * every (token, KV head)'s dKV rows in the workspace instead of adding them
  * into d_ori_kv / d_cmp_kv, and a second pass adds each row's terms in token
  * order and writes the rows (the workspace then holds Sq * Hk * (selected-row
@@ -197,16 +201,18 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
 /* Bytes of device workspace that attn_bwd_preprocess and attn_bwd need for
  * this problem: a status record, the fp16 staging of the operands of the
  * tensor-core path (lengths rounded up to whole 128-row tiles), and with
- * ATTN_FLAG_DETERMINISTIC the per-batch dbias slices (dense, B > 1) or the
- * per-slot dKV rows (sparse). Returns 0 if the arguments are invalid. */
+ * ATTN_FLAG_DETERMINISTIC the per-batch dbias slices (dense, B > 1, outside
+ * the D = 64 batch-inner case above) or the per-slot dKV rows (sparse).
+ * Returns 0 if the arguments are invalid. */
 size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
                                const attn_sparse_t* sparse);
 
 /* Backward pre-pass ("34_bwd_gqa_fmha.py" cpu_bwd_gqa: D = rowsum(dO * O);
  * Ascend formula phase 2: SoftmaxGrad(dO, O)):
  *  - delta[b, h, i] = sum_d dO[b, i, h, d] * O[b, i, h, d] in fp32;
- *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL; in
- *    the deterministic mode with B > 1, the per-batch dbias slices of the
+ *  - zeroes the outputs attn_bwd accumulates into: dbias (if non-NULL and
+ *    not in the D = 64 batch-inner case, where attn_bwd stores every entry;
+ *    in the deterministic mode with B > 1, the per-batch dbias slices of the
  *    workspace instead, which attn_bwd then sums into dbias), for the sparse
  *    variant sparse->d_ori_kv / d_cmp_kv, and dk / dv when the tensor-core
  *    path splits a KV head's query-head group over several CTAs that add

@@ -126,9 +126,13 @@ def test_dbias_support_is_the_mask(name, D):
     O_b, L_f, _, _ = H.dense_forward_inputs(w)
     plan = H.gpu_dense_plan(w, O_b, L_f)
     assert plan.path == 1
+    # every entry must be written by the call (zeroed, or computed), whatever
+    # the buffer held before
+    plan.dbias.fill_(float("nan"))
     plan.run()
     torch.cuda.synchronize()
     assert plan.device_status() == (0, 0)
+    assert torch.isfinite(plan.dbias).all()
     live = oracle.live_mask(w.Sq, w.Sk, w.window_left, w.window_right, w.num_sink,
                             w.bottom_right)
     multi = live & (live.sum(axis=1) >= 2)[:, None]

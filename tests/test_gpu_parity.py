@@ -69,6 +69,13 @@ SMALL_DENSE = {
     # Sq != Sk, GQA 8:1, no mask
     "gqa8_sq128_sk320_d128": lambda: make_dense("x", 22, B=1, Hq=8, Hk=1, Sq=128, Sk=320,
                                                 D=128),
+    # dbias in the batch-inner query-major CTAs with a mask that leaves whole
+    # tiles dead (zeroed first) and cuts others (per-element mask), GQA 2:1,
+    # four batches (the most those CTAs take)
+    "window_sinks_alibi_dbias_s512_d64": lambda: make_dense("qb", 29, B=4, Hq=4, Hk=2, Sq=512,
+                                                            Sk=512, D=64, window_left=150,
+                                                            window_right=0, num_sink=3,
+                                                            alibi=True, want_dbias=True),
     # Sq > Sk, two-sided window, bias without dbias request
     "window_lr_sq320_sk192_d64": lambda: make_dense("y", 23, B=2, Hq=2, Hk=1, Sq=320, Sk=192,
                                                     D=64, window_left=40, window_right=25,
