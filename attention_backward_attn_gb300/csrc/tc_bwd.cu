@@ -1482,15 +1482,6 @@ __device__ __forceinline__ void qb_cta(const CUtensorMap* tmQ, const CUtensorMap
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const int il = lg * 32 + lane;   // query row within the tile
     const int i = m0 + il;
-    // -LSE log2e and delta of this row in each batch (fixed lengths: every
-    // row exists)
-    float nl[4], dl[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int64_t row = ((int64_t)(b < B ? b : 0) * p.Hq + h) * p.Sq + i;
-      nl[b] = p.lse[row] * -kLog2e;
-      dl[b] = p.delta[row];
-    }
     // the bias tile's row il: chunk c of a box row sits at chunk c ^ (il & 7)
     const uint32_t brow_s = L::BIAS + il * 128;
     float* dbrow = p.dbias + ((int64_t)h * p.Sq + i) * p.Sk + wg * 64;
@@ -1508,10 +1499,13 @@ __device__ __forceinline__ void qb_cta(const CUtensorMap* tmQ, const CUtensorMap
       for (int b = 0; b < B; ++b) {
         const int T = t * B + b;
         const uint32_t t_S = t_buf0 + (T & 1) * 128;
+        // -LSE log2e and delta of this row in batch b (fixed lengths: every
+        // row exists), read before the wait for S
+        const int64_t row = ((int64_t)b * p.Hq + h) * p.Sq + i;
+        const float nlb = __ldg(p.lse + row) * -kLog2e;
+        const float dlb = __ldg(p.delta + row);
         if (!wait_bar(c, bSFull0 + (T & 1), (T >> 1) & 1, 57)) { ok = false; break; }
         ptx::tc_fence_after();
-        const float nlb = b == 0 ? nl[0] : b == 1 ? nl[1] : b == 2 ? nl[2] : nl[3];
-        const float dlb = b == 0 ? dl[0] : b == 1 ? dl[1] : b == 2 ? dl[2] : dl[3];
         // phase 1: P as fp16 pairs (the A operand precision of dQ)
         uint32_t pk[32];
 #pragma unroll
@@ -1610,9 +1604,12 @@ __device__ __forceinline__ void qb_cta(const CUtensorMap* tmQ, const CUtensorMap
         }
         float* grow = p.dq + (((int64_t)b * p.Sq + i) * p.Hq + h) * D + wg * (D / 2);
 #pragma unroll
-        for (int e = 0; e < D / 2; e += 4)
-          put4(grow + e, __uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
-               __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale, false);
+        for (int e = 0; e < D / 2; e += 8) {
+          float o8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) o8[u] = __uint_as_float(v[e + u]) * p.scale;
+          put8(grow + e, o8);
+        }
       }
     }
   }
