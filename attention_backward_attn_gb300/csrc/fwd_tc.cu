@@ -6,16 +6,18 @@
 // "22_sink_tokens_fmha.py" masked CPU forward), for dense problems with
 // D in {64, 128} whose q / k / v rows are packed over (batch, position).
 //
-// One CTA per (batch, query head, 128-row query tile), two passes over the
-// live key tiles of the mask:
-//   pass 1  S = Q K^T into TMEM; the softmax warps keep each row's running
-//           maximum and sum of exponentials and end with the row's LSE;
-//   pass 2  S again; P = exp(S - LSE) is exact (no rescaling of O), written
-//           as bf16 over S in TMEM, and O += P V accumulates in TMEM.
-// The second S costs one extra MMA per tile (3 instead of 2) and saves the
-// running rescale of the O accumulator. Operands are the caller's bf16 rows,
-// loaded by TMA through 3-D tensor maps (d, head, batch * position); P is
-// rounded to bf16 for its MMA (O is stored as bf16).
+// One CTA per (batch, query head, 128-row query tile), one pass over the
+// live key tiles of the mask (online softmax): per tile S = Q K^T into one of
+// two TMEM buffers, the two softmax warpgroups (64 keys of a row each) agree
+// on the tile's row maximum through shared memory, P = 2^(x - m) is written
+// as bf16 over S, and O += P V accumulates in TMEM. The scale m of the
+// accumulated terms moves only when a tile's row maximum exceeds it by more
+// than 2^8 (lazy rescaling: O's row and the partial sums are then scaled
+// down once the previous P V has completed), so most tiles need no
+// correction; O is divided by the row's sum at the end, and
+// LSE = m + log2(sum). Operands are the caller's bf16 rows, loaded by TMA
+// through 3-D tensor maps (d, head, batch * position); P is rounded to bf16
+// for its MMA (O is stored as bf16).
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 4-7 / 8-11 two softmax warpgroups (key columns 0-63 / 64-127
@@ -39,20 +41,22 @@ template <int D>
 struct FwdSmem {
   static constexpr int kTile = (D / 64) * kFSlab;
   static constexpr int Q = 0;
-  static constexpr int K = Q + kTile;       // 2 stages
-  static constexpr int V = K + 2 * kTile;   // 2 stages
-  static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] (max, sum)
-  static constexpr int BAR = STAT + 2 * 128 * 8;
+  static constexpr int K = Q + kTile;         // 2 stages
+  static constexpr int V = K + 2 * kTile;     // 2 stages
+  static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] partial sums
+  static constexpr int XCH = STAT + 2 * 128 * 4;  // [step parity][2 warpgroups][128 rows] maxima
+  static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
   static constexpr int MISC = BAR + 128;      // TMEM base, abort flag
   static constexpr int TOTAL = MISC + 16;
 };
 
-// fQFull: Q landed. fKvFull / fKvEmpty: key-tile stage (K, plus V in pass 2).
-// fSFull: S of a step in TMEM buffer 0 / 1. fSRead: pass-1 S read (256
-// arrivals). fPFull: pass-2 P written over S (256 arrivals). fPvDone: the
-// P V MMAs of a step completed. fOFull: every MMA completed.
-enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fSRead0 = 7, fPFull0 = 9,
-              fPvDone0 = 11, fOFull = 13, kFwdBars = 14 };
+// fQFull: Q landed. fKvFull / fKvEmpty: key-tile stage (K and V of a step).
+// fSFull: S of a step in TMEM buffer 0 / 1. fPFull: P written over S (256
+// arrivals). fPvDone: the P V MMAs of a step completed (its buffer is free
+// and O holds its terms). fOFull: every MMA completed. fXch: a step's row
+// maxima of both warpgroups are in shared memory (256 arrivals).
+enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fPFull0 = 7, fPvDone0 = 9,
+              fOFull = 11, fXch0 = 12, kFwdBars = 14 };
 
 struct FwdParams {
   int B, Hq, Hk, Sq, Sk;
@@ -88,13 +92,6 @@ struct KeyTiles {
   __device__ int tile(int k) const { return k < s_end ? k : w_first + (k - s_end); }
 };
 
-// Phase index of the use of S buffer bf by pass-2 step u (steps T.. 2T-1;
-// buffer bf = step parity): the count of earlier pass-2 steps of that parity.
-__device__ __forceinline__ int pass2_use(int u, int T) {
-  const int first = (T & 1) == (u & 1) ? T : T + 1;
-  return (u - first) >> 1;
-}
-
 template <int D, bool BIAS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -121,7 +118,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   c.status = nullptr;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFwdBars; ++i) {
-      const bool many = (i >= fSRead0 && i < fPvDone0);  // SRead / PFull: 256 arrivals
+      const bool many = (i >= fPFull0 && i < fPvDone0) || i >= fXch0;  // 256 arrivals
       ptx::mbar_init(c.bar(i), many ? 256u : 1u);
     }
     *c.abort = 0;
@@ -149,21 +146,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf)
         ptx::tma_load_3d(sbase + L::Q + hf * kFSlab, &tmQ, c.bar(fQFull), hf * 64, h, qrow);
+      // K and V of step u into stage u & 1, once P V(u - 2) read the stage
       int issued[2] = {0, 0};
-      for (int u = 0; u < 2 * T; ++u) {
+      for (int u = 0; u < T; ++u) {
         const int st = u & 1, use = u >> 1;
         if (use > 0 && !wait_bar(c, fKvEmpty0 + st, (use - 1) & 1, 1)) break;
-        const bool pass2 = u >= T;
-        const int krow = b * p.Sk + tiles.tile(pass2 ? u - T : u) * kBN;
+        const int krow = b * p.Sk + tiles.tile(u) * kBN;
         const uint32_t full = c.bar(fKvFull0 + st);
-        ptx::mbar_arrive_expect_tx(full, (pass2 ? 2 : 1) * L::kTile);
+        ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
 #pragma unroll
         for (int hf = 0; hf < D / 64; ++hf) {
-          ptx::tma_load_3d(sbase + L::K + st * L::kTile + hf * kFSlab, &tmK, full, hf * 64, g,
-                           krow);
-          if (pass2)
-            ptx::tma_load_3d(sbase + L::V + st * L::kTile + hf * kFSlab, &tmV, full, hf * 64, g,
-                             krow);
+          ptx::tma_load_3d(sbase + L::K + st * L::kTile + hf * kFSlab, &tmK, full, hf * 64, g, krow);
+          ptx::tma_load_3d(sbase + L::V + st * L::kTile + hf * kFSlab, &tmV, full, hf * 64, g, krow);
         }
         issued[st] = use + 1;
       }
@@ -181,41 +175,32 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t dK = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dVmn = ptx::smem_desc_sw128(sbase + L::V, kFSlab, 1024);
-      int n_kv[2] = {0, 0}, n_pv[2] = {0, 0};
-      // O += P V of pass-2 step v once P replaced S(v) in TMEM
+      int n_pv[2] = {0, 0};
+      // O += P V of step v once P replaced S(v) in TMEM
       auto issue_pv = [&](int v) -> bool {
         const int sv = v & 1;
-        if (!wait_bar(c, fPFull0 + sv, pass2_use(v, T) & 1, 6)) return false;
+        if (!wait_bar(c, fPFull0 + sv, (v >> 1) & 1, 6)) return false;
         ptx::tc_fence_after();
         const uint32_t t_S = t_S0 + sv * 128;
         const uint64_t dv = ptx::desc_add(dVmn, sv * L::kTile);
 #pragma unroll
         for (int s = 0; s < kBN / 16; ++s) {
           const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_O, a_col, ptx::desc_add(dv, s * 2048), id_O, (v > T || s > 0) ? 1u : 0u);
+          ptx::mma_ts(t_O, a_col, ptx::desc_add(dv, s * 2048), id_O, (v > 0 || s > 0) ? 1u : 0u);
         }
         ptx::mma_commit(c.bar(fKvEmpty0 + sv));  // K and V of the step read
-        ptx::mma_commit(c.bar(fPvDone0 + sv));   // its S buffer free again
-        ++n_kv[sv];
+        ptx::mma_commit(c.bar(fPvDone0 + sv));   // its S buffer free again, O up to date
         ++n_pv[sv];
         return true;
       };
-      // S(u) goes first, then the P V of the previous pass-2 step (its P is
-      // being written while S(u) runs)
+      // S(u) first, then the P V of step u - 1 (its P is being written while
+      // S(u) runs)
       bool ok = T == 0 || wait_bar(c, fQFull, 0, 2);
-      int pending = -1;
-      for (int u = 0; ok && u < 2 * T; ++u) {
-        const int st = u & 1, use = u >> 1;
-        if (!wait_bar(c, fKvFull0 + st, use & 1, 3)) break;
-        // the S buffer of step u - 2 must be free: read (pass 1) or consumed
-        // by its P V MMAs (pass 2, issued in the previous iteration)
-        if (u >= 2) {
-          const bool was_pass2 = u - 2 >= T;
-          const bool freed = was_pass2
-                                 ? wait_bar(c, fPvDone0 + st, pass2_use(u - 2, T) & 1, 4)
-                                 : wait_bar(c, fSRead0 + st, ((u - 2) >> 1) & 1, 5);
-          if (!freed) break;
-        }
+      for (int u = 0; ok && u < T; ++u) {
+        const int st = u & 1;
+        ok = wait_bar(c, fKvFull0 + st, (u >> 1) & 1, 3) &&
+             (u < 2 || wait_bar(c, fPvDone0 + st, ((u - 2) >> 1) & 1, 4));  // buffer of step u - 2
+        if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t t_S = t_S0 + st * 128;
         const uint64_t dk = ptx::desc_add(dK, st * L::kTile);
@@ -225,19 +210,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           ptx::mma_ss(t_S, ptx::desc_add(dQ, off), ptx::desc_add(dk, off), id_S, s > 0);
         }
         ptx::mma_commit(c.bar(fSFull0 + st));
-        if (u < T) {
-          ptx::mma_commit(c.bar(fKvEmpty0 + st));  // K read: the stage is free again
-          ++n_kv[st];
-        }
-        if (pending >= 0 && !issue_pv(pending)) break;
-        pending = u >= T ? u : -1;
+        if (u > 0) ok = issue_pv(u - 1);
       }
-      if (pending >= 0) issue_pv(pending);
+      if (ok && T > 0) issue_pv(T - 1);
       ptx::mma_commit(c.bar(fOFull));
       // commit arrivals no other role waits for: waited here before the CTA exits
       for (int st = 0; st < 2; ++st) {
-        if (n_kv[st] > 0) drain_bar(c, fKvEmpty0 + st, (n_kv[st] - 1) & 1);
-        if (n_pv[st] > 0) drain_bar(c, fPvDone0 + st, (n_pv[st] - 1) & 1);
+        if (n_pv[st] > 0) {
+          drain_bar(c, fKvEmpty0 + st, (n_pv[st] - 1) & 1);
+          drain_bar(c, fPvDone0 + st, (n_pv[st] - 1) & 1);
+        }
       }
     }
     __syncwarp();
@@ -255,14 +237,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // log2-domain logits of this thread's 64 keys of step u's tile (dead: -inf)
     auto logits = [&](int u, float* x) -> bool {
       const int st = u & 1;
-      if (!wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10)) return false;
+      // (warp-uniform outcome: the TMEM loads below are warp-collective)
+      const bool full = wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10);
+      if (!__all_sync(0xffffffffu, full)) return false;
       ptx::tc_fence_after();
       uint32_t sr[64];
       const uint32_t t_S = t_S0 + st * 128 + lane_off + wg * 64;
       ptx::tmem_ld32(t_S, sr);
       ptx::tmem_ld32(t_S + 32, sr + 32);
       ptx::tmem_wait_ld();
-      const int n0 = tiles.tile(u < T ? u : u - T) * kBN;
+      const int n0 = tiles.tile(u) * kBN;
       const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
       const bool partial = m0 + kBM > p.Sq || n0 + kBN > p.Sk ||
                            !tile_full(p.mask, m0, m0 + kBM, n0, n0 + kBN);
@@ -272,61 +256,97 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         khi = imin2(i + p.mask.wr - n0, kcap - 1);
         ksink = imin2(p.mask.sink - n0, kcap);
       }
+      // the row's bias: 16-byte loads when the tile's keys all exist and the
+      // bias rows are 16-byte aligned (Sk a multiple of 4), else clamped
+      // scalar loads (keys past Sk are dead anyway)
+      float bv[64];
+      if constexpr (BIAS) {
+        if (kcap >= kBN && (p.Sk & 3) == 0) {
+          const float4* b4 = reinterpret_cast<const float4*>(brow + n0 + wg * 64);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float4 t4 = __ldg(b4 + e);
+            bv[4 * e] = t4.x;
+            bv[4 * e + 1] = t4.y;
+            bv[4 * e + 2] = t4.z;
+            bv[4 * e + 3] = t4.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) bv[e] = __ldg(brow + n0 + imin2(wg * 64 + e, kcap - 1));
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const int kk = wg * 64 + e;  // key within the tile
         float xv = __uint_as_float(sr[e]) * p.scale_log2;
-        if constexpr (BIAS) xv = fmaf(__ldg(brow + n0 + imin2(kk, kcap - 1)), kLog2e, xv);
+        if constexpr (BIAS) xv = fmaf(bv[e], kLog2e, xv);
         const bool live = !partial || (kk >= klo && kk <= khi) || kk < ksink;
         x[e] = live ? xv : -INFINITY;
       }
       return true;
     };
+    // One pass over the live key tiles with a running row maximum. P is
+    // taken against m_used, the maximum the accumulated terms were scaled
+    // with; only when a tile's row maximum exceeds it by more than
+    // kRescaleLog2 (so P stays below 2^kRescaleLog2) does m_used move up,
+    // and then the row's O columns and partial sum are scaled down by
+    // 2^(old - new) once the previous P V has completed. O and the sum end
+    // in the same scale, so O / sum and LSE = m_used + log2(sum) are exact
+    // up to rounding whatever m_used is.
+    constexpr float kRescaleLog2 = 8.f;
+    float* xch = reinterpret_cast<float*>(smem + L::XCH);  // [step parity][warpgroup][row]
+    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    // pass 1: running maximum and sum of 2^x per row half
-    float m = -INFINITY, l = 0.f;
     for (int u = 0; u < T; ++u) {
       float x[64];
       if (!logits(u, x)) { ok = false; break; }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(fSRead0 + (u & 1)));
       float mx = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
-      const float mn = fmaxf(m, mx);
-      if (mn != -INFINITY) {
-        float sum = 0.f;
+      // the row maximum over both halves of the tile (bounded barrier wait)
+      xch[((u & 1) * 2 + wg) * 128 + il] = mx;
+      ptx::mbar_arrive(c.bar(fXch0 + (u & 1)));
+      const bool met = wait_bar(c, fXch0 + (u & 1), (u >> 1) & 1, 12);
+      if (!__all_sync(0xffffffffu, met)) { ok = false; break; }
+      const float m_tile = fmaxf(mx, xch[((u & 1) * 2 + (1 - wg)) * 128 + il]);
+      const bool raise = m_tile > m_used + kRescaleLog2;  // this row's scale moves up
+      const bool rescale = raise && m_used != -INFINITY;  // ... and O holds terms of it
+      // The TMEM loads / stores are warp-collective: the warp takes the
+      // rescale path when any of its rows needs it (factor 1 for the others).
+      if (__any_sync(0xffffffffu, rescale)) {
+        // once P V(u - 1) (and so every earlier one) completed, scale this
+        // half row of O from m_used to m_tile
+        const bool done = wait_bar(c, fPvDone0 + ((u - 1) & 1), ((u - 1) >> 1) & 1, 13);
+        if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const float f = rescale ? ptx::ex2(m_used - m_tile) : 1.f;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sum += ptx::ex2(x[e] - mn);
-        l = (m == -INFINITY ? 0.f : l * ptx::ex2(m - mn)) + sum;
-        m = mn;
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t ov[32];
+          const uint32_t t_o = t_O + lane_off + wg * (D / 2) + cc * 32;
+          ptx::tmem_ld32(t_o, ov);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+          ptx::tmem_st16(t_o, ov);
+          ptx::tmem_st16(t_o + 16, ov + 16);
+        }
+        l *= f;
       }
-    }
-    // the two halves of a row meet in shared memory
-    float* stat = reinterpret_cast<float*>(smem + L::STAT);
-    stat[(wg * 128 + il) * 2] = m;
-    stat[(wg * 128 + il) * 2 + 1] = l;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const float m_o = stat[((1 - wg) * 128 + il) * 2];
-    const float l_o = stat[((1 - wg) * 128 + il) * 2 + 1];
-    const float mm = fmaxf(m, m_o);
-    float lsum = 0.f;
-    if (m != -INFINITY) lsum += l * ptx::ex2(m - mm);
-    if (m_o != -INFINITY) lsum += l_o * ptx::ex2(m_o - mm);
-    const float lse2 = lsum > 0.f ? mm + log2f(lsum) : -INFINITY;  // log2 domain
-    if (wg == 0 && row_in)
-      p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = lse2 == -INFINITY ? -INFINITY : lse2 / kLog2e;
-    // pass 2: P = 2^(x - LSE2) as bf16 over S
-    for (int u = T; ok && u < 2 * T; ++u) {
-      float x[64];
-      if (!logits(u, x)) { ok = false; break; }
+      if (raise) m_used = m_tile;
+      // P = 2^(x - m_used) as bf16 over S (dead keys, and rows with no live
+      // key so far, give 0)
       uint32_t pk[32];
+      float sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
-        const float p0 = lse2 == -INFINITY ? 0.f : ptx::ex2(x[e] - lse2);
-        const float p1 = lse2 == -INFINITY ? 0.f : ptx::ex2(x[e + 1] - lse2);
+        const float p0 = m_used == -INFINITY ? 0.f : ptx::ex2(x[e] - m_used);
+        const float p1 = m_used == -INFINITY ? 0.f : ptx::ex2(x[e + 1] - m_used);
+        sum += p0 + p1;
         pk[e / 2] = pack_bf162(p0, p1);
       }
+      l += sum;
       const uint32_t t_S = t_S0 + (u & 1) * 128 + lane_off + wg * 64;
       ptx::tmem_st16(t_S, pk);
       ptx::tmem_st16(t_S + 16, pk + 16);
@@ -334,7 +354,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::tc_fence_before();
       ptx::mbar_arrive(c.bar(fPFull0 + (u & 1)));
     }
-    // O: this warpgroup writes columns [wg D/2, wg D/2 + D/2) of its row
+    // the row's sum: the two halves meet in shared memory (both used m_used)
+    float* stat = reinterpret_cast<float*>(smem + L::STAT);
+    stat[wg * 128 + il] = l;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float lsum = l + stat[(1 - wg) * 128 + il];
+    const float lse2 = lsum > 0.f ? m_used + log2f(lsum) : -INFINITY;  // log2 domain
+    if (wg == 0 && row_in)
+      p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = lse2 == -INFINITY ? -INFINITY : lse2 / kLog2e;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    // O / sum: this warpgroup writes columns [wg D/2, wg D/2 + D/2) of its row
     if (ok && (T == 0 || wait_bar(c, fOFull, 0, 11))) {
       ptx::tc_fence_after();
       __nv_bfloat16* orow = p.o + b * p.os0 + (int64_t)ic * p.os1 + h * p.os2 + wg * (D / 2);
@@ -352,10 +381,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 w;
-            w.x = pack_bf162(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-            w.y = pack_bf162(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-            w.z = pack_bf162(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-            w.w = pack_bf162(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+            w.x = pack_bf162(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
+            w.y = pack_bf162(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
+            w.z = pack_bf162(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
+            w.w = pack_bf162(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
             *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
           }
         }
