@@ -354,17 +354,6 @@ struct KTileIter {
   }
 };
 
-// Four fp32 values into global memory: a plain 16-byte store, or (add) an
-// fp32 addition of each (red.global.add.v4.f32).
-__device__ __forceinline__ void put4(float* dst, float a, float b, float c, float d, bool add) {
-  if (add)
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-  else
-    *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
-}
-
 // Eight fp32 values as one 32-byte store (one full sector: half the store
 // instructions of 16-byte stores when each thread writes its own row).
 __device__ __forceinline__ void put8(float* dst, const float* v) {
