@@ -144,6 +144,11 @@ bool use_tensor_cores(const Problem& p) {
   return p.sparse ? tc_sparse_supported(p) : tc_supported(p);
 }
 
+// One backward per problem: the tensor-core kernels, or the CUDA-core kernels
+// when the caller asks for them (ATTN_FLAG_CUDA_CORES). A problem outside the
+// tensor-core kernels' shapes is not sent to the CUDA-core kernels unasked.
+bool backward_available(const Problem& p) { return p.cuda_cores || use_tensor_cores(p); }
+
 // dbias computed by the tensor-core kernel's batch-inner query-major CTAs:
 // stored once per element, neither zeroed first nor split by batch.
 bool dbias_in_q(const Problem& p, const float* dbias) {
@@ -287,13 +292,14 @@ int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
                       const attn_sparse_t* sparse) {
   Problem p;
   if (make_problem(prob, mask, sparse, &p) != ATTN_OK) return 0;
+  if (!backward_available(p)) return 0;
   return use_tensor_cores(p) ? 1 : 2;
 }
 
 size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
                                const attn_sparse_t* sparse) {
   Problem p;
-  if (make_problem(prob, mask, sparse, &p) != ATTN_OK) return 0;
+  if (make_problem(prob, mask, sparse, &p) != ATTN_OK || !backward_available(p)) return 0;
   return workspace_layout(p, use_tensor_cores(p)).total;
 }
 
@@ -347,6 +353,7 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
   } else if (!need(dk, n.k) || !need(dv, n.k) || !aligned16(dk) || !aligned16(dv)) {
     return ATTN_ERR_INVALID_ARG;
   }
+  if (!backward_available(p)) return ATTN_ERR_UNSUPPORTED;
   const bool tc = use_tensor_cores(p);
   // the head-split tensor-core kernel adds partial dK / dV sums into zeroed buffers
   const bool zero_kv = tc && !p.sparse && tc_head_split(p) > 1;
@@ -408,6 +415,7 @@ attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,
         !aligned16(dbias))
       return ATTN_ERR_INVALID_ARG;
   }
+  if (!backward_available(p)) return ATTN_ERR_UNSUPPORTED;
   const bool tc = use_tensor_cores(p);
   if (tc && (!aligned16(lse) || !aligned16(delta))) return ATTN_ERR_INVALID_ARG;
   const WorkspaceLayout w = workspace_layout(p, tc);

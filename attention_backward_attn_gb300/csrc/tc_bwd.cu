@@ -1845,9 +1845,10 @@ bool tc_dbias_in_q(const Problem& p) {
          p.Sq % BM == 0 && p.Sk % BN == 0;
 }
 
+// A shape decision only: a driver without cuTensorMapEncodeTiled makes the
+// launch fail (ATTN_ERR_CUDA) rather than move the problem to other kernels.
 bool tc_supported(const Problem& p) {
-  return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0 &&
-         encode_fn() != nullptr;
+  return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0;
 }
 
 cudaError_t launch_mask_probe(const MaskSpec& m, int Sq, int Sk, bool aligned_variant,

@@ -809,7 +809,7 @@ bool tc_sparse_supported(const Problem& p) {
   return p.sparse && p.D == kSpD && p.B == 1 && p.Hq == kSpR * p.Hk && p.Sq > 0 && p.n_ori > 0 &&
          max_selected_rows(p) <= kSpMaxRows &&
          (int64_t)(p.n_ori + p.n_cmp) * p.Hk < (int64_t(1) << 31) && p.qs[1] > 0 &&
-         p.qs[2] > 0 && p.dos[1] > 0 && p.dos[2] > 0 && encode_fn() != nullptr;
+         p.qs[2] > 0 && p.dos[1] > 0 && p.dos[2] > 0;  // (shape only, as tc_supported)
 }
 
 cudaError_t launch_bwd_sparse_tc(const Problem& pr, const void* q, const void* dO,

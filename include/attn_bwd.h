@@ -125,10 +125,14 @@ typedef struct attn_problem {
  * default.) */
 #define ATTN_FLAG_DETERMINISTIC 1
 
-/* Run the CUDA-core kernels (no tensor cores, bf16 operands read directly)
- * even where the tensor-core path applies: a second, independent
- * implementation of the same backward, for cross-checks. attn_bwd_path then
- * returns 2. Slower. */
+/* Run the CUDA-core kernels (no tensor cores, bf16 operands read directly):
+ * a second, independent implementation of the same backward, for
+ * cross-checks and for the shapes the tensor-core kernels do not take
+ * (dense D = 512, sparse variants other than 64 query heads per KV head at
+ * D = 512). The backward runs on them only when this flag asks for it:
+ * without it such a problem returns ATTN_ERR_UNSUPPORTED (and
+ * attn_bwd_workspace_size / attn_bwd_path return 0). attn_bwd_path returns
+ * 2 with the flag. Much slower. */
 #define ATTN_FLAG_CUDA_CORES 2
 
 /* Key mask, positions aligned top-left ("22_sink_tokens_fmha.py"):
@@ -187,11 +191,12 @@ typedef struct attn_sparse {
  * sparse != NULL selects the sparse variant (k, v, bias must then be NULL).
  * Dense problems with D in {64, 128} whose q / k / v rows are evenly spaced
  * over (batch, position) (stride[0] == S * stride[1], or B == 1) run on the
- * tensor cores: bf16 operands, two passes over the live key tiles (row
- * statistics, then O with the exact probabilities), P rounded to bf16 for
- * its MMA; LSE is computed in fp32 from the exact logits. Other shapes, and
- * ATTN_FLAG_CUDA_CORES, run the fp32 CUDA-core forward. A variable-length
- * batch returns ATTN_ERR_UNSUPPORTED. */
+ * tensor cores: bf16 operands, one pass over the live key tiles (online
+ * softmax with a lazily rescaled fp32 O accumulator, divided by the row sum
+ * at the end), P rounded to bf16 for its MMA; LSE = max + log(sum) in fp32.
+ * Other shapes (this producer of the backward's inputs has no other
+ * implementation for them), and ATTN_FLAG_CUDA_CORES, run the fp32
+ * CUDA-core forward. A variable-length batch returns ATTN_ERR_UNSUPPORTED. */
 attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
                            const attn_sparse_t* sparse,
                            const void* q, const void* k, const void* v,
@@ -203,7 +208,8 @@ attn_status_t attn_fwd_lse(const attn_problem_t* prob, const attn_mask_t* mask,
  * tensor-core path (lengths rounded up to whole 128-row tiles), and with
  * ATTN_FLAG_DETERMINISTIC the per-batch dbias slices (dense, B > 1, outside
  * the D = 64 batch-inner case above) or the per-slot dKV rows (sparse).
- * Returns 0 if the arguments are invalid. */
+ * Returns 0 if the arguments are invalid or the problem needs the CUDA-core
+ * kernels without ATTN_FLAG_CUDA_CORES. */
 size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* mask,
                                const attn_sparse_t* sparse);
 
@@ -365,8 +371,9 @@ attn_status_t attn_debug_sparse_rows(const attn_problem_t* prob, const attn_spar
                                      cudaStream_t stream);
 
 /* Which backward kernel attn_bwd would launch for these arguments:
- * 0 = none (invalid / unsupported), 1 = tcgen05 tensor-core kernel,
- * 2 = SIMT kernels. For tests and benchmarks. */
+ * 0 = none (invalid, unsupported, or outside the tensor-core shapes without
+ * ATTN_FLAG_CUDA_CORES), 1 = tcgen05 tensor-core kernel, 2 = SIMT kernels
+ * (ATTN_FLAG_CUDA_CORES). For tests and benchmarks. */
 int32_t attn_bwd_path(const attn_problem_t* prob, const attn_mask_t* mask,
                       const attn_sparse_t* sparse);
 

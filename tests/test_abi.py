@@ -131,6 +131,10 @@ def test_preprocess_validates_dk_dv(ab):
     s.ori_kv, s.n_ori, s.ori_win_left, s.ori_win_right = fake, 128, 31, 0
     s.d_ori_kv = fake
     assert _call_pre(ab, sp, sparse=s, ptrs=dict(k=None, v=None)) == 1
+    # 16 query heads per KV head: CUDA-core kernels only, and only when asked for
+    assert _call_pre(ab, sp, sparse=s,
+                     ptrs=dict(k=None, v=None, dk=None, dv=None, ws=None)) == 2  # ATTN_ERR_UNSUPPORTED
+    sp.flags = ab.ATTN_FLAG_CUDA_CORES
     assert _call_pre(ab, sp, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None, ws=None)) == 7
 
 
@@ -140,6 +144,10 @@ def test_sparse_descriptor_validation(ab):
     s = ab.Sparse()
     s.ori_kv, s.n_ori, s.ori_win_left, s.ori_win_right = fake, 128, 31, 0
     s.d_ori_kv = fake
+    # 16 query heads per KV head: the SIMT kernels, only when asked for
+    assert ab.attn_bwd_path(p, None, s) == 0
+    assert ab.attn_bwd_workspace_size(p, None, s) == 0
+    p.flags = ab.ATTN_FLAG_CUDA_CORES
     assert ab.attn_bwd_path(p, None, s) == 2
     # k / v must be NULL for the shared-KV variant
     assert _call_bwd(ab, p, sparse=s) == 1
@@ -149,7 +157,7 @@ def test_sparse_descriptor_validation(ab):
     assert ab.attn_bwd_path(p, None, s) == 0
     assert _call_bwd(ab, p, sparse=s, ptrs=dict(k=None, v=None, dk=None, dv=None)) == 1
     s.cmp_ratio = 4
-    assert ab.attn_bwd_path(p, None, s) == 2  # 16 query heads per KV head: SIMT kernels
+    assert ab.attn_bwd_path(p, None, s) == 2  # 16 query heads per KV head: SIMT kernels (asked for)
     s.n_cmp = 0
     assert ab.attn_bwd_path(p, None, s) == 0  # compressed KV needs rows
     s.n_cmp = 32

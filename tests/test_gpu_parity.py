@@ -21,9 +21,10 @@ def _torch():
 
 
 def _run_dense(w, expect_path=None):
+    # path 2 (the SIMT kernels) runs only when the problem asks for it
     torch = _torch()
     O_b, L_f, _, _ = H.dense_forward_inputs(w)
-    plan = H.gpu_dense_plan(w, O_b, L_f)
+    plan = H.gpu_dense_plan(w, O_b, L_f, cuda_cores=expect_path == 2)
     if expect_path is not None:
         assert plan.path == expect_path
     plan.run()
@@ -101,7 +102,8 @@ SMALL_DENSE = {
 
 def _dense_path(w):
     """The tcgen05 kernel takes every dense problem with D in {64, 128}, of any
-    lengths (a ragged last tile is masked per element); the SIMT kernels the rest."""
+    lengths (a ragged last tile is masked per element); the SIMT kernels the
+    rest, when the problem asks for them (ATTN_FLAG_CUDA_CORES)."""
     return 1 if w.D in (64, 128) else 2
 
 
@@ -517,9 +519,10 @@ TC_SPARSE = {
 
 
 def _run_sparse(w, expect_path=None):
+    # path 2 (the SIMT kernels) runs only when the problem asks for it
     torch = _torch()
     O_b, L_f, _, _ = H.sparse_forward_inputs(w)
-    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    plan = H.gpu_sparse_plan(w, O_b, L_f, cuda_cores=expect_path == 2)
     if expect_path is not None:
         assert plan.path == expect_path
     plan.run()
@@ -636,7 +639,7 @@ def test_sparse_bad_index_is_reported_not_trapped():
     O_b, L_f, _, _ = H.sparse_forward_inputs(w)
     w.cmp_idx = w.cmp_idx.copy()
     w.cmp_idx[200, 0, 0] = w.n_cmp + 5  # out of range: must be skipped and reported
-    plan = H.gpu_sparse_plan(w, O_b, L_f)
+    plan = H.gpu_sparse_plan(w, O_b, L_f, cuda_cores=True)
     assert plan.path == 2
     plan.run()
     torch.cuda.synchronize()
