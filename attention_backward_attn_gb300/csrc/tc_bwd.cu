@@ -1731,8 +1731,9 @@ bool make_map(CUtensorMap* m, const __half* base, uint64_t rows, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// dbias entries of tiles the mask leaves dead (batch-inner dbias mode, which
-// stores only the tiles it visits); n a multiple of 4, p 16-byte aligned.
+// Zeros over n fp32 values (n a multiple of 4, p 16-byte aligned): dbias
+// entries of tiles the mask leaves dead (batch-inner dbias mode, which stores
+// only the tiles it visits), and the gradients of an empty problem.
 __global__ void zero_fill_kernel(float* p, int64_t n) {
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n / 4;
@@ -1848,7 +1849,7 @@ bool tc_dbias_in_q(const Problem& p) {
 // A shape decision only: a driver without cuTensorMapEncodeTiled makes the
 // launch fail (ATTN_ERR_CUDA) rather than move the problem to other kernels.
 bool tc_supported(const Problem& p) {
-  return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq > 0 && p.Sk > 0;
+  return !p.sparse && (p.D == 64 || p.D == 128) && p.B > 0 && p.Sq >= 0 && p.Sk >= 0;
 }
 
 cudaError_t launch_mask_probe(const MaskSpec& m, int Sq, int Sk, bool aligned_variant,
@@ -1872,6 +1873,21 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
                           const __half* v16, const __half* do16, const float* lse,
                           const float* delta, const float* bias, float* dq, float* dk,
                           float* dv, float* dbias, DevStatus* st, cudaStream_t stream) {
+  if (pr.Sq == 0 || pr.Sk == 0) {
+    // nothing to differentiate: the gradients are zero (dbias has no entry)
+    const int64_t rq = pr.varlen ? pr.total_q : (int64_t)pr.B * pr.Sq;
+    const int64_t rk = pr.varlen ? pr.total_k : (int64_t)pr.B * pr.Sk;
+    const int64_t n[3] = {rq * pr.Hq * pr.D, rk * pr.Hk * pr.D, rk * pr.Hk * pr.D};
+    float* out[3] = {dq, dk, dv};
+    for (int i = 0; i < 3; ++i) {
+      if (n[i] == 0) continue;
+      zero_fill_kernel<<<(unsigned)std::min<int64_t>((n[i] / 4 + 255) / 256, 4096), 256, 0,
+                         stream>>>(out[i], n[i]);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   CUtensorMap mq, mk, mv, mdo;
   const uint64_t qrows = (uint64_t)pr.B * pr.Hq * tc_rows(pr.Sq);
   const uint64_t krows = (uint64_t)pr.B * pr.Hk * tc_rows(pr.Sk);
