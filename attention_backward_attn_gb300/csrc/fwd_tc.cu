@@ -8,14 +8,15 @@
 //
 // One CTA per (batch, query head, 128-row query tile), one pass over the
 // live key tiles of the mask (online softmax): per tile S = Q K^T into one of
-// two TMEM buffers, the two softmax warpgroups (64 keys of a row each) agree
-// on the tile's row maximum through shared memory, P = 2^(x - m) is written
-// as bf16 over S, and O += P V accumulates in TMEM. The scale m of the
-// accumulated terms moves only when a tile's row maximum exceeds it by more
-// than 2^8 (lazy rescaling: O's row and the partial sums are then scaled
-// down once the previous P V has completed), so most tiles need no
-// correction; O is divided by the row's sum at the end, and
-// LSE = m + log2(sum). Operands are the caller's bf16 rows, loaded by TMA
+// two TMEM buffers; each of the two softmax warpgroups takes 64 keys of every
+// row and keeps its own running maximum m, sum and O accumulator for them
+// (O_wg += P(:, its keys) V(its keys, :) in TMEM), so the halves never wait
+// for each other. The scale m of the accumulated terms moves only when a
+// tile's maximum exceeds it by more than 2^8 (lazy rescaling: the row of
+// O_wg and the sum are then scaled down once the previous P V has
+// completed), so most tiles need no correction. At the end the halves meet
+// once: O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / sum and LSE = m + log2(sum)
+// with m = max(m_0, m_1). Operands are the caller's bf16 rows, loaded by TMA
 // through 3-D tensor maps (d, head, batch * position); P is rounded to bf16
 // for its MMA (O is stored as bf16).
 //
@@ -43,20 +44,19 @@ struct FwdSmem {
   static constexpr int Q = 0;
   static constexpr int K = Q + kTile;         // 2 stages
   static constexpr int V = K + 2 * kTile;     // 2 stages
-  static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] partial sums
-  static constexpr int XCH = STAT + 2 * 128 * 4;  // [step parity][2 warpgroups][128 rows] maxima
-  static constexpr int BAR = XCH + 2 * 2 * 128 * 4;
+  static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] (max, sum)
+  static constexpr int BAR = STAT + 2 * 128 * 8;
   static constexpr int MISC = BAR + 128;      // TMEM base, abort flag
   static constexpr int TOTAL = MISC + 16;
 };
 
 // fQFull: Q landed. fKvFull / fKvEmpty: key-tile stage (K and V of a step).
-// fSFull: S of a step in TMEM buffer 0 / 1. fPFull: P written over S (256
-// arrivals). fPvDone: the P V MMAs of a step completed (its buffer is free
-// and O holds its terms). fOFull: every MMA completed. fXch: a step's row
-// maxima of both warpgroups are in shared memory (256 arrivals).
-enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fPFull0 = 7, fPvDone0 = 9,
-              fOFull = 11, fXch0 = 12, kFwdBars = 14 };
+// fSFull: S of a step in TMEM buffer 0 / 1. fPFull: one warpgroup's half of P
+// written over S (128 arrivals; [warpgroup][buffer]). fPvDone: both P V
+// halves of a step completed (its buffer is free and both O accumulators hold
+// its terms). fOFull: every MMA completed.
+enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fPFull0 = 7, fPvDone0 = 11,
+              fOFull = 13, kFwdBars = 14 };
 
 struct FwdParams {
   int B, Hq, Hk, Sq, Sk;
@@ -118,8 +118,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   c.status = nullptr;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFwdBars; ++i) {
-      const bool many = (i >= fPFull0 && i < fPvDone0) || i >= fXch0;  // 256 arrivals
-      ptx::mbar_init(c.bar(i), many ? 256u : 1u);
+      const bool many = i >= fPFull0 && i < fPvDone0;  // a warpgroup: 128 arrivals
+      ptx::mbar_init(c.bar(i), many ? 128u : 1u);
     }
     *c.abort = 0;
     ptx::fence_mbar_init();
@@ -135,8 +135,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::MISC);
-  const uint32_t t_O = tmem;          // [0, D): O accumulator
-  const uint32_t t_S0 = tmem + 128;   // S buffers 0 / 1 (128 columns each)
+  // O accumulators: warpgroup wg's keys (64 of each tile) in [wg D, wg D + D)
+  const uint32_t t_O = tmem;
+  const uint32_t t_S0 = tmem + 2 * D;  // S buffers 0 / 1 (128 columns each)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -176,17 +177,22 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint64_t dK = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dVmn = ptx::smem_desc_sw128(sbase + L::V, kFSlab, 1024);
       int n_pv[2] = {0, 0};
-      // O += P V of step v once P replaced S(v) in TMEM
+      // O_wg += P(:, keys of wg) V(keys of wg, :) of step v, each half once
+      // its warpgroup has written its P over S(v) in TMEM
       auto issue_pv = [&](int v) -> bool {
         const int sv = v & 1;
-        if (!wait_bar(c, fPFull0 + sv, (v >> 1) & 1, 6)) return false;
-        ptx::tc_fence_after();
         const uint32_t t_S = t_S0 + sv * 128;
         const uint64_t dv = ptx::desc_add(dVmn, sv * L::kTile);
 #pragma unroll
-        for (int s = 0; s < kBN / 16; ++s) {
-          const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
-          ptx::mma_ts(t_O, a_col, ptx::desc_add(dv, s * 2048), id_O, (v > 0 || s > 0) ? 1u : 0u);
+        for (int wg = 0; wg < 2; ++wg) {
+          if (!wait_bar(c, fPFull0 + wg * 2 + sv, (v >> 1) & 1, 6)) return false;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int s = 4 * wg; s < 4 * wg + 4; ++s) {
+            const uint32_t a_col = t_S + (s >> 2) * 64 + (s & 3) * 8;
+            ptx::mma_ts(t_O + wg * D, a_col, ptx::desc_add(dv, s * 2048), id_O,
+                        (v > 0 || s > 4 * wg) ? 1u : 0u);
+          }
         }
         ptx::mma_commit(c.bar(fKvEmpty0 + sv));  // K and V of the step read
         ptx::mma_commit(c.bar(fPvDone0 + sv));   // its S buffer free again, O up to date
@@ -286,51 +292,43 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       return true;
     };
-    // One pass over the live key tiles with a running row maximum. P is
-    // taken against m_used, the maximum the accumulated terms were scaled
-    // with; only when a tile's row maximum exceeds it by more than
-    // kRescaleLog2 (so P stays below 2^kRescaleLog2) does m_used move up,
-    // and then the row's O columns and partial sum are scaled down by
-    // 2^(old - new) once the previous P V has completed. O and the sum end
-    // in the same scale, so O / sum and LSE = m_used + log2(sum) are exact
-    // up to rounding whatever m_used is.
+    // One pass over the live key tiles. Each warpgroup keeps, per row, its
+    // own running maximum m_used, sum l and O accumulator over its 64 keys of
+    // every tile, so the two halves of a row never wait for each other; they
+    // meet once at the end. P is taken against m_used, the maximum the
+    // accumulated terms were scaled with; only when a tile's maximum exceeds
+    // it by more than kRescaleLog2 (so P stays below 2^kRescaleLog2) does
+    // m_used move up, and then the row of this warpgroup's O and its sum are
+    // scaled down by 2^(old - new) once the previous P V has completed.
     constexpr float kRescaleLog2 = 8.f;
-    float* xch = reinterpret_cast<float*>(smem + L::XCH);  // [step parity][warpgroup][row]
     float m_used = -INFINITY, l = 0.f;
+    const uint32_t t_Ow = t_O + wg * D + lane_off;  // this warpgroup's O rows
     bool ok = true;
     for (int u = 0; u < T; ++u) {
       float x[64];
       if (!logits(u, x)) { ok = false; break; }
-      float mx = -INFINITY;
+      float m_tile = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) mx = fmaxf(mx, x[e]);
-      // the row maximum over both halves of the tile (bounded barrier wait)
-      xch[((u & 1) * 2 + wg) * 128 + il] = mx;
-      ptx::mbar_arrive(c.bar(fXch0 + (u & 1)));
-      const bool met = wait_bar(c, fXch0 + (u & 1), (u >> 1) & 1, 12);
-      if (!__all_sync(0xffffffffu, met)) { ok = false; break; }
-      const float m_tile = fmaxf(mx, xch[((u & 1) * 2 + (1 - wg)) * 128 + il]);
+      for (int e = 0; e < 64; ++e) m_tile = fmaxf(m_tile, x[e]);
       const bool raise = m_tile > m_used + kRescaleLog2;  // this row's scale moves up
       const bool rescale = raise && m_used != -INFINITY;  // ... and O holds terms of it
       // The TMEM loads / stores are warp-collective: the warp takes the
       // rescale path when any of its rows needs it (factor 1 for the others).
       if (__any_sync(0xffffffffu, rescale)) {
-        // once P V(u - 1) (and so every earlier one) completed, scale this
-        // half row of O from m_used to m_tile
+        // once P V(u - 1) (and so every earlier one) completed
         const bool done = wait_bar(c, fPvDone0 + ((u - 1) & 1), ((u - 1) >> 1) & 1, 13);
         if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
         ptx::tc_fence_after();
         const float f = rescale ? ptx::ex2(m_used - m_tile) : 1.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
-          const uint32_t t_o = t_O + lane_off + wg * (D / 2) + cc * 32;
-          ptx::tmem_ld32(t_o, ov);
+          ptx::tmem_ld32(t_Ow + cc * 32, ov);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-          ptx::tmem_st16(t_o, ov);
-          ptx::tmem_st16(t_o + 16, ov + 16);
+          ptx::tmem_st16(t_Ow + cc * 32, ov);
+          ptx::tmem_st16(t_Ow + cc * 32 + 16, ov + 16);
         }
         l *= f;
       }
@@ -352,39 +350,52 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::tmem_st16(t_S + 16, pk + 16);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(fPFull0 + (u & 1)));
+      ptx::mbar_arrive(c.bar(fPFull0 + wg * 2 + (u & 1)));
     }
-    // the row's sum: the two halves meet in shared memory (both used m_used)
+    // the two halves of the row meet in shared memory
     float* stat = reinterpret_cast<float*>(smem + L::STAT);
-    stat[wg * 128 + il] = l;
+    stat[(wg * 128 + il) * 2] = m_used;
+    stat[(wg * 128 + il) * 2 + 1] = l;
     asm volatile("bar.sync 1, 256;" ::: "memory");
-    const float lsum = l + stat[(1 - wg) * 128 + il];
-    const float lse2 = lsum > 0.f ? m_used + log2f(lsum) : -INFINITY;  // log2 domain
+    const float m_o = stat[((1 - wg) * 128 + il) * 2];
+    const float l_o = stat[((1 - wg) * 128 + il) * 2 + 1];
+    const float mm = fmaxf(m_used, m_o);
+    const float f0 = m_used == -INFINITY ? 0.f : ptx::ex2(m_used - mm);  // this half
+    const float f1 = m_o == -INFINITY ? 0.f : ptx::ex2(m_o - mm);        // the other
+    const float lsum = l * f0 + l_o * f1;
+    const float lse2 = lsum > 0.f ? mm + log2f(lsum) : -INFINITY;  // log2 domain
     if (wg == 0 && row_in)
       p.lse[((int64_t)b * p.Hq + h) * p.Sq + i] = lse2 == -INFINITY ? -INFINITY : lse2 / kLog2e;
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    // O / sum: this warpgroup writes columns [wg D/2, wg D/2 + D/2) of its row
+    // O = (O_self f0 + O_other f1) / sum: this warpgroup writes columns
+    // [wg D/2, wg D/2 + D/2) of its row
     if (ok && (T == 0 || wait_bar(c, fOFull, 0, 11))) {
       ptx::tc_fence_after();
       __nv_bfloat16* orow = p.o + b * p.os0 + (int64_t)ic * p.os1 + h * p.os2 + wg * (D / 2);
+      const float g_self = f0 * inv, g_other = f1 * inv;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
-        uint32_t v[32];
+        uint32_t va[32], vb[32];
         if (T > 0) {
-          ptx::tmem_ld32(t_O + lane_off + wg * (D / 2) + cc * 32, v);
+          ptx::tmem_ld32(t_O + wg * D + lane_off + wg * (D / 2) + cc * 32, va);
+          ptx::tmem_ld32(t_O + (1 - wg) * D + lane_off + wg * (D / 2) + cc * 32, vb);
           ptx::tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
+          for (int e = 0; e < 32; ++e) va[e] = vb[e] = 0u;
         }
         if (row_in) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
+            float o8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o8[k] = __uint_as_float(va[e + k]) * g_self + __uint_as_float(vb[e + k]) * g_other;
             uint4 w;
-            w.x = pack_bf162(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-            w.y = pack_bf162(__uint_as_float(v[e + 2]) * inv, __uint_as_float(v[e + 3]) * inv);
-            w.z = pack_bf162(__uint_as_float(v[e + 4]) * inv, __uint_as_float(v[e + 5]) * inv);
-            w.w = pack_bf162(__uint_as_float(v[e + 6]) * inv, __uint_as_float(v[e + 7]) * inv);
+            w.x = pack_bf162(o8[0], o8[1]);
+            w.y = pack_bf162(o8[2], o8[3]);
+            w.z = pack_bf162(o8[4], o8[5]);
+            w.w = pack_bf162(o8[6], o8[7]);
             *reinterpret_cast<uint4*>(orow + cc * 32 + e) = w;
           }
         }
