@@ -46,17 +46,18 @@ struct FwdSmem {
   static constexpr int V = K + 2 * kTile;     // 2 stages
   static constexpr int STAT = V + 2 * kTile;  // [2 warpgroups][128 rows] (max, sum)
   static constexpr int BAR = STAT + 2 * 128 * 8;
-  static constexpr int MISC = BAR + 128;      // TMEM base, abort flag
+  static constexpr int MISC = BAR + 256;      // TMEM base, abort flag
   static constexpr int TOTAL = MISC + 16;
 };
 
-// fQFull: Q landed. fKvFull / fKvEmpty: key-tile stage (K and V of a step).
-// fSFull: S of a step in TMEM buffer 0 / 1. fPFull: one warpgroup's half of P
+// fQFull: Q landed. fKFull / fKEmpty, fVFull / fVEmpty: K and V of a step in
+// stage 0 / 1 (K is read by S alone, so its stage frees once S completed; V
+// by P V). fSFull: S of a step in TMEM buffer 0 / 1. fPFull: one warpgroup's half of P
 // written over S (128 arrivals; [warpgroup][buffer]). fPvDone: both P V
 // halves of a step completed (its buffer is free and both O accumulators hold
 // its terms). fOFull: every MMA completed.
-enum FwdBar { fQFull = 0, fKvFull0 = 1, fKvEmpty0 = 3, fSFull0 = 5, fPFull0 = 7, fPvDone0 = 11,
-              fOFull = 13, kFwdBars = 14 };
+enum FwdBar { fQFull = 0, fKFull0 = 1, fVFull0 = 3, fKEmpty0 = 5, fVEmpty0 = 7, fSFull0 = 9,
+              fPFull0 = 11, fPvDone0 = 15, fOFull = 17, kFwdBars = 18 };
 
 struct FwdParams {
   int B, Hq, Hk, Sq, Sk;
@@ -147,25 +148,33 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int hf = 0; hf < D / 64; ++hf)
         ptx::tma_load_3d(sbase + L::Q + hf * kFSlab, &tmQ, c.bar(fQFull), hf * 64, h, qrow);
-      // K and V of step u into stage u & 1, once P V(u - 2) read the stage
-      int issued[2] = {0, 0};
+      // K of step u into stage u & 1 once S(u - 2) read the stage, then V of
+      // step u once P V(u - 2) did (loads issued per stage: nk, nv)
+      int nk[2] = {0, 0}, nv[2] = {0, 0};
       for (int u = 0; u < T; ++u) {
         const int st = u & 1, use = u >> 1;
-        if (use > 0 && !wait_bar(c, fKvEmpty0 + st, (use - 1) & 1, 1)) break;
         const int krow = b * p.Sk + tiles.tile(u) * kBN;
-        const uint32_t full = c.bar(fKvFull0 + st);
-        ptx::mbar_arrive_expect_tx(full, 2 * L::kTile);
+        if (use > 0 && !wait_bar(c, fKEmpty0 + st, (use - 1) & 1, 1)) break;
+        const uint32_t kfull = c.bar(fKFull0 + st);
+        ptx::mbar_arrive_expect_tx(kfull, L::kTile);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
-          ptx::tma_load_3d(sbase + L::K + st * L::kTile + hf * kFSlab, &tmK, full, hf * 64, g, krow);
-          ptx::tma_load_3d(sbase + L::V + st * L::kTile + hf * kFSlab, &tmV, full, hf * 64, g, krow);
-        }
-        issued[st] = use + 1;
+        for (int hf = 0; hf < D / 64; ++hf)
+          ptx::tma_load_3d(sbase + L::K + st * L::kTile + hf * kFSlab, &tmK, kfull, hf * 64, g, krow);
+        nk[st] = use + 1;
+        if (use > 0 && !wait_bar(c, fVEmpty0 + st, (use - 1) & 1, 7)) break;
+        const uint32_t vfull = c.bar(fVFull0 + st);
+        ptx::mbar_arrive_expect_tx(vfull, L::kTile);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          ptx::tma_load_3d(sbase + L::V + st * L::kTile + hf * kFSlab, &tmV, vfull, hf * 64, g, krow);
+        nv[st] = use + 1;
       }
       // no copy may still be landing in shared memory when the CTA ends
       drain_bar(c, fQFull, 0);
-      for (int st = 0; st < 2; ++st)
-        if (issued[st] > 0) drain_bar(c, fKvFull0 + st, (issued[st] - 1) & 1);
+      for (int st = 0; st < 2; ++st) {
+        if (nk[st] > 0) drain_bar(c, fKFull0 + st, (nk[st] - 1) & 1);
+        if (nv[st] > 0) drain_bar(c, fVFull0 + st, (nv[st] - 1) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -176,13 +185,14 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint64_t dQ = ptx::smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t dK = ptx::smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dVmn = ptx::smem_desc_sw128(sbase + L::V, kFSlab, 1024);
-      int n_pv[2] = {0, 0};
+      int n_s[2] = {0, 0}, n_pv[2] = {0, 0};  // S / P V steps issued per stage
       // O_wg += P(:, keys of wg) V(keys of wg, :) of step v, each half once
       // its warpgroup has written its P over S(v) in TMEM
       auto issue_pv = [&](int v) -> bool {
         const int sv = v & 1;
         const uint32_t t_S = t_S0 + sv * 128;
         const uint64_t dv = ptx::desc_add(dVmn, sv * L::kTile);
+        if (!wait_bar(c, fVFull0 + sv, (v >> 1) & 1, 5)) return false;
 #pragma unroll
         for (int wg = 0; wg < 2; ++wg) {
           if (!wait_bar(c, fPFull0 + wg * 2 + sv, (v >> 1) & 1, 6)) return false;
@@ -194,8 +204,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         (v > 0 || s > 4 * wg) ? 1u : 0u);
           }
         }
-        ptx::mma_commit(c.bar(fKvEmpty0 + sv));  // K and V of the step read
-        ptx::mma_commit(c.bar(fPvDone0 + sv));   // its S buffer free again, O up to date
+        ptx::mma_commit(c.bar(fVEmpty0 + sv));  // V of the step read
+        ptx::mma_commit(c.bar(fPvDone0 + sv));  // its S buffer free again, O up to date
         ++n_pv[sv];
         return true;
       };
@@ -204,7 +214,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       bool ok = T == 0 || wait_bar(c, fQFull, 0, 2);
       for (int u = 0; ok && u < T; ++u) {
         const int st = u & 1;
-        ok = wait_bar(c, fKvFull0 + st, (u >> 1) & 1, 3) &&
+        ok = wait_bar(c, fKFull0 + st, (u >> 1) & 1, 3) &&
              (u < 2 || wait_bar(c, fPvDone0 + st, ((u - 2) >> 1) & 1, 4));  // buffer of step u - 2
         if (!ok) break;
         ptx::tc_fence_after();
@@ -216,14 +226,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           ptx::mma_ss(t_S, ptx::desc_add(dQ, off), ptx::desc_add(dk, off), id_S, s > 0);
         }
         ptx::mma_commit(c.bar(fSFull0 + st));
+        ptx::mma_commit(c.bar(fKEmpty0 + st));  // K of the step read
+        ++n_s[st];
         if (u > 0) ok = issue_pv(u - 1);
       }
       if (ok && T > 0) issue_pv(T - 1);
       ptx::mma_commit(c.bar(fOFull));
       // commit arrivals no other role waits for: waited here before the CTA exits
       for (int st = 0; st < 2; ++st) {
+        if (n_s[st] > 0) drain_bar(c, fKEmpty0 + st, (n_s[st] - 1) & 1);
         if (n_pv[st] > 0) {
-          drain_bar(c, fKvEmpty0 + st, (n_pv[st] - 1) & 1);
+          drain_bar(c, fVEmpty0 + st, (n_pv[st] - 1) & 1);
           drain_bar(c, fPvDone0 + st, (n_pv[st] - 1) & 1);
         }
       }
@@ -240,8 +253,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int ic = row_in ? i : p.Sq - 1;
     const float* brow = nullptr;
     if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
-    // log2-domain logits of this thread's 64 keys of step u's tile (dead: -inf)
-    auto logits = [&](int u, float* x) -> bool {
+    // This thread's 64 keys of step u's tile, as x with the log2-domain logit
+    // = x * xs: on a tile where every key is live and there is no bias, x is
+    // the raw score and xs = scale log2(e) (the scaling folds into the
+    // exponent's fma); otherwise x is the logit itself (dead keys -inf) and
+    // xs = 1.
+    auto scores = [&](int u, float* x, float& xs) -> bool {
       const int st = u & 1;
       // (warp-uniform outcome: the TMEM loads below are warp-collective)
       const bool full = wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10);
@@ -254,8 +271,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       ptx::tmem_wait_ld();
       const int n0 = tiles.tile(u) * kBN;
       const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
+      // (uniform over the CTA: a property of the tile)
       const bool partial = m0 + kBM > p.Sq || n0 + kBN > p.Sk ||
                            !tile_full(p.mask, m0, m0 + kBM, n0, n0 + kBN);
+      if (!BIAS && !partial) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sr[e]);
+        xs = p.scale_log2;
+        return true;
+      }
       int klo = 0, khi = kBN - 1, ksink = 0;
       if (partial) {
         klo = i - p.mask.wl - n0;
@@ -290,6 +314,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const bool live = !partial || (kk >= klo && kk <= khi) || kk < ksink;
         x[e] = live ? xv : -INFINITY;
       }
+      xs = 1.f;
       return true;
     };
     // One pass over the live key tiles. Each warpgroup keeps, per row, its
@@ -305,11 +330,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t t_Ow = t_O + wg * D + lane_off;  // this warpgroup's O rows
     bool ok = true;
     for (int u = 0; u < T; ++u) {
-      float x[64];
-      if (!logits(u, x)) { ok = false; break; }
-      float m_tile = -INFINITY;
+      float x[64], xs;
+      if (!scores(u, x, xs)) { ok = false; break; }
+      // the tile's maximum logit: max(x) xs exactly, xs being positive
+      float mx[4];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) m_tile = fmaxf(m_tile, x[e]);
+      for (int r = 0; r < 4; ++r) {
+        mx[r] = x[16 * r];
+#pragma unroll
+        for (int e = 1; e < 15; e += 2) mx[r] = ptx::max3(mx[r], x[16 * r + e], x[16 * r + e + 1]);
+        mx[r] = fmaxf(mx[r], x[16 * r + 15]);
+      }
+      const float m_tile = ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * xs;
       const bool raise = m_tile > m_used + kRescaleLog2;  // this row's scale moves up
       const bool rescale = raise && m_used != -INFINITY;  // ... and O holds terms of it
       // The TMEM loads / stores are warp-collective: the warp takes the
@@ -333,18 +365,21 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         l *= f;
       }
       if (raise) m_used = m_tile;
-      // P = 2^(x - m_used) as bf16 over S (dead keys, and rows with no live
-      // key so far, give 0)
+      // P = 2^(x xs - m_used) as bf16 over S. Dead keys give 2^-inf = 0; a
+      // row with no live key so far (m_used = -inf, every x -inf) takes 0 as
+      // its offset, so its P is 0 too.
+      const float nm = m_used == -INFINITY ? 0.f : -m_used;
       uint32_t pk[32];
-      float sum = 0.f;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
-        const float p0 = m_used == -INFINITY ? 0.f : ptx::ex2(x[e] - m_used);
-        const float p1 = m_used == -INFINITY ? 0.f : ptx::ex2(x[e + 1] - m_used);
-        sum += p0 + p1;
+        float a0, a1;
+        ptx::fma2(a0, a1, x[e], x[e + 1], xs, xs, nm, nm);
+        const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+        ptx::add2(s0, s1, s0, s1, p0, p1);
         pk[e / 2] = pack_bf162(p0, p1);
       }
-      l += sum;
+      l += s0 + s1;
       const uint32_t t_S = t_S0 + (u & 1) * 128 + lane_off + wg * 64;
       ptx::tmem_st16(t_S, pk);
       ptx::tmem_st16(t_S + 16, pk + 16);

@@ -281,7 +281,7 @@ __device__ __forceinline__ uint4 ld_shared_v4_u32(uint32_t addr) {
 }
 
 // Packed pairs of fp32 (sm_100-family f32x2 arithmetic, one instruction per
-// pair): d = a * b + c, d = a * b, d = a - b, elementwise on (x0, x1).
+// pair): d = a * b + c, d = a * b, d = a - b, d = a + b, elementwise on (x0, x1).
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
                                      float c0, float c1) {
   asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
@@ -307,6 +307,22 @@ __device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, f
       "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// max(a, b, c) in one instruction (sm_100 family)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float ex2(float x) {
