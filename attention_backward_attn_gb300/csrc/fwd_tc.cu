@@ -253,66 +253,70 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int ic = row_in ? i : p.Sq - 1;
     const float* brow = nullptr;
     if constexpr (BIAS) brow = p.bias + ((int64_t)h * p.Sq + ic) * p.Sk;
-    // This thread's 64 keys of step u's tile, as x with the log2-domain logit
-    // = x * xs: on a tile where every key is live and there is no bias, x is
-    // the raw score and xs = scale log2(e) (the scaling folds into the
-    // exponent's fma); otherwise x is the logit itself (dead keys -inf) and
-    // xs = 1.
-    auto scores = [&](int u, float* x, float& xs) -> bool {
+    // This thread's 64 keys of step u's tile, as x (fp32 bits in x[]) with
+    // the log2-domain logit = x * xs: on a tile where every key is live and
+    // there is no bias, x is the raw score as it came from TMEM and xs =
+    // scale log2(e) (the scaling folds into the exponent's fma); otherwise x
+    // is the logit itself (dead keys -inf) and xs = 1.
+    auto scores = [&](int u, uint32_t* x, float& xs) -> bool {
       const int st = u & 1;
-      // (warp-uniform outcome: the TMEM loads below are warp-collective)
-      const bool full = wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10);
-      if (!__all_sync(0xffffffffu, full)) return false;
-      ptx::tc_fence_after();
-      uint32_t sr[64];
-      const uint32_t t_S = t_S0 + st * 128 + lane_off + wg * 64;
-      ptx::tmem_ld32(t_S, sr);
-      ptx::tmem_ld32(t_S + 32, sr + 32);
-      ptx::tmem_wait_ld();
+      // the tile's mask class (uniform over the CTA), worked out while S(u)
+      // may still be running
       const int n0 = tiles.tile(u) * kBN;
       const int kcap = p.Sk - n0;  // keys [0, kcap) of the tile exist
-      // (uniform over the CTA: a property of the tile)
       const bool partial = m0 + kBM > p.Sq || n0 + kBN > p.Sk ||
                            !tile_full(p.mask, m0, m0 + kBM, n0, n0 + kBN);
-      if (!BIAS && !partial) {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) x[e] = __uint_as_float(sr[e]);
-        xs = p.scale_log2;
-        return true;
-      }
       int klo = 0, khi = kBN - 1, ksink = 0;
       if (partial) {
         klo = i - p.mask.wl - n0;
         khi = imin2(i + p.mask.wr - n0, kcap - 1);
         ksink = imin2(p.mask.sink - n0, kcap);
       }
-      // the row's bias: 16-byte loads when the tile's keys all exist and the
-      // bias rows are 16-byte aligned (Sk a multiple of 4), else clamped
-      // scalar loads (keys past Sk are dead anyway)
-      float bv[64];
-      if constexpr (BIAS) {
-        if (kcap >= kBN && (p.Sk & 3) == 0) {
-          const float4* b4 = reinterpret_cast<const float4*>(brow + n0 + wg * 64);
+      // the row's bias for these keys: 16-byte loads when the tile's keys
+      // all exist and the bias rows are 16-byte aligned (Sk a multiple of 4),
+      // else clamped scalar loads (keys past Sk are dead). At D = 64 they are
+      // issued before S is waited for; at D = 128 after S is in registers (so
+      // that the two 64-value arrays are not live across the wait).
+      float bv[BIAS ? 64 : 1];
+      auto load_bias = [&]() {
+        if constexpr (BIAS) {
+          if (kcap >= kBN && (p.Sk & 3) == 0) {
+            const float4* b4 = reinterpret_cast<const float4*>(brow + n0 + wg * 64);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float4 t4 = __ldg(b4 + e);
-            bv[4 * e] = t4.x;
-            bv[4 * e + 1] = t4.y;
-            bv[4 * e + 2] = t4.z;
-            bv[4 * e + 3] = t4.w;
+            for (int e = 0; e < 16; ++e) {
+              const float4 t4 = __ldg(b4 + e);
+              bv[4 * e] = t4.x;
+              bv[4 * e + 1] = t4.y;
+              bv[4 * e + 2] = t4.z;
+              bv[4 * e + 3] = t4.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) bv[e] = __ldg(brow + n0 + imin2(wg * 64 + e, kcap - 1));
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) bv[e] = __ldg(brow + n0 + imin2(wg * 64 + e, kcap - 1));
         }
+      };
+      if constexpr (D == 64) load_bias();
+      // (warp-uniform outcome: the TMEM loads below are warp-collective)
+      const bool full = wait_bar(c, fSFull0 + st, (u >> 1) & 1, 10);
+      if (!__all_sync(0xffffffffu, full)) return false;
+      ptx::tc_fence_after();
+      const uint32_t t_S = t_S0 + st * 128 + lane_off + wg * 64;
+      ptx::tmem_ld32(t_S, x);
+      ptx::tmem_ld32(t_S + 32, x + 32);
+      ptx::tmem_wait_ld();
+      if (!BIAS && !partial) {
+        xs = p.scale_log2;
+        return true;
       }
+      if constexpr (D != 64) load_bias();
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const int kk = wg * 64 + e;  // key within the tile
-        float xv = __uint_as_float(sr[e]) * p.scale_log2;
+        float xv = __uint_as_float(x[e]) * p.scale_log2;
         if constexpr (BIAS) xv = fmaf(bv[e], kLog2e, xv);
         const bool live = !partial || (kk >= klo && kk <= khi) || kk < ksink;
-        x[e] = live ? xv : -INFINITY;
+        x[e] = __float_as_uint(live ? xv : -INFINITY);
       }
       xs = 1.f;
       return true;
@@ -330,16 +334,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t t_Ow = t_O + wg * D + lane_off;  // this warpgroup's O rows
     bool ok = true;
     for (int u = 0; u < T; ++u) {
-      float x[64], xs;
+      uint32_t x[64];
+      float xs;
       if (!scores(u, x, xs)) { ok = false; break; }
       // the tile's maximum logit: max(x) xs exactly, xs being positive
       float mx[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        mx[r] = x[16 * r];
+        mx[r] = __uint_as_float(x[16 * r]);
 #pragma unroll
-        for (int e = 1; e < 15; e += 2) mx[r] = ptx::max3(mx[r], x[16 * r + e], x[16 * r + e + 1]);
-        mx[r] = fmaxf(mx[r], x[16 * r + 15]);
+        for (int e = 1; e < 15; e += 2)
+          mx[r] = ptx::max3(mx[r], __uint_as_float(x[16 * r + e]), __uint_as_float(x[16 * r + e + 1]));
+        mx[r] = fmaxf(mx[r], __uint_as_float(x[16 * r + 15]));
       }
       const float m_tile = ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * xs;
       const bool raise = m_tile > m_used + kRescaleLog2;  // this row's scale moves up
@@ -374,7 +380,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int e = 0; e < 64; e += 2) {
         float a0, a1;
-        ptx::fma2(a0, a1, x[e], x[e + 1], xs, xs, nm, nm);
+        ptx::fma2(a0, a1, __uint_as_float(x[e]), __uint_as_float(x[e + 1]), xs, xs, nm, nm);
         const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
         ptx::add2(s0, s1, s0, s1, p0, p1);
         pk[e / 2] = pack_bf162(p0, p1);
