@@ -97,6 +97,14 @@ SMALL_DENSE = {
     # MHA D = 512 through the dense path
     "mha_s128_d512": lambda: make_dense("z", 24, B=1, Hq=2, Hk=2, Sq=128, Sk=128, D=512,
                                         window_left=-1, window_right=0),
+    # bias at D = 128: window + sinks on ragged lengths (bias rows clamped past
+    # Sk, partial tiles), and whole tiles without a mask (16-byte bias loads)
+    "bias_window_sinks_s300_d128": lambda: make_dense("fb1", 47, B=2, Hq=4, Hk=2, Sq=300,
+                                                      Sk=300, D=128, window_left=90,
+                                                      window_right=0, num_sink=2,
+                                                      alibi=True),
+    "bias_gqa2_s256_d128": lambda: make_dense("fb2", 48, B=1, Hq=4, Hk=2, Sq=256, Sk=256,
+                                              D=128, alibi=True),
 }
 
 
@@ -434,7 +442,8 @@ def test_fully_masked_rows_and_empty_query():
 FORWARD_CASES = ["window128_sink4_s640_d128", "alibi_dbias_s256_d64", "mha_s64_d64",
                  "ragged_causal_sink_s200_d64", "gqa8_sq128_sk320_d128",
                  "window_lr_sq320_sk192_d64", "br_causal_sq384_sk128_d64",
-                 "br_window_sink_sq150_sk230_d64", "gqa4_causal_s384_d128"]
+                 "br_window_sink_sq150_sk230_d64", "gqa4_causal_s384_d128",
+                 "bias_window_sinks_s300_d128", "bias_gqa2_s256_d128"]
 
 
 @pytest.mark.parametrize("cuda_cores", [False, True])
