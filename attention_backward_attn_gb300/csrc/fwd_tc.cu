@@ -17,8 +17,11 @@
 // completed), so most tiles need no correction. At the end the halves meet
 // once: O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / sum and LSE = m + log2(sum)
 // with m = max(m_0, m_1). Operands are the caller's bf16 rows, loaded by TMA
-// through 3-D tensor maps (d, head, batch * position); P is rounded to bf16
-// for its MMA (O is stored as bf16).
+// through 3-D tensor maps (d, head, batch * position), K and V of a tile
+// into stages released separately (K once S has read it, V once P V has);
+// P is rounded to bf16 for its MMA (O is stored as bf16). On tiles the mask
+// leaves whole and without bias the softmax works on the raw scores in the
+// registers the TMEM load filled (the scale is folded into the exponent).
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 4-7 / 8-11 two softmax warpgroups (key columns 0-63 / 64-127
