@@ -72,7 +72,9 @@
 #include "tc_ptx.cuh"
 #include "tc_util.cuh"
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 namespace attn {
 namespace {
@@ -187,7 +189,9 @@ struct TcParams {
   const int32_t* cu_k;
   int total_q, total_k;
   int br;
-  int cs;          // key-major CTAs per key tile (query-head split)
+  int cs;          // key-major CTAs per key tile (query-head split) of key tiles [0, n_split)
+  int n_split;     // key tiles from n_split on have fewer live query tiles and
+  int cs_lo;       // split over cs_lo CTAs only
   int kv_ctas;     // blocks [0, kv_ctas) are key-major, the rest query-major
   int qb_ctas;     // batch-inner dbias mode: blocks [0, qb_ctas) are batch-inner
                    // query-major, the rest key-major (without dbias)
@@ -400,11 +404,16 @@ __device__ __forceinline__ void kv_cta(const CUtensorMap* tmQ, const CUtensorMap
   constexpr bool kTB = tma_bias<D, BIAS, RB>();  // bias tiles through TMA (whole tiles)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int cs = p.cs;
-  const int rank = kvi % cs;
-  const int ci = kvi / cs;
-  const int bg = ci % (p.B * p.Hk);  // (batch, KV head); key tile slowest = heaviest first
-  const int nt = ci / (p.B * p.Hk);
+  // key tiles [0, n_split) over cs CTAs each, the rest over cs_lo
+  const int bhk = p.B * p.Hk;
+  const int n_hi = p.n_split * bhk * p.cs;  // CTAs of the first n_split key tiles
+  const bool lo_part = kvi >= n_hi;
+  const int cs = lo_part ? p.cs_lo : p.cs;
+  const int kk = lo_part ? kvi - n_hi : kvi;
+  const int rank = kk % cs;
+  const int ci = kk / cs;
+  const int bg = ci % bhk;  // (batch, KV head); key tile slowest = heaviest first when causal
+  const int nt = (lo_part ? p.n_split : 0) + ci / bhk;
   const int g = bg % p.Hk;
   const int b = bg / p.Hk;
   const int n0 = nt * BN;
@@ -1832,6 +1841,42 @@ EncodeFn encode_fn() {
   return fn;
 }
 
+// The key tiles that need less splitting: with the uniform split cs, a
+// key-major CTA takes at most (r / cs) max_n L_n query tiles (L_n = live query
+// tiles of key tile n, r = query heads per KV head). The trailing key tiles
+// whose (r / c) L_n stays within that bound can run as c < cs CTAs each (no
+// longer than the longest CTA, fewer fixed costs); of the divisors c of cs,
+// the one that removes the most CTAs is taken. Lengths of a variable-length
+// batch are taken at their maxima (a schedule choice only).
+static void tail_split(const Problem& pr, int cs, int* n_split, int* cs_lo) {
+  const int nkt = tc_rows(pr.Sk) / BN;
+  *n_split = nkt;
+  *cs_lo = cs;
+  if (cs == 1 || nkt == 0) return;
+  const int r = pr.Hq / pr.Hk;
+  std::vector<int> live(nkt);
+  int lmax = 0;
+  for (int n = 0; n < nkt; ++n) {
+    int lo, hi;
+    live_query_tiles(pr.mask, pr.Sq, pr.Sk, BM, BN, n * BN, &lo, &hi);
+    live[n] = hi >= lo ? hi - lo + 1 : 0;
+    lmax = std::max(lmax, live[n]);
+  }
+  const int64_t cap = (int64_t)(r / cs) * lmax;
+  int64_t best = 0;
+  for (int c = 1; c < cs; ++c) {
+    if (cs % c != 0) continue;
+    int ns = nkt;
+    while (ns > 0 && (int64_t)(r / c) * live[ns - 1] <= cap) --ns;
+    const int64_t saved = (int64_t)(nkt - ns) * (cs - c);
+    if (saved > best) {
+      best = saved;
+      *n_split = ns;
+      *cs_lo = c;
+    }
+  }
+}
+
 int tc_head_split(const Problem& p) {
   // deterministic: one CTA per key tile writes dK / dV (no partial sums added
   // in arrival order)
@@ -1909,7 +1954,8 @@ cudaError_t launch_bwd_tc(const Problem& pr, const __half* q16, const __half* k1
   p.br = pr.br ? 1 : 0;
   p.ragged = (p.Sqs != p.Sq || p.Sks != p.Sk || pr.varlen) ? 1 : 0;
   p.cs = tc_head_split(pr);
-  p.kv_ctas = pr.B * pr.Hk * (p.Sks / BN) * p.cs;
+  tail_split(pr, p.cs, &p.n_split, &p.cs_lo);
+  p.kv_ctas = pr.B * pr.Hk * (p.n_split * p.cs + (p.Sks / BN - p.n_split) * p.cs_lo);
   p.scale = pr.scale;
   p.scale_log2 = pr.scale * kLog2e;
   p.mask = pr.mask;
