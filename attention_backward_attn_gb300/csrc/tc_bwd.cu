@@ -359,11 +359,23 @@ struct KTileIter {
 };
 
 // Eight fp32 values as one 32-byte store (one full sector: half the store
-// instructions of 16-byte stores when each thread writes its own row).
+// instructions of 16-byte stores when each thread writes its own row). The
+// output buffers need only be 16-byte aligned: where dst is not 32-byte
+// aligned the values go out as two 16-byte stores.
 __device__ __forceinline__ void put8(float* dst, const float* v) {
-  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]),
-               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
-               : "memory");
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
+                 "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+                 "f"(v[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3])
+                 : "memory");
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4), "f"(v[4]),
+                 "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+  }
 }
 
 // Barrier set-up by thread 0 (the producer), which then issues the CTA's

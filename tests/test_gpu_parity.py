@@ -388,6 +388,40 @@ def test_deterministic_dbias_graph_replay_full_size():
     H.check_close("dbias", plan.dbias.cpu().numpy()[heads], dB)
 
 
+def test_batch_inner_outputs_only_16_byte_aligned():
+    # The API asks dq and dbias to be 16-byte aligned only; the batch-inner
+    # dbias CTAs store 32 bytes at a time where the address allows it and
+    # 16 bytes where it does not. Buffers that start 16 bytes past a 32-byte
+    # boundary must give the same bits as the regular ones.
+    torch = _torch()
+    import attention_backward_attn_gb300 as ab
+    w = SMALL_DENSE["alibi_dbias_s256_d64"]()
+    O_b, L_f, _, _ = H.dense_forward_inputs(w)
+    plan = H.gpu_dense_plan(w, O_b, L_f)
+    assert plan.path == 1
+    plan.run()
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+
+    def shifted_like(t):
+        big = torch.full((t.numel() + 8,), float("nan"), dtype=t.dtype, device=t.device)
+        assert big.data_ptr() % 32 == 0
+        v = big[4:4 + t.numel()].view(t.shape)
+        assert v.data_ptr() % 32 == 16
+        return v
+
+    dq16, db16 = shifted_like(plan.dq), shifted_like(plan.dbias)
+    ab.attn_bwd_preprocess(plan.prob, plan.sparse, plan.q, plan.k, plan.v, plan.o, plan.do,
+                           plan.delta, db16, plan.dk, plan.dv, plan.workspace, plan.ws_bytes)
+    ab.attn_bwd(plan.prob, plan.mask, plan.sparse, plan.q, plan.k, plan.v, plan.do, plan.lse,
+                plan.delta, plan.bias, dq16, plan.dk, plan.dv, db16, plan.workspace,
+                plan.ws_bytes)
+    torch.cuda.synchronize()
+    assert plan.device_status()[0] == 0
+    assert torch.equal(dq16, plan.dq)
+    assert torch.equal(db16, plan.dbias)
+
+
 def test_head_split_needs_the_prepared_dk_dv():
     # GQA 8:1 on a small problem splits each key tile's query heads over
     # several CTAs that add partial sums into dk / dv; the pre-pass zeroes the
