@@ -16,7 +16,10 @@
 // the KV head and loops over their live query tiles, accumulating its partial
 // dK / dV in TMEM over the group. At the end each CTA adds its partial rows
 // into dK / dV with TMA bulk reductions (the pre-pass zeroes the buffers when
-// cs > 1), so no post-pass over per-head gradients exists. Per
+// cs > 1), so no post-pass over per-head gradients exists. Trailing key tiles
+// with fewer live query tiles may use a smaller split (cs_lo, down to one CTA
+// that stores its rows), so that no CTA runs longer than the longest split
+// one while fewer CTAs pay the fixed costs. Per
 // tile, so that one thread owns one key row of the softmax:
 //   MMA1  S^T  = K  Q^T      (M = keys, N = queries, K = D; both K-major)
 //   MMA2  dP^T = V  dO^T     (into the same TMEM columns, once S^T was read)
