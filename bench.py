@@ -381,8 +381,8 @@ def run_ours(args):
 # entries, CTAs and bytes linear in S). An entry goes back to None when its kernel changes.
 NCU_TRAFFIC = {
     "gqa4_causal_s1024_d128": 25.5168e6 + 12.288e3,
-    "mha_alibi_dbias_s2048_d64": 2 * (368.76416e6 + 176.65536e6),
-    "gqa4_window1024_sink4_s8192_d128": 2 * (157.732096e6 + 66.527488e6),
+    "mha_alibi_dbias_s2048_d64": 2 * (366.990336e6 + 176.617728e6),
+    "gqa4_window1024_sink4_s8192_d128": 2 * (158.30016e6 + 66.37824e6),
     "sparse_scfa_s4096_h64_d512": 4 * (140.928e6 + 82.918912e6),
 }
 
