@@ -220,10 +220,9 @@ size_t attn_bwd_workspace_size(const attn_problem_t* prob, const attn_mask_t* ma
  *    not in the D = 64 batch-inner case, where attn_bwd stores every entry;
  *    in the deterministic mode with B > 1, the per-batch dbias slices of the
  *    workspace instead, which attn_bwd then sums into dbias), for the sparse
- *    variant sparse->d_ori_kv / d_cmp_kv, and the rows of dk / dv whose key
- *    tiles the tensor-core path splits over several CTAs by query head (they
- *    add their partial sums; the rows of unsplit key tiles are stored whole
- *    by attn_bwd);
+ *    variant sparse->d_ori_kv / d_cmp_kv, and dk / dv when the tensor-core
+ *    path splits a KV head's query-head group over several CTAs that add
+ *    their partial sums (small problems);
  *  - clears the workspace status record;
  *  - when attn_bwd will take the tensor-core path, writes fp16 copies of q,
  *    k, v and dO into the workspace (head-major rows, each head's length
