@@ -385,8 +385,8 @@ attn_status_t attn_bwd_preprocess(const attn_problem_t* prob, const attn_sparse_
       p.sparse ? sparse->cmp_kv : nullptr, (w.staged && p.sparse) ? staged(w.kv16) : nullptr,
       // dk / dv are recorded (for attn_bwd's check) only when zeroed here:
       // only then may the head-split kernel add partial sums into them
-      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, zero_kv ? tc_split_key_rows(p) : 0,
-      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, st, stream));
+      zero_kv ? dk : nullptr, zero_kv ? dv : nullptr, zero_kv ? dk : nullptr,
+      zero_kv ? dv : nullptr, st, stream));
 }
 
 attn_status_t attn_bwd(const attn_problem_t* prob, const attn_mask_t* mask,

@@ -60,9 +60,8 @@ cudaError_t launch_preprocess(const Problem& p, const void* q, const void* k, co
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
-                              __half* kv16, float* dk_zero, float* dv_zero,
-                              int64_t kv_zero_rows, float* dk, float* dv, DevStatus* st,
-                              cudaStream_t stream);
+                              __half* kv16, float* dk_zero, float* dv_zero, float* dk,
+                              float* dv, DevStatus* st, cudaStream_t stream);
 
 // out[e] = slices[0][e] + slices[1][e] + ... + slices[n - 1][e] (in that
 // order), slices `stride` floats apart, e < stride.
@@ -85,11 +84,6 @@ bool tc_dbias_in_q(const Problem& p);
 // Key-major CTAs per (key tile, KV head) of the dense tensor-core kernel; when
 // above 1 they add partial dK / dV sums into buffers the pre-pass zeroed.
 int tc_head_split(const Problem& p);
-// Key rows of each batch, from the first, whose dK / dV the key-major CTAs add
-// as partial sums (and the pre-pass must zero): 0 without a head split, Sk
-// when every key tile is split, fewer when only the leading key tiles are;
-// -1 for a variable-length batch (zero every row).
-int tc_split_key_rows(const Problem& p);
 // Diagnostic: the per-element live sets of the dense tensor-core kernel's
 // key-major and query-major CTAs for one sequence of lengths Sq x Sk
 // (mask_probe_kernel in tc_bwd.cu). aligned_variant selects the

@@ -24,8 +24,6 @@
 #include "internal.h"
 #include "tc_ptx.cuh"
 
-#include <algorithm>
-
 namespace attn {
 namespace {
 
@@ -62,12 +60,10 @@ struct PreParams {
   int64_t zero_nb;
   float* zero_c;
   int64_t zero_nc;
-  float* zero_d;  // dk, dv: zero_runs runs of zero_nd / zero_ne floats,
-  int64_t zero_nd;  // zero_step floats apart (one per batch)
+  float* zero_d;
+  int64_t zero_nd;
   float* zero_e;
   int64_t zero_ne;
-  int64_t zero_step;
-  int zero_runs;
   float* dk;  // recorded for the backward's check
   float* dv;
   DevStatus* st;
@@ -301,10 +297,8 @@ preprocess_kernel(const PreParams p) {
   zero_range(p.zero_a, p.zero_na, tid, nthreads);
   zero_range(p.zero_b, p.zero_nb, tid, nthreads);
   zero_range(p.zero_c, p.zero_nc, tid, nthreads);
-  for (int r = 0; r < p.zero_runs; ++r) {
-    zero_range(p.zero_d + r * p.zero_step, p.zero_nd, tid, nthreads);
-    zero_range(p.zero_e + r * p.zero_step, p.zero_ne, tid, nthreads);
-  }
+  zero_range(p.zero_d, p.zero_nd, tid, nthreads);
+  zero_range(p.zero_e, p.zero_ne, tid, nthreads);
 
   // Range overflow is handed to attn_bwd through this block's flag slot: a
   // report straight into the status record could race with the reset above.
@@ -393,9 +387,8 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
                               const void* o, const void* dO, float* delta,
                               float* dbias, float* d_ori, float* d_cmp, __half* q16, __half* k16,
                               __half* v16, __half* do16, const void* ori_kv, const void* cmp_kv,
-                              __half* kv16, float* dk_zero, float* dv_zero,
-                              int64_t kv_zero_rows, float* dk, float* dv, DevStatus* st,
-                              cudaStream_t stream) {
+                              __half* kv16, float* dk_zero, float* dv_zero, float* dk,
+                              float* dv, DevStatus* st, cudaStream_t stream) {
   PreParams p;
   p.B = pr.B;
   p.Hq = pr.Hq;
@@ -436,14 +429,7 @@ cudaError_t launch_preprocess(const Problem& pr, const void* q, const void* k, c
   p.zero_nb = d_ori ? (int64_t)pr.n_ori * pr.Hk * pr.D : 0;
   p.zero_c = d_cmp;
   p.zero_nc = d_cmp ? (int64_t)pr.n_cmp * pr.Hk * pr.D : 0;
-  // dk / dv: every row (kv_zero_rows < 0, or a variable-length batch), else
-  // the first kv_zero_rows key rows of each batch
-  const bool all_rows = kv_zero_rows < 0 || pr.varlen;
-  const int64_t row = (int64_t)pr.Hk * pr.D;
-  const int64_t nkd = all_rows ? (pr.varlen ? (int64_t)pr.total_k : (int64_t)pr.B * pr.Sk) * row
-                               : std::min<int64_t>(kv_zero_rows, pr.Sk) * row;
-  p.zero_runs = all_rows ? 1 : pr.B;
-  p.zero_step = all_rows ? 0 : (int64_t)pr.Sk * row;
+  const int64_t nkd = (pr.varlen ? (int64_t)pr.total_k : (int64_t)pr.B * pr.Sk) * pr.Hk * pr.D;
   p.zero_d = dk_zero;
   p.zero_nd = dk_zero ? nkd : 0;
   p.zero_e = dv_zero;

@@ -1899,16 +1899,6 @@ int tc_head_split(const Problem& p) {
   return head_split(p.Hq / p.Hk, p.B * p.Hk * (tc_rows(p.Sk) / BN), sm_count());
 }
 
-int tc_split_key_rows(const Problem& p) {
-  const int cs = tc_head_split(p);
-  if (cs <= 1) return 0;
-  if (p.varlen) return -1;
-  int n_split, cs_lo;
-  tail_split(p, cs, &n_split, &cs_lo);
-  if (cs_lo > 1) return p.Sk;  // the trailing key tiles add partial rows too
-  return std::min(p.Sk, n_split * BN);
-}
-
 bool tc_dbias_in_q(const Problem& p) {
   // dQ of B batches (B D columns) and two S / dP buffers fit TMEM at D = 64;
   // whole tiles and fixed lengths (the CTA's sub-tiles share one sequence view)
